@@ -1,0 +1,324 @@
+"""Seeded synthetic workloads for the DFlash drafter block step.
+
+This module only draws numbers and lays them out; it holds none of the
+drafter's arithmetic.  Both the CUDA path and the fp64 oracle consume the
+exact bytes produced here (weights rounded once to their storage dtype,
+features, token ids, positions, mismatch indices).
+
+Shapes follow the workloads described on the dflash-ops model card
+(section "Measured": 5 layers, n_embd 6656, 32/8 heads of 128, n_ff 19968,
+window 2048, block 16, vocabulary 8192) and the cross-sequence batch of
+dflash_head.rs (struct DflashBatch, enum DflashQuantization).  No trained
+weights exist here, so every tensor is random: weights ~ N(0, 1/fan_in),
+norm weights 1 + N(0, 0.02), features ~ N(0, 1), token embeddings ~ N(0, 1).
+
+FP8 weights are made the way dflash_head.rs describes its weight-only FP8
+copies: one f32 scale per output row, s[n] = max_k |w[n,k]| / 448, and the
+stored byte is the E4M3 (fn variant) code of w[n,k] / s[n], rounded to
+nearest-even and clamped to +-448.  That is weight preparation, not a step
+of the drafter; the cast itself is torch's float8_e4m3fn conversion.
+"""
+from __future__ import annotations
+
+import dataclasses
+from dataclasses import dataclass, field
+from typing import Dict, List, Optional, Tuple
+
+import numpy as np
+import torch
+
+BLOCK = 16          # tokens in one noise block (anchor + 15 masks)
+FP8_MAX = 448.0     # largest finite E4M3 (fn) magnitude
+
+DTYPES = ("f32", "bf16", "fp8")
+_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class DraftConfig:
+    """Drafter geometry, storage formats and the synthetic workload recipe."""
+
+    name: str
+    n_layer: int
+    n_embd: int
+    n_head: int
+    n_head_kv: int
+    head_dim: int
+    n_ff: int
+    window: int
+    n_vocab: int
+    weight_dtype: str           # q/k/v/o/gate/up/down and lm_head: f32 | bf16 | fp8
+    dense_dtype: str            # tok_embd, fc, norm weights, target features: f32 | bf16
+    ring_dtype: str             # ring K/V: f32 | bf16
+    n_seq: int = 1
+    n_target_layers: int = 5
+    target_embd: int = 0        # 0 -> n_embd
+    rope_theta: float = 1e6
+    eps: float = 1e-6
+    # inject schedule for one-sequence workloads: list of (first_pos, count)
+    inject: Tuple[Tuple[int, int], ...] = ()
+    # batched workloads: fill ~ U{fill_lo..fill_hi}, offset ~ U{0..offset_hi}
+    fill_lo: int = 0
+    fill_hi: int = 0
+    offset_hi: int = 0
+    mismatch: str = "uniform"   # uniform in 0..15 | geometric(p) capped at 15
+    mismatch_p: float = 0.35
+    seed: int = 1000
+
+    @property
+    def d_t(self) -> int:
+        return self.target_embd or self.n_embd
+
+    @property
+    def feat_dim(self) -> int:
+        return self.n_target_layers * self.d_t
+
+    @property
+    def qd(self) -> int:
+        return self.n_head * self.head_dim
+
+    @property
+    def kvd(self) -> int:
+        return self.n_head_kv * self.head_dim
+
+    @property
+    def mask_token_id(self) -> int:
+        return self.n_vocab - 1
+
+    def weight_params(self) -> int:
+        """Parameters of the GEMM weights streamed by one block step."""
+        per_layer = (self.qd + 2 * self.kvd) * self.n_embd + self.n_embd * self.qd \
+            + 3 * self.n_ff * self.n_embd
+        return self.n_layer * per_layer + self.n_vocab * self.n_embd
+
+    def with_(self, **kw) -> "DraftConfig":
+        return dataclasses.replace(self, **kw)
+
+
+def _cfg_list() -> List[DraftConfig]:
+    tiny = DraftConfig(
+        name="tiny_f32", n_layer=1, n_embd=256, n_head=4, n_head_kv=2, head_dim=64,
+        n_ff=768, window=64, n_vocab=512, weight_dtype="f32", dense_dtype="f32",
+        ring_dtype="f32", inject=((0, 64), (64, 16)), seed=1000)
+    small = DraftConfig(
+        name="small_bf16", n_layer=3, n_embd=2048, n_head=16, n_head_kv=4, head_dim=128,
+        n_ff=6144, window=512, n_vocab=32000, weight_dtype="bf16", dense_dtype="bf16",
+        ring_dtype="bf16", inject=((0, 512), (512, 37)), seed=1001)
+    real_bf16 = DraftConfig(
+        name="real_bf16", n_layer=5, n_embd=6656, n_head=32, n_head_kv=8, head_dim=128,
+        n_ff=19968, window=2048, n_vocab=8192, weight_dtype="bf16", dense_dtype="bf16",
+        ring_dtype="bf16", inject=((0, 2048),), seed=1002)
+    real_f32 = real_bf16.with_(name="real_f32", weight_dtype="f32", dense_dtype="f32",
+                               ring_dtype="f32", seed=1003)
+    batched_fp8 = DraftConfig(
+        name="batched_fp8", n_layer=5, n_embd=4096, n_head=32, n_head_kv=8, head_dim=128,
+        n_ff=12288, window=2048, n_vocab=32768, weight_dtype="fp8", dense_dtype="bf16",
+        ring_dtype="bf16", n_seq=32, fill_lo=256, fill_hi=2048, offset_hi=65535,
+        mismatch="geometric", mismatch_p=0.35, seed=1004)
+    return [tiny, small, real_bf16, real_f32, batched_fp8]
+
+
+CONFIGS: List[DraftConfig] = _cfg_list()
+BY_NAME: Dict[str, DraftConfig] = {c.name: c for c in CONFIGS}
+
+# Test-only geometries: ragged vocab / n_ff / row counts, several sequences,
+# and a batched FP8 case small enough for the oracle to finish in seconds.
+RAGGED = DraftConfig(
+    name="ragged_bf16", n_layer=2, n_embd=320, n_head=5, n_head_kv=1, head_dim=64,
+    n_ff=800, window=48, n_vocab=1001, weight_dtype="bf16", dense_dtype="bf16",
+    ring_dtype="bf16", n_seq=3, fill_lo=20, fill_hi=48, offset_hi=300, seed=2001)
+SMALL_FP8 = DraftConfig(
+    name="small_fp8", n_layer=2, n_embd=512, n_head=8, n_head_kv=2, head_dim=64,
+    n_ff=1536, window=128, n_vocab=3000, weight_dtype="fp8", dense_dtype="bf16",
+    ring_dtype="bf16", n_seq=5, fill_lo=32, fill_hi=128, offset_hi=65535,
+    mismatch="geometric", seed=2002)
+MIXED_F32 = DraftConfig(
+    name="mixed_f32w_bf16ring", n_layer=2, n_embd=256, n_head=4, n_head_kv=4, head_dim=64,
+    n_ff=544, window=40, n_vocab=777, weight_dtype="f32", dense_dtype="f32",
+    ring_dtype="bf16", n_seq=2, fill_lo=8, fill_hi=40, offset_hi=1000, seed=2003)
+TEST_CONFIGS: Dict[str, DraftConfig] = {c.name: c for c in (RAGGED, SMALL_FP8, MIXED_F32)}
+
+
+def get_config(name: str) -> DraftConfig:
+    if name in BY_NAME:
+        return BY_NAME[name]
+    return TEST_CONFIGS[name]
+
+
+# --------------------------------------------------------------------------
+# storage helpers (no drafter arithmetic: rounding a draw to its format)
+# --------------------------------------------------------------------------
+
+def _store_dense(x: torch.Tensor, dtype: str) -> torch.Tensor:
+    return x.to(_TORCH[dtype]).contiguous()
+
+
+def quantize_fp8_rows(w: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-row FP8 E4M3 copy of a f32 matrix: (codes uint8 [N,K], scales f32 [N])."""
+    amax = w.abs().amax(dim=1)
+    s = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax)).to(torch.float32)
+    q = (w / s[:, None]).clamp_(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).contiguous(), s.contiguous()
+
+
+@dataclass
+class Weight:
+    """One stored matrix or vector: raw tensor in its storage format (+ FP8 scales)."""
+
+    data: torch.Tensor                  # f32 / bf16 tensor, or uint8 codes for fp8
+    dtype: str
+    scale: Optional[torch.Tensor] = None  # f32 [rows] for fp8
+
+    @property
+    def shape(self):
+        return tuple(self.data.shape)
+
+    def nbytes(self) -> int:
+        n = self.data.numel() * self.data.element_size()
+        if self.scale is not None:
+            n += self.scale.numel() * 4
+        return n
+
+
+@dataclass
+class Workload:
+    cfg: DraftConfig
+    weights: Dict[str, Weight]           # global names and "l{i}.{name}"
+    feats: List[torch.Tensor]            # per sequence [T_s, feat_dim], dense dtype
+    inject_calls: List[Tuple[int, int, int, int]]  # (seq, first_pos, count, feat_row0)
+    id_last: torch.Tensor                # int32 [n_seq]
+    n_past: torch.Tensor                 # int32 [n_seq]
+    mismatch: torch.Tensor               # int32 [n_seq], 15 = no mismatch
+    tail: torch.Tensor                   # int32 [n_seq, 15], random target tokens
+    fills: List[int] = field(default_factory=list)
+    offsets: List[int] = field(default_factory=list)
+
+    def positions(self, call: Tuple[int, int, int, int]) -> torch.Tensor:
+        _, p0, cnt, _ = call
+        return torch.arange(p0, p0 + cnt, dtype=torch.int32)
+
+    def call_feats(self, call: Tuple[int, int, int, int]) -> torch.Tensor:
+        seq, _, cnt, r0 = call
+        return self.feats[seq][r0:r0 + cnt]
+
+    def weight_bytes(self) -> int:
+        names = ["lm_head"] + [f"l{i}.{n}" for i in range(self.cfg.n_layer)
+                               for n in ("wq", "wk", "wv", "wo", "gate", "up", "down")]
+        return sum(self.weights[n].nbytes() for n in names)
+
+
+LAYER_ORDER = ("attn_norm", "wq", "wk", "wv", "wo", "q_norm", "k_norm", "ffn_norm",
+               "gate", "up", "down")
+PROJ = ("wq", "wk", "wv", "wo", "gate", "up", "down")
+
+
+def _layer_shape(cfg: DraftConfig, name: str) -> Tuple[int, ...]:
+    d, qd, kvd, f, hd = cfg.n_embd, cfg.qd, cfg.kvd, cfg.n_ff, cfg.head_dim
+    return {
+        "attn_norm": (d,), "ffn_norm": (d,), "q_norm": (hd,), "k_norm": (hd,),
+        "wq": (qd, d), "wk": (kvd, d), "wv": (kvd, d), "wo": (d, qd),
+        "gate": (f, d), "up": (f, d), "down": (d, f),
+    }[name]
+
+
+def make_weights(cfg: DraftConfig, g: torch.Generator) -> Dict[str, Weight]:
+    """Draw every weight in the fixed order tok_embd, fc, hidden_norm, the layers'
+    [attn_norm, wq, wk, wv, wo, q_norm, k_norm, ffn_norm, gate, up, down],
+    out_norm, lm_head."""
+    w: Dict[str, Weight] = {}
+
+    def proj(shape):
+        fan_in = shape[1]
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        x.mul_(1.0 / np.sqrt(fan_in))
+        if cfg.weight_dtype == "fp8":
+            q, s = quantize_fp8_rows(x)
+            return Weight(q, "fp8", s)
+        return Weight(_store_dense(x, cfg.weight_dtype), cfg.weight_dtype)
+
+    def dense_mat(shape, std):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        return Weight(_store_dense(x, cfg.dense_dtype), cfg.dense_dtype)
+
+    def norm_vec(n):
+        x = 1.0 + 0.02 * torch.randn((n,), generator=g, dtype=torch.float32)
+        return Weight(_store_dense(x, cfg.dense_dtype), cfg.dense_dtype)
+
+    w["tok_embd"] = dense_mat((cfg.n_vocab, cfg.n_embd), 1.0)
+    w["fc"] = dense_mat((cfg.n_embd, cfg.feat_dim), 1.0 / np.sqrt(cfg.feat_dim))
+    w["hidden_norm"] = norm_vec(cfg.n_embd)
+    for i in range(cfg.n_layer):
+        for n in LAYER_ORDER:
+            shp = _layer_shape(cfg, n)
+            w[f"l{i}.{n}"] = norm_vec(shp[0]) if len(shp) == 1 else proj(shp)
+    w["out_norm"] = norm_vec(cfg.n_embd)
+    w["lm_head"] = proj((cfg.n_vocab, cfg.n_embd))
+    return w
+
+
+def make_workload(cfg: DraftConfig, weights: Optional[Dict[str, Weight]] = None) -> Workload:
+    """The full seeded workload of one configuration (seed = cfg.seed)."""
+    g = torch.Generator().manual_seed(cfg.seed)
+    w = make_weights(cfg, g)
+    if weights is not None:       # caller-provided replacement weights (same draw order kept)
+        w = weights
+    fills: List[int] = []
+    offsets: List[int] = []
+    calls: List[Tuple[int, int, int, int]] = []
+    if cfg.inject:
+        assert cfg.n_seq == 1
+        row = 0
+        for p0, cnt in cfg.inject:
+            calls.append((0, p0, cnt, row))
+            row += cnt
+        n_rows = [row]
+        n_past = [max(p0 + cnt for p0, cnt in cfg.inject)]
+    else:
+        fl = torch.randint(cfg.fill_lo, cfg.fill_hi + 1, (cfg.n_seq,), generator=g)
+        of = torch.randint(0, cfg.offset_hi + 1, (cfg.n_seq,), generator=g)
+        fills = [int(x) for x in fl]
+        offsets = [int(x) for x in of]
+        n_rows, n_past = [], []
+        for s in range(cfg.n_seq):
+            calls.append((s, offsets[s], fills[s], 0))
+            n_rows.append(fills[s])
+            n_past.append(offsets[s] + fills[s])
+    feats = [_store_dense(torch.randn((n, cfg.feat_dim), generator=g, dtype=torch.float32),
+                          cfg.dense_dtype) for n in n_rows]
+    id_last = torch.randint(0, cfg.n_vocab, (cfg.n_seq,), generator=g, dtype=torch.int64)
+    if cfg.mismatch == "geometric":
+        # failures before the first success of a Bernoulli(p) sequence, capped at 15
+        u = torch.rand((cfg.n_seq,), generator=g, dtype=torch.float64)
+        m = torch.floor(torch.log1p(-u) / np.log1p(-cfg.mismatch_p)).clamp_(max=BLOCK - 1)
+    else:
+        m = torch.randint(0, BLOCK, (cfg.n_seq,), generator=g)
+    tail = torch.randint(0, cfg.n_vocab, (cfg.n_seq, BLOCK - 1), generator=g)
+    return Workload(cfg=cfg, weights=w, feats=feats, inject_calls=calls,
+                    id_last=id_last.to(torch.int32), n_past=torch.tensor(n_past, dtype=torch.int32),
+                    mismatch=m.to(torch.int32), tail=tail.to(torch.int32),
+                    fills=fills, offsets=offsets)
+
+
+def make_targets(drafts: np.ndarray, mismatch: np.ndarray, tail: np.ndarray,
+                 n_vocab: int) -> np.ndarray:
+    """Target tokens that agree with `drafts` before the drawn mismatch index m,
+    differ at m (draft + 1 mod vocab) and are random after it.  m = 15 means the
+    whole block agrees."""
+    drafts = np.asarray(drafts, dtype=np.int64)
+    out = np.array(tail, dtype=np.int64, copy=True)
+    for s in range(drafts.shape[0]):
+        m = int(mismatch[s])
+        out[s, :m] = drafts[s, :m]
+        if m < BLOCK - 1:
+            out[s, m] = (drafts[s, m] + 1) % n_vocab
+    return out.astype(np.int32)
+
+
+def raw_numpy(t: torch.Tensor) -> np.ndarray:
+    """Storage bytes of a tensor as numpy: bf16 -> uint16 bit patterns, f32 -> float32,
+    fp8 codes -> uint8, ints unchanged."""
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()

@@ -1,0 +1,181 @@
+"""Plant plausible mistakes in the oracle (on the CPU, by patching its
+functions) and check that at least one pin fails for each: a dropped term, a
+wrong sign or index, a transposed operand, an off-by-one in the window rule."""
+import numpy as np
+import pytest
+
+import pins
+from oracle import dflash_oracle as O
+
+_orig = {name: getattr(O, name) for name in dir(O) if callable(getattr(O, name))}
+
+
+def _rms_no_eps(x, w, eps):
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) * w
+
+
+def _rms_sum(x, w, eps):
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps) * w
+
+
+def _rms_no_weight(x, w, eps):
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def _rope_sign(x, pos, inv):
+    half = x.shape[-1] // 2
+    y = _orig["rope_neox"](x, -np.asarray(pos), inv)
+    return y if half else y
+
+
+def _rope_interleaved(x, pos, inv):
+    # GPT-J pairing (2j, 2j+1) instead of NEOX (j, j + hd/2)
+    half = x.shape[-1] // 2
+    perm = np.concatenate([np.arange(0, 2 * half, 2), np.arange(1, 2 * half, 2)])
+    inv_perm = np.argsort(perm)
+    return _orig["rope_neox"](x[..., perm], pos, inv)[..., inv_perm]
+
+
+def _rope_pos_plus_one(x, pos, inv):
+    return _orig["rope_neox"](x, np.asarray(pos) + 1, inv)
+
+
+def _inv_freq_half(theta, hd):
+    j = np.arange(hd // 2, dtype=np.float64)
+    return np.power(np.float64(theta), -j / hd)
+
+
+def _attention_gqa_mod(q, kb, vb, kr, vr, valid):
+    hq, hkv = q.shape[1], kb.shape[1]
+    perm = np.array([h % hkv for h in range(hq)])
+    group = hq // hkv
+    # feed heads so that the original contiguous grouping yields the modulo grouping
+    order = np.argsort(np.array([perm[h] * group + (h // hkv) for h in range(hq)]))
+    out = _orig["attention"](q[:, order], kb, vb, kr, vr, valid)
+    return out[:, np.argsort(order)]
+
+
+def _attention_no_scale(q, kb, vb, kr, vr, valid):
+    return _orig["attention"](q * np.sqrt(q.shape[-1]), kb, vb, kr, vr, valid)
+
+
+def _mask_le(ring_pos, n_past, window):
+    return _orig["ring_mask"](ring_pos, n_past, window + 1)
+
+
+def _mask_no_past_check(ring_pos, n_past, window):
+    p = np.asarray(ring_pos, dtype=np.int64)[None, :]
+    q = n_past + np.arange(16)[:, None]
+    return (p >= 0) & (q - p < window)
+
+
+def _attention_causal(q, kb, vb, kr, vr, valid):
+    return _orig["_causal_attention"](q, kb, vb, kr, vr, valid)
+
+
+def _silu_sign(z):
+    return z / (1.0 + np.exp(z))
+
+
+def _accept_count(drafts, targets):
+    return (np.asarray(drafts) == np.asarray(targets)).sum(axis=1).astype(np.int32)
+
+
+def _bf16_truncate(x):
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    return (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def _e4m3_bias8(codes):
+    return _orig["e4m3_to_f64"](codes) / 2.0
+
+
+def _decode_no_scale(raw, dtype, scale=None):
+    return _orig["decode"](raw, dtype, None if dtype != "fp8" else np.ones_like(scale))
+
+
+def _inject_kv_v_roped(w, layer, H_t, positions, inv_freq):
+    k, v = _orig["inject_kv"](w, layer, H_t, positions, inv_freq)
+    return k, O.rope_neox(v, positions, inv_freq)
+
+
+def _inject_kv_no_knorm(w, layer, H_t, positions, inv_freq):
+    cfg = w.cfg
+    k = O.linear(H_t, w.get(f"l{layer}.wk")).reshape(H_t.shape[0], cfg.n_head_kv, cfg.head_dim)
+    k = O.rope_neox(k, positions, inv_freq)
+    _, v = _orig["inject_kv"](w, layer, H_t, positions, inv_freq)
+    return k, v
+
+
+def _encode_no_norm_weight(w, feats):
+    cfg = w.cfg
+    f = O.decode(feats, cfg.dense_dtype)
+    return _rms_no_weight(O.linear(f, w.get("fc")), None, cfg.eps)
+
+
+def _drafts_rows_0_14(logits):
+    l32 = np.asarray(logits).astype(np.float32)
+    return np.argmax(l32[..., :-1, :], axis=-1).astype(np.int32)
+
+
+def _block_tokens_anchor_last(cfg, id_last):
+    t = np.full((16,), cfg.mask_token_id, dtype=np.int64)
+    t[-1] = id_last
+    return t
+
+
+def _logits_no_norm(w, h):
+    return O.linear(h, w.get("lm_head"))
+
+
+def _silu_on_identity(z):
+    return z
+
+
+MUTANTS = {
+    "rmsnorm drops eps": ("rmsnorm", _rms_no_eps),
+    "rmsnorm sums instead of mean": ("rmsnorm", _rms_sum),
+    "rmsnorm drops weight": ("rmsnorm", _rms_no_weight),
+    "rope wrong sign": ("rope_neox", _rope_sign),
+    "rope interleaved pairs": ("rope_neox", _rope_interleaved),
+    "rope position off by one": ("rope_neox", _rope_pos_plus_one),
+    "inv_freq exponent halved": ("inv_freq_table", _inv_freq_half),
+    "gqa head modulo": ("attention", _attention_gqa_mod),
+    "attention without 1/sqrt(hd)": ("attention", _attention_no_scale),
+    "attention causal in block": ("attention", _attention_causal),
+    "window off by one": ("ring_mask", _mask_le),
+    "future ring slots visible": ("ring_mask", _mask_no_past_check),
+    "silu sign": ("silu", _silu_sign),
+    "silu dropped": ("silu", _silu_on_identity),
+    "accept counts all matches": ("accept", _accept_count),
+    "bf16 truncation": ("f64_to_bf16", _bf16_truncate),
+    "e4m3 wrong bias": ("e4m3_to_f64", _e4m3_bias8),
+    "fp8 scale dropped": ("decode", _decode_no_scale),
+    "V roped at injection": ("inject_kv", _inject_kv_v_roped),
+    "K not normed at injection": ("inject_kv", _inject_kv_no_knorm),
+    "encode drops hidden_norm": ("encode", _encode_no_norm_weight),
+    "drafts read rows 0..14": ("greedy_drafts", _drafts_rows_0_14),
+    "anchor in the last row": ("block_tokens", _block_tokens_anchor_last),
+    "output norm dropped": ("logits_from_hidden", _logits_no_norm),
+}
+
+
+def _some_pin_fails():
+    for pin in pins.ALL_PINS:
+        try:
+            pin()
+        except Exception:        # noqa: BLE001 - any failure or crash counts
+            return pin.__name__
+    return None
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(O, attr, fn)
+    caught = _some_pin_fails()
+    assert caught is not None, f"no pin catches the mutant: {name}"
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert _some_pin_fails() is None
