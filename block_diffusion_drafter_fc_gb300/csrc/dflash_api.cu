@@ -1,0 +1,599 @@
+// C ABI of libdflash: handle, validation, device-memory layout, work planning,
+// the order of launches of encode / inject / step / accept, and graph capture.
+#include "../../include/dflash.h"
+#include "common.cuh"
+#include "internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+using namespace dflash;
+
+namespace {
+
+constexpr int kPlanSMs = 152;        // GB300: 2 dies x 76 SMs
+constexpr int kCtasPerSmTarget = 2;
+constexpr int kXkMax = 960;          // activation stage width (3 CTAs of ~72 KB per SM)
+constexpr int kAttnChunk = 64;       // ring slots per attention CTA
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+int wtype_of(int dtype) {
+  return dtype == DFLASH_DTYPE_F32 ? W_F32 : dtype == DFLASH_DTYPE_BF16 ? W_BF16 : W_FP8;
+}
+int chunk_of(int wt) { return wt == W_FP8 ? 64 : 32; }
+
+struct Plan {
+  int n_tiles = 0, n_kt = 1, kt = 0, xk = 0;
+};
+
+// Tile count, split-K factor and stage width of one projection launch.
+Plan plan_gemm(int n_tiles, int K, int kc, int n_mb) {
+  Plan p;
+  p.n_tiles = n_tiles;
+  const int chunks = K / kc;
+  int want = cdiv(kCtasPerSmTarget * kPlanSMs, std::max(1, n_tiles * n_mb));
+  want = std::max(1, std::min(want, chunks));
+  const int per = cdiv(chunks, want);
+  p.n_kt = cdiv(chunks, per);
+  p.kt = per * kc;
+  p.xk = std::min(p.kt, (kXkMax / kc) * kc);
+  return p;
+}
+
+struct Geometry {
+  int d, qd, kvd, hd, F, V, L, W, Hq, Hkv, fdim, max_seq, max_inject, M_max;
+  int wt, kc, dense_bf16, ring_bf16;
+};
+
+Geometry geometry(const dflash_config& c) {
+  Geometry g;
+  g.d = c.n_embd;
+  g.hd = c.head_dim;
+  g.Hq = c.n_head;
+  g.Hkv = c.n_head_kv;
+  g.qd = c.n_head * c.head_dim;
+  g.kvd = c.n_head_kv * c.head_dim;
+  g.F = c.n_ff;
+  g.V = c.n_vocab;
+  g.L = c.n_layer;
+  g.W = c.window;
+  g.fdim = c.n_target_layers * c.target_embd;
+  g.max_seq = c.max_seq;
+  g.max_inject = c.max_inject;
+  g.M_max = c.max_seq * DFLASH_BLOCK;
+  g.wt = wtype_of(c.weight_dtype);
+  g.kc = chunk_of(g.wt);
+  g.dense_bf16 = c.dense_dtype == DFLASH_DTYPE_BF16;
+  g.ring_bf16 = c.ring_dtype == DFLASH_DTYPE_BF16;
+  return g;
+}
+
+// the projection launches of one step / inject, as (tiles, K, chunk width)
+struct GemmShape {
+  int n_tiles, K, kc;
+};
+
+void step_shapes(const Geometry& g, GemmShape out[5]) {
+  out[0] = {cdiv(g.qd + 2 * g.kvd, kTileRows), g.d, g.kc};   // q/k/v
+  out[1] = {cdiv(g.d, kTileRows), g.qd, g.kc};               // o
+  out[2] = {cdiv(g.F, kTileRows / 2), g.d, g.kc};            // gate/up
+  out[3] = {cdiv(g.d, kTileRows), g.F, g.kc};                // down
+  out[4] = {cdiv(g.V, kTileRows), g.d, g.kc};                // lm head
+}
+
+void inject_shapes(const Geometry& g, GemmShape out[2]) {
+  const int dense_kc = 32;
+  out[0] = {cdiv(g.d, kTileRows), g.fdim, dense_kc};               // fc
+  out[1] = {cdiv(2 * g.L * g.kvd, kTileRows), g.d, g.kc};          // all-layer wk/wv
+}
+
+struct Layout {
+  size_t status, inv_freq, counters, h, ss, qbuf, kblk, vblk, attn, act, rope_step, am_part;
+  size_t apart_acc, apart_ml, logits_int, drafts_int, idl_int, npast_int, partial;
+  size_t inj_raw, inj_ss, inj_rope, total;
+  size_t partial_floats;
+  int n_counters, ss_parts, ss_ld, lm_tiles, attn_chunks;
+  size_t ring_seq_bytes, ring_kv_bytes, ring_total;
+};
+
+Layout layout(const dflash_config& c) {
+  const Geometry g = geometry(c);
+  Layout L{};
+  GemmShape ss_[5], is_[2];
+  step_shapes(g, ss_);
+  inject_shapes(g, is_);
+  size_t partial = 0;
+  int counters = 0;
+  auto account = [&](const GemmShape& s, int n_mb) {
+    const Plan p = plan_gemm(s.n_tiles, s.K, s.kc, n_mb);
+    counters = std::max(counters, n_mb * s.n_tiles);
+    if (p.n_kt > 1)
+      partial = std::max(partial, (size_t)n_mb * s.n_tiles * p.n_kt * 16 * kTileRows);
+  };
+  for (int mb = 1; mb <= g.max_seq; ++mb)
+    for (auto& s : ss_) account(s, mb);
+  for (int mb = 1; mb <= cdiv(g.max_inject, 16); ++mb)
+    for (auto& s : is_) account(s, mb);
+  L.partial_floats = partial;
+  L.n_counters = counters + 1;            // + the logits-argmax ticket
+  L.ss_parts = cdiv(g.d, kTileRows);
+  L.ss_ld = std::max(g.M_max, g.max_inject);
+  L.lm_tiles = ss_[4].n_tiles;
+  L.attn_chunks = cdiv(g.W, kAttnChunk);
+  const int G = g.Hq / g.Hkv, R = 16 * G;
+  const size_t attn_slots = (size_t)g.max_seq * g.Hkv * (L.attn_chunks + 1);
+
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes);
+    return o;
+  };
+  L.status = take(sizeof(unsigned));
+  L.inv_freq = take(sizeof(double) * (g.hd / 2));
+  L.counters = take(sizeof(int) * L.n_counters);
+  L.h = take(sizeof(float) * g.M_max * g.d);
+  L.ss = take(sizeof(float) * (size_t)L.ss_parts * L.ss_ld);
+  L.qbuf = take(sizeof(float) * g.M_max * g.qd);
+  L.kblk = take(sizeof(float) * g.M_max * g.kvd);
+  L.vblk = take(sizeof(float) * g.M_max * g.kvd);
+  L.attn = take(sizeof(float) * g.M_max * g.qd);
+  L.act = take(sizeof(float) * (size_t)g.M_max * g.F);
+  L.rope_step = take(sizeof(float2) * g.M_max * (g.hd / 2));
+  L.am_part = take(sizeof(float2) * (size_t)L.lm_tiles * g.M_max);
+  L.apart_acc = take(sizeof(float) * attn_slots * R * g.hd);
+  L.apart_ml = take(sizeof(float) * attn_slots * R * 2);
+  L.logits_int = take(sizeof(float) * (size_t)g.M_max * g.V);
+  L.drafts_int = take(sizeof(int32_t) * g.max_seq * (DFLASH_BLOCK - 1));
+  L.idl_int = take(sizeof(int32_t) * g.max_seq);
+  L.npast_int = take(sizeof(int32_t) * g.max_seq);
+  L.partial = take(sizeof(float) * std::max<size_t>(partial, 1));
+  L.inj_raw = take(sizeof(float) * (size_t)g.max_inject * g.d);
+  L.inj_ss = take(sizeof(float) * (size_t)L.ss_parts * L.ss_ld);
+  L.inj_rope = take(sizeof(float2) * (size_t)g.max_inject * (g.hd / 2));
+  L.total = off;
+
+  L.ring_kv_bytes = (size_t)g.L * 2 * g.Hkv * g.W * g.hd * (g.ring_bf16 ? 2 : 4);
+  L.ring_seq_bytes = L.ring_kv_bytes;
+  L.ring_total = align_up(L.ring_kv_bytes * g.max_seq) + sizeof(int32_t) * (size_t)g.max_seq * g.W;
+  return L;
+}
+
+int validate(const dflash_config* c) {
+  if (!c) return DFLASH_ERR_INVALID_ARG;
+  if (c->n_layer < 1 || c->n_embd < 1 || c->n_head < 1 || c->n_head_kv < 1 || c->head_dim < 1 ||
+      c->n_ff < 1 || c->window < 1 || c->n_vocab < 1 || c->n_target_layers < 1 ||
+      c->target_embd < 1 || c->max_seq < 1 || c->max_inject < 0)
+    return DFLASH_ERR_INVALID_ARG;
+  if (c->mask_token_id < 0 || c->mask_token_id >= c->n_vocab) return DFLASH_ERR_INVALID_ARG;
+  if (!(c->eps >= 0.f) || !(c->rope_theta > 0.0)) return DFLASH_ERR_INVALID_ARG;
+  if (c->weight_dtype < DFLASH_DTYPE_F32 || c->weight_dtype > DFLASH_DTYPE_FP8_E4M3)
+    return DFLASH_ERR_INVALID_ARG;
+  if ((c->dense_dtype != DFLASH_DTYPE_F32 && c->dense_dtype != DFLASH_DTYPE_BF16) ||
+      (c->ring_dtype != DFLASH_DTYPE_F32 && c->ring_dtype != DFLASH_DTYPE_BF16))
+    return DFLASH_ERR_UNSUPPORTED;
+  if (c->n_layer > DFLASH_MAX_LAYERS) return DFLASH_ERR_UNSUPPORTED;
+  if (c->n_head % c->n_head_kv) return DFLASH_ERR_UNSUPPORTED;
+  if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128) return DFLASH_ERR_UNSUPPORTED;
+  const int kc = c->weight_dtype == DFLASH_DTYPE_FP8_E4M3 ? 64 : 32;
+  const int qd = c->n_head * c->head_dim;
+  if (c->n_embd % kc || qd % kc || c->n_ff % kc) return DFLASH_ERR_UNSUPPORTED;
+  if ((c->n_target_layers * c->target_embd) % 32) return DFLASH_ERR_UNSUPPORTED;
+  if (c->n_head / c->n_head_kv > 16) return DFLASH_ERR_UNSUPPORTED;
+  // the attention CTA keeps a whole kv group's queries and one key chunk on chip
+  if (attn_smem_bytes(c->n_head / c->n_head_kv, c->head_dim, kAttnChunk) > 227 * 1024)
+    return DFLASH_ERR_UNSUPPORTED;
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+struct dflash_handle {
+  dflash_config cfg;
+  dflash_weights w;
+  Geometry g;
+  Layout L;
+  char* ring;
+  char* scratch;
+  cudaStream_t cap_stream = nullptr;
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  char err[512];
+
+  template <typename T>
+  T* S(size_t off) const { return reinterpret_cast<T*>(scratch + off); }
+  unsigned* status() const { return S<unsigned>(L.status); }
+  int32_t* ring_pos(int seq) const {
+    return reinterpret_cast<int32_t*>(ring + align_up(L.ring_kv_bytes * g.max_seq)) + (size_t)seq * g.W;
+  }
+  char* ring_seq(int seq) const { return ring + (size_t)seq * L.ring_seq_bytes; }
+};
+
+namespace {
+
+int cuda_fail(dflash_handle* h, cudaError_t e, const char* where) {
+  if (h) std::snprintf(h->err, sizeof(h->err), "%s: %s", where, cudaGetErrorString(e));
+  return DFLASH_ERR_CUDA;
+}
+
+#define DF_CHECK(h, call)                                   \
+  do {                                                      \
+    cudaError_t e_ = (call);                                \
+    if (e_ != cudaSuccess) return cuda_fail(h, e_, #call);  \
+  } while (0)
+
+GemmParams base_params(const dflash_handle* h) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.eps = h->cfg.eps;
+  p.norm_bf16 = h->g.dense_bf16;
+  p.partial = h->S<float>(h->L.partial);
+  p.counters = h->S<int>(h->L.counters);
+  p.status = h->status();
+  p.hd = h->g.hd;
+  p.qd = h->g.qd;
+  p.kvd = h->g.kvd;
+  p.window = h->g.W;
+  p.n_head_kv = h->g.Hkv;
+  p.ring_bf16 = h->g.ring_bf16;
+  return p;
+}
+
+void set_plan(GemmParams& p, const GemmShape& s, int n_mb) {
+  const Plan pl = plan_gemm(s.n_tiles, s.K, s.kc, n_mb);
+  p.n_tiles = pl.n_tiles;
+  p.n_kt = pl.n_kt;
+  p.kt = pl.kt;
+  p.xk = pl.xk;
+  p.K = s.K;
+}
+
+int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t* n_past,
+             float* logits, int32_t* drafts, cudaStream_t st) {
+  const Geometry& g = h->g;
+  const Layout& L = h->L;
+  const int M = n_seq * DFLASH_BLOCK;
+  GemmShape sh[5];
+  step_shapes(g, sh);
+  float* hbuf = h->S<float>(L.h);
+  float* ss = h->S<float>(L.ss);
+  float2* rope = h->S<float2>(L.rope_step);
+  DF_CHECK(h, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id, id_last,
+                           n_past, n_seq, h->S<double>(L.inv_freq), g.hd, hbuf, ss, rope,
+                           h->status(), st));
+  int n_ss = 1;
+  for (int l = 0; l < g.L; ++l) {
+    const dflash_layer_weights& lw = h->w.layers[l];
+    // attn_norm + q/k/v projection + per-head q/k norm + rope
+    GemmParams p = base_params(h);
+    set_plan(p, sh[0], n_seq);
+    p.x = hbuf; p.x_mode = X_F32; p.ldx = g.d; p.M = M;
+    p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.normw = lw.attn_norm;
+    p.seg[0] = {lw.wq, lw.wq_scale, 0, g.qd};
+    p.seg[1] = {lw.wk, lw.wk_scale, g.qd, g.kvd};
+    p.seg[2] = {lw.wv, lw.wv_scale, g.qd + g.kvd, g.kvd};
+    p.nseg = 3; p.N = g.qd + 2 * g.kvd; p.map = MAP_SEGMENTS;
+    p.epi = EPI_QKV; p.out = h->S<float>(L.qbuf); p.ldo = g.qd;
+    p.kblk = h->S<float>(L.kblk); p.vblk = h->S<float>(L.vblk);
+    p.q_norm = lw.q_norm; p.k_norm = lw.k_norm; p.rope_cs = rope;
+    DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+    // attention over ring chunks + the block, then the chunk merge
+    AttnParams a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = h->S<float>(L.qbuf); a.kblk = h->S<float>(L.kblk); a.vblk = h->S<float>(L.vblk);
+    a.ring = h->ring; a.ring_pos = h->ring_pos(0); a.n_past = n_past;
+    a.ring_bf16 = g.ring_bf16; a.layer = l; a.n_layer = g.L;
+    a.n_head = g.Hq; a.n_head_kv = g.Hkv; a.hd = g.hd; a.window = g.W;
+    a.chunk = kAttnChunk; a.n_chunks = L.attn_chunks;
+    a.scale = (float)(1.0 / std::sqrt((double)g.hd));
+    a.part_acc = h->S<float>(L.apart_acc); a.part_ml = h->S<float>(L.apart_ml);
+    a.out = h->S<float>(L.attn);
+    DF_CHECK(h, launch_attention(a, n_seq, st));
+    DF_CHECK(h, launch_attn_combine(a, n_seq, st));
+    // o projection + residual
+    p = base_params(h);
+    set_plan(p, sh[1], n_seq);
+    p.x = h->S<float>(L.attn); p.x_mode = X_F32; p.ldx = g.qd; p.M = M;
+    p.seg[0] = {lw.wo, lw.wo_scale, 0, g.d};
+    p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
+    p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
+    DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+    n_ss = sh[1].n_tiles;
+    // ffn_norm + gate/up + SwiGLU
+    p = base_params(h);
+    set_plan(p, sh[2], n_seq);
+    p.x = hbuf; p.x_mode = X_F32; p.ldx = g.d; p.M = M;
+    p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.normw = lw.ffn_norm;
+    p.seg[0] = {lw.gate, lw.gate_scale, 0, g.F};
+    p.seg[1] = {lw.up, lw.up_scale, 0, g.F};
+    p.nseg = 2; p.N = 2 * g.F; p.map = MAP_SWIGLU;
+    p.epi = EPI_SWIGLU; p.out = h->S<float>(L.act); p.ldo = g.F;
+    DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+    // down projection + residual
+    p = base_params(h);
+    set_plan(p, sh[3], n_seq);
+    p.x = h->S<float>(L.act); p.x_mode = X_F32; p.ldx = g.F; p.M = M;
+    p.seg[0] = {lw.down, lw.down_scale, 0, g.d};
+    p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
+    p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
+    DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+    n_ss = sh[3].n_tiles;
+  }
+  // output norm + LM head + greedy drafts
+  GemmParams p = base_params(h);
+  set_plan(p, sh[4], n_seq);
+  p.x = hbuf; p.x_mode = X_F32; p.ldx = g.d; p.M = M;
+  p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.normw = h->w.out_norm;
+  p.seg[0] = {h->w.lm_head, h->w.lm_head_scale, 0, g.V};
+  p.nseg = 1; p.N = g.V; p.map = MAP_SEGMENTS;
+  p.epi = EPI_LOGITS; p.out = logits; p.ldo = g.V;
+  p.am_part = h->S<float2>(L.am_part);
+  p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
+  p.drafts = drafts;
+  DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+  return DFLASH_OK;
+}
+
+bool bad_ptr(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u); }
+
+int check_weights(const dflash_config* c, const dflash_weights* w) {
+  if (!w) return DFLASH_ERR_INVALID_ARG;
+  const bool fp8 = c->weight_dtype == DFLASH_DTYPE_FP8_E4M3;
+  if (bad_ptr(w->tok_embd) || bad_ptr(w->lm_head) || bad_ptr(w->fc) || bad_ptr(w->hidden_norm) ||
+      bad_ptr(w->out_norm))
+    return DFLASH_ERR_INVALID_ARG;
+  if (fp8 && !w->lm_head_scale) return DFLASH_ERR_INVALID_ARG;
+  for (int l = 0; l < c->n_layer; ++l) {
+    const dflash_layer_weights& L = w->layers[l];
+    const void* ps[] = {L.attn_norm, L.wq, L.wk, L.wv, L.wo, L.q_norm, L.k_norm, L.ffn_norm,
+                        L.gate, L.up, L.down};
+    for (const void* q : ps)
+      if (bad_ptr(q)) return DFLASH_ERR_INVALID_ARG;
+    if (fp8) {
+      const float* sc[] = {L.wq_scale, L.wk_scale, L.wv_scale, L.wo_scale,
+                           L.gate_scale, L.up_scale, L.down_scale};
+      for (const float* q : sc)
+        if (!q) return DFLASH_ERR_INVALID_ARG;
+    }
+  }
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dflash_workspace_size(const dflash_config* cfg, size_t* ring_bytes, size_t* scratch_bytes) {
+  const int v = validate(cfg);
+  if (v != DFLASH_OK) return v;
+  if (!ring_bytes || !scratch_bytes) return DFLASH_ERR_INVALID_ARG;
+  const Layout L = layout(*cfg);
+  *ring_bytes = L.ring_total;
+  *scratch_bytes = L.total;
+  return DFLASH_OK;
+}
+
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_mem,
+                  void* scratch_mem, dflash_handle** out) {
+  if (!out) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  int v = validate(cfg);
+  if (v != DFLASH_OK) return v;
+  if ((v = check_weights(cfg, w)) != DFLASH_OK) return v;
+  if (!ring_mem || !scratch_mem || (reinterpret_cast<uintptr_t>(ring_mem) & (kAlign - 1)) ||
+      (reinterpret_cast<uintptr_t>(scratch_mem) & (kAlign - 1)))
+    return DFLASH_ERR_INVALID_ARG;
+  dflash_handle* h = new (std::nothrow) dflash_handle();
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  h->cfg = *cfg;
+  h->w = *w;
+  h->g = geometry(*cfg);
+  h->L = layout(*cfg);
+  h->ring = static_cast<char*>(ring_mem);
+  h->scratch = static_cast<char*>(scratch_mem);
+  h->err[0] = 0;
+  // host fp64 inverse-frequency table theta^(-2j/head_dim)
+  const int half = cfg->head_dim / 2;
+  double inv[64];
+  for (int j = 0; j < half; ++j) inv[j] = std::pow(cfg->rope_theta, -2.0 * j / cfg->head_dim);
+  cudaError_t e = cudaMemcpy(h->S<double>(h->L.inv_freq), inv, sizeof(double) * half,
+                             cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.counters, 0, sizeof(int) * h->L.n_counters);
+  if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.status, 0, sizeof(unsigned));
+  if (e == cudaSuccess)
+    e = launch_fill_i32(h->ring_pos(0), cfg->max_seq * cfg->window, -1, nullptr);
+  if (e == cudaSuccess) e = configure_gemm(kXkMax);
+  if (e == cudaSuccess)
+    e = configure_attention(attn_smem_bytes(cfg->n_head / cfg->n_head_kv, cfg->head_dim, kAttnChunk));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cuda_fail(h, e, "dflash_create");
+    std::fprintf(stderr, "dflash_create: %s\n", h->err);
+    if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+    delete h;
+    return DFLASH_ERR_CUDA;
+  }
+  *out = h;
+  return DFLASH_OK;
+}
+
+void dflash_destroy(dflash_handle* h) {
+  if (!h) return;
+  if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->graph) cudaGraphDestroy(h->graph);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  delete h;
+}
+
+int dflash_encode(dflash_handle* h, const void* feats, int32_t T, float* H_t, void* stream) {
+  if (!h || T < 0) return DFLASH_ERR_INVALID_ARG;
+  if (T > h->g.max_inject) return DFLASH_ERR_TOO_MANY_ROWS;
+  if (T == 0) return DFLASH_OK;
+  if (bad_ptr(feats) || bad_ptr(H_t)) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Geometry& g = h->g;
+  GemmShape sh[2];
+  inject_shapes(g, sh);
+  const int n_mb = cdiv(T, 16);
+  GemmParams p = base_params(h);
+  set_plan(p, sh[0], n_mb);
+  p.x = feats; p.x_mode = g.dense_bf16 ? X_BF16 : X_F32; p.ldx = g.fdim; p.M = T;
+  p.seg[0] = {h->w.fc, nullptr, 0, g.d};
+  p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
+  p.epi = EPI_STORE_SS; p.out = h->S<float>(h->L.inj_raw); p.ldo = g.d;
+  p.ss_out = h->S<float>(h->L.inj_ss); p.ss_out_ld = h->L.ss_ld;
+  DF_CHECK(h, launch_gemm(g.dense_bf16 ? W_BF16 : W_F32, p, n_mb, st));
+  DF_CHECK(h, launch_rms_apply(h->S<float>(h->L.inj_raw), h->S<float>(h->L.inj_ss), sh[0].n_tiles,
+                               h->L.ss_ld, T, g.d, h->w.hidden_norm, g.dense_bf16, h->cfg.eps, H_t,
+                               st));
+  return DFLASH_OK;
+}
+
+int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, const int32_t* pos, int32_t T,
+                  void* stream) {
+  if (!h || T < 0) return DFLASH_ERR_INVALID_ARG;
+  if (seq < 0 || seq >= h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  if (T > h->g.W || T > h->g.max_inject) return DFLASH_ERR_TOO_MANY_ROWS;
+  if (T == 0) return DFLASH_OK;
+  if (bad_ptr(H_t) || !pos) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Geometry& g = h->g;
+  GemmShape sh[2];
+  inject_shapes(g, sh);
+  float2* rope = h->S<float2>(h->L.inj_rope);
+  DF_CHECK(h, launch_rope_table(pos, T, h->S<double>(h->L.inv_freq), g.hd, rope, h->ring_pos(seq),
+                                g.W, h->status(), st));
+  const int n_mb = cdiv(T, 16);
+  GemmParams p = base_params(h);
+  set_plan(p, sh[1], n_mb);
+  p.x = H_t; p.x_mode = X_F32; p.ldx = g.d; p.M = T;
+  for (int l = 0; l < g.L; ++l) {
+    const dflash_layer_weights& lw = h->w.layers[l];
+    p.seg[2 * l] = {lw.wk, lw.wk_scale, 2 * l * g.kvd, g.kvd};
+    p.seg[2 * l + 1] = {lw.wv, lw.wv_scale, 2 * l * g.kvd + g.kvd, g.kvd};
+    p.k_norm_l[l] = lw.k_norm;
+  }
+  p.nseg = 2 * g.L; p.N = 2 * g.L * g.kvd; p.map = MAP_SEGMENTS;
+  p.epi = EPI_INJECT; p.ring_seq = h->ring_seq(seq); p.pos = pos; p.rope_cs = rope;
+  DF_CHECK(h, launch_gemm(g.wt, p, n_mb, st));
+  return DFLASH_OK;
+}
+
+int dflash_step(dflash_handle* h, int32_t n_seq, const int32_t* id_last, const int32_t* n_past,
+                float* logits, int32_t* drafts, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (n_seq < 1 || n_seq > h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  if (!id_last || !n_past || !drafts) return DFLASH_ERR_INVALID_ARG;
+  return run_step(h, n_seq, id_last, n_past, logits, drafts, static_cast<cudaStream_t>(stream));
+}
+
+int dflash_accept(dflash_handle* h, int32_t n_seq, const int32_t* drafts, const int32_t* targets,
+                  int32_t* n_ok, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (n_seq < 1 || n_seq > h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  if (!drafts || !targets || !n_ok) return DFLASH_ERR_INVALID_ARG;
+  DF_CHECK(h, launch_accept(drafts, targets, n_ok, n_seq, static_cast<cudaStream_t>(stream)));
+  return DFLASH_OK;
+}
+
+int dflash_capture(dflash_handle* h, int32_t n_seq, const int32_t* id_last, const int32_t* n_past,
+                   float* logits, int32_t* drafts, const int32_t* targets, int32_t* n_ok,
+                   void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (n_seq < 1 || n_seq > h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  if (!id_last || !n_past || !drafts || (!targets != !n_ok)) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // order the capture after the caller's queued work (nothing is launched here)
+  DF_CHECK(h, cudaStreamSynchronize(st));
+  if (h->exec) { cudaGraphExecDestroy(h->exec); h->exec = nullptr; }
+  if (h->graph) { cudaGraphDestroy(h->graph); h->graph = nullptr; }
+  DF_CHECK(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  int rc = run_step(h, n_seq, id_last, n_past, logits, drafts, h->cap_stream);
+  if (rc == DFLASH_OK && targets) {
+    cudaError_t e = launch_accept(drafts, targets, n_ok, n_seq, h->cap_stream);
+    if (e != cudaSuccess) rc = cuda_fail(h, e, "accept (capture)");
+  }
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
+  if (rc != DFLASH_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
+  h->graph = graph;
+  DF_CHECK(h, cudaGraphInstantiate(&h->exec, h->graph, 0));
+  return DFLASH_OK;
+}
+
+int dflash_replay(dflash_handle* h, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (!h->exec) return DFLASH_ERR_NOT_CAPTURED;
+  DF_CHECK(h, cudaGraphLaunch(h->exec, static_cast<cudaStream_t>(stream)));
+  return DFLASH_OK;
+}
+
+int dflash_step_host(dflash_handle* h, int32_t n_seq, const int32_t* id_last,
+                     const int32_t* n_past, float* logits, int32_t* drafts, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (n_seq < 1 || n_seq > h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  if (!id_last || !n_past || !drafts) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* d_idl = h->S<int32_t>(h->L.idl_int);
+  int32_t* d_np = h->S<int32_t>(h->L.npast_int);
+  int32_t* d_dr = h->S<int32_t>(h->L.drafts_int);
+  float* d_lg = logits ? h->S<float>(h->L.logits_int) : nullptr;
+  DF_CHECK(h, cudaMemcpyAsync(d_idl, id_last, sizeof(int32_t) * n_seq, cudaMemcpyHostToDevice, st));
+  DF_CHECK(h, cudaMemcpyAsync(d_np, n_past, sizeof(int32_t) * n_seq, cudaMemcpyHostToDevice, st));
+  const int rc = run_step(h, n_seq, d_idl, d_np, d_lg, d_dr, st);
+  if (rc != DFLASH_OK) return rc;
+  DF_CHECK(h, cudaMemcpyAsync(drafts, d_dr, sizeof(int32_t) * n_seq * (DFLASH_BLOCK - 1),
+                              cudaMemcpyDeviceToHost, st));
+  if (logits)
+    DF_CHECK(h, cudaMemcpyAsync(logits, d_lg, sizeof(float) * (size_t)n_seq * DFLASH_BLOCK * h->g.V,
+                                cudaMemcpyDeviceToHost, st));
+  DF_CHECK(h, cudaStreamSynchronize(st));
+  return DFLASH_OK;
+}
+
+int dflash_ring_reset(dflash_handle* h, int32_t seq, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (seq < 0 || seq >= h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  DF_CHECK(h, launch_fill_i32(h->ring_pos(seq), h->g.W, -1, static_cast<cudaStream_t>(stream)));
+  return DFLASH_OK;
+}
+
+int dflash_read_status(dflash_handle* h, uint32_t* status, void* stream) {
+  if (!h || !status) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  DF_CHECK(h, cudaStreamSynchronize(st));
+  DF_CHECK(h, cudaMemcpy(&v, h->status(), sizeof(unsigned), cudaMemcpyDeviceToHost));
+  DF_CHECK(h, cudaMemset(h->status(), 0, sizeof(unsigned)));
+  *status = v;
+  return v ? DFLASH_ERR_DEVICE : DFLASH_OK;
+}
+
+const char* dflash_status_string(int s) {
+  switch (s) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED: return "unsupported geometry or dtype";
+    case DFLASH_ERR_TOO_MANY_ROWS: return "too many rows (T > window or T > max_inject)";
+    case DFLASH_ERR_SEQ_RANGE: return "sequence index out of range";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_NOT_CAPTURED: return "no captured graph";
+    case DFLASH_ERR_DEVICE: return "device status flag set";
+  }
+  return "unknown status";
+}
+
+const char* dflash_last_error(const dflash_handle* h) { return h ? h->err : ""; }
+
+}  // extern "C"

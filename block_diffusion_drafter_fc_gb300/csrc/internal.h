@@ -1,0 +1,132 @@
+// Internal interface between the C-ABI layer and the kernels of libdflash.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dflash {
+
+// weight storage of a projection matrix
+enum WType { W_F32 = 0, W_BF16 = 1, W_FP8 = 2 };
+// activation storage fed to a projection kernel
+enum XMode { X_F32 = 0, X_BF16 = 1, X_F32_DENSE = 2 };
+// what the split-K fix-up does with a finished 16 x 128 output tile
+enum Epi {
+  EPI_STORE = 0,     // out[m][n] = y
+  EPI_STORE_SS = 1,  // out[m][n] = y; ss_out[tile][m] = sum over the tile of y^2
+  EPI_RESID_SS = 2,  // out[m][n] += y; ss_out[tile][m] = sum over the tile of out^2
+  EPI_SWIGLU = 3,    // out[m][f] = silu(gate) * up (tile = 64 gate rows + 64 up rows)
+  EPI_QKV = 4,       // per-head RMSNorm + rope of q/k, raw v, into the block buffers
+  EPI_INJECT = 5,    // per-head RMSNorm + rope of k, raw v, scattered into the ring
+  EPI_LOGITS = 6     // logits + argmax partials; the last tile emits the drafts
+};
+enum RowMap { MAP_SEGMENTS = 0, MAP_SWIGLU = 1 };
+
+constexpr int kTileRows = 128;     // output rows (weight rows) of one CTA tile
+constexpr int kGemmThreads = 256;  // 8 warps x 16 weight rows
+constexpr int kMaxSeg = 2 * 16;
+constexpr int kMaxLayers = 16;
+
+struct GemmSeg {
+  const void* w;        // [rows][K] row-major, weight dtype
+  const float* scale;   // FP8: per-row scale; else null
+  int row0;             // first virtual output row of this segment
+  int rows;
+};
+
+struct GemmParams {
+  // activations: x[m][k], m < M, row stride ldx (elements)
+  const void* x;
+  int x_mode;
+  int ldx;
+  int M;
+  int K;
+  // optional RMSNorm prologue: x[m][k] * inv_rms[m] * normw[k], with
+  // inv_rms[m] = 1 / sqrt(sum_p ss[p * ss_ld + m] / K + eps)
+  const float* ss;
+  int n_ss;
+  int ss_ld;
+  const void* normw;
+  int norm_bf16;
+  float eps;
+  // weights
+  GemmSeg seg[kMaxSeg];
+  int nseg;
+  int N;      // virtual output rows
+  int map;
+  // tiling
+  int n_tiles;
+  int n_kt;
+  int kt;     // k extent of one CTA (multiple of the chunk width)
+  int xk;     // k extent of one shared-memory activation stage
+  float* partial;
+  int* counters;
+  // epilogue
+  int epi;
+  float* out;
+  int ldo;
+  float* ss_out;
+  int ss_out_ld;
+  // q/k/v epilogues
+  float* kblk;
+  float* vblk;
+  int qd, kvd, hd;
+  const void* q_norm;
+  const void* k_norm;
+  const float2* rope_cs;  // [row][hd/2] (cos, sin)
+  // injection epilogue
+  void* ring_seq;         // this sequence's ring: [L][2][Hkv][W][hd]
+  int ring_bf16;
+  int window;
+  int n_head_kv;
+  const int32_t* pos;     // [T]
+  const void* k_norm_l[kMaxLayers];
+  unsigned* status;
+  // logits epilogue
+  float2* am_part;        // [n_tiles][M] (value, index bits)
+  int* am_counter;
+  int32_t* drafts;        // [M/16][15]
+};
+
+struct AttnParams {
+  const float* q;         // [M][qd], roped
+  const float* kblk;      // [M][kvd], roped
+  const float* vblk;      // [M][kvd]
+  const void* ring;       // all rings: [max_seq][L][2][Hkv][W][hd]
+  const int32_t* ring_pos;  // [max_seq][W]
+  const int32_t* n_past;  // [n_seq]
+  int ring_bf16;
+  int layer, n_layer;
+  int n_head, n_head_kv, hd, window;
+  int chunk, n_chunks;    // ring slots per CTA, ring chunks (the block is chunk n_chunks)
+  float scale;
+  float* part_acc;        // [n_seq][Hkv][n_chunks+1][R][hd]
+  float* part_ml;         // [n_seq][Hkv][n_chunks+1][R][2]
+  float* out;             // [M][qd]
+};
+
+size_t gemm_smem_bytes(int wt, int xk);
+cudaError_t configure_gemm(int xk_max);
+cudaError_t launch_gemm(int wt, const GemmParams& p, int n_mb, cudaStream_t st);
+
+size_t attn_smem_bytes(int group, int hd, int chunk);
+cudaError_t configure_attention(size_t smem);
+cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st);
+cudaError_t launch_attn_combine(const AttnParams& p, int n_seq, cudaStream_t st);
+
+cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
+                         int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
+                         const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
+                         unsigned* status, cudaStream_t st);
+cudaError_t launch_rope_table(const int32_t* pos, int T, const double* inv_freq, int hd,
+                              float2* rope_cs, int32_t* ring_pos, int window, unsigned* status,
+                              cudaStream_t st);
+cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss_ld, int T,
+                             int n, const void* normw, int norm_bf16, float eps, float* out,
+                             cudaStream_t st);
+cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t* n_ok, int n_seq,
+                          cudaStream_t st);
+cudaError_t launch_fill_i32(int32_t* p, int n, int32_t v, cudaStream_t st);
+
+}  // namespace dflash

@@ -1,0 +1,261 @@
+"""ctypes binding of libdflash (include/dflash.h): argument marshalling only.
+
+Every step of the drafter runs in the library's CUDA kernels.  torch is used
+for device memory (the ring, the scratch area, inputs and outputs) and for the
+current stream.  Importing this module loads the library; a missing or
+unloadable library raises immediately - there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import pathlib
+import re
+from typing import Dict, List, Optional
+
+import torch
+
+from .synth import BLOCK, DraftConfig, Workload
+
+PKG = pathlib.Path(__file__).resolve().parent
+LIB_PATH = PKG / "libdflash.so"
+HEADER = PKG.parent / "include" / "dflash.h"
+
+DTYPE = {"f32": 0, "bf16": 1, "fp8": 2}
+MAX_LAYERS = 16
+STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "too many rows",
+          -4: "sequence out of range", -5: "CUDA error", -6: "not captured", -7: "device status"}
+
+
+class dflash_config(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in (
+        "n_layer", "n_embd", "n_head", "n_head_kv", "head_dim", "n_ff", "window", "n_vocab",
+        "n_target_layers", "target_embd", "max_seq", "max_inject", "mask_token_id",
+        "weight_dtype", "dense_dtype", "ring_dtype")] + [
+        ("eps", C.c_float), ("reserved0", C.c_int32), ("rope_theta", C.c_double)]
+
+
+_LAYER_PTRS = ("attn_norm", "wq", "wk", "wv", "wo", "q_norm", "k_norm", "ffn_norm", "gate", "up",
+               "down")
+_LAYER_SCALES = ("wq_scale", "wk_scale", "wv_scale", "wo_scale", "gate_scale", "up_scale",
+                 "down_scale")
+
+
+class dflash_layer_weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in _LAYER_PTRS + _LAYER_SCALES]
+
+
+class dflash_weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("tok_embd", "lm_head", "lm_head_scale", "fc",
+                                           "hidden_norm", "out_norm")] + [
+        ("layers", dflash_layer_weights * MAX_LAYERS)]
+
+
+class DFlashError(RuntimeError):
+    pass
+
+
+def _load() -> C.CDLL:
+    if not LIB_PATH.exists():
+        raise DFlashError(f"{LIB_PATH} is missing: build it with block_diffusion_drafter_fc_gb300.build")
+    lib = C.CDLL(str(LIB_PATH))
+    vp, i32, szp = C.c_void_p, C.c_int32, C.POINTER(C.c_size_t)
+    sig = {
+        "dflash_workspace_size": (C.c_int, [C.POINTER(dflash_config), szp, szp]),
+        "dflash_create": (C.c_int, [C.POINTER(dflash_config), C.POINTER(dflash_weights), vp, vp,
+                                    C.POINTER(vp)]),
+        "dflash_destroy": (None, [vp]),
+        "dflash_encode": (C.c_int, [vp, vp, i32, vp, vp]),
+        "dflash_inject": (C.c_int, [vp, i32, vp, vp, i32, vp]),
+        "dflash_step": (C.c_int, [vp, i32, vp, vp, vp, vp, vp]),
+        "dflash_accept": (C.c_int, [vp, i32, vp, vp, vp, vp]),
+        "dflash_capture": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "dflash_replay": (C.c_int, [vp, vp]),
+        "dflash_step_host": (C.c_int, [vp, i32, vp, vp, vp, vp, vp]),
+        "dflash_ring_reset": (C.c_int, [vp, i32, vp]),
+        "dflash_read_status": (C.c_int, [vp, C.POINTER(C.c_uint32), vp]),
+        "dflash_status_string": (C.c_char_p, [C.c_int]),
+        "dflash_last_error": (C.c_char_p, [vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+def header_symbols() -> List[str]:
+    """Every function the public header declares."""
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"^\s*DFLASH_API\s+(?:const\s+)?\w+\s*\*?\s*(dflash_\w+)\s*\(", text, re.M)))
+
+
+def _check(rc: int, h: Optional[int] = None, what: str = "") -> None:
+    if rc != 0:
+        msg = LIB.dflash_status_string(rc).decode()
+        if h:
+            extra = LIB.dflash_last_error(h).decode()
+            if extra:
+                msg += f" ({extra})"
+        raise DFlashError(f"{what}: {msg} [{rc}]")
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def make_config(cfg: DraftConfig, max_seq: Optional[int] = None,
+                max_inject: Optional[int] = None) -> dflash_config:
+    c = dflash_config()
+    c.n_layer, c.n_embd, c.n_head, c.n_head_kv = cfg.n_layer, cfg.n_embd, cfg.n_head, cfg.n_head_kv
+    c.head_dim, c.n_ff, c.window, c.n_vocab = cfg.head_dim, cfg.n_ff, cfg.window, cfg.n_vocab
+    c.n_target_layers, c.target_embd = cfg.n_target_layers, cfg.d_t
+    c.max_seq = max_seq if max_seq is not None else cfg.n_seq
+    c.max_inject = max_inject if max_inject is not None else cfg.window
+    c.mask_token_id = cfg.mask_token_id
+    c.weight_dtype, c.dense_dtype = DTYPE[cfg.weight_dtype], DTYPE[cfg.dense_dtype]
+    c.ring_dtype = DTYPE[cfg.ring_dtype]
+    c.eps, c.rope_theta = cfg.eps, cfg.rope_theta
+    return c
+
+
+def workspace_size(c: dflash_config):
+    rb, sb = C.c_size_t(), C.c_size_t()
+    _check(LIB.dflash_workspace_size(C.byref(c), C.byref(rb), C.byref(sb)), what="workspace_size")
+    return rb.value, sb.value
+
+
+class Drafter:
+    """A libdflash handle over device copies of a workload's weights.
+
+    The ring and scratch areas are torch uint8 tensors owned by this object; the
+    weights are the caller's device tensors (kept referenced here)."""
+
+    def __init__(self, cfg: DraftConfig, dev_weights: Dict[str, "DeviceWeight"],
+                 max_seq: Optional[int] = None, max_inject: Optional[int] = None,
+                 device: str = "cuda"):
+        self.cfg = cfg
+        self.c = make_config(cfg, max_seq, max_inject)
+        self.ring_bytes, self.scratch_bytes = workspace_size(self.c)
+        self.ring_mem = torch.empty(self.ring_bytes + 256, dtype=torch.uint8, device=device)
+        self.scratch = torch.empty(self.scratch_bytes + 256, dtype=torch.uint8, device=device)
+        self.dev_weights = dev_weights
+        w = dflash_weights()
+        for n in ("tok_embd", "lm_head", "fc", "hidden_norm", "out_norm"):
+            setattr(w, n, dev_weights[n].data.data_ptr())
+        if dev_weights["lm_head"].scale is not None:
+            w.lm_head_scale = dev_weights["lm_head"].scale.data_ptr()
+        for i in range(cfg.n_layer):
+            lw = w.layers[i]
+            for n in _LAYER_PTRS:
+                setattr(lw, n, dev_weights[f"l{i}.{n}"].data.data_ptr())
+            for n in ("wq", "wk", "wv", "wo", "gate", "up", "down"):
+                sc = dev_weights[f"l{i}.{n}"].scale
+                if sc is not None:
+                    setattr(lw, n + "_scale", sc.data_ptr())
+        self.w = w
+        h = C.c_void_p()
+        _check(LIB.dflash_create(C.byref(self.c), C.byref(w), self._aligned(self.ring_mem),
+                                 self._aligned(self.scratch), C.byref(h)), what="create")
+        self.h = h.value
+
+    @staticmethod
+    def _aligned(t: torch.Tensor) -> int:
+        p = t.data_ptr()
+        return (p + 255) // 256 * 256
+
+    def close(self):
+        if getattr(self, "h", None):
+            LIB.dflash_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- views of caller-visible state
+    def ring_views(self):
+        """(K, V, ring_pos) as torch views: K/V [max_seq][L][Hkv][W][hd]."""
+        cfg, ms = self.cfg, self.c.max_seq
+        el = 2 if cfg.ring_dtype == "bf16" else 4
+        kv_bytes = cfg.n_layer * 2 * cfg.n_head_kv * cfg.window * cfg.head_dim * el
+        base = self._aligned(self.ring_mem) - self.ring_mem.data_ptr()
+        raw = self.ring_mem[base:base + kv_bytes * ms]
+        dt = torch.bfloat16 if cfg.ring_dtype == "bf16" else torch.float32
+        kv = raw.view(dt).view(ms, cfg.n_layer, 2, cfg.n_head_kv, cfg.window, cfg.head_dim)
+        pos_off = base + (kv_bytes * ms + 255) // 256 * 256
+        pos = self.ring_mem[pos_off:pos_off + 4 * ms * cfg.window].view(torch.int32).view(ms, cfg.window)
+        return kv[:, :, 0], kv[:, :, 1], pos
+
+    # ---- C-ABI calls (same names)
+    def dflash_encode(self, feats: torch.Tensor, H_t: torch.Tensor, stream=None):
+        _check(LIB.dflash_encode(self.h, _ptr(feats), feats.shape[0], _ptr(H_t), _stream(stream)),
+               self.h, "encode")
+
+    def dflash_inject(self, seq: int, H_t: torch.Tensor, pos: torch.Tensor, stream=None):
+        _check(LIB.dflash_inject(self.h, seq, _ptr(H_t), _ptr(pos), pos.shape[0], _stream(stream)),
+               self.h, "inject")
+
+    def dflash_step(self, id_last, n_past, logits, drafts, stream=None):
+        _check(LIB.dflash_step(self.h, id_last.shape[0], _ptr(id_last), _ptr(n_past), _ptr(logits),
+                               _ptr(drafts), _stream(stream)), self.h, "step")
+
+    def dflash_accept(self, drafts, targets, n_ok, stream=None):
+        _check(LIB.dflash_accept(self.h, drafts.shape[0], _ptr(drafts), _ptr(targets), _ptr(n_ok),
+                                 _stream(stream)), self.h, "accept")
+
+    def dflash_capture(self, id_last, n_past, logits, drafts, targets=None, n_ok=None, stream=None):
+        _check(LIB.dflash_capture(self.h, id_last.shape[0], _ptr(id_last), _ptr(n_past),
+                                  _ptr(logits), _ptr(drafts), _ptr(targets), _ptr(n_ok),
+                                  _stream(stream)), self.h, "capture")
+
+    def dflash_replay(self, stream=None):
+        _check(LIB.dflash_replay(self.h, _stream(stream)), self.h, "replay")
+
+    def dflash_step_host(self, id_last: torch.Tensor, n_past: torch.Tensor, drafts: torch.Tensor,
+                         logits: Optional[torch.Tensor] = None, stream=None):
+        _check(LIB.dflash_step_host(self.h, id_last.shape[0], _ptr(id_last), _ptr(n_past),
+                                    _ptr(logits), _ptr(drafts), _stream(stream)), self.h, "step_host")
+
+    def dflash_ring_reset(self, seq: int, stream=None):
+        _check(LIB.dflash_ring_reset(self.h, seq, _stream(stream)), self.h, "ring_reset")
+
+    def dflash_read_status(self, stream=None) -> int:
+        v = C.c_uint32()
+        rc = LIB.dflash_read_status(self.h, C.byref(v), _stream(stream))
+        if rc not in (0, -7):
+            _check(rc, self.h, "read_status")
+        return v.value
+
+    # ---- convenience: run a workload's prefill (encode + inject per call)
+    def prefill(self, wl: Workload, dev_feats: List[torch.Tensor], stream=None):
+        dev = self.ring_mem.device
+        for call in wl.inject_calls:
+            seq, p0, cnt, r0 = call
+            f = dev_feats[seq][r0:r0 + cnt]
+            H = torch.empty((cnt, self.cfg.n_embd), dtype=torch.float32, device=dev)
+            self.dflash_encode(f, H, stream)
+            pos = torch.arange(p0, p0 + cnt, dtype=torch.int32, device=dev)
+            self.dflash_inject(seq, H, pos, stream)
+
+
+class DeviceWeight:
+    def __init__(self, data: torch.Tensor, scale: Optional[torch.Tensor]):
+        self.data, self.scale = data, scale
+
+
+def to_device(wl: Workload, device: str = "cuda"):
+    """Device copies of a workload's weights and features (same bytes)."""
+    dw = {n: DeviceWeight(w.data.to(device), None if w.scale is None else w.scale.to(device))
+          for n, w in wl.weights.items()}
+    feats = [f.to(device) for f in wl.feats]
+    return dw, feats

@@ -1,0 +1,211 @@
+"""CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+Bars (from the drafter's statement of the target): ring slot positions,
+draft tokens and acceptance counts bit-exact; logits max |diff| <= 1e-3 with
+fp32 storage, <= 2e-2 with bf16 storage, <= 5e-2 with FP8 weights.  Encoded
+features H_t: max |diff| <= 1e-4 relative to their largest magnitude (fp32
+math with the bf16 hi/lo activation split: ~2^-17 per product).  Ring K/V:
+within one unit of the ring dtype's rounding of the oracle's value (plus
+1e-5 of the tensor's scale for values near zero), since both sides round a
+slightly different fp32/fp64 value once.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_drafter_fc_gb300.synth import (
+    BLOCK, get_config, make_targets, make_workload)
+import gpu_harness as GH
+import oracle_bridge as OB
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny_f32", "ragged_bf16", "mixed_f32w_bf16ring", "small_fp8"]
+
+
+@functools.lru_cache(maxsize=None)
+def _case(name):
+    wl = make_workload(get_config(name))
+    ref = OB.oracle_full(wl)
+    gpu = GH.gpu_run(wl, targets=ref["targets"])
+    return wl, ref, gpu
+
+
+def _check_ring(wl, ref, gpu):
+    cfg = wl.cfg
+    for s in range(cfg.n_seq):
+        assert np.array_equal(gpu["ring_pos"][s], ref["rings"][s].pos), f"ring_pos seq {s}"
+        filled = ref["rings"][s].pos >= 0
+        for name, gk, rk in (("K", gpu["ring_k"][s], ref["rings"][s].k),
+                             ("V", gpu["ring_v"][s], ref["rings"][s].v)):
+            from oracle import dflash_oracle as O
+            refv = O.decode(rk, cfg.ring_dtype)[:, :, filled, :]
+            g = gk[:, :, filled, :].astype(np.float64)
+            scale = float(np.abs(refv).max())
+            rel = 2.0 ** -8 if cfg.ring_dtype == "bf16" else 2.0 ** -20
+            bad = np.abs(g - refv) > rel * np.abs(refv) + 1e-5 * scale
+            assert not bad.any(), f"ring {name} seq {s}: {int(bad.sum())} elements off"
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_encode_matches_oracle(name):
+    wl, ref, gpu = _case(name)
+    for a, b in zip(gpu["H_t"], ref["H_t"]):
+        err = np.abs(a - b).max()
+        assert err <= 1e-4 * np.abs(b).max(), err
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_ring_matches_oracle(name):
+    wl, ref, gpu = _case(name)
+    _check_ring(wl, ref, gpu)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_step_logits_drafts_accept(name):
+    wl, ref, gpu = _case(name)
+    err = float(np.abs(gpu["logits"] - ref["logits"]).max())
+    assert err <= GH.logit_tol(wl.cfg), err
+    amb = GH.compare_drafts(gpu["logits"], gpu["drafts"], ref["logits"], ref["drafts"], err)
+    if amb == 0:
+        assert np.array_equal(gpu["drafts"], ref["drafts"])
+        assert np.array_equal(gpu["n_ok"], ref["n_ok"])
+    assert gpu["status"] == 0
+
+
+def test_accept_synthetic_against_oracle():
+    """Accept kernel alone on synthetic drafts/targets with planted mismatches,
+    including all-match (15) and mismatch at 0, for 37 sequences."""
+    from block_diffusion_drafter_fc_gb300 import dflash as D
+    from oracle import dflash_oracle as O
+    wl = make_workload(get_config("ragged_bf16"))
+    dw, _ = D.to_device(wl)
+    dr = D.Drafter(wl.cfg, dw, max_seq=37)
+    g = np.random.default_rng(3)
+    drafts = g.integers(0, 1000, size=(37, 15)).astype(np.int32)
+    m = g.integers(0, 16, size=37)
+    m[0], m[1] = 0, 15
+    targets = make_targets(drafts, m, g.integers(0, 1000, size=(37, 15)), 1001)
+    n_ok = torch.empty(37, dtype=torch.int32, device="cuda")
+    dr.dflash_accept(torch.from_numpy(drafts).cuda(), torch.from_numpy(targets).cuda(), n_ok)
+    got = n_ok.cpu().numpy()
+    assert np.array_equal(got, O.accept(drafts, targets))
+    assert np.array_equal(got, m)
+    dr.close()
+
+
+def test_fewer_sequences_than_handle():
+    """n_seq = 2 on a 3-sequence handle: the first two sequences' outputs equal
+    the oracle on those sequences."""
+    wl = make_workload(get_config("ragged_bf16"))
+    ref = OB.oracle_full(wl, n_seq=2)
+    gpu = GH.gpu_run(wl, n_seq=2, targets=ref["targets"])
+    err = float(np.abs(gpu["logits"] - ref["logits"]).max())
+    assert err <= GH.logit_tol(wl.cfg)
+    assert np.array_equal(gpu["drafts"], ref["drafts"])
+    assert np.array_equal(gpu["n_ok"], ref["n_ok"])
+
+
+def test_empty_ring_step():
+    """A step before any injection attends only the block's own 16 keys."""
+    from oracle import dflash_oracle as O
+    wl = make_workload(get_config("tiny_f32"))
+    w = OB.oracle_weights(wl)
+    rings = [O.OracleRing(w.cfg)]
+    lg, dr_ = O.step(w, rings, [int(wl.id_last[0])], [0])
+    from block_diffusion_drafter_fc_gb300 import dflash as D
+    dw, _ = D.to_device(wl)
+    d = D.Drafter(wl.cfg, dw)
+    logits = torch.empty((1, BLOCK, wl.cfg.n_vocab), device="cuda")
+    drafts = torch.empty((1, 15), dtype=torch.int32, device="cuda")
+    d.dflash_step(wl.id_last[:1].cuda(), torch.zeros(1, dtype=torch.int32, device="cuda"), logits, drafts)
+    err = float(np.abs(logits.cpu().numpy() - lg).max())
+    assert err <= 1e-3
+    assert np.array_equal(drafts.cpu().numpy(), dr_)
+    d.close()
+
+
+def test_graph_replay_bitwise_with_eager_traffic():
+    """The captured step (+accept) replays bitwise equal to the eager step, before
+    and after eager GEMMs run on the same stream between replays (dflash-ops
+    model card, Method: interleaved eager traffic between replays)."""
+    wl = make_workload(get_config("small_fp8"))
+    ref = OB.oracle_full(wl)
+    g = GH.gpu_run(wl, targets=ref["targets"], keep=True)
+    dr = g["drafter"]
+    n = wl.cfg.n_seq
+    logits = torch.zeros((n, BLOCK, wl.cfg.n_vocab), device="cuda")
+    drafts = torch.zeros((n, 15), dtype=torch.int32, device="cuda")
+    targets = torch.from_numpy(ref["targets"]).cuda()
+    n_ok = torch.zeros(n, dtype=torch.int32, device="cuda")
+    dr.dflash_capture(g["id_last_d"], g["n_past_d"], logits, drafts, targets, n_ok)
+    a = torch.randn(2048, 2048, device="cuda", dtype=torch.bfloat16)
+    outs = []
+    for it in range(4):
+        logits.zero_()
+        drafts.zero_()
+        dr.dflash_replay()
+        torch.cuda.synchronize()
+        outs.append((logits.clone(), drafts.clone(), n_ok.clone()))
+        for _ in range(3):
+            a = (a @ a).clamp_(-1, 1)
+    for lg, d, k in outs:
+        assert torch.equal(lg.cpu(), torch.from_numpy(g["logits"])), "replay differs from eager"
+        assert np.array_equal(d.cpu().numpy(), g["drafts"])
+        assert np.array_equal(k.cpu().numpy(), g["n_ok"])
+    # new scalars without re-capture: a different anchor token changes the output
+    g["id_last_d"].copy_((g["id_last_d"] + 1) % wl.cfg.n_vocab)
+    dr.dflash_replay()
+    torch.cuda.synchronize()
+    assert not torch.equal(logits.cpu(), torch.from_numpy(g["logits"]))
+    dr.close()
+
+
+def test_step_host_matches_device_step():
+    wl = make_workload(get_config("ragged_bf16"))
+    g = GH.gpu_run(wl, keep=True)
+    dr = g["drafter"]
+    n = wl.cfg.n_seq
+    drafts = torch.zeros((n, 15), dtype=torch.int32).pin_memory()
+    logits = torch.zeros((n, BLOCK, wl.cfg.n_vocab), dtype=torch.float32).pin_memory()
+    dr.dflash_step_host(wl.id_last.clone(), wl.n_past.clone(), drafts, logits)
+    assert np.array_equal(drafts.numpy(), g["drafts"])
+    assert np.array_equal(logits.numpy(), g["logits"])
+    dr.close()
+
+
+def test_host_side_errors_on_gpu_handle():
+    from block_diffusion_drafter_fc_gb300 import dflash as D
+    wl = make_workload(get_config("tiny_f32"))
+    dw, feats = D.to_device(wl)
+    dr = D.Drafter(wl.cfg, dw, max_inject=80)
+    H = torch.zeros((80, wl.cfg.n_embd), device="cuda")
+    pos = torch.arange(80, dtype=torch.int32, device="cuda")
+    with pytest.raises(D.DFlashError, match="too many rows"):
+        dr.dflash_inject(0, H, pos)                      # 80 > window 64
+    with pytest.raises(D.DFlashError, match="out of range"):
+        dr.dflash_inject(1, H[:8], pos[:8])
+    with pytest.raises(D.DFlashError, match="no captured graph"):
+        dr.dflash_replay()
+    ids = torch.tensor([wl.cfg.n_vocab + 5], dtype=torch.int32, device="cuda")
+    lg = torch.empty((1, BLOCK, wl.cfg.n_vocab), device="cuda")
+    drf = torch.empty((1, 15), dtype=torch.int32, device="cuda")
+    dr.dflash_step(ids, torch.zeros(1, dtype=torch.int32, device="cuda"), lg, drf)
+    assert dr.dflash_read_status() & 0x1
+    assert dr.dflash_read_status() == 0                  # cleared by the read
+    # zero-row encode / inject are no-ops
+    dr.dflash_encode(feats[0][:0], H[:0])
+    dr.dflash_inject(0, H[:0], pos[:0])
+    dr.close()
+
+
+@pytest.mark.slow
+def test_small_bf16_full():
+    wl, ref, gpu = _case("small_bf16")
+    _check_ring(wl, ref, gpu)
+    err = float(np.abs(gpu["logits"] - ref["logits"]).max())
+    assert err <= GH.logit_tol(wl.cfg), err
+    GH.compare_drafts(gpu["logits"], gpu["drafts"], ref["logits"], ref["drafts"], err)
+    assert np.array_equal(gpu["n_ok"], ref["n_ok"])
