@@ -1,0 +1,359 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash drafter block step on GB300.
+
+One "step" is one pass of the whole hot path: embedding of the 16-row noise
+block, every drafter layer (q/k/v + head norm + rope, sliding-window attention
+over the ring and the block, o, gate/up + SwiGLU, down), output norm + LM
+head + greedy drafts, and the acceptance scan, replayed from a CUDA graph with
+the ring already filled (inputs resident in HBM).  Default workload: the real
+drafter dimensions with bf16 storage (5 layers, n_embd 6656, 32/8 heads of 128,
+n_ff 19968, window 2048 full, vocab 8192) - the configuration the dflash-ops
+model card measures.  The metric is block steps per second (and us/step, and
+the HBM bandwidth that implies); one JSON line on rank 0.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (the
+comparison arm of this tier): each step is a bounded sample of the same
+workload's projections, scaled to steps/s.
+
+Multi-GPU (torchrun): every rank runs an independent replica (sequences are
+independent; no collective in the data path); value = steps of all ranks /
+max wall time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "drafter block steps/s (us/step) at real dims; achieved HBM GB/s vs GB300 peak"
+UNIT = "steps/s"
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="real_bf16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=30)
+    return ap.parse_args()
+
+
+def peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def step_bytes(cfg, wl):
+    """Algorithmic bytes of one step: GEMM weights (+FP8 scales) + ring K/V read + logits."""
+    el = 2 if cfg.ring_dtype == "bf16" else 4
+    ring = 2 * cfg.n_layer * cfg.n_head_kv * cfg.window * cfg.head_dim * el * cfg.n_seq
+    if not cfg.inject:                       # batched: only the filled slots are keys
+        ring = sum(2 * cfg.n_layer * cfg.n_head_kv * f * cfg.head_dim * el for f in wl.fills)
+    logits = cfg.n_seq * 16 * cfg.n_vocab * 4
+    return wl.weight_bytes() + ring + logits
+
+
+def class_bytes(cfg, wl):
+    """Algorithmic bytes per launch of each projection class (weights + scales)."""
+    def wb(name):
+        return wl.weights[name].nbytes()
+    L = cfg.n_layer
+    return {
+        "qkv": sum(wb(f"l{i}.{n}") for i in range(L) for n in ("wq", "wk", "wv")) / L,
+        "o_proj": sum(wb(f"l{i}.wo") for i in range(L)) / L,
+        "gate_up": sum(wb(f"l{i}.{n}") for i in range(L) for n in ("gate", "up")) / L,
+        "down": sum(wb(f"l{i}.down") for i in range(L)) / L,
+        "lm_head": wb("lm_head") + cfg.n_seq * 16 * cfg.n_vocab * 4,
+    }
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "common.cuh", "internal.h"):
+        h.update((ROOT / "block_diffusion_drafter_fc_gb300" / "csrc" / f).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(cfg_name, cls):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text())
+    e = d.get(f"{cfg_name}/{cls}")
+    if not e or e.get("source_sha") != gemm_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+                                       "-lms", "100", "-i", str(gpu_index)], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        os.unlink(self.f.name)
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from block_diffusion_drafter_fc_gb300 import dflash as D
+    from block_diffusion_drafter_fc_gb300.synth import BLOCK, get_config, make_targets, make_workload
+
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    cfg = get_config(args.config)
+    wl = make_workload(cfg)
+    dw, feats = D.to_device(wl, dev)
+    max_inject = max(c[2] for c in wl.inject_calls)
+    dr = D.Drafter(cfg, dw, max_seq=cfg.n_seq, max_inject=max_inject, device=dev)
+    dr.prefill(wl, feats)
+    n = cfg.n_seq
+    id_last = wl.id_last.to(dev)
+    n_past = wl.n_past.to(dev)
+    logits = torch.empty((n, BLOCK, cfg.n_vocab), dtype=torch.float32, device=dev)
+    drafts = torch.empty((n, BLOCK - 1), dtype=torch.int32, device=dev)
+    n_ok = torch.empty((n,), dtype=torch.int32, device=dev)
+    dr.dflash_step(id_last, n_past, logits, drafts)
+    targets = torch.from_numpy(make_targets(drafts.cpu().numpy(), wl.mismatch.numpy(),
+                                            wl.tail.numpy(), cfg.n_vocab)).to(dev)
+    dr.dflash_capture(id_last, n_past, logits, drafts, targets, n_ok)
+    launches_per_step = 2 + 6 * cfg.n_layer + 1
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        dr.dflash_replay(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    t_soak = time.time()                      # keep the GPU busy ~1 s before timing
+    while time.time() - t_soak < 1.0:
+        for _ in range(20):
+            dr.dflash_replay(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        dr.dflash_replay(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * args.steps / (ms / 1e3)
+
+    # live per-class device times of eager steps (events on the launching stream)
+    dr.dflash_profile_enable(True)
+    for _ in range(args.profile_steps):
+        dr.dflash_step(id_last, n_past, logits, drafts, stream)
+    prof = dr.dflash_profile_read()
+    dr.dflash_profile_enable(False)
+    cb = class_bytes(cfg, wl)
+    dom = max(cb, key=lambda k: prof[k][0])
+    dom_ms, dom_n = prof[dom]
+    achieved = cb[dom] / (dom_ms / dom_n / 1e3) / 1e9
+    peak, peak_src = peaks()
+    sbytes = step_bytes(cfg, wl)
+
+    # end to end through the C ABI from host buffers (copies inside the timed region)
+    hid = wl.id_last.clone().pin_memory()
+    hnp = wl.n_past.clone().pin_memory()
+    hdr = torch.empty((n, BLOCK - 1), dtype=torch.int32).pin_memory()
+    n_e2e = max(10, min(args.steps, 200))
+    for _ in range(3):
+        dr.dflash_step_host(hid, hnp, hdr)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        dr.dflash_step_host(hid, hnp, hdr)
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    assert np.array_equal(hdr.numpy(), drafts.cpu().numpy())
+
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "us_per_step": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded random weights ~N(0,1/fan_in), features ~N(0,1))",
+        "config": {"workload": f"{cfg.name}: {cfg.n_layer} layers, n_embd {cfg.n_embd}, heads "
+                               f"{cfg.n_head}/{cfg.n_head_kv} x {cfg.head_dim}, n_ff {cfg.n_ff}, window "
+                               f"{cfg.window} (ring full), block 16, vocab {cfg.n_vocab}, "
+                               f"{cfg.weight_dtype} weights, {cfg.ring_dtype} ring, fp32 arithmetic",
+                   "sequences": cfg.n_seq, "rows_per_step": 16 * cfg.n_seq,
+                   "l2": f"inputs larger than L2: {wl.weight_bytes() / 1e9:.2f} GB of weights per step",
+                   "timing": "CUDA-graph replays (step + accept), CUDA events on the replay stream",
+                   "parallelism": f"replicas x{world}"},
+        "step_bytes": sbytes,
+        "hbm_gbs": round(sbytes / (ms_step / 1e3) / 1e9, 1),
+        "hbm_frac_of_measured": round(sbytes / (ms_step / 1e3) / 1e9 / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": f"{dom} projection ({cfg.weight_dtype} weights)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": committed_traffic(cfg.name, dom),
+                     "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": cb[dom],
+                     "avg_launch_us": round(dom_ms / dom_n * 1e3, 2)},
+        "kernel_classes_us_per_step": {k: round(v[0] / args.profile_steps * 1e3, 2)
+                                       for k, v in prof.items() if v[1]},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": {"value": round(1.0 / e2e_s * world, 3), "unit": UNIT,
+                "h2d_bytes_per_step": 8 * n, "d2h_bytes_per_step": 4 * n * (BLOCK - 1)},
+    }
+    dr.close()
+    del dw, feats
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl)
+    return out
+
+
+def cpu_baseline(wl):
+    """The oracle as it stands: one full block step (all layers + LM head) on the
+    host cores, ring empty (attention over the 16 block keys only; the ring's
+    share of the oracle's step is < 1%)."""
+    sys.path.insert(0, str(ROOT / "tests"))
+    from oracle import dflash_oracle as O
+    import oracle_bridge as OB
+    w = OB.oracle_weights(wl)
+    rings = [O.OracleRing(w.cfg) for _ in range(wl.cfg.n_seq)]
+    t0 = time.perf_counter()
+    O.step(w, rings, wl.id_last.numpy(), wl.n_past.numpy())
+    dt = time.perf_counter() - t0
+    return {"value": round(1.0 / dt, 5), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one full fp64 oracle block step of {wl.cfg.name} ({wl.cfg.n_seq} seq, "
+                      f"empty ring), {dt:.1f} s"}
+
+
+def run_reference(args):
+    """Oracle arm: each step is a bounded sample - the oracle's decode + linear of a
+    row block of the step's projection weights (cycling over every layer's
+    q/k/v/o/gate/up/down and the LM head) on 16 activation rows; steps/s =
+    fraction of the step's weight elements processed / time."""
+    import numpy as np
+    sys.path.insert(0, str(ROOT / "tests"))
+    from oracle import dflash_oracle as O
+    import oracle_bridge as OB
+    from block_diffusion_drafter_fc_gb300.synth import get_config, make_workload
+
+    cfg = get_config(args.config)
+    wl = make_workload(cfg)
+    w = OB.oracle_weights(wl)
+    names = [f"l{i}.{n}" for i in range(cfg.n_layer) for n in ("wq", "wk", "wv", "wo", "gate", "up", "down")]
+    names.append("lm_head")
+    total = sum(int(np.prod(w.raw[n].shape)) for n in names)
+    rng = np.random.default_rng(0)
+    x = {k: rng.standard_normal((16 * cfg.n_seq, k)) for k in {w.raw[n].shape[1] for n in names}}
+
+    def sample(i, rows):
+        n = names[i % len(names)]
+        raw = w.raw[n]
+        r0 = (i * rows) % max(1, raw.shape[0] - rows)
+        sc = w.scales.get(n)
+        W = O.decode(raw[r0:r0 + rows], w.dtype_of(n), None if sc is None else sc[r0:r0 + rows])
+        O.linear(x[raw.shape[1]], W)
+        return rows * raw.shape[1]
+
+    # size a sample so warmup + steps end within ~3 minutes
+    t0 = time.perf_counter()
+    el = sample(0, 256)
+    rate = el / max(time.perf_counter() - t0, 1e-6)
+    per_step_s = 180.0 / max(1, args.steps + args.warmup)
+    avg_k = total / sum(w.raw[n].shape[0] for n in names)
+    rows = int(max(16, min(4096, rate * per_step_s / avg_k)))
+    for i in range(args.warmup):
+        sample(i, rows)
+    done = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        done += sample(i + args.warmup, rows)
+    dt = time.perf_counter() - t0
+    value = (done / total) / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 / value, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "sequences": cfg.n_seq},
+            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"{rows} weight rows of one projection per step (decode + "
+                                       f"linear on {16 * cfg.n_seq} rows), cycling all projections"},
+            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    out = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -97,6 +97,16 @@ DF_DEVICE uint4 ldg_stream(const void* p) {
   return r;
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: let the next kernel of the stream be scheduled
+// now (it only starts where this grid frees resources), and, before reading
+// anything an earlier kernel wrote, wait until the preceding grid has completed
+// and its memory is visible.  Only immutable data (weights) is touched before
+// the wait.  Both are no-ops for a kernel launched without the attribute.
+DF_DEVICE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+DF_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tensor cores
 
 // D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.

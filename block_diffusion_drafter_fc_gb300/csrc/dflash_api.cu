@@ -9,13 +9,15 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <vector>
 
 using namespace dflash;
 
 namespace {
 
 constexpr int kPlanSMs = 152;        // GB300: 2 dies x 76 SMs
-constexpr int kCtasPerSmTarget = 2;
+constexpr int kCtasPerSm = 2;        // projection CTAs resident per SM (registers bound it)
+constexpr int kGemmGrid = kPlanSMs * kCtasPerSm;
 constexpr int kXkMax = 960;          // activation stage width (3 CTAs of ~72 KB per SM)
 constexpr int kAttnChunk = 64;       // ring slots per attention CTA
 constexpr size_t kAlign = 256;
@@ -29,20 +31,19 @@ int wtype_of(int dtype) {
 int chunk_of(int wt) { return wt == W_FP8 ? 64 : 32; }
 
 struct Plan {
-  int n_tiles = 0, n_kt = 1, kt = 0, xk = 0;
+  int n_tiles = 0, n_mb = 1, cpt = 0, grid = 0, xk = 0;
 };
 
-// Tile count, split-K factor and stage width of one projection launch.
+// Stream-K plan of one projection launch: one resident wave of CTAs sharing
+// n_tiles x n_mb x (K / kc) chunk units equally.
 Plan plan_gemm(int n_tiles, int K, int kc, int n_mb) {
   Plan p;
   p.n_tiles = n_tiles;
-  const int chunks = K / kc;
-  int want = cdiv(kCtasPerSmTarget * kPlanSMs, std::max(1, n_tiles * n_mb));
-  want = std::max(1, std::min(want, chunks));
-  const int per = cdiv(chunks, want);
-  p.n_kt = cdiv(chunks, per);
-  p.kt = per * kc;
-  p.xk = std::min(p.kt, (kXkMax / kc) * kc);
+  p.n_mb = n_mb;
+  p.cpt = K / kc;
+  const long long units = (long long)n_tiles * n_mb * p.cpt;
+  p.grid = (int)std::min<long long>(kGemmGrid, units);
+  p.xk = std::min(p.cpt * kc, (kXkMax / kc) * kc);
   return p;
 }
 
@@ -108,18 +109,11 @@ Layout layout(const dflash_config& c) {
   GemmShape ss_[5], is_[2];
   step_shapes(g, ss_);
   inject_shapes(g, is_);
-  size_t partial = 0;
+  // two partial tiles per CTA of the stream-K grid; one ticket per output tile
+  const size_t partial = (size_t)2 * kGemmGrid * 16 * kTileRows;
   int counters = 0;
-  auto account = [&](const GemmShape& s, int n_mb) {
-    const Plan p = plan_gemm(s.n_tiles, s.K, s.kc, n_mb);
-    counters = std::max(counters, n_mb * s.n_tiles);
-    if (p.n_kt > 1)
-      partial = std::max(partial, (size_t)n_mb * s.n_tiles * p.n_kt * 16 * kTileRows);
-  };
-  for (int mb = 1; mb <= g.max_seq; ++mb)
-    for (auto& s : ss_) account(s, mb);
-  for (int mb = 1; mb <= cdiv(g.max_inject, 16); ++mb)
-    for (auto& s : is_) account(s, mb);
+  for (auto& s : ss_) counters = std::max(counters, g.max_seq * s.n_tiles);
+  for (auto& s : is_) counters = std::max(counters, cdiv(g.max_inject, 16) * s.n_tiles);
   L.partial_floats = partial;
   L.n_counters = counters + 1;            // + the logits-argmax ticket
   L.ss_parts = cdiv(g.d, kTileRows);
@@ -187,7 +181,7 @@ int validate(const dflash_config* c) {
   if ((c->n_target_layers * c->target_embd) % 32) return DFLASH_ERR_UNSUPPORTED;
   if (c->n_head / c->n_head_kv > 16) return DFLASH_ERR_UNSUPPORTED;
   // the attention CTA keeps a whole kv group's queries and one key chunk on chip
-  if (attn_smem_bytes(c->n_head / c->n_head_kv, c->head_dim, kAttnChunk) > 227 * 1024)
+  if (attn_smem_bytes(c->n_head / c->n_head_kv, c->head_dim, 1) > 227 * 1024)
     return DFLASH_ERR_UNSUPPORTED;
   return DFLASH_OK;
 }
@@ -205,6 +199,15 @@ struct dflash_handle {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
   char err[512];
+  // launch-class profiling (eager calls only)
+  bool prof = false;
+  bool capturing = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  struct Rec { int cls; cudaEvent_t a, b; };
+  std::vector<Rec> recs;
+  int open_cls = -1;
+  cudaEvent_t open_ev = nullptr;
 
   template <typename T>
   T* S(size_t off) const { return reinterpret_cast<T*>(scratch + off); }
@@ -228,6 +231,44 @@ int cuda_fail(dflash_handle* h, cudaError_t e, const char* where) {
     if (e_ != cudaSuccess) return cuda_fail(h, e_, #call);  \
   } while (0)
 
+enum ProfClass {
+  PC_EMBED = 0, PC_QKV, PC_ATTN, PC_MERGE, PC_O, PC_GATEUP, PC_DOWN, PC_LM, PC_ENCODE, PC_INJECT,
+  PC_ACCEPT
+};
+
+cudaEvent_t prof_event(dflash_handle* h) {
+  if (h->ev_used == h->ev_pool.size()) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    h->ev_pool.push_back(e);
+  }
+  return h->ev_pool[h->ev_used++];
+}
+
+// bracket the launches of one class with events on the launching stream
+void prof_begin(dflash_handle* h, int cls, cudaStream_t st) {
+  if (!h->prof || h->capturing) return;
+  h->open_ev = prof_event(h);
+  h->open_cls = cls;
+  if (h->open_ev) cudaEventRecord(h->open_ev, st);
+}
+
+void prof_end(dflash_handle* h, cudaStream_t st) {
+  if (!h->prof || h->capturing || !h->open_ev) return;
+  cudaEvent_t b = prof_event(h);
+  if (!b) return;
+  cudaEventRecord(b, st);
+  h->recs.push_back({h->open_cls, h->open_ev, b});
+  h->open_ev = nullptr;
+}
+
+#define PROF(h, cls, st, call)     \
+  do {                             \
+    prof_begin(h, cls, st);        \
+    DF_CHECK(h, call);             \
+    prof_end(h, st);               \
+  } while (0)
+
 GemmParams base_params(const dflash_handle* h) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -248,8 +289,9 @@ GemmParams base_params(const dflash_handle* h) {
 void set_plan(GemmParams& p, const GemmShape& s, int n_mb) {
   const Plan pl = plan_gemm(s.n_tiles, s.K, s.kc, n_mb);
   p.n_tiles = pl.n_tiles;
-  p.n_kt = pl.n_kt;
-  p.kt = pl.kt;
+  p.n_mb = pl.n_mb;
+  p.cpt = pl.cpt;
+  p.grid = pl.grid;
   p.xk = pl.xk;
   p.K = s.K;
 }
@@ -264,7 +306,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   float* hbuf = h->S<float>(L.h);
   float* ss = h->S<float>(L.ss);
   float2* rope = h->S<float2>(L.rope_step);
-  DF_CHECK(h, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id, id_last,
+  PROF(h, PC_EMBED, st, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id, id_last,
                            n_past, n_seq, h->S<double>(L.inv_freq), g.hd, hbuf, ss, rope,
                            h->status(), st));
   int n_ss = 1;
@@ -282,7 +324,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.epi = EPI_QKV; p.out = h->S<float>(L.qbuf); p.ldo = g.qd;
     p.kblk = h->S<float>(L.kblk); p.vblk = h->S<float>(L.vblk);
     p.q_norm = lw.q_norm; p.k_norm = lw.k_norm; p.rope_cs = rope;
-    DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+    PROF(h, PC_QKV, st, launch_gemm(g.wt, p, st));
     // attention over ring chunks + the block, then the chunk merge
     AttnParams a;
     std::memset(&a, 0, sizeof(a));
@@ -290,12 +332,12 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.ring = h->ring; a.ring_pos = h->ring_pos(0); a.n_past = n_past;
     a.ring_bf16 = g.ring_bf16; a.layer = l; a.n_layer = g.L;
     a.n_head = g.Hq; a.n_head_kv = g.Hkv; a.hd = g.hd; a.window = g.W;
-    a.chunk = kAttnChunk; a.n_chunks = L.attn_chunks;
+    a.n_chunks = L.attn_chunks;
     a.scale = (float)(1.0 / std::sqrt((double)g.hd));
     a.part_acc = h->S<float>(L.apart_acc); a.part_ml = h->S<float>(L.apart_ml);
     a.out = h->S<float>(L.attn);
-    DF_CHECK(h, launch_attention(a, n_seq, st));
-    DF_CHECK(h, launch_attn_combine(a, n_seq, st));
+    PROF(h, PC_ATTN, st, launch_attention(a, n_seq, st));
+    PROF(h, PC_MERGE, st, launch_attn_combine(a, n_seq, st));
     // o projection + residual
     p = base_params(h);
     set_plan(p, sh[1], n_seq);
@@ -303,7 +345,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.seg[0] = {lw.wo, lw.wo_scale, 0, g.d};
     p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
     p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
-    DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+    PROF(h, PC_O, st, launch_gemm(g.wt, p, st));
     n_ss = sh[1].n_tiles;
     // ffn_norm + gate/up + SwiGLU
     p = base_params(h);
@@ -314,7 +356,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.seg[1] = {lw.up, lw.up_scale, 0, g.F};
     p.nseg = 2; p.N = 2 * g.F; p.map = MAP_SWIGLU;
     p.epi = EPI_SWIGLU; p.out = h->S<float>(L.act); p.ldo = g.F;
-    DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+    PROF(h, PC_GATEUP, st, launch_gemm(g.wt, p, st));
     // down projection + residual
     p = base_params(h);
     set_plan(p, sh[3], n_seq);
@@ -322,7 +364,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.seg[0] = {lw.down, lw.down_scale, 0, g.d};
     p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
     p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
-    DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+    PROF(h, PC_DOWN, st, launch_gemm(g.wt, p, st));
     n_ss = sh[3].n_tiles;
   }
   // output norm + LM head + greedy drafts
@@ -336,7 +378,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   p.am_part = h->S<float2>(L.am_part);
   p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
   p.drafts = drafts;
-  DF_CHECK(h, launch_gemm(g.wt, p, n_seq, st));
+  PROF(h, PC_LM, st, launch_gemm(g.wt, p, st));
   return DFLASH_OK;
 }
 
@@ -410,7 +452,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
     e = launch_fill_i32(h->ring_pos(0), cfg->max_seq * cfg->window, -1, nullptr);
   if (e == cudaSuccess) e = configure_gemm(kXkMax);
   if (e == cudaSuccess)
-    e = configure_attention(attn_smem_bytes(cfg->n_head / cfg->n_head_kv, cfg->head_dim, kAttnChunk));
+    e = configure_attention(attn_smem_bytes(cfg->n_head / cfg->n_head_kv, cfg->head_dim,
+                                            cfg->ring_dtype == DFLASH_DTYPE_F32));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -426,6 +469,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
 
 void dflash_destroy(dflash_handle* h) {
   if (!h) return;
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
   if (h->exec) cudaGraphExecDestroy(h->exec);
   if (h->graph) cudaGraphDestroy(h->graph);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
@@ -449,10 +493,12 @@ int dflash_encode(dflash_handle* h, const void* feats, int32_t T, float* H_t, vo
   p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
   p.epi = EPI_STORE_SS; p.out = h->S<float>(h->L.inj_raw); p.ldo = g.d;
   p.ss_out = h->S<float>(h->L.inj_ss); p.ss_out_ld = h->L.ss_ld;
-  DF_CHECK(h, launch_gemm(g.dense_bf16 ? W_BF16 : W_F32, p, n_mb, st));
+  prof_begin(h, PC_ENCODE, st);
+  DF_CHECK(h, launch_gemm(g.dense_bf16 ? W_BF16 : W_F32, p, st));
   DF_CHECK(h, launch_rms_apply(h->S<float>(h->L.inj_raw), h->S<float>(h->L.inj_ss), sh[0].n_tiles,
                                h->L.ss_ld, T, g.d, h->w.hidden_norm, g.dense_bf16, h->cfg.eps, H_t,
                                st));
+  prof_end(h, st);
   return DFLASH_OK;
 }
 
@@ -468,6 +514,7 @@ int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, const int32_t
   GemmShape sh[2];
   inject_shapes(g, sh);
   float2* rope = h->S<float2>(h->L.inj_rope);
+  prof_begin(h, PC_INJECT, st);
   DF_CHECK(h, launch_rope_table(pos, T, h->S<double>(h->L.inv_freq), g.hd, rope, h->ring_pos(seq),
                                 g.W, h->status(), st));
   const int n_mb = cdiv(T, 16);
@@ -482,7 +529,8 @@ int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, const int32_t
   }
   p.nseg = 2 * g.L; p.N = 2 * g.L * g.kvd; p.map = MAP_SEGMENTS;
   p.epi = EPI_INJECT; p.ring_seq = h->ring_seq(seq); p.pos = pos; p.rope_cs = rope;
-  DF_CHECK(h, launch_gemm(g.wt, p, n_mb, st));
+  DF_CHECK(h, launch_gemm(g.wt, p, st));
+  prof_end(h, st);
   return DFLASH_OK;
 }
 
@@ -499,7 +547,8 @@ int dflash_accept(dflash_handle* h, int32_t n_seq, const int32_t* drafts, const 
   if (!h) return DFLASH_ERR_INVALID_ARG;
   if (n_seq < 1 || n_seq > h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
   if (!drafts || !targets || !n_ok) return DFLASH_ERR_INVALID_ARG;
-  DF_CHECK(h, launch_accept(drafts, targets, n_ok, n_seq, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  PROF(h, PC_ACCEPT, st, launch_accept(drafts, targets, n_ok, n_seq, st));
   return DFLASH_OK;
 }
 
@@ -515,6 +564,7 @@ int dflash_capture(dflash_handle* h, int32_t n_seq, const int32_t* id_last, cons
   if (h->exec) { cudaGraphExecDestroy(h->exec); h->exec = nullptr; }
   if (h->graph) { cudaGraphDestroy(h->graph); h->graph = nullptr; }
   DF_CHECK(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  h->capturing = true;
   int rc = run_step(h, n_seq, id_last, n_past, logits, drafts, h->cap_stream);
   if (rc == DFLASH_OK && targets) {
     cudaError_t e = launch_accept(drafts, targets, n_ok, n_seq, h->cap_stream);
@@ -522,6 +572,7 @@ int dflash_capture(dflash_handle* h, int32_t n_seq, const int32_t* id_last, cons
   }
   cudaGraph_t graph = nullptr;
   cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
+  h->capturing = false;
   if (rc != DFLASH_OK) {
     if (graph) cudaGraphDestroy(graph);
     return rc;
@@ -578,6 +629,31 @@ int dflash_read_status(dflash_handle* h, uint32_t* status, void* stream) {
   DF_CHECK(h, cudaMemset(h->status(), 0, sizeof(unsigned)));
   *status = v;
   return v ? DFLASH_ERR_DEVICE : DFLASH_OK;
+}
+
+int dflash_profile_enable(dflash_handle* h, int enable) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (h->capturing) return DFLASH_ERR_INVALID_ARG;
+  h->prof = enable != 0;
+  return DFLASH_OK;
+}
+
+int dflash_profile_read(dflash_handle* h, double* ms, int32_t* launches) {
+  if (!h || !ms || !launches) return DFLASH_ERR_INVALID_ARG;
+  for (int i = 0; i < DFLASH_PROF_N; ++i) {
+    ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  for (const auto& r : h->recs) {
+    DF_CHECK(h, cudaEventSynchronize(r.b));
+    float t = 0.f;
+    DF_CHECK(h, cudaEventElapsedTime(&t, r.a, r.b));
+    ms[r.cls] += t;
+    launches[r.cls] += (r.cls == PC_ENCODE) ? 2 : (r.cls == PC_INJECT ? 2 : 1);
+  }
+  h->recs.clear();
+  h->ev_used = 0;
+  return DFLASH_OK;
 }
 
 const char* dflash_status_string(int s) {

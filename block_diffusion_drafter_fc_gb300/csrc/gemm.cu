@@ -277,7 +277,7 @@ DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* sca
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const int total = p.n_tiles * gridDim.x;
+    const int total = p.n_tiles * p.n_mb;
     *s_flag = atomicAdd(p.am_counter, 1) == total - 1;
   }
   __syncthreads();
@@ -399,6 +399,17 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
 
 // ------------------------------------------------------------------ kernel
 
+// Stream-K schedule: the work is n_items = n_tiles x n_mb output tiles (128
+// weight rows x 16 activation rows), each cut into cpt chunks along k.  The
+// grid is one resident wave; CTA b owns units [U b / G, U (b+1) / G) of the
+// U = n_items * cpt units in item-major order, so every CTA streams the same
+// number of weight bytes and there is no tail wave.  A tile finished inside one
+// CTA goes straight to the epilogue; a tile shared by several CTAs is summed by
+// the last of them (atomic ticket) in CTA order, which keeps results
+// deterministic.  CTA c keeps at most two partial tiles: slot 2c for the tile
+// its range starts inside, slot 2c + 1 for the tile its range ends inside.
+DF_DEVICE long long owner_of(long long u, long long U, int G) { return ((u + 1) * G - 1) / U; }
+
 template <int WT>
 __global__ void __launch_bounds__(kGemmThreads) gemm_rows_kernel(const __grid_constant__ GemmParams p) {
   using T = WTraits<WT>;
@@ -412,94 +423,114 @@ __global__ void __launch_bounds__(kGemmThreads) gemm_rows_kernel(const __grid_co
   float* scale_s = inv_rms + 16;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  const int mb = blockIdx.x;
-  const int tile = blockIdx.y / p.n_kt, kt = blockIdx.y - tile * p.n_kt;
-  const int m0 = mb * 16;
-  const int k0 = kt * p.kt, k1 = min(p.K, k0 + p.kt);
-
-  if (tid < kTileRows) {
-    const float* sc = nullptr;
-    const uint8_t* r = map_row(p, tile, tid, T::ESZ, &sc);
-    scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
-  }
-  if (tid < 16) {
-    float inv = 1.f;
-    if (p.normw && m0 + tid < p.M) {
-      float s = 0.f;
-      for (int q = 0; q < p.n_ss; ++q) s += p.ss[(size_t)q * p.ss_ld + m0 + tid];
-      inv = 1.f / sqrtf(s / (float)p.K + p.eps);
-    }
-    inv_rms[tid] = inv;
-  }
-
-  const float* dummy;
-  const uint8_t* wa = map_row(p, tile, warp * 16 + g, T::ESZ, &dummy);
-  const uint8_t* wb = map_row(p, tile, warp * 16 + g + 8, T::ESZ, &dummy);
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  const int G = gridDim.x, b = blockIdx.x;
+  const long long U = (long long)p.n_tiles * p.n_mb * p.cpt;
+  const long long ub0 = U * b / G, ub1 = U * (b + 1) / G;
   const bool has_lo = p.x_mode != X_BF16;
+  bool waited = false;
+  pdl_trigger();
 
-  for (int xs0 = k0; xs0 < k1; xs0 += p.xk) {
-    const int xlen = min(p.xk, k1 - xs0);
-    const int nch = xlen / T::KC;
-    const uint8_t* pa = wa ? wa + (size_t)(xs0 + T::EPL * t) * T::ESZ : nullptr;
-    const uint8_t* pb = wb ? wb + (size_t)(xs0 + T::EPL * t) * T::ESZ : nullptr;
-    uint4 ra[T::U][T::NV], rb[T::U][T::NV], na[T::U][T::NV], nb[T::U][T::NV];
-    // weights do not depend on the activations: start streaming before staging x
-    load_stage<WT>(ra, rb, pa, pb, 0, nch);
-    __syncthreads();
-    stage_x(p, xs_hi, xs_lo, XS, inv_rms, m0, xs0, xlen);
-    __syncthreads();
-    for (int c0 = 0; c0 < nch; c0 += 2 * T::U) {
-      load_stage<WT>(na, nb, pa, pb, c0 + T::U, nch);
-      compute_stage<WT>(ra, rb, xs_hi, xs_lo, XS, c0, nch, g, t, has_lo, acc);
-      if (c0 + T::U >= nch) break;
-      load_stage<WT>(ra, rb, pa, pb, c0 + 2 * T::U, nch);
-      compute_stage<WT>(na, nb, xs_hi, xs_lo, XS, c0 + T::U, nch, g, t, has_lo, acc);
+  for (long long u = ub0; u < ub1;) {
+    const int item = (int)(u / p.cpt);
+    const int c0 = (int)(u - (long long)item * p.cpt);
+    const int c1 = (int)min((long long)p.cpt, c0 + (ub1 - u));
+    u += c1 - c0;
+    const int tile = item / p.n_mb, mb = item - tile * p.n_mb;
+    const int m0 = mb * 16;
+
+    __syncthreads();  // the previous segment is done with shared memory
+    if (tid < kTileRows) {
+      const float* sc = nullptr;
+      const uint8_t* r = map_row(p, tile, tid, T::ESZ, &sc);
+      scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
     }
-  }
+    const float* dummy;
+    const uint8_t* wa = map_row(p, tile, warp * 16 + g, T::ESZ, &dummy);
+    const uint8_t* wb = map_row(p, tile, warp * 16 + g + 8, T::ESZ, &dummy);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const int k0 = c0 * T::KC, k1 = c1 * T::KC;
 
-  // accumulators -> shared tile [act row][weight row]
+    for (int xs0 = k0; xs0 < k1; xs0 += p.xk) {
+      const int xlen = min(p.xk, k1 - xs0);
+      const int nch = xlen / T::KC;
+      const uint8_t* pa = wa ? wa + (size_t)(xs0 + T::EPL * t) * T::ESZ : nullptr;
+      const uint8_t* pb = wb ? wb + (size_t)(xs0 + T::EPL * t) * T::ESZ : nullptr;
+      uint4 ra[T::U][T::NV], rb[T::U][T::NV], na[T::U][T::NV], nb[T::U][T::NV];
+      // weights do not depend on the activations: start streaming before staging x
+      load_stage<WT>(ra, rb, pa, pb, 0, nch);
+      if (!waited) {
+        pdl_wait();  // everything below may read what earlier kernels wrote
+        waited = true;
+      }
+      if (xs0 == k0 && tid < 16) {
+        float inv = 1.f;
+        if (p.normw && m0 + tid < p.M) {
+          float sum = 0.f;
+          for (int q = 0; q < p.n_ss; ++q) sum += p.ss[(size_t)q * p.ss_ld + m0 + tid];
+          inv = 1.f / sqrtf(sum / (float)p.K + p.eps);
+        }
+        inv_rms[tid] = inv;
+      }
+      __syncthreads();
+      stage_x(p, xs_hi, xs_lo, XS, inv_rms, m0, xs0, xlen);
+      __syncthreads();
+      for (int cc = 0; cc < nch; cc += 2 * T::U) {
+        load_stage<WT>(na, nb, pa, pb, cc + T::U, nch);
+        compute_stage<WT>(ra, rb, xs_hi, xs_lo, XS, cc, nch, g, t, has_lo, acc);
+        if (cc + T::U >= nch) break;
+        load_stage<WT>(ra, rb, pa, pb, cc + 2 * T::U, nch);
+        compute_stage<WT>(na, nb, xs_hi, xs_lo, XS, cc + T::U, nch, g, t, has_lo, acc);
+      }
+    }
+
+    // accumulators -> shared tile [act row][weight row]
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int c = 8 * j + 2 * t, r = warp * 16 + g;
-    acc_s[c * kTileRows + r] = acc[j][0];
-    acc_s[(c + 1) * kTileRows + r] = acc[j][1];
-    acc_s[c * kTileRows + r + 8] = acc[j][2];
-    acc_s[(c + 1) * kTileRows + r + 8] = acc[j][3];
-  }
-  __syncthreads();
-
-  if (p.n_kt > 1) {
-    const size_t tile_id = (size_t)mb * p.n_tiles + tile;
-    float* part = p.partial + (tile_id * p.n_kt + kt) * (16 * kTileRows);
-    for (int i = tid; i < 16 * kTileRows; i += blockDim.x) part[i] = acc_s[i];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_flag = atomicAdd(p.counters + tile_id, 1) == p.n_kt - 1;
-    __syncthreads();
-    if (!s_flag) return;
-    __threadfence();
-    const float* base = p.partial + tile_id * p.n_kt * (16 * kTileRows);
-    for (int i = tid; i < 16 * kTileRows; i += blockDim.x) {
-      float s = 0.f;
-      for (int q = 0; q < p.n_kt; ++q) s += __ldcg(base + (size_t)q * (16 * kTileRows) + i);
-      acc_s[i] = s;
+    for (int j = 0; j < 2; ++j) {
+      const int c = 8 * j + 2 * t, r = warp * 16 + g;
+      acc_s[c * kTileRows + r] = acc[j][0];
+      acc_s[(c + 1) * kTileRows + r] = acc[j][1];
+      acc_s[c * kTileRows + r + 8] = acc[j][2];
+      acc_s[(c + 1) * kTileRows + r + 8] = acc[j][3];
     }
-    if (tid == 0) p.counters[tile_id] = 0;
     __syncthreads();
-  }
 
-  switch (p.epi) {
-    case EPI_SWIGLU:
-      epilogue_swiglu(p, acc_s, scale_s, mb, tile);
-      break;
-    case EPI_QKV:
-    case EPI_INJECT:
-      epilogue_heads(p, acc_s, scale_s, mb, tile);
-      break;
-    default:
-      epilogue_rows(p, acc_s, scale_s, mb, tile, &s_flag);
-      break;
+    if (c0 != 0 || c1 != p.cpt) {
+      const long long iu0 = (long long)item * p.cpt;
+      const int first = (int)owner_of(iu0, U, G);
+      const int last = (int)owner_of(iu0 + p.cpt - 1, U, G);
+      const size_t slot = 2 * (size_t)b + (b == first ? 1 : 0);
+      float* part = p.partial + slot * (16 * kTileRows);
+      for (int i = tid; i < 16 * kTileRows; i += blockDim.x) part[i] = acc_s[i];
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) s_flag = atomicAdd(p.counters + item, 1) == last - first;
+      __syncthreads();
+      if (!s_flag) continue;
+      __threadfence();
+      for (int i = tid; i < 16 * kTileRows; i += blockDim.x) {
+        float sum = 0.f;
+        for (int c = first; c <= last; ++c) {
+          const size_t sl = 2 * (size_t)c + (c == first ? 1 : 0);
+          sum += __ldcg(p.partial + sl * (16 * kTileRows) + i);
+        }
+        acc_s[i] = sum;
+      }
+      if (tid == 0) p.counters[item] = 0;
+      __syncthreads();
+    }
+
+    switch (p.epi) {
+      case EPI_SWIGLU:
+        epilogue_swiglu(p, acc_s, scale_s, mb, tile);
+        break;
+      case EPI_QKV:
+      case EPI_INJECT:
+        epilogue_heads(p, acc_s, scale_s, mb, tile);
+        break;
+      default:
+        epilogue_rows(p, acc_s, scale_s, mb, tile, &s_flag);
+        break;
+    }
   }
 }
 
@@ -517,18 +548,25 @@ cudaError_t configure_gemm(int xk_max) {
 }
 
 template <int WT>
-static cudaError_t launch_t(const GemmParams& p, int n_mb, cudaStream_t st) {
-  const size_t smem = gemm_smem_bytes(WT, p.xk);
-  dim3 grid(n_mb, p.n_tiles * p.n_kt);
-  gemm_rows_kernel<WT><<<grid, kGemmThreads, smem, st>>>(p);
-  return cudaGetLastError();
+static cudaError_t launch_t(const GemmParams& p, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(WT, p.xk);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<WT>, p);
 }
 
-cudaError_t launch_gemm(int wt, const GemmParams& p, int n_mb, cudaStream_t st) {
+cudaError_t launch_gemm(int wt, const GemmParams& p, cudaStream_t st) {
   switch (wt) {
-    case W_F32: return launch_t<W_F32>(p, n_mb, st);
-    case W_BF16: return launch_t<W_BF16>(p, n_mb, st);
-    case W_FP8: return launch_t<W_FP8>(p, n_mb, st);
+    case W_F32: return launch_t<W_F32>(p, st);
+    case W_BF16: return launch_t<W_BF16>(p, st);
+    case W_FP8: return launch_t<W_FP8>(p, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -55,13 +55,14 @@ struct GemmParams {
   int nseg;
   int N;      // virtual output rows
   int map;
-  // tiling
-  int n_tiles;
-  int n_kt;
-  int kt;     // k extent of one CTA (multiple of the chunk width)
-  int xk;     // k extent of one shared-memory activation stage
-  float* partial;
-  int* counters;
+  // stream-K schedule (see gemm.cu)
+  int n_tiles;  // 128-row output tiles
+  int n_mb;     // 16-row activation blocks
+  int cpt;      // k chunks per tile
+  int grid;     // CTAs (one resident wave)
+  int xk;       // k extent of one shared-memory activation stage
+  float* partial;  // [2 * grid][16][128]
+  int* counters;   // [n_tiles * n_mb], zero between launches
   // epilogue
   int epi;
   float* out;
@@ -99,7 +100,7 @@ struct AttnParams {
   int ring_bf16;
   int layer, n_layer;
   int n_head, n_head_kv, hd, window;
-  int chunk, n_chunks;    // ring slots per CTA, ring chunks (the block is chunk n_chunks)
+  int n_chunks;           // 64-slot ring chunks (the block is chunk n_chunks)
   float scale;
   float* part_acc;        // [n_seq][Hkv][n_chunks+1][R][hd]
   float* part_ml;         // [n_seq][Hkv][n_chunks+1][R][2]
@@ -108,9 +109,9 @@ struct AttnParams {
 
 size_t gemm_smem_bytes(int wt, int xk);
 cudaError_t configure_gemm(int xk_max);
-cudaError_t launch_gemm(int wt, const GemmParams& p, int n_mb, cudaStream_t st);
+cudaError_t launch_gemm(int wt, const GemmParams& p, cudaStream_t st);
 
-size_t attn_smem_bytes(int group, int hd, int chunk);
+size_t attn_smem_bytes(int group, int hd, int ring_f32);
 cudaError_t configure_attention(size_t smem);
 cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams& p, int n_seq, cudaStream_t st);

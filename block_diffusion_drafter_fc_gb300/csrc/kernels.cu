@@ -125,168 +125,259 @@ cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss
 
 // ------------------------------------------------------------------ attention
 
-// One CTA = one (sequence, kv head, key chunk).  The G = n_head / n_head_kv
-// query heads of the kv group (16 rows each) share the chunk's K/V tile in
-// shared memory.  Chunk c < n_chunks covers ring slots [c*chunk, (c+1)*chunk);
-// chunk n_chunks is the block's own 16 keys, visible to every row (non-causal).
-// A ring slot holding position kp is a key of row i iff 0 <= kp < n_past and
-// (n_past + i) - kp < window (dflash-ops model card, Method).  Each CTA writes
-// the chunk's row max, sum of exponentials and unnormalised P V.
-__global__ void __launch_bounds__(256) attn_chunk_kernel(const __grid_constant__ AttnParams p) {
+// One CTA = one (sequence, kv head, key chunk); one warp per query head of the
+// kv group (16 block rows each), all warps sharing the chunk's K/V tile in
+// shared memory.  Chunk c < n_chunks covers ring slots [c*64, c*64 + 64);
+// chunk n_chunks is the block's own 16 keys, visible to every row
+// (non-causal).  A ring slot holding position kp is a key of row i iff
+// 0 <= kp < n_past and (n_past + i) - kp < window (dflash-ops model card,
+// Method).  Both products run on the tensor cores with fp32 accumulation:
+// q (fp32, pre-scaled by 1/sqrt(hd)) and the probabilities p (fp32) are split
+// into bf16 hi + lo, bf16 ring K/V are exact (an fp32 ring is split too), so
+// S = q k^T and O = p V keep fp32 accuracy (~2^-17 per product).  Each CTA
+// writes the chunk's row max, row sum of exp and unnormalised O.
+constexpr int kAttnChunk = 64;
+constexpr int kQPad = 8, kVPad = 8;
+
+template <bool RING_F32>
+__global__ void attn_chunk_kernel(const __grid_constant__ AttnParams p) {
   const int c = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
   const int G = p.n_head / p.n_head_kv, R = kBlock * G, hd = p.hd;
   const int qd = p.n_head * hd, kvd = p.n_head_kv * hd;
   const bool blk = c == p.n_chunks;
-  const int CH = p.chunk < kBlock ? kBlock : p.chunk;
-  const int s0 = c * p.chunk;
-  const int nk = blk ? kBlock : min(p.chunk, p.window - s0);
-  extern __shared__ __align__(16) float sm[];
-  float* qT = sm;                 // [hd][R]
-  float* kT = qT + hd * R;        // [hd][CH]
-  float* vS = kT + hd * CH;       // [CH][hd]
-  float* pT = vS + CH * hd;       // [CH][R]
-  float* rowm = pT + CH * R;
-  float* rowl = rowm + R;
-  int* kpos = reinterpret_cast<int*>(rowl + R);
-  const int tid = threadIdx.x;
+  const int s0 = c * kAttnChunk;
+  const int CH = blk ? kBlock : kAttnChunk;               // keys in this tile (padded)
+  const int nk = blk ? kBlock : min(kAttnChunk, p.window - s0);
+  const int QS = hd + kQPad, VS = kAttnChunk + kVPad;
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  uint16_t* q_hi = reinterpret_cast<uint16_t*>(sm_raw);   // [R][QS]
+  uint16_t* q_lo = q_hi + R * QS;
+  uint16_t* k_hi = q_lo + R * QS;                         // [64][QS]
+  uint16_t* k_lo = k_hi + kAttnChunk * QS;
+  uint16_t* v_hi = k_lo + (RING_F32 ? kAttnChunk * QS : 0);  // transposed [hd][VS]
+  uint16_t* v_lo = v_hi + hd * VS;
+  int* kpos = reinterpret_cast<int*>(v_lo + (RING_F32 ? hd * VS : 0));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+
+  pdl_trigger();
+  pdl_wait();
   const int p0 = max(p.n_past[seq], 0);
 
-  for (int idx = tid; idx < R * hd; idx += blockDim.x) {
-    const int r = idx / hd, d = idx - r * hd;
+  // q rows of the group (row r = head_local * 16 + i), scaled, split hi/lo
+  for (int idx = tid; idx < R * hd / 4; idx += blockDim.x) {
+    const int r = idx / (hd / 4), d = (idx - r * (hd / 4)) * 4;
     const int hl = r / kBlock, i = r - hl * kBlock;
-    qT[d * R + r] = p.q[(size_t)(seq * kBlock + i) * qd + (kvh * G + hl) * hd + d] * p.scale;
+    float4 v = *reinterpret_cast<const float4*>(p.q + (size_t)(seq * kBlock + i) * qd + (kvh * G + hl) * hd + d);
+    v.x *= p.scale; v.y *= p.scale; v.z *= p.scale; v.w *= p.scale;
+    uint2 h, l;
+    split_bf16x2(v.x, v.y, h.x, l.x);
+    split_bf16x2(v.z, v.w, h.y, l.y);
+    *reinterpret_cast<uint2*>(q_hi + r * QS + d) = h;
+    *reinterpret_cast<uint2*>(q_lo + r * QS + d) = l;
   }
-  if (blk) {
-    for (int idx = tid; idx < kBlock * hd; idx += blockDim.x) {
-      const int j = idx / hd, d = idx - j * hd;
-      const size_t src = (size_t)(seq * kBlock + j) * kvd + kvh * hd + d;
-      kT[d * CH + j] = p.kblk[src];
-      vS[j * hd + d] = p.vblk[src];
-    }
-  } else {
-    const size_t plane = (size_t)p.window * hd;
-    const size_t kbase = ((((size_t)seq * p.n_layer + p.layer) * 2 + 0) * p.n_head_kv + kvh) * plane;
-    const size_t vbase = ((((size_t)seq * p.n_layer + p.layer) * 2 + 1) * p.n_head_kv + kvh) * plane;
-    for (int idx = tid; idx < nk * hd; idx += blockDim.x) {
-      const int j = idx / hd, d = idx - j * hd;
-      const size_t o = (size_t)(s0 + j) * hd + d;
-      float kv, vv;
-      if (p.ring_bf16) {
-        const uint16_t* r = reinterpret_cast<const uint16_t*>(p.ring);
-        kv = bf16_bits_to_f32(r[kbase + o]);
-        vv = bf16_bits_to_f32(r[vbase + o]);
-      } else {
+  // keys / values of the chunk (rows past nk are zero and masked)
+  const size_t plane = (size_t)p.window * hd;
+  const size_t kbase = ((((size_t)seq * p.n_layer + p.layer) * 2 + 0) * p.n_head_kv + kvh) * plane;
+  const size_t vbase = ((((size_t)seq * p.n_layer + p.layer) * 2 + 1) * p.n_head_kv + kvh) * plane;
+  for (int idx = tid; idx < CH * hd / 4; idx += blockDim.x) {
+    const int j = idx / (hd / 4), d = (idx - j * (hd / 4)) * 4;
+    float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+    if (j < nk) {
+      if (blk) {
+        const size_t o = (size_t)(seq * kBlock + j) * kvd + kvh * hd + d;
+        kv = *reinterpret_cast<const float4*>(p.kblk + o);
+        vv = *reinterpret_cast<const float4*>(p.vblk + o);
+      } else if (RING_F32) {
         const float* r = reinterpret_cast<const float*>(p.ring);
-        kv = r[kbase + o];
-        vv = r[vbase + o];
-      }
-      kT[d * CH + j] = kv;
-      vS[j * hd + d] = vv;
-    }
-    for (int j = tid; j < nk; j += blockDim.x) kpos[j] = p.ring_pos[(size_t)seq * p.window + s0 + j];
-  }
-  __syncthreads();
-
-  // scores (4 rows x 4 keys per thread), masked, stored transposed [key][row]
-  const int nrt = R / 4, nct = (nk + 3) / 4;
-  for (int tt = tid; tt < nrt * nct; tt += blockDim.x) {
-    const int rt = tt / nct, ct = tt - rt * nct;
-    float a[4][4] = {};
-    for (int d = 0; d < hd; ++d) {
-      const float4 qv = *reinterpret_cast<const float4*>(qT + d * R + 4 * rt);
-      const float4 kv = *reinterpret_cast<const float4*>(kT + d * CH + 4 * ct);
-      const float qa[4] = {qv.x, qv.y, qv.z, qv.w}, ka[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) a[ii][jj] = fmaf(qa[ii], ka[jj], a[ii][jj]);
-    }
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int key = 4 * ct + jj;
-      if (key >= nk) continue;
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii) {
-        const int r = 4 * rt + ii;
-        bool ok = true;
-        if (!blk) {
-          const int kp = kpos[key], qp = p0 + (r % kBlock);
-          ok = kp >= 0 && kp < p0 && qp - kp < p.window;
-        }
-        pT[key * R + r] = ok ? a[ii][jj] : -CUDART_INF_F;
+        kv = *reinterpret_cast<const float4*>(r + kbase + (size_t)(s0 + j) * hd + d);
+        vv = *reinterpret_cast<const float4*>(r + vbase + (size_t)(s0 + j) * hd + d);
+      } else {
+        const uint16_t* r = reinterpret_cast<const uint16_t*>(p.ring);
+        const uint2 kb = *reinterpret_cast<const uint2*>(r + kbase + (size_t)(s0 + j) * hd + d);
+        const uint2 vb = *reinterpret_cast<const uint2*>(r + vbase + (size_t)(s0 + j) * hd + d);
+        kv = make_float4(__uint_as_float(kb.x << 16), __uint_as_float(kb.x & 0xffff0000u),
+                         __uint_as_float(kb.y << 16), __uint_as_float(kb.y & 0xffff0000u));
+        vv = make_float4(__uint_as_float(vb.x << 16), __uint_as_float(vb.x & 0xffff0000u),
+                         __uint_as_float(vb.y << 16), __uint_as_float(vb.y & 0xffff0000u));
       }
     }
-  }
-  __syncthreads();
-  for (int r = tid; r < R; r += blockDim.x) {
-    float m = -CUDART_INF_F;
-    for (int key = 0; key < nk; ++key) m = fmaxf(m, pT[key * R + r]);
-    float l = 0.f;
-    for (int key = 0; key < nk; ++key) {
-      const float e = m == -CUDART_INF_F ? 0.f : expf(pT[key * R + r] - m);
-      pT[key * R + r] = e;
-      l += e;
+    uint2 kh, kl;
+    split_bf16x2(kv.x, kv.y, kh.x, kl.x);
+    split_bf16x2(kv.z, kv.w, kh.y, kl.y);
+    *reinterpret_cast<uint2*>(k_hi + j * QS + d) = kh;
+    if (RING_F32) *reinterpret_cast<uint2*>(k_lo + j * QS + d) = kl;
+    const float va[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint16_t vh = f32_to_bf16_bits(va[e]);
+      v_hi[(d + e) * VS + j] = vh;
+      if (RING_F32) v_lo[(d + e) * VS + j] = f32_to_bf16_bits(va[e] - bf16_bits_to_f32(vh));
     }
-    rowm[r] = m;
-    rowl[r] = l;
   }
+  for (int j = tid; j < CH; j += blockDim.x)
+    kpos[j] = (blk || j >= nk) ? -1 : p.ring_pos[(size_t)seq * p.window + s0 + j];
   __syncthreads();
+  if (warp >= G) return;
 
+  // S = q k^T for this warp's 16 rows (head `warp`) and up to 64 keys
+  const uint16_t* qh = q_hi + warp * kBlock * QS;
+  const uint16_t* ql = q_lo + warp * kBlock * QS;
+  float S[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
+  const int nt = CH / 8;
+  for (int k0 = 0; k0 < hd; k0 += 16) {
+    const uint32_t ah[4] = {*reinterpret_cast<const uint32_t*>(qh + g * QS + k0 + 2 * t),
+                            *reinterpret_cast<const uint32_t*>(qh + (g + 8) * QS + k0 + 2 * t),
+                            *reinterpret_cast<const uint32_t*>(qh + g * QS + k0 + 2 * t + 8),
+                            *reinterpret_cast<const uint32_t*>(qh + (g + 8) * QS + k0 + 2 * t + 8)};
+    const uint32_t al[4] = {*reinterpret_cast<const uint32_t*>(ql + g * QS + k0 + 2 * t),
+                            *reinterpret_cast<const uint32_t*>(ql + (g + 8) * QS + k0 + 2 * t),
+                            *reinterpret_cast<const uint32_t*>(ql + g * QS + k0 + 2 * t + 8),
+                            *reinterpret_cast<const uint32_t*>(ql + (g + 8) * QS + k0 + 2 * t + 8)};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j >= nt) break;
+      const uint16_t* kr = k_hi + (8 * j + g) * QS + k0 + 2 * t;
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr);
+      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 8);
+      mma_bf16_16816(S[j], ah, b0, b1);
+      mma_bf16_16816(S[j], al, b0, b1);
+      if (RING_F32) {
+        const uint16_t* kl2 = k_lo + (8 * j + g) * QS + k0 + 2 * t;
+        mma_bf16_16816(S[j], ah, *reinterpret_cast<const uint32_t*>(kl2),
+                       *reinterpret_cast<const uint32_t*>(kl2 + 8));
+      }
+    }
+  }
+  // mask, row max, exp, row sum (rows g and g + 8; a row lives in one lane quad)
+  const int qpos0 = p0 + g, qpos1 = p0 + g + 8;
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= nt) break;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int key = 8 * j + 2 * t + e;
+      bool ok0 = true, ok1 = true;
+      if (!blk) {
+        const int kp = kpos[key];
+        const bool past = kp >= 0 && kp < p0;
+        ok0 = past && qpos0 - kp < p.window;
+        ok1 = past && qpos1 - kp < p.window;
+      }
+      if (!ok0) S[j][e] = -CUDART_INF_F;
+      if (!ok1) S[j][2 + e] = -CUDART_INF_F;
+      m0 = fmaxf(m0, S[j][e]);
+      m1 = fmaxf(m1, S[j][2 + e]);
+    }
+  }
+  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+  m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+  m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+  float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= nt) break;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      S[j][e] = m0 == -CUDART_INF_F ? 0.f : expf(S[j][e] - m0);
+      S[j][2 + e] = m1 == -CUDART_INF_F ? 0.f : expf(S[j][2 + e] - m1);
+      l0 += S[j][e];
+      l1 += S[j][2 + e];
+    }
+  }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+  // O = p V: p from the S accumulators (two key n8 tiles = one k16 step)
   const size_t slot = ((size_t)seq * p.n_head_kv + kvh) * (p.n_chunks + 1) + c;
-  float* oacc = p.part_acc + slot * R * hd;
-  const int nd8 = hd / 8;
-  for (int tt = tid; tt < (R / 4) * nd8; tt += blockDim.x) {
-    const int rt = tt / nd8, dt = tt - rt * nd8;
-    float o[4][8] = {};
-    for (int key = 0; key < nk; ++key) {
-      const float4 pv = *reinterpret_cast<const float4*>(pT + key * R + 4 * rt);
-      const float4 v0 = *reinterpret_cast<const float4*>(vS + key * hd + 8 * dt);
-      const float4 v1 = *reinterpret_cast<const float4*>(vS + key * hd + 8 * dt + 4);
-      const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
-      const float va[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float* oacc = p.part_acc + (slot * R + warp * kBlock) * hd;
+  for (int jd = 0; jd < hd / 8; ++jd) {
+    float O[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) o[ii][jj] = fmaf(pa[ii], va[jj], o[ii][jj]);
+    for (int kk = 0; kk < 4; ++kk) {
+      if (2 * kk >= nt) break;
+      uint32_t ph[4], pl[4];
+      split_bf16x2(S[2 * kk][0], S[2 * kk][1], ph[0], pl[0]);
+      split_bf16x2(S[2 * kk][2], S[2 * kk][3], ph[1], pl[1]);
+      split_bf16x2(S[2 * kk + 1][0], S[2 * kk + 1][1], ph[2], pl[2]);
+      split_bf16x2(S[2 * kk + 1][2], S[2 * kk + 1][3], ph[3], pl[3]);
+      const uint16_t* vr = v_hi + (8 * jd + g) * VS + 16 * kk + 2 * t;
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vr);
+      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vr + 8);
+      mma_bf16_16816(O, ph, b0, b1);
+      mma_bf16_16816(O, pl, b0, b1);
+      if (RING_F32) {
+        const uint16_t* vl = v_lo + (8 * jd + g) * VS + 16 * kk + 2 * t;
+        mma_bf16_16816(O, ph, *reinterpret_cast<const uint32_t*>(vl),
+                       *reinterpret_cast<const uint32_t*>(vl + 8));
+      }
     }
-#pragma unroll
-    for (int ii = 0; ii < 4; ++ii) {
-      float* dst = oacc + (size_t)(4 * rt + ii) * hd + 8 * dt;
-      *reinterpret_cast<float4*>(dst) = make_float4(o[ii][0], o[ii][1], o[ii][2], o[ii][3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(o[ii][4], o[ii][5], o[ii][6], o[ii][7]);
-    }
+    *reinterpret_cast<float2*>(oacc + (size_t)g * hd + 8 * jd + 2 * t) = make_float2(O[0], O[1]);
+    *reinterpret_cast<float2*>(oacc + (size_t)(g + 8) * hd + 8 * jd + 2 * t) = make_float2(O[2], O[3]);
   }
-  for (int r = tid; r < R; r += blockDim.x) {
-    p.part_ml[(slot * R + r) * 2 + 0] = rowm[r];
-    p.part_ml[(slot * R + r) * 2 + 1] = rowl[r];
+  if (t == 0) {
+    float* ml = p.part_ml + (slot * R + warp * kBlock) * 2;
+    ml[g * 2 + 0] = m0;
+    ml[g * 2 + 1] = l0;
+    ml[(g + 8) * 2 + 0] = m1;
+    ml[(g + 8) * 2 + 1] = l1;
   }
 }
 
-size_t attn_smem_bytes(int group, int hd, int chunk) {
-  const int R = kBlock * group, CH = chunk < kBlock ? kBlock : chunk;
-  return sizeof(float) * ((size_t)hd * R + (size_t)hd * CH + (size_t)CH * hd + (size_t)CH * R + 2 * R) +
-         sizeof(int) * CH;
+size_t attn_smem_bytes(int group, int hd, int ring_f32) {
+  const int R = kBlock * group, QS = hd + kQPad, VS = kAttnChunk + kVPad;
+  size_t b = sizeof(uint16_t) * (2 * (size_t)R * QS + (size_t)kAttnChunk * QS + (size_t)hd * VS);
+  if (ring_f32) b += sizeof(uint16_t) * ((size_t)kAttnChunk * QS + (size_t)hd * VS);
+  return b + sizeof(int) * kAttnChunk;
 }
 
 cudaError_t configure_attention(size_t smem) {
   static size_t configured = 0;   // only ever raised, so every live handle still fits
   if (smem <= configured) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel,
+  cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
   if (e == cudaSuccess) configured = smem;
   return e;
 }
 
+static cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                     cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
 cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st) {
-  const size_t smem = attn_smem_bytes(p.n_head / p.n_head_kv, p.hd, p.chunk);
-  dim3 grid(p.n_chunks + 1, p.n_head_kv, n_seq);
-  attn_chunk_kernel<<<grid, 256, smem, st>>>(p);
-  return cudaGetLastError();
+  const int G = p.n_head / p.n_head_kv;
+  const int f32 = !p.ring_bf16;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.n_chunks + 1, p.n_head_kv, n_seq),
+                                      dim3(32 * G),
+                                      attn_smem_bytes(G, p.hd, f32), st, attr);
+  return f32 ? cudaLaunchKernelEx(&cfg, attn_chunk_kernel<true>, p)
+             : cudaLaunchKernelEx(&cfg, attn_chunk_kernel<false>, p);
 }
 
 // Merge the chunk partials of one (sequence, query head) in chunk order:
 // out = sum_c exp(m_c - M) acc_c / sum_c exp(m_c - M) l_c.
 __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int seq = blockIdx.x / p.n_head, h = blockIdx.x % p.n_head;
   const int G = p.n_head / p.n_head_kv, kvh = h / G, hl = h - kvh * G;
   const int R = kBlock * G, hd = p.hd, nc = p.n_chunks + 1;
@@ -308,8 +399,9 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant
 }
 
 cudaError_t launch_attn_combine(const AttnParams& p, int n_seq, cudaStream_t st) {
-  attn_combine_kernel<<<n_seq * p.n_head, 128, 0, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(dim3(n_seq * p.n_head), dim3(128), 0, st, attr);
+  return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p);
 }
 
 // ------------------------------------------------------------------ acceptance

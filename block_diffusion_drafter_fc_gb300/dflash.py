@@ -22,6 +22,9 @@ HEADER = PKG.parent / "include" / "dflash.h"
 
 DTYPE = {"f32": 0, "bf16": 1, "fp8": 2}
 MAX_LAYERS = 16
+PROF_N = 11
+PROF_CLASSES = ("embed", "qkv", "attention", "attn_merge", "o_proj", "gate_up", "down", "lm_head",
+                "encode", "inject", "accept")
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "too many rows",
           -4: "sequence out of range", -5: "CUDA error", -6: "not captured", -7: "device status"}
 
@@ -73,6 +76,8 @@ def _load() -> C.CDLL:
         "dflash_step_host": (C.c_int, [vp, i32, vp, vp, vp, vp, vp]),
         "dflash_ring_reset": (C.c_int, [vp, i32, vp]),
         "dflash_read_status": (C.c_int, [vp, C.POINTER(C.c_uint32), vp]),
+        "dflash_profile_enable": (C.c_int, [vp, C.c_int]),
+        "dflash_profile_read": (C.c_int, [vp, C.POINTER(C.c_double), C.POINTER(C.c_int32)]),
         "dflash_status_string": (C.c_char_p, [C.c_int]),
         "dflash_last_error": (C.c_char_p, [vp]),
     }
@@ -235,6 +240,15 @@ class Drafter:
         if rc not in (0, -7):
             _check(rc, self.h, "read_status")
         return v.value
+
+    def dflash_profile_enable(self, enable: bool = True):
+        _check(LIB.dflash_profile_enable(self.h, int(enable)), self.h, "profile_enable")
+
+    def dflash_profile_read(self):
+        ms = (C.c_double * PROF_N)()
+        n = (C.c_int32 * PROF_N)()
+        _check(LIB.dflash_profile_read(self.h, ms, n), self.h, "profile_read")
+        return {PROF_CLASSES[i]: (ms[i], n[i]) for i in range(PROF_N)}
 
     # ---- convenience: run a workload's prefill (encode + inject per call)
     def prefill(self, wl: Workload, dev_feats: List[torch.Tensor], stream=None):

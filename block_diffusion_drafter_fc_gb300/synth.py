@@ -20,7 +20,9 @@ of the drafter; the cast itself is torch's float8_e4m3fn conversion.
 """
 from __future__ import annotations
 
+import concurrent.futures as _cf
 import dataclasses
+import os
 from dataclasses import dataclass, field
 from typing import Dict, List, Optional, Tuple
 
@@ -154,11 +156,22 @@ def _store_dense(x: torch.Tensor, dtype: str) -> torch.Tensor:
 
 
 def quantize_fp8_rows(w: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Per-row FP8 E4M3 copy of a f32 matrix: (codes uint8 [N,K], scales f32 [N])."""
-    amax = w.abs().amax(dim=1)
-    s = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax)).to(torch.float32)
-    q = (w / s[:, None]).clamp_(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
-    return q.view(torch.uint8).contiguous(), s.contiguous()
+    """Per-row FP8 E4M3 copy of a f32 matrix: (codes uint8 [N,K], scales f32 [N]),
+    computed in row blocks on the thread pool."""
+    n_rows = w.shape[0]
+    q = torch.empty(w.shape, dtype=torch.uint8)
+    s = torch.empty(n_rows, dtype=torch.float32)
+    step = max(1, _CHUNK // max(1, w.shape[1]))
+
+    def blk(r0):
+        x = w[r0:r0 + step]
+        amax = x.abs().amax(dim=1)
+        sc = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax)).to(torch.float32)
+        s[r0:r0 + step] = sc
+        q[r0:r0 + step] = (x / sc[:, None]).clamp_(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+
+    list(_POOL.map(blk, range(0, n_rows, step)))
+    return q, s
 
 
 @dataclass
@@ -221,30 +234,66 @@ def _layer_shape(cfg: DraftConfig, name: str) -> Tuple[int, ...]:
     }[name]
 
 
-def make_weights(cfg: DraftConfig, g: torch.Generator) -> Dict[str, Weight]:
-    """Draw every weight in the fixed order tok_embd, fc, hidden_norm, the layers'
-    [attn_norm, wq, wk, wv, wo, q_norm, k_norm, ffn_norm, gate, up, down],
-    out_norm, lm_head."""
+_CHUNK = 1 << 22
+_POOL = _cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 4))
+
+
+def _mix(*keys: int) -> int:
+    """splitmix64 of a key tuple: the seed of one chunk of one drawn tensor."""
+    z = 0x9E3779B97F4A7C15
+    for k in keys:
+        z = (z ^ (k & 0xFFFFFFFFFFFFFFFF)) * 0xBF58476D1CE4E5B9 & 0xFFFFFFFFFFFFFFFF
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EB & 0xFFFFFFFFFFFFFFFF
+        z ^= z >> 31
+    return z & 0x7FFFFFFFFFFFFFFF
+
+
+def randn(shape, seed: int, index: int, scale: float = 1.0, shift: float = 0.0,
+          dtype: torch.dtype = torch.float32) -> torch.Tensor:
+    """shift + scale * N(0,1), tensor number `index` of a workload, stored as `dtype`.
+    4 Mi-element chunks: chunk c is drawn in f32 by torch's CPU generator seeded
+    with mix(seed, index, c), scaled in f32 and rounded once to `dtype`; chunks
+    run in parallel threads (the result does not depend on the thread count)."""
+    n = int(np.prod(shape))
+    out = torch.empty(n, dtype=dtype)
+
+    def fill(c):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        g = torch.Generator().manual_seed(_mix(seed, index, c))
+        x = torch.randn(hi - lo, generator=g, dtype=torch.float32)
+        if scale != 1.0:
+            x.mul_(scale)
+        if shift != 0.0:
+            x.add_(shift)
+        out[lo:hi] = x.to(dtype)
+
+    list(_POOL.map(fill, range((n + _CHUNK - 1) // _CHUNK)))
+    return out.view(shape)
+
+
+def make_weights(cfg: DraftConfig, g: torch.Generator = None) -> Dict[str, Weight]:
+    """Draw every weight; tensor indices follow the fixed order tok_embd, fc,
+    hidden_norm, the layers' [attn_norm, wq, wk, wv, wo, q_norm, k_norm, ffn_norm,
+    gate, up, down], out_norm, lm_head."""
     w: Dict[str, Weight] = {}
+    counter = [0]
+
+    def draw(shape, scale=1.0, shift=0.0, dtype="f32"):
+        counter[0] += 1
+        return randn(shape, cfg.seed, counter[0], scale, shift, _TORCH[dtype])
 
     def proj(shape):
-        fan_in = shape[1]
-        x = torch.randn(shape, generator=g, dtype=torch.float32)
-        x.mul_(1.0 / np.sqrt(fan_in))
+        std = float(np.float32(1.0 / np.sqrt(shape[1])))
         if cfg.weight_dtype == "fp8":
-            q, s = quantize_fp8_rows(x)
+            q, s = quantize_fp8_rows(draw(shape, std))
             return Weight(q, "fp8", s)
-        return Weight(_store_dense(x, cfg.weight_dtype), cfg.weight_dtype)
+        return Weight(draw(shape, std, dtype=cfg.weight_dtype), cfg.weight_dtype)
 
     def dense_mat(shape, std):
-        x = torch.randn(shape, generator=g, dtype=torch.float32)
-        if std != 1.0:
-            x.mul_(std)
-        return Weight(_store_dense(x, cfg.dense_dtype), cfg.dense_dtype)
+        return Weight(draw(shape, std, dtype=cfg.dense_dtype), cfg.dense_dtype)
 
     def norm_vec(n):
-        x = 1.0 + 0.02 * torch.randn((n,), generator=g, dtype=torch.float32)
-        return Weight(_store_dense(x, cfg.dense_dtype), cfg.dense_dtype)
+        return Weight(draw((n,), 0.02, 1.0, dtype=cfg.dense_dtype), cfg.dense_dtype)
 
     w["tok_embd"] = dense_mat((cfg.n_vocab, cfg.n_embd), 1.0)
     w["fc"] = dense_mat((cfg.n_embd, cfg.feat_dim), 1.0 / np.sqrt(cfg.feat_dim))
@@ -261,7 +310,7 @@ def make_weights(cfg: DraftConfig, g: torch.Generator) -> Dict[str, Weight]:
 def make_workload(cfg: DraftConfig, weights: Optional[Dict[str, Weight]] = None) -> Workload:
     """The full seeded workload of one configuration (seed = cfg.seed)."""
     g = torch.Generator().manual_seed(cfg.seed)
-    w = make_weights(cfg, g)
+    w = make_weights(cfg)
     if weights is not None:       # caller-provided replacement weights (same draw order kept)
         w = weights
     fills: List[int] = []
@@ -285,8 +334,8 @@ def make_workload(cfg: DraftConfig, weights: Optional[Dict[str, Weight]] = None)
             calls.append((s, offsets[s], fills[s], 0))
             n_rows.append(fills[s])
             n_past.append(offsets[s] + fills[s])
-    feats = [_store_dense(torch.randn((n, cfg.feat_dim), generator=g, dtype=torch.float32),
-                          cfg.dense_dtype) for n in n_rows]
+    feats = [randn((n, cfg.feat_dim), cfg.seed, 10_000 + i, dtype=_TORCH[cfg.dense_dtype])
+             for i, n in enumerate(n_rows)]
     id_last = torch.randint(0, cfg.n_vocab, (cfg.n_seq,), generator=g, dtype=torch.int64)
     if cfg.mismatch == "geometric":
         # failures before the first success of a Bernoulli(p) sequence, capped at 15

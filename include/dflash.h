@@ -266,6 +266,22 @@ DFLASH_API int dflash_ring_reset(dflash_handle* h, int32_t seq, void* stream);
  */
 DFLASH_API int dflash_read_status(dflash_handle* h, uint32_t* status, void* stream);
 
+/*
+ * Launch-class profiling of eager calls (not of captured graphs).  While
+ * enabled, every kernel launch of dflash_step / dflash_encode / dflash_inject /
+ * dflash_accept is bracketed by CUDA events recorded on the launching stream.
+ * dflash_profile_read waits for those events, writes the summed device time in
+ * milliseconds and the launch count of each class (arrays of DFLASH_PROF_N
+ * entries, host memory) and clears the record.  Classes: 0 embedding + rope
+ * table, 1 q/k/v projection, 2 attention chunks, 3 attention merge, 4 o
+ * projection, 5 gate/up projection, 6 down projection, 7 LM head + drafts,
+ * 8 encode (fc + norm), 9 injection (rope table + wk/wv + ring scatter),
+ * 10 acceptance scan.  Enabling while a capture is in progress is refused.
+ */
+#define DFLASH_PROF_N 11
+DFLASH_API int dflash_profile_enable(dflash_handle* h, int enable);
+DFLASH_API int dflash_profile_read(dflash_handle* h, double* ms, int32_t* launches);
+
 /* Text of a dflash_status code (static storage). */
 DFLASH_API const char* dflash_status_string(int status);
 
