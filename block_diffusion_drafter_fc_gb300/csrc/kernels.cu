@@ -133,120 +133,136 @@ cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss
 // 0 <= kp < n_past and (n_past + i) - kp < window (dflash-ops model card,
 // Method).  Both products run on the tensor cores with fp32 accumulation:
 // q (fp32, pre-scaled by 1/sqrt(hd)) and the probabilities p (fp32) are split
-// into bf16 hi + lo, bf16 ring K/V are exact (an fp32 ring is split too), so
-// S = q k^T and O = p V keep fp32 accuracy (~2^-17 per product).  Each CTA
-// writes the chunk's row max, row sum of exp and unnormalised O.
+// into bf16 hi + lo; bf16 ring K/V are exact, fp32 K/V (an fp32 ring, or the
+// block's own keys) are split too, so S = q k^T and O = p V keep fp32
+// accuracy (~2^-17 per product).  Each CTA writes the chunk's row max, row sum
+// of exp and unnormalised O for the merge kernel.
 constexpr int kAttnChunk = 64;
-constexpr int kQPad = 8, kVPad = 8;
+constexpr int kKPad = 8;   // bf16 elements of row padding (16 B): conflict-free fragment loads
 
-template <bool RING_F32>
+DF_DEVICE void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+DF_DEVICE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// four 8x8 bf16 matrices, transposed on the way out (B fragments of p V)
+DF_DEVICE void ldmatrix_x4_trans(uint32_t (&r)[4], const void* smem) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
+
+template <int HD>
 __global__ void attn_chunk_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int KS = HD + kKPad;     // row stride of K / V tiles (bf16 elements)
+  constexpr int NK16 = HD / 16;      // k16 steps over the head dimension
   const int c = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
-  const int G = p.n_head / p.n_head_kv, R = kBlock * G, hd = p.hd;
-  const int qd = p.n_head * hd, kvd = p.n_head_kv * hd;
+  const int G = p.n_head / p.n_head_kv;
+  const int qd = p.n_head * HD, kvd = p.n_head_kv * HD;
   const bool blk = c == p.n_chunks;
   const int s0 = c * kAttnChunk;
-  const int CH = blk ? kBlock : kAttnChunk;               // keys in this tile (padded)
   const int nk = blk ? kBlock : min(kAttnChunk, p.window - s0);
-  const int QS = hd + kQPad, VS = kAttnChunk + kVPad;
+  const bool split_kv = blk || !p.ring_bf16;     // K/V arrive as fp32 -> hi + lo
   extern __shared__ __align__(16) uint8_t sm_raw[];
-  uint16_t* q_hi = reinterpret_cast<uint16_t*>(sm_raw);   // [R][QS]
-  uint16_t* q_lo = q_hi + R * QS;
-  uint16_t* k_hi = q_lo + R * QS;                         // [64][QS]
-  uint16_t* k_lo = k_hi + kAttnChunk * QS;
-  uint16_t* v_hi = k_lo + (RING_F32 ? kAttnChunk * QS : 0);  // transposed [hd][VS]
-  uint16_t* v_lo = v_hi + hd * VS;
-  int* kpos = reinterpret_cast<int*>(v_lo + (RING_F32 ? hd * VS : 0));
+  uint16_t* k_hi = reinterpret_cast<uint16_t*>(sm_raw);   // [64][KS]
+  uint16_t* k_lo = k_hi + kAttnChunk * KS;
+  uint16_t* v_hi = k_lo + kAttnChunk * KS;                // [64][KS] (row-major, keys x dims)
+  uint16_t* v_lo = v_hi + kAttnChunk * KS;
+  int* kpos = reinterpret_cast<int*>(v_lo + kAttnChunk * KS);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
 
   pdl_trigger();
   pdl_wait();
   const int p0 = max(p.n_past[seq], 0);
 
-  // q rows of the group (row r = head_local * 16 + i), scaled, split hi/lo
-  for (int idx = tid; idx < R * hd / 4; idx += blockDim.x) {
-    const int r = idx / (hd / 4), d = (idx - r * (hd / 4)) * 4;
-    const int hl = r / kBlock, i = r - hl * kBlock;
-    float4 v = *reinterpret_cast<const float4*>(p.q + (size_t)(seq * kBlock + i) * qd + (kvh * G + hl) * hd + d);
-    v.x *= p.scale; v.y *= p.scale; v.z *= p.scale; v.w *= p.scale;
-    uint2 h, l;
-    split_bf16x2(v.x, v.y, h.x, l.x);
-    split_bf16x2(v.z, v.w, h.y, l.y);
-    *reinterpret_cast<uint2*>(q_hi + r * QS + d) = h;
-    *reinterpret_cast<uint2*>(q_lo + r * QS + d) = l;
-  }
-  // keys / values of the chunk (rows past nk are zero and masked)
-  const size_t plane = (size_t)p.window * hd;
+  // K/V tile: bf16 ring rows by 16-byte async copies; fp32 rows split hi/lo
+  const size_t plane = (size_t)p.window * HD;
   const size_t kbase = ((((size_t)seq * p.n_layer + p.layer) * 2 + 0) * p.n_head_kv + kvh) * plane;
-  const size_t vbase = ((((size_t)seq * p.n_layer + p.layer) * 2 + 1) * p.n_head_kv + kvh) * plane;
-  for (int idx = tid; idx < CH * hd / 4; idx += blockDim.x) {
-    const int j = idx / (hd / 4), d = (idx - j * (hd / 4)) * 4;
-    float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-    if (j < nk) {
-      if (blk) {
-        const size_t o = (size_t)(seq * kBlock + j) * kvd + kvh * hd + d;
-        kv = *reinterpret_cast<const float4*>(p.kblk + o);
-        vv = *reinterpret_cast<const float4*>(p.vblk + o);
-      } else if (RING_F32) {
-        const float* r = reinterpret_cast<const float*>(p.ring);
-        kv = *reinterpret_cast<const float4*>(r + kbase + (size_t)(s0 + j) * hd + d);
-        vv = *reinterpret_cast<const float4*>(r + vbase + (size_t)(s0 + j) * hd + d);
+  const size_t vbase = kbase + (size_t)p.n_head_kv * plane;
+  if (!split_kv) {
+    const uint16_t* r = reinterpret_cast<const uint16_t*>(p.ring);
+    for (int idx = tid; idx < kAttnChunk * (HD / 8); idx += blockDim.x) {
+      const int j = idx / (HD / 8), d = (idx - j * (HD / 8)) * 8;
+      if (j < nk) {
+        cp_async16(k_hi + j * KS + d, r + kbase + (size_t)(s0 + j) * HD + d);
+        cp_async16(v_hi + j * KS + d, r + vbase + (size_t)(s0 + j) * HD + d);
       } else {
-        const uint16_t* r = reinterpret_cast<const uint16_t*>(p.ring);
-        const uint2 kb = *reinterpret_cast<const uint2*>(r + kbase + (size_t)(s0 + j) * hd + d);
-        const uint2 vb = *reinterpret_cast<const uint2*>(r + vbase + (size_t)(s0 + j) * hd + d);
-        kv = make_float4(__uint_as_float(kb.x << 16), __uint_as_float(kb.x & 0xffff0000u),
-                         __uint_as_float(kb.y << 16), __uint_as_float(kb.y & 0xffff0000u));
-        vv = make_float4(__uint_as_float(vb.x << 16), __uint_as_float(vb.x & 0xffff0000u),
-                         __uint_as_float(vb.y << 16), __uint_as_float(vb.y & 0xffff0000u));
+        *reinterpret_cast<uint4*>(k_hi + j * KS + d) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(v_hi + j * KS + d) = make_uint4(0, 0, 0, 0);
       }
     }
-    uint2 kh, kl;
-    split_bf16x2(kv.x, kv.y, kh.x, kl.x);
-    split_bf16x2(kv.z, kv.w, kh.y, kl.y);
-    *reinterpret_cast<uint2*>(k_hi + j * QS + d) = kh;
-    if (RING_F32) *reinterpret_cast<uint2*>(k_lo + j * QS + d) = kl;
-    const float va[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint16_t vh = f32_to_bf16_bits(va[e]);
-      v_hi[(d + e) * VS + j] = vh;
-      if (RING_F32) v_lo[(d + e) * VS + j] = f32_to_bf16_bits(va[e] - bf16_bits_to_f32(vh));
+  } else {
+    const int rows = blk ? kBlock : kAttnChunk;
+    for (int idx = tid; idx < rows * (HD / 4); idx += blockDim.x) {
+      const int j = idx / (HD / 4), d = (idx - j * (HD / 4)) * 4;
+      float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+      if (j < nk) {
+        if (blk) {
+          const size_t o = (size_t)(seq * kBlock + j) * kvd + kvh * HD + d;
+          kv = *reinterpret_cast<const float4*>(p.kblk + o);
+          vv = *reinterpret_cast<const float4*>(p.vblk + o);
+        } else {
+          const float* r = reinterpret_cast<const float*>(p.ring);
+          kv = *reinterpret_cast<const float4*>(r + kbase + (size_t)(s0 + j) * HD + d);
+          vv = *reinterpret_cast<const float4*>(r + vbase + (size_t)(s0 + j) * HD + d);
+        }
+      }
+      uint2 h, l;
+      split_bf16x2(kv.x, kv.y, h.x, l.x);
+      split_bf16x2(kv.z, kv.w, h.y, l.y);
+      *reinterpret_cast<uint2*>(k_hi + j * KS + d) = h;
+      *reinterpret_cast<uint2*>(k_lo + j * KS + d) = l;
+      split_bf16x2(vv.x, vv.y, h.x, l.x);
+      split_bf16x2(vv.z, vv.w, h.y, l.y);
+      *reinterpret_cast<uint2*>(v_hi + j * KS + d) = h;
+      *reinterpret_cast<uint2*>(v_lo + j * KS + d) = l;
     }
   }
-  for (int j = tid; j < CH; j += blockDim.x)
+  for (int j = tid; j < kAttnChunk; j += blockDim.x)
     kpos[j] = (blk || j >= nk) ? -1 : p.ring_pos[(size_t)seq * p.window + s0 + j];
-  __syncthreads();
-  if (warp >= G) return;
 
-  // S = q k^T for this warp's 16 rows (head `warp`) and up to 64 keys
-  const uint16_t* qh = q_hi + warp * kBlock * QS;
-  const uint16_t* ql = q_lo + warp * kBlock * QS;
+  // q fragments of this warp's head straight from global (fp32 -> hi/lo), while
+  // the K/V copies are in flight
+  const int head = kvh * G + warp;
+  const float* qrow0 = p.q + (size_t)(seq * kBlock + g) * qd + head * HD;
+  const float* qrow1 = qrow0 + (size_t)8 * qd;
+  uint32_t qh[NK16][4], ql[NK16][4];
+#pragma unroll
+  for (int ks = 0; ks < NK16; ++ks) {
+    const int k0 = ks * 16 + 2 * t;
+    const float2 a0 = *reinterpret_cast<const float2*>(qrow0 + k0);
+    const float2 a1 = *reinterpret_cast<const float2*>(qrow1 + k0);
+    const float2 a2 = *reinterpret_cast<const float2*>(qrow0 + k0 + 8);
+    const float2 a3 = *reinterpret_cast<const float2*>(qrow1 + k0 + 8);
+    split_bf16x2(a0.x * p.scale, a0.y * p.scale, qh[ks][0], ql[ks][0]);
+    split_bf16x2(a1.x * p.scale, a1.y * p.scale, qh[ks][1], ql[ks][1]);
+    split_bf16x2(a2.x * p.scale, a2.y * p.scale, qh[ks][2], ql[ks][2]);
+    split_bf16x2(a3.x * p.scale, a3.y * p.scale, qh[ks][3], ql[ks][3]);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // S = q k^T: 16 rows x up to 64 keys (8 n8 tiles)
+  const int nt = blk ? 2 : 8;
   float S[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
-  const int nt = CH / 8;
-  for (int k0 = 0; k0 < hd; k0 += 16) {
-    const uint32_t ah[4] = {*reinterpret_cast<const uint32_t*>(qh + g * QS + k0 + 2 * t),
-                            *reinterpret_cast<const uint32_t*>(qh + (g + 8) * QS + k0 + 2 * t),
-                            *reinterpret_cast<const uint32_t*>(qh + g * QS + k0 + 2 * t + 8),
-                            *reinterpret_cast<const uint32_t*>(qh + (g + 8) * QS + k0 + 2 * t + 8)};
-    const uint32_t al[4] = {*reinterpret_cast<const uint32_t*>(ql + g * QS + k0 + 2 * t),
-                            *reinterpret_cast<const uint32_t*>(ql + (g + 8) * QS + k0 + 2 * t),
-                            *reinterpret_cast<const uint32_t*>(ql + g * QS + k0 + 2 * t + 8),
-                            *reinterpret_cast<const uint32_t*>(ql + (g + 8) * QS + k0 + 2 * t + 8)};
+#pragma unroll
+  for (int ks = 0; ks < NK16; ++ks) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      if (j >= nt) break;
-      const uint16_t* kr = k_hi + (8 * j + g) * QS + k0 + 2 * t;
-      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr);
-      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 8);
-      mma_bf16_16816(S[j], ah, b0, b1);
-      mma_bf16_16816(S[j], al, b0, b1);
-      if (RING_F32) {
-        const uint16_t* kl2 = k_lo + (8 * j + g) * QS + k0 + 2 * t;
-        mma_bf16_16816(S[j], ah, *reinterpret_cast<const uint32_t*>(kl2),
-                       *reinterpret_cast<const uint32_t*>(kl2 + 8));
+      if (j < nt) {
+        const uint16_t* kr = k_hi + (8 * j + g) * KS + ks * 16 + 2 * t;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 8);
+        mma_bf16_16816(S[j], qh[ks], b0, b1);
+        mma_bf16_16816(S[j], ql[ks], b0, b1);
+        if (split_kv) {
+          const uint16_t* kl = k_lo + (8 * j + g) * KS + ks * 16 + 2 * t;
+          mma_bf16_16816(S[j], qh[ks], *reinterpret_cast<const uint32_t*>(kl),
+                         *reinterpret_cast<const uint32_t*>(kl + 8));
+        }
       }
     }
   }
@@ -255,21 +271,22 @@ __global__ void attn_chunk_kernel(const __grid_constant__ AttnParams p) {
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    if (j >= nt) break;
+    if (j < nt) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int key = 8 * j + 2 * t + e;
-      bool ok0 = true, ok1 = true;
-      if (!blk) {
-        const int kp = kpos[key];
-        const bool past = kp >= 0 && kp < p0;
-        ok0 = past && qpos0 - kp < p.window;
-        ok1 = past && qpos1 - kp < p.window;
+      for (int e = 0; e < 2; ++e) {
+        const int key = 8 * j + 2 * t + e;
+        bool ok0 = true, ok1 = true;
+        if (!blk) {
+          const int kp = kpos[key];
+          const bool past = kp >= 0 && kp < p0;
+          ok0 = past && qpos0 - kp < p.window;
+          ok1 = past && qpos1 - kp < p.window;
+        }
+        if (!ok0) S[j][e] = -CUDART_INF_F;
+        if (!ok1) S[j][2 + e] = -CUDART_INF_F;
+        m0 = fmaxf(m0, S[j][e]);
+        m1 = fmaxf(m1, S[j][2 + e]);
       }
-      if (!ok0) S[j][e] = -CUDART_INF_F;
-      if (!ok1) S[j][2 + e] = -CUDART_INF_F;
-      m0 = fmaxf(m0, S[j][e]);
-      m1 = fmaxf(m1, S[j][2 + e]);
     }
   }
   m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
@@ -279,13 +296,14 @@ __global__ void attn_chunk_kernel(const __grid_constant__ AttnParams p) {
   float l0 = 0.f, l1 = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    if (j >= nt) break;
+    if (j < nt) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      S[j][e] = m0 == -CUDART_INF_F ? 0.f : expf(S[j][e] - m0);
-      S[j][2 + e] = m1 == -CUDART_INF_F ? 0.f : expf(S[j][2 + e] - m1);
-      l0 += S[j][e];
-      l1 += S[j][2 + e];
+      for (int e = 0; e < 2; ++e) {
+        S[j][e] = m0 == -CUDART_INF_F ? 0.f : expf(S[j][e] - m0);
+        S[j][2 + e] = m1 == -CUDART_INF_F ? 0.f : expf(S[j][2 + e] - m1);
+        l0 += S[j][e];
+        l1 += S[j][2 + e];
+      }
     }
   }
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -293,32 +311,48 @@ __global__ void attn_chunk_kernel(const __grid_constant__ AttnParams p) {
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  // O = p V: p from the S accumulators (two key n8 tiles = one k16 step)
+  // O = p V: p from the S accumulators (two key n8 tiles = one k16 step); the
+  // V fragments come from the row-major tile through ldmatrix.trans
+  uint32_t ph[4][4], pl[4][4];
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    split_bf16x2(S[2 * kk][0], S[2 * kk][1], ph[kk][0], pl[kk][0]);
+    split_bf16x2(S[2 * kk][2], S[2 * kk][3], ph[kk][1], pl[kk][1]);
+    split_bf16x2(S[2 * kk + 1][0], S[2 * kk + 1][1], ph[kk][2], pl[kk][2]);
+    split_bf16x2(S[2 * kk + 1][2], S[2 * kk + 1][3], ph[kk][3], pl[kk][3]);
+  }
   const size_t slot = ((size_t)seq * p.n_head_kv + kvh) * (p.n_chunks + 1) + c;
-  float* oacc = p.part_acc + (slot * R + warp * kBlock) * hd;
-  for (int jd = 0; jd < hd / 8; ++jd) {
-    float O[4] = {0.f, 0.f, 0.f, 0.f};
+  const int R = kBlock * G;
+  float* oacc = p.part_acc + (slot * R + warp * kBlock) * HD;
+  // lane -> row of the 8x8 matrix it addresses for ldmatrix: matrices 0/1 are
+  // keys [0,8) / [8,16) of dims [8jd, 8jd+8), matrices 2/3 the next 8 dims
+  const int lrow = lane & 7, lmat = lane >> 3;
+#pragma unroll
+  for (int jd = 0; jd < HD / 8; jd += 2) {
+    float O0[4] = {0.f, 0.f, 0.f, 0.f}, O1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      if (2 * kk >= nt) break;
-      uint32_t ph[4], pl[4];
-      split_bf16x2(S[2 * kk][0], S[2 * kk][1], ph[0], pl[0]);
-      split_bf16x2(S[2 * kk][2], S[2 * kk][3], ph[1], pl[1]);
-      split_bf16x2(S[2 * kk + 1][0], S[2 * kk + 1][1], ph[2], pl[2]);
-      split_bf16x2(S[2 * kk + 1][2], S[2 * kk + 1][3], ph[3], pl[3]);
-      const uint16_t* vr = v_hi + (8 * jd + g) * VS + 16 * kk + 2 * t;
-      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vr);
-      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vr + 8);
-      mma_bf16_16816(O, ph, b0, b1);
-      mma_bf16_16816(O, pl, b0, b1);
-      if (RING_F32) {
-        const uint16_t* vl = v_lo + (8 * jd + g) * VS + 16 * kk + 2 * t;
-        mma_bf16_16816(O, ph, *reinterpret_cast<const uint32_t*>(vl),
-                       *reinterpret_cast<const uint32_t*>(vl + 8));
+      if (2 * kk < nt) {
+        const int key = 16 * kk + (lmat & 1) * 8 + lrow;
+        const int dim = 8 * jd + (lmat >> 1) * 8;
+        uint32_t b[4];
+        ldmatrix_x4_trans(b, v_hi + key * KS + dim);
+        mma_bf16_16816(O0, ph[kk], b[0], b[1]);
+        mma_bf16_16816(O0, pl[kk], b[0], b[1]);
+        mma_bf16_16816(O1, ph[kk], b[2], b[3]);
+        mma_bf16_16816(O1, pl[kk], b[2], b[3]);
+        if (split_kv) {
+          uint32_t bl[4];
+          ldmatrix_x4_trans(bl, v_lo + key * KS + dim);
+          mma_bf16_16816(O0, ph[kk], bl[0], bl[1]);
+          mma_bf16_16816(O1, ph[kk], bl[2], bl[3]);
+        }
       }
     }
-    *reinterpret_cast<float2*>(oacc + (size_t)g * hd + 8 * jd + 2 * t) = make_float2(O[0], O[1]);
-    *reinterpret_cast<float2*>(oacc + (size_t)(g + 8) * hd + 8 * jd + 2 * t) = make_float2(O[2], O[3]);
+    *reinterpret_cast<float2*>(oacc + (size_t)g * HD + 8 * jd + 2 * t) = make_float2(O0[0], O0[1]);
+    *reinterpret_cast<float2*>(oacc + (size_t)(g + 8) * HD + 8 * jd + 2 * t) = make_float2(O0[2], O0[3]);
+    *reinterpret_cast<float2*>(oacc + (size_t)g * HD + 8 * jd + 8 + 2 * t) = make_float2(O1[0], O1[1]);
+    *reinterpret_cast<float2*>(oacc + (size_t)(g + 8) * HD + 8 * jd + 8 + 2 * t) = make_float2(O1[2], O1[3]);
   }
   if (t == 0) {
     float* ml = p.part_ml + (slot * R + warp * kBlock) * 2;
@@ -330,19 +364,21 @@ __global__ void attn_chunk_kernel(const __grid_constant__ AttnParams p) {
 }
 
 size_t attn_smem_bytes(int group, int hd, int ring_f32) {
-  const int R = kBlock * group, QS = hd + kQPad, VS = kAttnChunk + kVPad;
-  size_t b = sizeof(uint16_t) * (2 * (size_t)R * QS + (size_t)kAttnChunk * QS + (size_t)hd * VS);
-  if (ring_f32) b += sizeof(uint16_t) * ((size_t)kAttnChunk * QS + (size_t)hd * VS);
-  return b + sizeof(int) * kAttnChunk;
+  (void)group;
+  (void)ring_f32;
+  return sizeof(uint16_t) * 4 * (size_t)kAttnChunk * (hd + kKPad) + sizeof(int) * kAttnChunk;
 }
 
 cudaError_t configure_attention(size_t smem) {
   static size_t configured = 0;   // only ever raised, so every live handle still fits
   if (smem <= configured) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel<false>,
+  cudaError_t e = cudaFuncSetAttribute(attn_chunk_kernel<32>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_chunk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_chunk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem);
   if (e == cudaSuccess) configured = smem;
   return e;
@@ -364,43 +400,54 @@ static cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
 
 cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st) {
   const int G = p.n_head / p.n_head_kv;
-  const int f32 = !p.ring_bf16;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(p.n_chunks + 1, p.n_head_kv, n_seq),
-                                      dim3(32 * G),
-                                      attn_smem_bytes(G, p.hd, f32), st, attr);
-  return f32 ? cudaLaunchKernelEx(&cfg, attn_chunk_kernel<true>, p)
-             : cudaLaunchKernelEx(&cfg, attn_chunk_kernel<false>, p);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(p.n_chunks + 1, p.n_head_kv, n_seq), dim3(32 * G),
+                                      attn_smem_bytes(G, p.hd, !p.ring_bf16), st, attr);
+  switch (p.hd) {
+    case 32: return cudaLaunchKernelEx(&cfg, attn_chunk_kernel<32>, p);
+    case 64: return cudaLaunchKernelEx(&cfg, attn_chunk_kernel<64>, p);
+    case 128: return cudaLaunchKernelEx(&cfg, attn_chunk_kernel<128>, p);
+  }
+  return cudaErrorInvalidValue;
 }
 
-// Merge the chunk partials of one (sequence, query head) in chunk order:
-// out = sum_c exp(m_c - M) acc_c / sum_c exp(m_c - M) l_c.
-__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+// Merge the chunk partials of one (sequence, query head, 4 block rows) in chunk
+// order: out = sum_c exp(m_c - M) O_c / sum_c exp(m_c - M) l_c.  One thread per
+// (row, dim); the chunk loops issue independent loads.
+constexpr int kMergeRows = 4;
+
+__global__ void __launch_bounds__(512) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   pdl_trigger();
   pdl_wait();
-  const int seq = blockIdx.x / p.n_head, h = blockIdx.x % p.n_head;
+  const int per_head = kBlock / kMergeRows;
+  const int rb = blockIdx.x % per_head, h = (blockIdx.x / per_head) % p.n_head;
+  const int seq = blockIdx.x / (per_head * p.n_head);
   const int G = p.n_head / p.n_head_kv, kvh = h / G, hl = h - kvh * G;
   const int R = kBlock * G, hd = p.hd, nc = p.n_chunks + 1;
+  const int i = rb * kMergeRows + threadIdx.x / hd, d = threadIdx.x % hd;
+  if (threadIdx.x >= kMergeRows * hd) return;
+  const int r = hl * kBlock + i;
   const size_t slot0 = ((size_t)seq * p.n_head_kv + kvh) * nc;
-  for (int e = threadIdx.x; e < kBlock * hd; e += blockDim.x) {
-    const int i = e / hd, d = e - i * hd, r = hl * kBlock + i;
-    float M = -CUDART_INF_F;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, p.part_ml[((slot0 + c) * R + r) * 2]);
-    float L = 0.f, A = 0.f;
-    for (int c = 0; c < nc; ++c) {
-      const float m = p.part_ml[((slot0 + c) * R + r) * 2];
-      if (m == -CUDART_INF_F) continue;
-      const float w = expf(m - M);
-      L += p.part_ml[((slot0 + c) * R + r) * 2 + 1] * w;
-      A += p.part_acc[((slot0 + c) * R + r) * hd + d] * w;
-    }
-    p.out[(size_t)(seq * kBlock + i) * (p.n_head * hd) + h * hd + d] = A / L;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  float M = -CUDART_INF_F;
+#pragma unroll 8
+  for (int c = 0; c < nc; ++c) M = fmaxf(M, ml[(slot0 + c) * R + r].x);
+  float L = 0.f, A = 0.f;
+#pragma unroll 8
+  for (int c = 0; c < nc; ++c) {
+    const float2 e = ml[(slot0 + c) * R + r];
+    const float o = p.part_acc[((slot0 + c) * R + r) * hd + d];
+    const float w = e.x == -CUDART_INF_F ? 0.f : expf(e.x - M);
+    L += e.y * w;
+    A += o * w;
   }
+  p.out[(size_t)(seq * kBlock + i) * (p.n_head * hd) + h * hd + d] = A / L;
 }
 
 cudaError_t launch_attn_combine(const AttnParams& p, int n_seq, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = pdl_config(dim3(n_seq * p.n_head), dim3(128), 0, st, attr);
+  cudaLaunchConfig_t cfg = pdl_config(dim3(n_seq * p.n_head * (kBlock / kMergeRows)),
+                                      dim3(kMergeRows * p.hd), 0, st, attr);
   return cudaLaunchKernelEx(&cfg, attn_combine_kernel, p);
 }
 

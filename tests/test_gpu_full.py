@@ -1,0 +1,60 @@
+"""Full-size parity: every workload at its real dimensions, in the launch
+configuration the benchmark times (the captured graph of step + accept,
+replayed), against the complete fp64 oracle run on the same seeded inputs.
+
+Each case checks: ring positions exact and ring K/V within one rounding unit;
+logits within the storage format's bound; drafts equal (outside near ties,
+which are reported); acceptance counts equal; graph replay bitwise equal to
+the eager step.
+"""
+import numpy as np
+import pytest
+import torch
+
+from block_diffusion_drafter_fc_gb300.synth import BLOCK, get_config, make_workload
+import gpu_harness as GH
+import oracle_bridge as OB
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+FULL = ["small_bf16", "real_bf16", "real_f32", "batched_fp8"]
+
+
+def _replay(g, wl, targets):
+    dr = g["drafter"]
+    n = wl.cfg.n_seq
+    logits = torch.zeros((n, BLOCK, wl.cfg.n_vocab), device="cuda")
+    drafts = torch.zeros((n, 15), dtype=torch.int32, device="cuda")
+    t = torch.from_numpy(np.ascontiguousarray(targets)).cuda()
+    n_ok = torch.zeros(n, dtype=torch.int32, device="cuda")
+    dr.dflash_capture(g["id_last_d"], g["n_past_d"], logits, drafts, t, n_ok)
+    for _ in range(3):
+        dr.dflash_replay()
+    torch.cuda.synchronize()
+    return logits.cpu().numpy(), drafts.cpu().numpy(), n_ok.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_against_oracle(name):
+    wl = make_workload(get_config(name))
+    ref = OB.oracle_full(wl)
+    g = GH.gpu_run(wl, targets=ref["targets"], keep=True)
+    try:
+        from test_gpu_parity import _check_ring
+        _check_ring(wl, ref, g)
+        lg, dr_, n_ok = _replay(g, wl, ref["targets"])
+        assert np.array_equal(lg, g["logits"]), "graph replay differs from the eager step"
+        assert np.array_equal(dr_, g["drafts"])
+        err = float(np.abs(lg - ref["logits"]).max())
+        tol = GH.logit_tol(wl.cfg)
+        print(f"{name}: max |logit diff| {err:.3e} (bound {tol})")
+        assert err <= tol, err
+        amb = GH.compare_drafts(lg, dr_, ref["logits"], ref["drafts"], err)
+        if amb == 0:
+            assert np.array_equal(dr_, ref["drafts"])
+            assert np.array_equal(n_ok, ref["n_ok"])
+        else:
+            print(f"{name}: {amb} near-tie draft positions")
+        assert g["status"] == 0
+    finally:
+        g["drafter"].close()

@@ -106,6 +106,8 @@ def test_fewer_sequences_than_handle():
     wl = make_workload(get_config("ragged_bf16"))
     ref = OB.oracle_full(wl, n_seq=2)
     gpu = GH.gpu_run(wl, n_seq=2, targets=ref["targets"])
+    bad = np.argwhere(~np.isfinite(gpu["logits"]))
+    assert bad.size == 0, f"non-finite logits at (seq, row) {sorted(set(map(tuple, bad[:, :2].tolist())))}"
     err = float(np.abs(gpu["logits"] - ref["logits"]).max())
     assert err <= GH.logit_tol(wl.cfg)
     assert np.array_equal(gpu["drafts"], ref["drafts"])
