@@ -97,6 +97,12 @@ DF_DEVICE uint4 ldg_stream(const void* p) {
   return r;
 }
 
+// Bulk prefetch of a contiguous global range into L2 (no registers, no shared
+// memory); address 16-byte aligned, size a multiple of 16.
+DF_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- dependent launch
 
 // Programmatic dependent launch: let the next kernel of the stream be scheduled

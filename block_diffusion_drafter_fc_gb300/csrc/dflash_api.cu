@@ -40,7 +40,7 @@ Plan plan_gemm(int n_tiles, int K, int kc, int n_mb) {
   Plan p;
   p.n_tiles = n_tiles;
   p.n_mb = n_mb;
-  p.cpt = K / kc;
+  p.cpt = cdiv(K, kc);
   const long long units = (long long)n_tiles * n_mb * p.cpt;
   p.grid = (int)std::min<long long>(kGemmGrid, units);
   p.xk = std::min(p.cpt * kc, (kXkMax / kc) * kc);
@@ -81,11 +81,12 @@ struct GemmShape {
 };
 
 void step_shapes(const Geometry& g, GemmShape out[5]) {
-  out[0] = {cdiv(g.qd + 2 * g.kvd, kTileRows), g.d, g.kc};   // q/k/v
-  out[1] = {cdiv(g.d, kTileRows), g.qd, g.kc};               // o
-  out[2] = {cdiv(g.F, kTileRows / 2), g.d, g.kc};            // gate/up
-  out[3] = {cdiv(g.d, kTileRows), g.F, g.kc};                // down
-  out[4] = {cdiv(g.V, kTileRows), g.d, g.kc};                // lm head
+  const int kc = tma_chunk_k(g.wt);
+  out[0] = {cdiv(g.qd + 2 * g.kvd, kTileRows), g.d, kc};   // q/k/v
+  out[1] = {cdiv(g.d, kTileRows), g.qd, kc};               // o
+  out[2] = {cdiv(g.F, kTileRows / 2), g.d, kc};            // gate/up
+  out[3] = {cdiv(g.d, kTileRows), g.F, kc};                // down
+  out[4] = {cdiv(g.V, kTileRows), g.d, kc};                // lm head
 }
 
 void inject_shapes(const Geometry& g, GemmShape out[2]) {
@@ -95,7 +96,8 @@ void inject_shapes(const Geometry& g, GemmShape out[2]) {
 }
 
 struct Layout {
-  size_t status, inv_freq, counters, h, ss, qbuf, kblk, vblk, attn, act, rope_step, am_part;
+  size_t status, inv_freq, counters, h, ss, qbuf, kblk, vblk, rope_step, am_part;
+  size_t xn_hi, xn_lo, attn_hi, attn_lo, act_hi, act_lo;
   size_t apart_acc, apart_ml, logits_int, drafts_int, idl_int, npast_int, partial;
   size_t inj_raw, inj_ss, inj_rope, total;
   size_t partial_floats;
@@ -137,8 +139,12 @@ Layout layout(const dflash_config& c) {
   L.qbuf = take(sizeof(float) * g.M_max * g.qd);
   L.kblk = take(sizeof(float) * g.M_max * g.kvd);
   L.vblk = take(sizeof(float) * g.M_max * g.kvd);
-  L.attn = take(sizeof(float) * g.M_max * g.qd);
-  L.act = take(sizeof(float) * (size_t)g.M_max * g.F);
+  L.xn_hi = take(sizeof(uint16_t) * (size_t)g.M_max * g.d);
+  L.xn_lo = take(sizeof(uint16_t) * (size_t)g.M_max * g.d);
+  L.attn_hi = take(sizeof(uint16_t) * (size_t)g.M_max * g.qd);
+  L.attn_lo = take(sizeof(uint16_t) * (size_t)g.M_max * g.qd);
+  L.act_hi = take(sizeof(uint16_t) * (size_t)g.M_max * g.F);
+  L.act_lo = take(sizeof(uint16_t) * (size_t)g.M_max * g.F);
   L.rope_step = take(sizeof(float2) * g.M_max * (g.hd / 2));
   L.am_part = take(sizeof(float2) * (size_t)L.lm_tiles * g.M_max);
   L.apart_acc = take(sizeof(float) * attn_slots * R * g.hd);
@@ -195,6 +201,11 @@ struct dflash_handle {
   Layout L;
   char* ring;
   char* scratch;
+  // tensor maps of the step's weights (wq, wk, wv, wo, gate, up, down per layer,
+  // the LM head) and of the three activation-pair buffers
+  CUtensorMap tm_layer[DFLASH_MAX_LAYERS][7];
+  CUtensorMap tm_lm;
+  CUtensorMap tm_xn[2], tm_attn[2], tm_act[2];
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -230,6 +241,44 @@ int cuda_fail(dflash_handle* h, cudaError_t e, const char* where) {
     cudaError_t e_ = (call);                                \
     if (e_ != cudaSuccess) return cuda_fail(h, e_, #call);  \
   } while (0)
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (the library
+// does not link libcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// 2-D map of a row-major [rows][cols] matrix, 16-row x 128-byte boxes, 128-byte
+// swizzle; out-of-range rows / columns read as zero.
+bool make_map(CUtensorMap* m, const void* base, int wt, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const CUtensorMapDataType dt = wt == W_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : wt == W_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const uint32_t esz = wt == W_F32 ? 4 : wt == W_BF16 ? 2 : 1;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * esz};
+  const cuuint32_t box[2] = {128 / esz, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 enum ProfClass {
   PC_EMBED = 0, PC_QKV, PC_ATTN, PC_MERGE, PC_O, PC_GATEUP, PC_DOWN, PC_LM, PC_ENCODE, PC_INJECT,
@@ -273,6 +322,7 @@ GemmParams base_params(const dflash_handle* h) {
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   p.eps = h->cfg.eps;
+  p.rms_len = h->g.d;
   p.norm_bf16 = h->g.dense_bf16;
   p.partial = h->S<float>(h->L.partial);
   p.counters = h->S<int>(h->L.counters);
@@ -296,6 +346,14 @@ void set_plan(GemmParams& p, const GemmShape& s, int n_mb) {
   p.K = s.K;
 }
 
+// Projection launch on the TMA kernel: X is one of the activation-pair buffers.
+void set_tma_inputs(GemmParams& p, const CUtensorMap* x) {
+  p.tm_xh = x[0];
+  p.tm_xl = x[1];
+  p.has_lo = 1;
+  p.x_mode = X_BF16;
+}
+
 int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t* n_past,
              float* logits, int32_t* drafts, cudaStream_t st) {
   const Geometry& g = h->g;
@@ -306,26 +364,32 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   float* hbuf = h->S<float>(L.h);
   float* ss = h->S<float>(L.ss);
   float2* rope = h->S<float2>(L.rope_step);
-  PROF(h, PC_EMBED, st, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id, id_last,
-                           n_past, n_seq, h->S<double>(L.inv_freq), g.hd, hbuf, ss, rope,
-                           h->status(), st));
+  uint16_t* xn_hi = h->S<uint16_t>(L.xn_hi);
+  uint16_t* xn_lo = h->S<uint16_t>(L.xn_lo);
+  // h = embeddings; xn = split(h * attn_norm_0); ss = row sums of squares
+  PROF(h, PC_EMBED, st, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id,
+                                     id_last, n_past, n_seq, h->S<double>(L.inv_freq), g.hd, hbuf, ss,
+                                     rope, h->w.layers[0].attn_norm, xn_hi, xn_lo, h->status(), st));
   int n_ss = 1;
   for (int l = 0; l < g.L; ++l) {
     const dflash_layer_weights& lw = h->w.layers[l];
-    // attn_norm + q/k/v projection + per-head q/k norm + rope
+    // q/k/v of RMSNorm(h) (the 1/rms row scale after the product), per-head
+    // q/k norm + rope
     GemmParams p = base_params(h);
     set_plan(p, sh[0], n_seq);
-    p.x = hbuf; p.x_mode = X_F32; p.ldx = g.d; p.M = M;
-    p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.normw = lw.attn_norm;
+    set_tma_inputs(p, h->tm_xn);
+    p.M = M;
+    p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
     p.seg[0] = {lw.wq, lw.wq_scale, 0, g.qd};
     p.seg[1] = {lw.wk, lw.wk_scale, g.qd, g.kvd};
     p.seg[2] = {lw.wv, lw.wv_scale, g.qd + g.kvd, g.kvd};
+    p.tm_w[0] = h->tm_layer[l][0]; p.tm_w[1] = h->tm_layer[l][1]; p.tm_w[2] = h->tm_layer[l][2];
     p.nseg = 3; p.N = g.qd + 2 * g.kvd; p.map = MAP_SEGMENTS;
     p.epi = EPI_QKV; p.out = h->S<float>(L.qbuf); p.ldo = g.qd;
     p.kblk = h->S<float>(L.kblk); p.vblk = h->S<float>(L.vblk);
     p.q_norm = lw.q_norm; p.k_norm = lw.k_norm; p.rope_cs = rope;
-    PROF(h, PC_QKV, st, launch_gemm(g.wt, p, st));
-    // attention over ring chunks + the block, then the chunk merge
+    PROF(h, PC_QKV, st, launch_gemm_tma(g.wt, p, st));
+    // attention over ring chunks + the block, then the chunk merge (-> attn pair)
     AttnParams a;
     std::memset(&a, 0, sizeof(a));
     a.q = h->S<float>(L.qbuf); a.kblk = h->S<float>(L.kblk); a.vblk = h->S<float>(L.vblk);
@@ -335,51 +399,85 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.n_chunks = L.attn_chunks;
     a.scale = (float)(1.0 / std::sqrt((double)g.hd));
     a.part_acc = h->S<float>(L.apart_acc); a.part_ml = h->S<float>(L.apart_ml);
-    a.out = h->S<float>(L.attn);
+    a.out_hi = h->S<uint16_t>(L.attn_hi); a.out_lo = h->S<uint16_t>(L.attn_lo);
     PROF(h, PC_ATTN, st, launch_attention(a, n_seq, st));
     PROF(h, PC_MERGE, st, launch_attn_combine(a, n_seq, st));
-    // o projection + residual
+    // o projection + residual; next input xn = split(h * ffn_norm)
     p = base_params(h);
     set_plan(p, sh[1], n_seq);
-    p.x = h->S<float>(L.attn); p.x_mode = X_F32; p.ldx = g.qd; p.M = M;
+    set_tma_inputs(p, h->tm_attn);
+    p.M = M;
     p.seg[0] = {lw.wo, lw.wo_scale, 0, g.d};
+    p.tm_w[0] = h->tm_layer[l][3];
     p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
     p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
-    PROF(h, PC_O, st, launch_gemm(g.wt, p, st));
+    p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d; p.pair_norm = lw.ffn_norm;
+    PROF(h, PC_O, st, launch_gemm_tma(g.wt, p, st));
     n_ss = sh[1].n_tiles;
-    // ffn_norm + gate/up + SwiGLU
+    // gate/up of RMSNorm(h) + SwiGLU -> act pair
     p = base_params(h);
     set_plan(p, sh[2], n_seq);
-    p.x = hbuf; p.x_mode = X_F32; p.ldx = g.d; p.M = M;
-    p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.normw = lw.ffn_norm;
+    set_tma_inputs(p, h->tm_xn);
+    p.M = M;
+    p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
     p.seg[0] = {lw.gate, lw.gate_scale, 0, g.F};
     p.seg[1] = {lw.up, lw.up_scale, 0, g.F};
+    p.tm_w[0] = h->tm_layer[l][4]; p.tm_w[1] = h->tm_layer[l][5];
     p.nseg = 2; p.N = 2 * g.F; p.map = MAP_SWIGLU;
-    p.epi = EPI_SWIGLU; p.out = h->S<float>(L.act); p.ldo = g.F;
-    PROF(h, PC_GATEUP, st, launch_gemm(g.wt, p, st));
-    // down projection + residual
+    p.epi = EPI_SWIGLU; p.out = nullptr;
+    p.pair_hi = h->S<uint16_t>(L.act_hi); p.pair_lo = h->S<uint16_t>(L.act_lo); p.pair_ld = g.F;
+    PROF(h, PC_GATEUP, st, launch_gemm_tma(g.wt, p, st));
+    // down projection + residual; next input xn = split(h * next norm)
     p = base_params(h);
     set_plan(p, sh[3], n_seq);
-    p.x = h->S<float>(L.act); p.x_mode = X_F32; p.ldx = g.F; p.M = M;
+    set_tma_inputs(p, h->tm_act);
+    p.M = M;
     p.seg[0] = {lw.down, lw.down_scale, 0, g.d};
+    p.tm_w[0] = h->tm_layer[l][6];
     p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
     p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
-    PROF(h, PC_DOWN, st, launch_gemm(g.wt, p, st));
+    p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d;
+    p.pair_norm = l + 1 < g.L ? h->w.layers[l + 1].attn_norm : h->w.out_norm;
+    PROF(h, PC_DOWN, st, launch_gemm_tma(g.wt, p, st));
     n_ss = sh[3].n_tiles;
   }
-  // output norm + LM head + greedy drafts
+  // LM head of RMSNorm(h) (out_norm folded into xn by the last down projection)
   GemmParams p = base_params(h);
   set_plan(p, sh[4], n_seq);
-  p.x = hbuf; p.x_mode = X_F32; p.ldx = g.d; p.M = M;
-  p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.normw = h->w.out_norm;
+  set_tma_inputs(p, h->tm_xn);
+  p.M = M;
+  p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
   p.seg[0] = {h->w.lm_head, h->w.lm_head_scale, 0, g.V};
+  p.tm_w[0] = h->tm_lm;
   p.nseg = 1; p.N = g.V; p.map = MAP_SEGMENTS;
   p.epi = EPI_LOGITS; p.out = logits; p.ldo = g.V;
   p.am_part = h->S<float2>(L.am_part);
   p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
   p.drafts = drafts;
-  PROF(h, PC_LM, st, launch_gemm(g.wt, p, st));
+  PROF(h, PC_LM, st, launch_gemm_tma(g.wt, p, st));
   return DFLASH_OK;
+}
+
+// Tensor maps of every weight the step streams and of the activation pairs.
+bool build_maps(dflash_handle* h) {
+  const Geometry& g = h->g;
+  const Layout& L = h->L;
+  for (int l = 0; l < g.L; ++l) {
+    const dflash_layer_weights& w = h->w.layers[l];
+    const void* mats[7] = {w.wq, w.wk, w.wv, w.wo, w.gate, w.up, w.down};
+    const int rows[7] = {g.qd, g.kvd, g.kvd, g.d, g.F, g.F, g.d};
+    const int cols[7] = {g.d, g.d, g.d, g.qd, g.d, g.d, g.F};
+    for (int i = 0; i < 7; ++i)
+      if (!make_map(&h->tm_layer[l][i], mats[i], g.wt, cols[i], rows[i])) return false;
+  }
+  if (!make_map(&h->tm_lm, h->w.lm_head, g.wt, g.d, g.V)) return false;
+  const size_t pairs[3][2] = {{L.xn_hi, L.xn_lo}, {L.attn_hi, L.attn_lo}, {L.act_hi, L.act_lo}};
+  const int kdim[3] = {g.d, g.qd, g.F};
+  CUtensorMap* dst[3] = {h->tm_xn, h->tm_attn, h->tm_act};
+  for (int i = 0; i < 3; ++i)
+    for (int j = 0; j < 2; ++j)
+      if (!make_map(&dst[i][j], h->scratch + pairs[i][j], W_BF16, kdim[i], g.M_max)) return false;
+  return true;
 }
 
 bool bad_ptr(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u); }
@@ -448,9 +546,14 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
                              cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.counters, 0, sizeof(int) * h->L.n_counters);
   if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.status, 0, sizeof(unsigned));
+  // zero K/V (empty slots are masked, but p = 0 times a NaN left in reused memory
+  // is NaN) and mark every slot empty
+  if (e == cudaSuccess) e = cudaMemset(h->ring, 0, h->L.ring_kv_bytes * cfg->max_seq);
   if (e == cudaSuccess)
     e = launch_fill_i32(h->ring_pos(0), cfg->max_seq * cfg->window, -1, nullptr);
   if (e == cudaSuccess) e = configure_gemm(kXkMax);
+  if (e == cudaSuccess) e = configure_gemm_tma();
+  if (e == cudaSuccess && !build_maps(h)) e = cudaErrorNotSupported;
   if (e == cudaSuccess)
     e = configure_attention(attn_smem_bytes(cfg->n_head / cfg->n_head_kv, cfg->head_dim,
                                             cfg->ring_dtype == DFLASH_DTYPE_F32));
@@ -616,7 +719,9 @@ int dflash_step_host(dflash_handle* h, int32_t n_seq, const int32_t* id_last,
 int dflash_ring_reset(dflash_handle* h, int32_t seq, void* stream) {
   if (!h) return DFLASH_ERR_INVALID_ARG;
   if (seq < 0 || seq >= h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
-  DF_CHECK(h, launch_fill_i32(h->ring_pos(seq), h->g.W, -1, static_cast<cudaStream_t>(stream)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DF_CHECK(h, cudaMemsetAsync(h->ring_seq(seq), 0, h->L.ring_seq_bytes, st));
+  DF_CHECK(h, launch_fill_i32(h->ring_pos(seq), h->g.W, -1, st));
   return DFLASH_OK;
 }
 

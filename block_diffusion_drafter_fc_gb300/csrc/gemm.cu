@@ -26,10 +26,7 @@
 //    deterministic and graph replays are bitwise identical, then runs the fused
 //    epilogue (residual + sum of squares for the next RMSNorm, SwiGLU, per-head
 //    q/k norm + rope, ring scatter, logits + argmax).
-#include "common.cuh"
-#include "internal.h"
-
-#include <math_constants.h>
+#include "gemm_common.cuh"
 
 namespace dflash {
 
@@ -56,52 +53,69 @@ size_t gemm_smem_bytes(int wt, int xk) {
          kTileRows * sizeof(float);
 }
 
-// Weight row `local` of `tile` -> its first byte (null when the row is past N).
-DF_DEVICE const uint8_t* map_row(const GemmParams& p, int tile, int local, int esz,
-                                 const float** scale) {
-  int s = 0, r = 0;
-  if (p.map == MAP_SWIGLU) {
-    s = local < kTileRows / 2 ? 0 : 1;
-    r = tile * (kTileRows / 2) + (local & (kTileRows / 2 - 1));
-    if (r >= p.seg[s].rows) return nullptr;
-  } else {
-    const int vr = tile * kTileRows + local;
-    if (vr >= p.N) return nullptr;
-    while (s + 1 < p.nseg && vr >= p.seg[s + 1].row0) ++s;
-    r = vr - p.seg[s].row0;
+// Four consecutive norm weights as fp32 (vector load of the dense dtype).
+DF_DEVICE float4 load_norm4(const void* w, int bf16, int k) {
+  if (bf16) {
+    const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(w) + k);
+    return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                       __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
   }
-  *scale = p.seg[s].scale ? p.seg[s].scale + r : nullptr;
-  return reinterpret_cast<const uint8_t*>(p.seg[s].w) + (size_t)r * p.K * esz;
+  return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(w) + k);
 }
 
-// Activation rows m0..m0+15, columns [xs0, xs0+xlen) -> bf16 hi/lo in shared memory.
+// Activation rows m0..m0+15, columns [xs0, xs0+xlen) -> bf16 hi/lo in shared
+// memory.  Each thread first issues all of its loads (up to kStageVec groups of
+// four elements), then normalises, splits and stores, so one stage costs about
+// one L2 round trip.
+constexpr int kStageVec = 4;
+
 DF_DEVICE void stage_x(const GemmParams& p, uint16_t* xh, uint16_t* xl, int XS,
                        const float* inv_rms, int m0, int xs0, int xlen) {
-  const int q4 = xlen >> 2;
-  for (int idx = threadIdx.x; idx < 16 * q4; idx += blockDim.x) {
-    const int m = idx / q4, c = (idx - m * q4) * 4;
-    const int row = m0 + m, k = xs0 + c;
-    uint2 hi = make_uint2(0, 0), lo = make_uint2(0, 0);
-    if (row < p.M) {
-      if (p.x_mode == X_BF16) {
-        hi = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.x) +
-                                             (size_t)row * p.ldx + k);
-      } else {
-        float4 f = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.x) +
+  const int q4 = xlen >> 2, total = 16 * q4;
+  for (int base = 0; base < total; base += kStageVec * kGemmThreads) {
+    float4 v[kStageVec];
+    float4 w[kStageVec];
+#pragma unroll
+    for (int u = 0; u < kStageVec; ++u) {
+      const int idx = base + u * kGemmThreads + threadIdx.x;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      w[u] = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (idx < total) {
+        const int m = idx / q4, c = (idx - m * q4) * 4;
+        const int row = m0 + m, k = xs0 + c;
+        if (row < p.M) {
+          if (p.x_mode == X_BF16) {
+            const uint2 b = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(p.x) +
+                                                            (size_t)row * p.ldx + k);
+            v[u] = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u),
+                               __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xffff0000u));
+          } else {
+            v[u] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.x) +
                                                     (size_t)row * p.ldx + k);
-        if (p.normw) {
-          const float r = inv_rms[m];
-          f.x = f.x * r * load_dense(p.normw, p.norm_bf16, k + 0);
-          f.y = f.y * r * load_dense(p.normw, p.norm_bf16, k + 1);
-          f.z = f.z * r * load_dense(p.normw, p.norm_bf16, k + 2);
-          f.w = f.w * r * load_dense(p.normw, p.norm_bf16, k + 3);
+          }
         }
-        split_bf16x2(f.x, f.y, hi.x, lo.x);
-        split_bf16x2(f.z, f.w, hi.y, lo.y);
+        if (p.normw) w[u] = load_norm4(p.normw, p.norm_bf16, k);
       }
     }
-    *reinterpret_cast<uint2*>(xh + m * XS + c) = hi;
-    *reinterpret_cast<uint2*>(xl + m * XS + c) = lo;
+#pragma unroll
+    for (int u = 0; u < kStageVec; ++u) {
+      const int idx = base + u * kGemmThreads + threadIdx.x;
+      if (idx >= total) continue;
+      const int m = idx / q4, c = (idx - m * q4) * 4;
+      float4 f = v[u];
+      if (p.normw) {
+        const float r = inv_rms[m];
+        f.x = f.x * r * w[u].x;
+        f.y = f.y * r * w[u].y;
+        f.z = f.z * r * w[u].z;
+        f.w = f.w * r * w[u].w;
+      }
+      uint2 hi, lo;
+      split_bf16x2(f.x, f.y, hi.x, lo.x);
+      split_bf16x2(f.z, f.w, hi.y, lo.y);
+      *reinterpret_cast<uint2*>(xh + m * XS + c) = hi;
+      *reinterpret_cast<uint2*>(xl + m * XS + c) = lo;
+    }
   }
 }
 
@@ -228,190 +242,10 @@ DF_DEVICE void compute_stage(const uint4 (&A)[WTraits<WT>::U][WTraits<WT>::NV],
   }
 }
 
-// ------------------------------------------------------------------ epilogues
-
-DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* scale_s, int mb,
-                             int tile, int* s_flag) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = mb * 16;
-  const bool logits = p.epi == EPI_LOGITS;
-  for (int i = tid; i < 16 * kTileRows; i += blockDim.x) {
-    const int m = i / kTileRows, r = i - m * kTileRows;
-    const int n = tile * kTileRows + r, row = m0 + m;
-    float y = acc_s[i] * scale_s[r];
-    if (n < p.N && row < p.M) {
-      if (p.epi == EPI_RESID_SS) {
-        float* o = p.out + (size_t)row * p.ldo + n;
-        y += *o;
-        *o = y;
-      } else if (p.out) {
-        p.out[(size_t)row * p.ldo + n] = y;
-      }
-    } else {
-      y = logits ? -CUDART_INF_F : 0.f;
-    }
-    acc_s[i] = y;
-  }
-  __syncthreads();
-  if (p.epi == EPI_STORE_SS || p.epi == EPI_RESID_SS) {
-    for (int m = warp; m < 16; m += kGemmThreads / 32) {
-      float s = 0.f;
-      for (int r = lane; r < kTileRows; r += 32) s += acc_s[m * kTileRows + r] * acc_s[m * kTileRows + r];
-      s = warp_sum(s);
-      if (lane == 0 && m0 + m < p.M) p.ss_out[(size_t)tile * p.ss_out_ld + m0 + m] = s;
-    }
-  }
-  if (!logits) return;
-  for (int m = warp; m < 16; m += kGemmThreads / 32) {
-    float v = -CUDART_INF_F;
-    int idx = 0x7fffffff;
-    for (int r = lane; r < kTileRows; r += 32) {
-      const int n = tile * kTileRows + r;
-      if (n < p.N) argmax_merge(v, idx, acc_s[m * kTileRows + r], n);
-    }
-    warp_argmax(v, idx);
-    if (lane == 0 && m0 + m < p.M)
-      p.am_part[(size_t)tile * p.M + m0 + m] = make_float2(v, __int_as_float(idx));
-  }
-  // the last finished tile of the whole launch reduces the argmax partials
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int total = p.n_tiles * p.n_mb;
-    *s_flag = atomicAdd(p.am_counter, 1) == total - 1;
-  }
-  __syncthreads();
-  if (!*s_flag) return;
-  __threadfence();
-  for (int row = warp; row < p.M; row += kGemmThreads / 32) {
-    const int i = row & 15;
-    if (i == 0) continue;
-    float v = -CUDART_INF_F;
-    int idx = 0x7fffffff;
-    for (int tt = lane; tt < p.n_tiles; tt += 32) {
-      const float2 e = __ldcg(p.am_part + (size_t)tt * p.M + row);
-      argmax_merge(v, idx, e.x, __float_as_int(e.y));
-    }
-    warp_argmax(v, idx);
-    if (lane == 0) p.drafts[(row >> 4) * 15 + i - 1] = idx;
-  }
-  if (tid == 0) *p.am_counter = 0;
-}
-
-DF_DEVICE void epilogue_swiglu(const GemmParams& p, const float* acc_s, const float* scale_s,
-                               int mb, int tile) {
-  const int half = kTileRows / 2, F = p.seg[0].rows;
-  for (int i = threadIdx.x; i < 16 * half; i += blockDim.x) {
-    const int m = i / half, j = i - m * half;
-    const int f = tile * half + j, row = mb * 16 + m;
-    if (f >= F || row >= p.M) continue;
-    const float gv = acc_s[m * kTileRows + j] * scale_s[j];
-    const float uv = acc_s[m * kTileRows + half + j] * scale_s[half + j];
-    p.out[(size_t)row * p.ldo + f] = gv / (1.f + expf(-gv)) * uv;
-  }
-}
-
-// Per-head RMSNorm + NEOX rope of q/k (raw v) for the block (EPI_QKV) or for
-// injected context rows scattered into the ring (EPI_INJECT).
-DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const float* scale_s,
-                              int mb, int tile) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hd = p.hd, half = hd >> 1, hpt = kTileRows / hd;
-  for (int item = warp; item < 16 * hpt; item += kGemmThreads / 32) {
-    const int m = item / hpt, hh = item - m * hpt;
-    const int n0 = tile * kTileRows + hh * hd, row = mb * 16 + m;
-    if (n0 >= p.N || row >= p.M) continue;
-    int kind, layer = 0, head = 0;
-    const void* normw;
-    if (p.epi == EPI_QKV) {
-      kind = n0 < p.qd ? 0 : (n0 < p.qd + p.kvd ? 1 : 2);
-      normw = kind == 0 ? p.q_norm : p.k_norm;
-    } else {
-      layer = n0 / (2 * p.kvd);
-      const int w = n0 - layer * 2 * p.kvd;
-      kind = w < p.kvd ? 1 : 2;
-      head = (w - (kind == 2 ? p.kvd : 0)) / hd;
-      normw = p.k_norm_l[layer];
-    }
-    const float* src = acc_s + m * kTileRows + hh * hd;
-    const float* sc = scale_s + hh * hd;
-    float x1[4], x2[4];
-    float ss = 0.f;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = lane + 32 * u;
-      x1[u] = j < half ? src[j] * sc[j] : 0.f;
-      x2[u] = j < half ? src[j + half] * sc[j + half] : 0.f;
-      ss += x1[u] * x1[u] + x2[u] * x2[u];
-    }
-    if (kind != 2) {
-      ss = warp_sum(ss);
-      const float inv = 1.f / sqrtf(ss / (float)hd + p.eps);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = lane + 32 * u;
-        if (j >= half) continue;
-        const float a = x1[u] * inv * load_dense(normw, p.norm_bf16, j);
-        const float b = x2[u] * inv * load_dense(normw, p.norm_bf16, j + half);
-        const float2 cs = p.rope_cs[(size_t)row * half + j];
-        x1[u] = a * cs.x - b * cs.y;
-        x2[u] = b * cs.x + a * cs.y;
-      }
-    }
-    if (p.epi == EPI_QKV) {
-      float* dst = kind == 0 ? p.out + (size_t)row * p.qd + n0
-                 : kind == 1 ? p.kblk + (size_t)row * p.kvd + (n0 - p.qd)
-                             : p.vblk + (size_t)row * p.kvd + (n0 - p.qd - p.kvd);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = lane + 32 * u;
-        if (j < half) {
-          dst[j] = x1[u];
-          dst[j + half] = x2[u];
-        }
-      }
-    } else {
-      const int pos = p.pos[row];
-      if (pos < 0) {
-        if (lane == 0) atomicOr(p.status, 0x2u);
-        continue;
-      }
-      const int slot = pos % p.window;
-      const size_t off =
-          ((((size_t)layer * 2 + (kind == 2)) * p.n_head_kv + head) * p.window + slot) * hd;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = lane + 32 * u;
-        if (j >= half) continue;
-        if (p.ring_bf16) {
-          uint16_t* d = reinterpret_cast<uint16_t*>(p.ring_seq) + off;
-          d[j] = f32_to_bf16_bits(x1[u]);
-          d[j + half] = f32_to_bf16_bits(x2[u]);
-        } else {
-          float* d = reinterpret_cast<float*>(p.ring_seq) + off;
-          d[j] = x1[u];
-          d[j + half] = x2[u];
-        }
-      }
-    }
-  }
-}
-
 // ------------------------------------------------------------------ kernel
 
-// Stream-K schedule: the work is n_items = n_tiles x n_mb output tiles (128
-// weight rows x 16 activation rows), each cut into cpt chunks along k.  The
-// grid is one resident wave; CTA b owns units [U b / G, U (b+1) / G) of the
-// U = n_items * cpt units in item-major order, so every CTA streams the same
-// number of weight bytes and there is no tail wave.  A tile finished inside one
-// CTA goes straight to the epilogue; a tile shared by several CTAs is summed by
-// the last of them (atomic ticket) in CTA order, which keeps results
-// deterministic.  CTA c keeps at most two partial tiles: slot 2c for the tile
-// its range starts inside, slot 2c + 1 for the tile its range ends inside.
-DF_DEVICE long long owner_of(long long u, long long U, int G) { return ((u + 1) * G - 1) / U; }
-
 template <int WT>
-__global__ void __launch_bounds__(kGemmThreads) gemm_rows_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 2) gemm_rows_kernel(const __grid_constant__ GemmParams p) {
   using T = WTraits<WT>;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_flag;
@@ -456,21 +290,19 @@ __global__ void __launch_bounds__(kGemmThreads) gemm_rows_kernel(const __grid_co
       const uint8_t* pa = wa ? wa + (size_t)(xs0 + T::EPL * t) * T::ESZ : nullptr;
       const uint8_t* pb = wb ? wb + (size_t)(xs0 + T::EPL * t) * T::ESZ : nullptr;
       uint4 ra[T::U][T::NV], rb[T::U][T::NV], na[T::U][T::NV], nb[T::U][T::NV];
-      // weights do not depend on the activations: start streaming before staging x
+      // weights do not depend on the activations: pull this stage's rows into L2
+      // and start the register pipeline before staging x (and, for the first
+      // stage, before waiting for the previous kernel)
+      if (lane < 16) {
+        const uint8_t* row = map_row(p, tile, warp * 16 + lane, T::ESZ, &dummy);
+        if (row) prefetch_l2(row + (size_t)xs0 * T::ESZ, (uint32_t)(xlen * T::ESZ));
+      }
       load_stage<WT>(ra, rb, pa, pb, 0, nch);
       if (!waited) {
         pdl_wait();  // everything below may read what earlier kernels wrote
         waited = true;
       }
-      if (xs0 == k0 && tid < 16) {
-        float inv = 1.f;
-        if (p.normw && m0 + tid < p.M) {
-          float sum = 0.f;
-          for (int q = 0; q < p.n_ss; ++q) sum += p.ss[(size_t)q * p.ss_ld + m0 + tid];
-          inv = 1.f / sqrtf(sum / (float)p.K + p.eps);
-        }
-        inv_rms[tid] = inv;
-      }
+      if (xs0 == k0 && p.normw) compute_inv_rms(p, inv_rms, m0);
       __syncthreads();
       stage_x(p, xs_hi, xs_lo, XS, inv_rms, m0, xs0, xlen);
       __syncthreads();
@@ -494,43 +326,8 @@ __global__ void __launch_bounds__(kGemmThreads) gemm_rows_kernel(const __grid_co
     }
     __syncthreads();
 
-    if (c0 != 0 || c1 != p.cpt) {
-      const long long iu0 = (long long)item * p.cpt;
-      const int first = (int)owner_of(iu0, U, G);
-      const int last = (int)owner_of(iu0 + p.cpt - 1, U, G);
-      const size_t slot = 2 * (size_t)b + (b == first ? 1 : 0);
-      float* part = p.partial + slot * (16 * kTileRows);
-      for (int i = tid; i < 16 * kTileRows; i += blockDim.x) part[i] = acc_s[i];
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) s_flag = atomicAdd(p.counters + item, 1) == last - first;
-      __syncthreads();
-      if (!s_flag) continue;
-      __threadfence();
-      for (int i = tid; i < 16 * kTileRows; i += blockDim.x) {
-        float sum = 0.f;
-        for (int c = first; c <= last; ++c) {
-          const size_t sl = 2 * (size_t)c + (c == first ? 1 : 0);
-          sum += __ldcg(p.partial + sl * (16 * kTileRows) + i);
-        }
-        acc_s[i] = sum;
-      }
-      if (tid == 0) p.counters[item] = 0;
-      __syncthreads();
-    }
-
-    switch (p.epi) {
-      case EPI_SWIGLU:
-        epilogue_swiglu(p, acc_s, scale_s, mb, tile);
-        break;
-      case EPI_QKV:
-      case EPI_INJECT:
-        epilogue_heads(p, acc_s, scale_s, mb, tile);
-        break;
-      default:
-        epilogue_rows(p, acc_s, scale_s, mb, tile, &s_flag);
-        break;
-    }
+    if (!segment_fixup(p, acc_s, item, c0, c1, U, G, b, &s_flag)) continue;
+    run_epilogue(p, acc_s, scale_s, inv_rms, mb, tile, &s_flag);
   }
 }
 
@@ -556,7 +353,7 @@ static cudaError_t launch_t(const GemmParams& p, cudaStream_t st) {
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_rows_kernel<WT>, p);

@@ -1,0 +1,395 @@
+// Projection kernel of the block step fed by the Tensor Memory Accelerator.
+//
+// Same contract as gemm_rows_kernel (y[m][n] = sum_k x[m][k] W[n][k] for 16-row
+// activation blocks, stream-K split, fused epilogues) for activations that
+// their producer already stored as bf16 hi + lo pairs.  Warp 8 is a producer:
+// one lane walks this CTA's stream-K units and, per k chunk (128 bytes of every
+// weight row), issues cp.async.bulk.tensor loads of the 128 weight rows (eight
+// 16-row boxes, each from the segment's own tensor map) and of the 16 activation
+// rows (hi and lo) into a ring of shared-memory stages, completing on the
+// stage's "full" mbarrier.  Warps 0..7 are consumers: each owns 16 weight rows,
+// reads its A fragments and the shared B fragments with ldmatrix from the
+// 128-byte-swizzled tiles, runs mma.sync m16n8k16 (fp32 accumulation), and
+// releases the stage on its "empty" mbarrier.  The first stages' weight loads
+// are issued before griddepcontrol.wait, so they overlap the previous kernel.
+// Every mbarrier wait gives up after ~2 s, sets the device status bit
+// DFLASH_DEV_TIMEOUT and lets the CTA run to completion without further waits;
+// before exiting, the producer waits (with the same bound) for its last copies.
+#include "gemm_common.cuh"
+
+namespace dflash {
+
+template <int WT>
+struct TT;
+template <>
+struct TT<W_BF16> {  // 64 k per chunk: one 128-byte weight box, one activation box
+  static constexpr int CK = 64, WBOX_K = 64, WBOXES = 1, XBOXES = 1, S = 4, STEPS = 4;
+};
+template <>
+struct TT<W_F32> {   // 64 k per chunk: two 128-byte weight boxes of 32 fp32
+  static constexpr int CK = 64, WBOX_K = 32, WBOXES = 2, XBOXES = 1, S = 2, STEPS = 4;
+};
+template <>
+struct TT<W_FP8> {   // 128 k per chunk: one 128-byte E4M3 box, two activation boxes
+  static constexpr int CK = 128, WBOX_K = 128, WBOXES = 1, XBOXES = 2, S = 4, STEPS = 8;
+};
+
+constexpr int kBox = 16 * 128;  // one 16-row x 128-byte box
+constexpr long long kWaitCycles = 4000000000LL;
+
+template <int WT>
+struct Layout {
+  static constexpr int W_BYTES = 8 * kBox * TT<WT>::WBOXES;
+  static constexpr int X_BYTES = kBox * TT<WT>::XBOXES;  // one of hi / lo
+  static constexpr int STAGE = W_BYTES + 2 * X_BYTES;
+  static constexpr int ACC = TT<WT>::S * STAGE;
+  static constexpr int INV = ACC + 16 * kTileRows * 4;
+  static constexpr int SCALE = INV + 16 * 4;
+  static constexpr int BARS = SCALE + kTileRows * 4;
+  static constexpr int TOTAL = BARS + 2 * TT<WT>::S * 8 + 1024;  // + alignment slack
+};
+
+size_t gemm_tma_smem_bytes(int wt) {
+  switch (wt) {
+    case W_F32: return Layout<W_F32>::TOTAL;
+    case W_BF16: return Layout<W_BF16>::TOTAL;
+    case W_FP8: return Layout<W_FP8>::TOTAL;
+  }
+  return 0;
+}
+
+// ------------------------------------------------------------------ primitives
+
+DF_DEVICE uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+DF_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(bar)), "r"(count) : "memory");
+}
+DF_DEVICE void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes)
+               : "memory");
+}
+DF_DEVICE void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
+}
+DF_DEVICE bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(su32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for completion of the phase with this parity; false after ~2 s.
+DF_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return false;
+  return true;
+}
+
+DF_DEVICE void tma_load(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+
+DF_DEVICE void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(su32(p)));
+}
+
+// byte offset of (row, 16-byte chunk) inside a 128-byte-swizzled box
+DF_DEVICE int swz(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
+
+// ------------------------------------------------------------------ consumer math
+
+template <int WT>
+struct Consume;
+
+// B fragments (two n8 tiles) of k16 step `kc2` (16-byte chunk pair index) from
+// one activation box
+DF_DEVICE void x_frags(uint32_t (&b)[4], const uint8_t* box, int kchunk0, int lane) {
+  const int lmat = lane >> 3, lrow = lane & 7;
+  const int row = (lmat >> 1) * 8 + lrow, chunk = kchunk0 + (lmat & 1);
+  ldsm_x4(b, box + swz(row, chunk));
+}
+
+template <>
+struct Consume<W_BF16> {
+  static DF_DEVICE void run(const uint8_t* w, const uint8_t* xh, const uint8_t* xl, bool has_lo,
+                            int lane, float (&acc)[2][4]) {
+    const int lmat = lane >> 3, lrow = lane & 7;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t a[4], b[4];
+      const int arow = (lmat & 1) * 8 + lrow;
+      ldsm_x4(a, w + swz(arow, 2 * s + (lmat >> 1)));
+      x_frags(b, xh, 2 * s, lane);
+      mma_bf16_16816(acc[0], a, b[0], b[1]);
+      mma_bf16_16816(acc[1], a, b[2], b[3]);
+      if (has_lo) {
+        x_frags(b, xl, 2 * s, lane);
+        mma_bf16_16816(acc[0], a, b[0], b[1]);
+        mma_bf16_16816(acc[1], a, b[2], b[3]);
+      }
+    }
+  }
+};
+
+template <>
+struct Consume<W_FP8> {
+  static DF_DEVICE void run(const uint8_t* w, const uint8_t* xh, const uint8_t* xl, bool has_lo,
+                            int lane, float (&acc)[2][4]) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      // E4M3 pairs (k = 16s + 2t and + 8) of rows g and g + 8, widened to bf16
+      const uint16_t q0 = *reinterpret_cast<const uint16_t*>(w + swz(g, s) + 2 * t);
+      const uint16_t q1 = *reinterpret_cast<const uint16_t*>(w + swz(g + 8, s) + 2 * t);
+      const uint16_t q2 = *reinterpret_cast<const uint16_t*>(w + swz(g, s) + 2 * t + 8);
+      const uint16_t q3 = *reinterpret_cast<const uint16_t*>(w + swz(g + 8, s) + 2 * t + 8);
+      const uint32_t a[4] = {e4m3x2_to_bf16x2(q0), e4m3x2_to_bf16x2(q1), e4m3x2_to_bf16x2(q2),
+                             e4m3x2_to_bf16x2(q3)};
+      uint32_t b[4];
+      x_frags(b, xh + (s >> 2) * kBox, 2 * (s & 3), lane);
+      mma_bf16_16816(acc[0], a, b[0], b[1]);
+      mma_bf16_16816(acc[1], a, b[2], b[3]);
+      if (has_lo) {
+        x_frags(b, xl + (s >> 2) * kBox, 2 * (s & 3), lane);
+        mma_bf16_16816(acc[0], a, b[0], b[1]);
+        mma_bf16_16816(acc[1], a, b[2], b[3]);
+      }
+    }
+  }
+};
+
+template <>
+struct Consume<W_F32> {
+  static DF_DEVICE void run(const uint8_t* w, const uint8_t* xh, const uint8_t* xl, bool has_lo,
+                            int lane, float (&acc)[2][4]) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      // fp32 pairs of rows g, g + 8 at k = 16s + 2t (+8): box s/2, byte 64(s&1) + 8t (+32)
+      const uint8_t* bx = w + (s >> 1) * kBox;
+      const int byte0 = 64 * (s & 1) + 8 * t, byte1 = byte0 + 32;
+      const float2 f0 = *reinterpret_cast<const float2*>(bx + swz(g, byte0 >> 4) + (byte0 & 15));
+      const float2 f1 = *reinterpret_cast<const float2*>(bx + swz(g + 8, byte0 >> 4) + (byte0 & 15));
+      const float2 f2 = *reinterpret_cast<const float2*>(bx + swz(g, byte1 >> 4) + (byte1 & 15));
+      const float2 f3 = *reinterpret_cast<const float2*>(bx + swz(g + 8, byte1 >> 4) + (byte1 & 15));
+      uint32_t ah[4], al[4];
+      split_bf16x2(f0.x, f0.y, ah[0], al[0]);
+      split_bf16x2(f1.x, f1.y, ah[1], al[1]);
+      split_bf16x2(f2.x, f2.y, ah[2], al[2]);
+      split_bf16x2(f3.x, f3.y, ah[3], al[3]);
+      uint32_t b[4];
+      x_frags(b, xh, 2 * s, lane);
+      mma_bf16_16816(acc[0], ah, b[0], b[1]);
+      mma_bf16_16816(acc[1], ah, b[2], b[3]);
+      mma_bf16_16816(acc[0], al, b[0], b[1]);
+      mma_bf16_16816(acc[1], al, b[2], b[3]);
+      if (has_lo) {
+        x_frags(b, xl, 2 * s, lane);
+        mma_bf16_16816(acc[0], ah, b[0], b[1]);
+        mma_bf16_16816(acc[1], ah, b[2], b[3]);
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+
+// Tensor-map index and row coordinate of 16-row group `grp` of `tile`: rows past
+// the matrix are addressed out of bounds, which the copy fills with zeros.
+DF_DEVICE void group_coord(const GemmParams& p, int tile, int grp, int& map, int& row) {
+  if (p.map == MAP_SWIGLU) {
+    map = grp < 4 ? 0 : 1;
+    row = tile * (kTileRows / 2) + (grp & 3) * 16;
+    return;
+  }
+  const int vr = tile * kTileRows + grp * 16;
+  int s = 0;
+  while (s + 1 < p.nseg && vr >= p.seg[s + 1].row0) ++s;
+  map = s;
+  row = vr - p.seg[s].row0;
+}
+
+template <int WT>
+__global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __grid_constant__ GemmParams p) {
+  using T = TT<WT>;
+  using Lt = Layout<WT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* acc_s = reinterpret_cast<float*>(sm + Lt::ACC);
+  float* inv_rms = reinterpret_cast<float*>(sm + Lt::INV);
+  float* scale_s = reinterpret_cast<float*>(sm + Lt::SCALE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + Lt::BARS);
+  uint64_t* empty = full + T::S;
+  __shared__ int s_flag;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < T::S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 8);
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  const int G = gridDim.x, b = blockIdx.x;
+  const long long U = (long long)p.n_tiles * p.n_mb * p.cpt;
+  const long long ub0 = U * b / G, ub1 = U * (b + 1) / G;
+  const bool has_lo = p.has_lo != 0;
+  const uint32_t stage_bytes = Lt::W_BYTES + Lt::X_BYTES * (has_lo ? 2 : 1);
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    long long it = 0;
+    bool waited = false;
+    for (long long u = ub0; u < ub1 && !s_abort;) {
+      const int item = (int)(u / p.cpt);
+      const int c0 = (int)(u - (long long)item * p.cpt);
+      const int c1 = (int)min((long long)p.cpt, c0 + (ub1 - u));
+      u += c1 - c0;
+      const int tile = item / p.n_mb, mb = item - tile * p.n_mb;
+      int gmap[8], grow[8];
+#pragma unroll
+      for (int grp = 0; grp < 8; ++grp) group_coord(p, tile, grp, gmap[grp], grow[grp]);
+      for (int c = c0; c < c1; ++c, ++it) {
+        const int st = (int)(it % T::S);
+        const uint32_t ph = (uint32_t)((it / T::S) & 1);
+        if (!mbar_wait(&empty[st], ph ^ 1)) {
+          atomicOr(p.status, 0x4u);
+          s_abort = 1;
+          break;
+        }
+        uint8_t* dst = sm + st * Lt::STAGE;
+        const int k = c * T::CK;
+        mbar_expect_tx(&full[st], stage_bytes);
+#pragma unroll
+        for (int grp = 0; grp < 8; ++grp)
+#pragma unroll
+          for (int wb = 0; wb < T::WBOXES; ++wb)
+            tma_load(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]], k + wb * T::WBOX_K,
+                     grow[grp], &full[st]);
+        if (!waited) {  // activations may come from the previous kernel
+          pdl_wait();
+          waited = true;
+        }
+#pragma unroll
+        for (int xb = 0; xb < T::XBOXES; ++xb) {
+          tma_load(dst + Lt::W_BYTES + xb * kBox, &p.tm_xh, k + xb * 64, mb * 16, &full[st]);
+          if (has_lo)
+            tma_load(dst + Lt::W_BYTES + Lt::X_BYTES + xb * kBox, &p.tm_xl, k + xb * 64, mb * 16,
+                     &full[st]);
+        }
+      }
+    }
+    // no copy may still be landing when the CTA exits: wait for the last stages
+    for (long long j = it > T::S ? it - T::S : 0; j < it; ++j) {
+      if (!mbar_wait(&full[j % T::S], (uint32_t)((j / T::S) & 1))) {
+        atomicOr(p.status, 0x4u);
+        break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  pdl_wait();
+  long long it = 0;
+  for (long long u = ub0; u < ub1;) {
+    const int item = (int)(u / p.cpt);
+    const int c0 = (int)(u - (long long)item * p.cpt);
+    const int c1 = (int)min((long long)p.cpt, c0 + (ub1 - u));
+    u += c1 - c0;
+    const int tile = item / p.n_mb, mb = item - tile * p.n_mb;
+    csync();  // the previous segment is done with acc_s / scale_s / inv_rms
+    if (tid < kTileRows) {
+      const float* sc = nullptr;
+      const uint8_t* r = map_row(p, tile, tid, 1, &sc);
+      scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
+    }
+    if (p.row_scale) compute_inv_rms(p, inv_rms, mb * 16);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    for (int c = c0; c < c1; ++c, ++it) {
+      const int st = (int)(it % T::S);
+      if (!s_abort) {
+        if (mbar_wait(&full[st], (uint32_t)((it / T::S) & 1))) {
+          const uint8_t* base = sm + st * Lt::STAGE;
+          Consume<WT>::run(base + warp * T::WBOXES * kBox, base + Lt::W_BYTES,
+                           base + Lt::W_BYTES + Lt::X_BYTES, has_lo, lane, acc);
+        } else {
+          if (lane == 0) atomicOr(p.status, 0x4u);
+          s_abort = 1;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int cc = 8 * j + 2 * t, r = warp * 16 + g;
+      acc_s[cc * kTileRows + r] = acc[j][0];
+      acc_s[(cc + 1) * kTileRows + r] = acc[j][1];
+      acc_s[cc * kTileRows + r + 8] = acc[j][2];
+      acc_s[(cc + 1) * kTileRows + r + 8] = acc[j][3];
+    }
+    csync();
+    if (!segment_fixup(p, acc_s, item, c0, c1, U, G, b, &s_flag)) continue;
+    run_epilogue(p, acc_s, scale_s, inv_rms, mb, tile, &s_flag);
+  }
+}
+
+cudaError_t configure_gemm_tma() {
+  cudaError_t e = cudaFuncSetAttribute(gemm_tma_kernel<W_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)gemm_tma_smem_bytes(W_F32));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tma_kernel<W_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gemm_tma_smem_bytes(W_BF16));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tma_kernel<W_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)gemm_tma_smem_bytes(W_FP8));
+  return e;
+}
+
+template <int WT>
+static cudaError_t launch_tma_t(const GemmParams& p, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(kGemmThreads + 32);
+  cfg.dynamicSmemBytes = gemm_tma_smem_bytes(WT);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tma_kernel<WT>, p);
+}
+
+cudaError_t launch_gemm_tma(int wt, const GemmParams& p, cudaStream_t st) {
+  switch (wt) {
+    case W_F32: return launch_tma_t<W_F32>(p, st);
+    case W_BF16: return launch_tma_t<W_BF16>(p, st);
+    case W_FP8: return launch_tma_t<W_FP8>(p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int tma_chunk_k(int wt) { return wt == W_FP8 ? 128 : 64; }
+
+}  // namespace dflash

@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer and the kernels of libdflash.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -23,6 +24,12 @@ enum Epi {
 };
 enum RowMap { MAP_SEGMENTS = 0, MAP_SWIGLU = 1 };
 
+// Programmatic dependent launch between the step's kernels.  Measured slower
+// than plain stream order inside the replayed graph (2.18 vs 1.78 ms per
+// real-dimension step), so launches do not request it; the kernels keep their
+// griddepcontrol points, which are no-ops without the launch attribute.
+constexpr bool kDependentLaunch = false;
+
 constexpr int kTileRows = 128;     // output rows (weight rows) of one CTA tile
 constexpr int kGemmThreads = 256;  // 8 warps x 16 weight rows
 constexpr int kMaxSeg = 2 * 16;
@@ -36,20 +43,29 @@ struct GemmSeg {
 };
 
 struct GemmParams {
+  // TMA path: tensor maps of the weight segments and of the activation pair
+  CUtensorMap tm_w[4];
+  CUtensorMap tm_xh;
+  CUtensorMap tm_xl;
+  int has_lo;
   // activations: x[m][k], m < M, row stride ldx (elements)
   const void* x;
   int x_mode;
   int ldx;
   int M;
   int K;
-  // optional RMSNorm prologue: x[m][k] * inv_rms[m] * normw[k], with
-  // inv_rms[m] = 1 / sqrt(sum_p ss[p * ss_ld + m] / K + eps)
+  // RMSNorm of the activation rows: inv_rms[m] = 1 / sqrt(sum_p ss[p * ss_ld + m]
+  // / rms_len + eps).  Raw inputs apply x * inv_rms * normw while staging; pre-split
+  // inputs (x = h * normw, made by the producer) apply inv_rms to the output rows
+  // (row_scale).
   const float* ss;
   int n_ss;
   int ss_ld;
+  int rms_len;
   const void* normw;
   int norm_bf16;
   float eps;
+  int row_scale;
   // weights
   GemmSeg seg[kMaxSeg];
   int nseg;
@@ -69,6 +85,12 @@ struct GemmParams {
   int ldo;
   float* ss_out;
   int ss_out_ld;
+  // bf16 hi/lo pair output for the next projection (EPI_RESID_SS: split(out * pair_norm);
+  // EPI_SWIGLU: split(silu(g) u)), row stride pair_ld
+  uint16_t* pair_hi;
+  uint16_t* pair_lo;
+  int pair_ld;
+  const void* pair_norm;
   // q/k/v epilogues
   float* kblk;
   float* vblk;
@@ -104,12 +126,18 @@ struct AttnParams {
   float scale;
   float* part_acc;        // [n_seq][Hkv][n_chunks+1][R][hd]
   float* part_ml;         // [n_seq][Hkv][n_chunks+1][R][2]
-  float* out;             // [M][qd]
+  uint16_t* out_hi;       // [M][qd] bf16 hi/lo pair (the o projection's input)
+  uint16_t* out_lo;
 };
 
 size_t gemm_smem_bytes(int wt, int xk);
 cudaError_t configure_gemm(int xk_max);
 cudaError_t launch_gemm(int wt, const GemmParams& p, cudaStream_t st);
+
+size_t gemm_tma_smem_bytes(int wt);
+cudaError_t configure_gemm_tma();
+cudaError_t launch_gemm_tma(int wt, const GemmParams& p, cudaStream_t st);
+int tma_chunk_k(int wt);   // k per pipeline stage of the TMA projection kernel
 
 size_t attn_smem_bytes(int group, int hd, int ring_f32);
 cudaError_t configure_attention(size_t smem);
@@ -119,7 +147,8 @@ cudaError_t launch_attn_combine(const AttnParams& p, int n_seq, cudaStream_t st)
 cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
                          const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
-                         unsigned* status, cudaStream_t st);
+                         const void* norm0, uint16_t* x_hi, uint16_t* x_lo, unsigned* status,
+                         cudaStream_t st);
 cudaError_t launch_rope_table(const int32_t* pos, int T, const double* inv_freq, int hd,
                               float2* rope_cs, int32_t* ring_pos, int window, unsigned* status,
                               cudaStream_t st);

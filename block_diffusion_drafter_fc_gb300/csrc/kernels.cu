@@ -19,7 +19,9 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
                                                     int V, int mask_token, const int32_t* id_last,
                                                     const int32_t* n_past, int n_seq,
                                                     const double* inv_freq, int half, float* h,
-                                                    float* ss, float2* rope_cs, unsigned* status) {
+                                                    float* ss, float2* rope_cs, const void* norm0,
+                                                    uint16_t* x_hi, uint16_t* x_lo,
+                                                    unsigned* status) {
   const int M = n_seq * kBlock;
   if ((int)blockIdx.x < M) {
     const int m = blockIdx.x, seq = m / kBlock, i = m % kBlock;
@@ -28,11 +30,55 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
       if (threadIdx.x == 0) atomicOr(status, 0x1u);
       tok = tok < 0 ? 0 : V - 1;
     }
+    // 8 elements per thread and round (one 16-byte bf16 load or two float4
+    // loads), all loads of a round issued before any store
     float s = 0.f;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) {
-      const float v = load_dense(tok_embd, dense_bf16, (size_t)tok * d + k);
-      h[(size_t)m * d + k] = v;
-      s += v * v;
+    constexpr int kRound = 4;
+    for (int k0 = threadIdx.x * 8; k0 < d; k0 += kRound * (int)blockDim.x * 8) {
+      float v[kRound][8];
+#pragma unroll
+      for (int r = 0; r < kRound; ++r) {
+        const int k = k0 + r * blockDim.x * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[r][e] = 0.f;
+        if (k >= d) continue;
+        if (dense_bf16) {
+          const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(tok_embd) +
+                                                         (size_t)tok * d + k);
+          const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[r][2 * e] = __uint_as_float(w[e] << 16);
+            v[r][2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(tok_embd) +
+                                                              (size_t)tok * d + k);
+          const float4 a = src[0], b = src[1];
+          v[r][0] = a.x; v[r][1] = a.y; v[r][2] = a.z; v[r][3] = a.w;
+          v[r][4] = b.x; v[r][5] = b.y; v[r][6] = b.z; v[r][7] = b.w;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kRound; ++r) {
+        const int k = k0 + r * blockDim.x * 8;
+        if (k >= d) continue;
+        float4* dst = reinterpret_cast<float4*>(h + (size_t)m * d + k);
+        dst[0] = make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
+        dst[1] = make_float4(v[r][4], v[r][5], v[r][6], v[r][7]);
+        // first layer's projection input: h * attn_norm, split into bf16 hi + lo
+        uint32_t hh[4], ll[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float z0 = v[r][2 * e] * load_dense(norm0, dense_bf16, k + 2 * e);
+          const float z1 = v[r][2 * e + 1] * load_dense(norm0, dense_bf16, k + 2 * e + 1);
+          split_bf16x2(z0, z1, hh[e], ll[e]);
+        }
+        *reinterpret_cast<uint4*>(x_hi + (size_t)m * d + k) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+        *reinterpret_cast<uint4*>(x_lo + (size_t)m * d + k) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += v[r][e] * v[r][e];
+      }
     }
     __shared__ float red[8];
     s = warp_sum(s);
@@ -61,11 +107,13 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
 cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
                          const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
-                         unsigned* status, cudaStream_t st) {
+                         const void* norm0, uint16_t* x_hi, uint16_t* x_lo, unsigned* status,
+                         cudaStream_t st) {
   const int M = n_seq * kBlock, half = hd / 2;
   const int tb = (M * half + 255) / 256;
   embed_kernel<<<M + tb, 256, 0, st>>>(tok_embd, dense_bf16, n_embd, n_vocab, mask_token, id_last,
-                                       n_past, n_seq, inv_freq, half, h, ss, rope_cs, status);
+                                       n_past, n_seq, inv_freq, half, h, ss, rope_cs, norm0, x_hi,
+                                       x_lo, status);
   return cudaGetLastError();
 }
 
@@ -392,7 +440,7 @@ static cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cfg;
@@ -441,7 +489,11 @@ __global__ void __launch_bounds__(512) attn_combine_kernel(const __grid_constant
     L += e.y * w;
     A += o * w;
   }
-  p.out[(size_t)(seq * kBlock + i) * (p.n_head * hd) + h * hd + d] = A / L;
+  const float o = A / L;
+  const size_t at = (size_t)(seq * kBlock + i) * (p.n_head * hd) + h * hd + d;
+  const uint16_t oh = f32_to_bf16_bits(o);
+  p.out_hi[at] = oh;
+  p.out_lo[at] = f32_to_bf16_bits(o - bf16_bits_to_f32(oh));
 }
 
 cudaError_t launch_attn_combine(const AttnParams& p, int n_seq, cudaStream_t st) {

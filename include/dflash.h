@@ -70,6 +70,7 @@ typedef enum {
 /* Bits of the device status word (dflash_read_status). */
 #define DFLASH_DEV_BAD_TOKEN 0x1u     /* an id_last outside [0, n_vocab): clamped */
 #define DFLASH_DEV_BAD_POSITION 0x2u  /* a negative inject position or n_past: row skipped */
+#define DFLASH_DEV_TIMEOUT 0x4u       /* a pipeline wait gave up after ~2 s: outputs invalid */
 
 /*
  * Drafter geometry and storage formats.
@@ -169,8 +170,8 @@ DFLASH_API int dflash_workspace_size(const dflash_config* cfg, size_t* ring_byte
 /*
  * Build a handle: validate the configuration, compute the host fp64 rope
  * inverse-frequency table theta^(-2j/head_dim) (dflash-ops model card, Method),
- * copy it into scratch, clear counters and the status word, and mark every
- * ring slot empty (ring_pos = -1).  Synchronous.  `w` is copied (the pointer
+ * copy it into scratch, clear counters and the status word, zero the ring K/V
+ * and mark every ring slot empty (ring_pos = -1).  Synchronous.  `w` is copied (the pointer
  * values, not the weights).  ring_mem and scratch_mem are device areas of at
  * least the dflash_workspace_size sizes.  On success *out receives the handle.
  */
@@ -257,7 +258,7 @@ DFLASH_API int dflash_replay(dflash_handle* h, void* stream);
 DFLASH_API int dflash_step_host(dflash_handle* h, int32_t n_seq, const int32_t* id_last,
                      const int32_t* n_past, float* logits, int32_t* drafts, void* stream);
 
-/* Mark every slot of sequence `seq`'s ring empty (ring_pos = -1), on `stream`. */
+/* Zero sequence `seq`'s ring K/V and mark every slot empty (ring_pos = -1), on `stream`. */
 DFLASH_API int dflash_ring_reset(dflash_handle* h, int32_t seq, void* stream);
 
 /*

@@ -67,7 +67,8 @@ def compare_drafts(gpu_logits, gpu_drafts, ref_logits, ref_drafts, err):
     than twice the measured logit error; inside that band (a near tie the two
     precisions may order differently) the GPU's token must be one of the
     oracle's two best.  The GPU's drafts must always be the argmax of its own
-    logits (lowest index on ties)."""
+    logits (lowest index on ties).  Returns the number of positions whose token
+    differs from the oracle's (0 unless a near tie flipped)."""
     own = np.argmax(gpu_logits[:, 1:, :], axis=-1)
     assert np.array_equal(own, gpu_drafts), "drafts are not the argmax of the GPU logits"
     r32 = ref_logits.astype(np.float32)[:, 1:, :]
@@ -80,7 +81,8 @@ def compare_drafts(gpu_logits, gpu_drafts, ref_logits, ref_drafts, err):
         amb = np.nonzero(~clear)
         for s, j in zip(*amb):
             assert gpu_drafts[s, j] in best2[s, j], (s, j)
-    return int((~clear).sum())
+    # positions where the tokens actually differ (only possible inside the band)
+    return int((gpu_drafts != ref_drafts).sum())
 
 
 def ring_ulps(gpu_vals: np.ndarray, ref_raw: np.ndarray, dtype: str) -> np.ndarray:

@@ -33,24 +33,43 @@ def _case(name):
     return wl, ref, gpu
 
 
-def _check_ring(wl, ref, gpu):
+def ring_stats(wl, ref, gpu):
+    """Per sequence and K/V: positions equal, and error statistics of the stored
+    values against the oracle's (in units of the tensor's max magnitude and in
+    units in the last place of the ring dtype)."""
+    from oracle import dflash_oracle as O
     cfg = wl.cfg
+    out = []
     for s in range(cfg.n_seq):
         assert np.array_equal(gpu["ring_pos"][s], ref["rings"][s].pos), f"ring_pos seq {s}"
         filled = ref["rings"][s].pos >= 0
         for name, gk, rk in (("K", gpu["ring_k"][s], ref["rings"][s].k),
                              ("V", gpu["ring_v"][s], ref["rings"][s].v)):
-            from oracle import dflash_oracle as O
             refv = O.decode(rk, cfg.ring_dtype)[:, :, filled, :]
             g = gk[:, :, filled, :].astype(np.float64)
             scale = float(np.abs(refv).max())
-            # bf16: one unit in the last place of the larger magnitude (8 significant
-            # bits); f32: 16 units (fp32 arithmetic error ahead of the final
-            # rounding); plus 1e-5 of the tensor's scale for values near zero
+            d = np.abs(g - refv)
             _, e = np.frexp(np.maximum(np.abs(g), np.abs(refv)))
-            bits = 8.0 if cfg.ring_dtype == "bf16" else 20.0
-            bad = np.abs(g - refv) > np.exp2(e - bits) + 1e-5 * scale
-            assert not bad.any(), f"ring {name} seq {s}: {int(bad.sum())} elements off"
+            ulp = np.exp2(e - (8.0 if cfg.ring_dtype == "bf16" else 24.0))
+            # per element: one bf16 unit (bf16 ring), or 2^-12 of the tensor's scale.
+            # The GPU value ahead of the final rounding carries the error of two
+            # chained fp32-emulating projections (fc, then wk/wv: each product split
+            # to 16 significant bits, ~2^-16 of the output's scale per projection),
+            # and the largest of ~10^7 elements sits ~4 sigma out: 2^-12 bounds it.
+            allow = np.maximum(ulp if cfg.ring_dtype == "bf16" else 0.0, 2.0 ** -12 * scale)
+            out.append(dict(seq=s, name=name, max_rel_scale=float(d.max() / scale),
+                            max_ulps=float((d / ulp).max()), frac_differ=float((d > 0).mean()),
+                            n_bad=int((d > allow).sum()), n=int(d.size)))
+    return out
+
+
+def _check_ring(wl, ref, gpu):
+    """bf16 ring: each stored value within one bf16 unit of the oracle's, or
+    within 2^-12 of the tensor's largest magnitude (the fp32 arithmetic's error
+    ahead of the final rounding, which moves values near zero by more than one
+    of their own units).  fp32 ring: within 2^-12 of the tensor's scale."""
+    for st in ring_stats(wl, ref, gpu):
+        assert st["n_bad"] == 0, f"ring {st}"
 
 
 @pytest.mark.parametrize("name", SMALL)
