@@ -192,6 +192,35 @@ DFLASH_API void dflash_destroy(dflash_handle* h);
 DFLASH_API int dflash_encode(dflash_handle* h, const void* feats, int32_t T, float* H_t, void* stream);
 
 /*
+ * dflash_encode for callers that cannot allocate device memory.  No page
+ * defines this call; it exists for code that may not call cudaMalloc (an
+ * allocator-free runtime, a plug-in limited to the buffers it is handed, a host
+ * whose device memory is all owned by a pool) and therefore cannot provide the
+ * scratch area dflash_create needs.  It computes exactly what dflash_encode
+ * computes with the same kernels, without a handle:
+ *   cfg:        geometry (n_embd, n_target_layers, target_embd, dense_dtype, eps;
+ *               other fields are not read);
+ *   fc:         device [n_embd][n_target_layers*target_embd], dense_dtype;
+ *   hidden_norm: device [n_embd], dense_dtype;
+ *   feats:      device [T][n_target_layers*target_embd], dense_dtype;
+ *   H_t:        device f32 [T][n_embd], written (it also holds the intermediate
+ *               un-normalised projection during the call).
+ * Its intermediate memory is one 8 MiB file-scope __device__ array that every
+ * GPU loading this library holds until the process exits.  Limits: with
+ * tiles = ceil(n_embd / 128), tiles * ceil(T / 16) <= 16384 and
+ * tiles * T <= 835,584 (T <= 5040 at n_embd 6656); larger calls return
+ * DFLASH_ERR_TOO_MANY_ROWS and launch nothing.  The first call on a device looks
+ * up the array's device address and sets kernel attributes for that device
+ * (the device current at the call); make that first call before any stream
+ * capture.  Nothing is allocated or freed, by this library or any library it
+ * calls.  All calls share the array: calls that overlap on the GPU (on
+ * different streams, or from different threads) race; it is cleared where it
+ * must start at zero at the start of every call.  Asynchronous on `stream`.
+ */
+DFLASH_API int dflash_encode_noalloc(const dflash_config* cfg, const void* fc, const void* hidden_norm,
+                                     const void* feats, int32_t T, float* H_t, void* stream);
+
+/*
  * Inject encoded rows into sequence `seq`'s ring (dflash-ops model card, Method
  * and Requirements): for every layer l and row t,
  *   K = rope(RMSNorm_head(H_t[t] wk_l^T) * k_norm_l, pos[t]),  V = H_t[t] wv_l^T,
