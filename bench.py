@@ -168,7 +168,7 @@ def run_ours(args, rank, world, local):
     targets = torch.from_numpy(make_targets(drafts.cpu().numpy(), wl.mismatch.numpy(),
                                             wl.tail.numpy(), cfg.n_vocab)).to(dev)
     dr.dflash_capture(id_last, n_past, logits, drafts, targets, n_ok)
-    launches_per_step = 2 + 6 * cfg.n_layer + 1
+    launches_per_step = 5 * cfg.n_layer + 3   # embed, 5 per layer, LM head, accept
 
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -249,7 +249,7 @@ def run_ours(args, rank, world, local):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": committed_traffic(cfg.name, dom),
                      "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": cb[dom],
-                     "avg_launch_us": round(dom_ms / dom_n * 1e3, 2)},
+                     "avg_launch_us": round(dom_ms / dom_n * 1e3, 2) if dom_n else None},
         "kernel_classes_us_per_step": {k: round(v[0] / max(1, args.profile_steps) * 1e3, 2)
                                        for k, v in prof.items() if v[1]},
         "gpu_launches": launches_per_step * args.steps,

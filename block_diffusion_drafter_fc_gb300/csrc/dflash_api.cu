@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <new>
 #include <vector>
 
@@ -185,9 +186,11 @@ int validate(const dflash_config* c) {
   const int qd = c->n_head * c->head_dim;
   if (c->n_embd % kc || qd % kc || c->n_ff % kc) return DFLASH_ERR_UNSUPPORTED;
   if ((c->n_target_layers * c->target_embd) % 32) return DFLASH_ERR_UNSUPPORTED;
-  if (c->n_head / c->n_head_kv > 16) return DFLASH_ERR_UNSUPPORTED;
-  // the attention CTA keeps a whole kv group's queries and one key chunk on chip
-  if (attn_smem_bytes(c->n_head / c->n_head_kv, c->head_dim, 1) > 227 * 1024)
+  // one warp per query head of a kv group in the attention CTA
+  if (c->n_head / c->n_head_kv > 8) return DFLASH_ERR_UNSUPPORTED;
+  // the attention CTA's staging must fit one SM's shared memory (227 KB per block)
+  if (attn_cluster_smem(c->n_head / c->n_head_kv, c->head_dim, c->ring_dtype == DFLASH_DTYPE_F32, 0) >
+      232448)
     return DFLASH_ERR_UNSUPPORTED;
   return DFLASH_OK;
 }
@@ -206,6 +209,11 @@ struct dflash_handle {
   CUtensorMap tm_layer[DFLASH_MAX_LAYERS][7];
   CUtensorMap tm_lm;
   CUtensorMap tm_xn[2], tm_attn[2], tm_act[2];
+  // the same for the tcgen05 kernel (128-row activation boxes, 32-row weight boxes)
+  bool dense = false;
+  CUtensorMap td_layer[DFLASH_MAX_LAYERS][7];
+  CUtensorMap td_lm;
+  CUtensorMap td_xn[2], td_attn[2], td_act[2];
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
@@ -236,6 +244,10 @@ int cuda_fail(dflash_handle* h, cudaError_t e, const char* where) {
   return DFLASH_ERR_CUDA;
 }
 
+// The runtime's last-error slot is shared with every other user of CUDA in the
+// process; clear it on entry so a stale error is not reported as this call's.
+inline void clear_stale_error() { (void)cudaGetLastError(); }
+
 #define DF_CHECK(h, call)                                   \
   do {                                                      \
     cudaError_t e_ = (call);                                \
@@ -262,9 +274,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D map of a row-major [rows][cols] matrix, 16-row x 128-byte boxes, 128-byte
-// swizzle; out-of-range rows / columns read as zero.
-bool make_map(CUtensorMap* m, const void* base, int wt, uint64_t cols, uint64_t rows) {
+// 2-D map of a row-major [rows][cols] matrix with boxes of box_cols x box_rows
+// elements; out-of-range rows / columns read as zero.
+bool make_map(CUtensorMap* m, const void* base, int wt, uint64_t cols, uint64_t rows,
+              uint32_t box_cols, uint32_t box_rows, bool swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const CUtensorMapDataType dt = wt == W_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -273,11 +286,17 @@ bool make_map(CUtensorMap* m, const void* base, int wt, uint64_t cols, uint64_t 
   const uint32_t esz = wt == W_F32 ? 4 : wt == W_BF16 ? 2 : 1;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * esz};
-  const cuuint32_t box[2] = {128 / esz, 16};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 16-row x 128-byte swizzled boxes (the 16-row TMA kernel)
+bool make_map(CUtensorMap* m, const void* base, int wt, uint64_t cols, uint64_t rows) {
+  const uint32_t esz = wt == W_F32 ? 4 : wt == W_BF16 ? 2 : 1;
+  return make_map(m, base, wt, cols, rows, 128 / esz, 16, true);
 }
 
 enum ProfClass {
@@ -354,8 +373,29 @@ void set_tma_inputs(GemmParams& p, const CUtensorMap* x) {
   p.x_mode = X_BF16;
 }
 
+// Launch one step projection: the tcgen05 kernel for >= 128 activation rows (its
+// own maps, 64-wide k chunks), else the 16-row TMA kernel.  Weight maps: layer l,
+// matrices wi[0..nw) (l < 0: the LM head); activations: pair xi (0 xn, 1 attn, 2 act).
+enum { XP_XN = 0, XP_ATTN = 1, XP_ACT = 2 };
+
+cudaError_t launch_projection(const dflash_handle* h, GemmParams& p, int l,
+                              std::initializer_list<int> wi, int xi, cudaStream_t st) {
+  const bool dense = h->dense && p.M >= 128;
+  const CUtensorMap* xs[3] = {dense ? h->td_xn : h->tm_xn, dense ? h->td_attn : h->tm_attn,
+                              dense ? h->td_act : h->tm_act};
+  set_tma_inputs(p, xs[xi]);
+  int i = 0;
+  for (int w : wi)
+    p.tm_w[i++] = l < 0 ? (dense ? h->td_lm : h->tm_lm)
+                        : (dense ? h->td_layer[l][w] : h->tm_layer[l][w]);
+  if (!dense) return launch_gemm_tma(h->g.wt, p, st);
+  p.cpt = cdiv(p.K, 64);
+  return launch_gemm_umma(h->g.wt, p, st);
+}
+
 int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t* n_past,
              float* logits, int32_t* drafts, cudaStream_t st) {
+  clear_stale_error();
   const Geometry& g = h->g;
   const Layout& L = h->L;
   const int M = n_seq * DFLASH_BLOCK;
@@ -377,18 +417,16 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     // q/k norm + rope
     GemmParams p = base_params(h);
     set_plan(p, sh[0], n_seq);
-    set_tma_inputs(p, h->tm_xn);
     p.M = M;
     p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
     p.seg[0] = {lw.wq, lw.wq_scale, 0, g.qd};
     p.seg[1] = {lw.wk, lw.wk_scale, g.qd, g.kvd};
     p.seg[2] = {lw.wv, lw.wv_scale, g.qd + g.kvd, g.kvd};
-    p.tm_w[0] = h->tm_layer[l][0]; p.tm_w[1] = h->tm_layer[l][1]; p.tm_w[2] = h->tm_layer[l][2];
     p.nseg = 3; p.N = g.qd + 2 * g.kvd; p.map = MAP_SEGMENTS;
     p.epi = EPI_QKV; p.out = h->S<float>(L.qbuf); p.ldo = g.qd;
     p.kblk = h->S<float>(L.kblk); p.vblk = h->S<float>(L.vblk);
     p.q_norm = lw.q_norm; p.k_norm = lw.k_norm; p.rope_cs = rope;
-    PROF(h, PC_QKV, st, launch_gemm_tma(g.wt, p, st));
+    PROF(h, PC_QKV, st, launch_projection(h, p, l, {0, 1, 2}, XP_XN, st));
     // attention over ring chunks + the block, then the chunk merge (-> attn pair)
     AttnParams a;
     std::memset(&a, 0, sizeof(a));
@@ -400,61 +438,52 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.scale = (float)(1.0 / std::sqrt((double)g.hd));
     a.part_acc = h->S<float>(L.apart_acc); a.part_ml = h->S<float>(L.apart_ml);
     a.out_hi = h->S<uint16_t>(L.attn_hi); a.out_lo = h->S<uint16_t>(L.attn_lo);
-    PROF(h, PC_ATTN, st, launch_attention(a, n_seq, st));
-    PROF(h, PC_MERGE, st, launch_attn_combine(a, n_seq, st));
+    PROF(h, PC_ATTN, st, launch_attention_cluster(a, n_seq, st));
     // o projection + residual; next input xn = split(h * ffn_norm)
     p = base_params(h);
     set_plan(p, sh[1], n_seq);
-    set_tma_inputs(p, h->tm_attn);
     p.M = M;
     p.seg[0] = {lw.wo, lw.wo_scale, 0, g.d};
-    p.tm_w[0] = h->tm_layer[l][3];
     p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
     p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
     p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d; p.pair_norm = lw.ffn_norm;
-    PROF(h, PC_O, st, launch_gemm_tma(g.wt, p, st));
+    PROF(h, PC_O, st, launch_projection(h, p, l, {3}, XP_ATTN, st));
     n_ss = sh[1].n_tiles;
     // gate/up of RMSNorm(h) + SwiGLU -> act pair
     p = base_params(h);
     set_plan(p, sh[2], n_seq);
-    set_tma_inputs(p, h->tm_xn);
     p.M = M;
     p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
     p.seg[0] = {lw.gate, lw.gate_scale, 0, g.F};
     p.seg[1] = {lw.up, lw.up_scale, 0, g.F};
-    p.tm_w[0] = h->tm_layer[l][4]; p.tm_w[1] = h->tm_layer[l][5];
     p.nseg = 2; p.N = 2 * g.F; p.map = MAP_SWIGLU;
     p.epi = EPI_SWIGLU; p.out = nullptr;
     p.pair_hi = h->S<uint16_t>(L.act_hi); p.pair_lo = h->S<uint16_t>(L.act_lo); p.pair_ld = g.F;
-    PROF(h, PC_GATEUP, st, launch_gemm_tma(g.wt, p, st));
+    PROF(h, PC_GATEUP, st, launch_projection(h, p, l, {4, 5}, XP_XN, st));
     // down projection + residual; next input xn = split(h * next norm)
     p = base_params(h);
     set_plan(p, sh[3], n_seq);
-    set_tma_inputs(p, h->tm_act);
     p.M = M;
     p.seg[0] = {lw.down, lw.down_scale, 0, g.d};
-    p.tm_w[0] = h->tm_layer[l][6];
     p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
     p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
     p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d;
     p.pair_norm = l + 1 < g.L ? h->w.layers[l + 1].attn_norm : h->w.out_norm;
-    PROF(h, PC_DOWN, st, launch_gemm_tma(g.wt, p, st));
+    PROF(h, PC_DOWN, st, launch_projection(h, p, l, {6}, XP_ACT, st));
     n_ss = sh[3].n_tiles;
   }
   // LM head of RMSNorm(h) (out_norm folded into xn by the last down projection)
   GemmParams p = base_params(h);
   set_plan(p, sh[4], n_seq);
-  set_tma_inputs(p, h->tm_xn);
   p.M = M;
   p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
   p.seg[0] = {h->w.lm_head, h->w.lm_head_scale, 0, g.V};
-  p.tm_w[0] = h->tm_lm;
   p.nseg = 1; p.N = g.V; p.map = MAP_SEGMENTS;
   p.epi = EPI_LOGITS; p.out = logits; p.ldo = g.V;
   p.am_part = h->S<float2>(L.am_part);
   p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
   p.drafts = drafts;
-  PROF(h, PC_LM, st, launch_gemm_tma(g.wt, p, st));
+  PROF(h, PC_LM, st, launch_projection(h, p, -1, {0}, XP_XN, st));
   return DFLASH_OK;
 }
 
@@ -477,6 +506,24 @@ bool build_maps(dflash_handle* h) {
   for (int i = 0; i < 3; ++i)
     for (int j = 0; j < 2; ++j)
       if (!make_map(&dst[i][j], h->scratch + pairs[i][j], W_BF16, kdim[i], g.M_max)) return false;
+  // tcgen05 path: batches of >= 128 activation rows with bf16 or E4M3 weights
+  h->dense = g.M_max >= 128 && (g.wt == W_BF16 || g.wt == W_FP8);
+  if (!h->dense) return true;
+  const bool sw = g.wt == W_BF16;   // raw E4M3 tiles are widened by threads, not read by the MMA
+  for (int l = 0; l < g.L; ++l) {
+    const dflash_layer_weights& w = h->w.layers[l];
+    const void* mats[7] = {w.wq, w.wk, w.wv, w.wo, w.gate, w.up, w.down};
+    const int rows[7] = {g.qd, g.kvd, g.kvd, g.d, g.F, g.F, g.d};
+    const int cols[7] = {g.d, g.d, g.d, g.qd, g.d, g.d, g.F};
+    for (int i = 0; i < 7; ++i)
+      if (!make_map(&h->td_layer[l][i], mats[i], g.wt, cols[i], rows[i], 64, 32, sw)) return false;
+  }
+  if (!make_map(&h->td_lm, h->w.lm_head, g.wt, g.d, g.V, 64, 32, sw)) return false;
+  CUtensorMap* ddst[3] = {h->td_xn, h->td_attn, h->td_act};
+  for (int i = 0; i < 3; ++i)
+    for (int j = 0; j < 2; ++j)
+      if (!make_map(&ddst[i][j], h->scratch + pairs[i][j], W_BF16, kdim[i], g.M_max, 64, 128, true))
+        return false;
   return true;
 }
 
@@ -529,6 +576,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
   if (!ring_mem || !scratch_mem || (reinterpret_cast<uintptr_t>(ring_mem) & (kAlign - 1)) ||
       (reinterpret_cast<uintptr_t>(scratch_mem) & (kAlign - 1)))
     return DFLASH_ERR_INVALID_ARG;
+  clear_stale_error();
   dflash_handle* h = new (std::nothrow) dflash_handle();
   if (!h) return DFLASH_ERR_INVALID_ARG;
   h->cfg = *cfg;
@@ -553,10 +601,11 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
     e = launch_fill_i32(h->ring_pos(0), cfg->max_seq * cfg->window, -1, nullptr);
   if (e == cudaSuccess) e = configure_gemm(kXkMax);
   if (e == cudaSuccess) e = configure_gemm_tma();
+  if (e == cudaSuccess) e = configure_gemm_umma();
   if (e == cudaSuccess && !build_maps(h)) e = cudaErrorNotSupported;
   if (e == cudaSuccess)
-    e = configure_attention(attn_smem_bytes(cfg->n_head / cfg->n_head_kv, cfg->head_dim,
-                                            cfg->ring_dtype == DFLASH_DTYPE_F32));
+    e = configure_attention_cluster(cfg->n_head / cfg->n_head_kv, cfg->head_dim,
+                                    cfg->ring_dtype == DFLASH_DTYPE_F32);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -580,6 +629,7 @@ void dflash_destroy(dflash_handle* h) {
 }
 
 int dflash_encode(dflash_handle* h, const void* feats, int32_t T, float* H_t, void* stream) {
+  clear_stale_error();
   if (!h || T < 0) return DFLASH_ERR_INVALID_ARG;
   if (T > h->g.max_inject) return DFLASH_ERR_TOO_MANY_ROWS;
   if (T == 0) return DFLASH_OK;
@@ -607,6 +657,7 @@ int dflash_encode(dflash_handle* h, const void* feats, int32_t T, float* H_t, vo
 
 int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, const int32_t* pos, int32_t T,
                   void* stream) {
+  clear_stale_error();
   if (!h || T < 0) return DFLASH_ERR_INVALID_ARG;
   if (seq < 0 || seq >= h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
   if (T > h->g.W || T > h->g.max_inject) return DFLASH_ERR_TOO_MANY_ROWS;
@@ -651,6 +702,7 @@ int dflash_accept(dflash_handle* h, int32_t n_seq, const int32_t* drafts, const 
   if (n_seq < 1 || n_seq > h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
   if (!drafts || !targets || !n_ok) return DFLASH_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  clear_stale_error();
   PROF(h, PC_ACCEPT, st, launch_accept(drafts, targets, n_ok, n_seq, st));
   return DFLASH_OK;
 }

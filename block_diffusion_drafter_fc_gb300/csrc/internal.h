@@ -124,6 +124,7 @@ struct AttnParams {
   int n_head, n_head_kv, hd, window;
   int n_chunks;           // 64-slot ring chunks (the block is chunk n_chunks)
   float scale;
+  int depth;              // ring sub-chunks in flight per CTA (set by the launcher)
   float* part_acc;        // [n_seq][Hkv][n_chunks+1][R][hd]
   float* part_ml;         // [n_seq][Hkv][n_chunks+1][R][2]
   uint16_t* out_hi;       // [M][qd] bf16 hi/lo pair (the o projection's input)
@@ -139,10 +140,22 @@ cudaError_t configure_gemm_tma();
 cudaError_t launch_gemm_tma(int wt, const GemmParams& p, cudaStream_t st);
 int tma_chunk_k(int wt);   // k per pipeline stage of the TMA projection kernel
 
+// tcgen05 projection for >= 128 activation rows (bf16 or E4M3 weights)
+size_t gemm_umma_smem_bytes();
+cudaError_t configure_gemm_umma();
+cudaError_t launch_gemm_umma(int wt, const GemmParams& p, cudaStream_t st);
+
 size_t attn_smem_bytes(int group, int hd, int ring_f32);
 cudaError_t configure_attention(size_t smem);
 cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams& p, int n_seq, cudaStream_t st);
+
+// one cluster per (sequence, kv head), partials merged in distributed shared memory
+int attn_cluster_size(int window);
+// depth 0: the largest pipeline depth the launcher may pick
+size_t attn_cluster_smem(int group, int hd, int ring_f32, int depth);
+cudaError_t configure_attention_cluster(int group, int hd, int ring_f32);
+cudaError_t launch_attention_cluster(const AttnParams& p, int n_seq, cudaStream_t st);
 
 cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,

@@ -138,7 +138,13 @@ MIXED_F32 = DraftConfig(
     name="mixed_f32w_bf16ring", n_layer=2, n_embd=256, n_head=4, n_head_kv=4, head_dim=64,
     n_ff=544, window=40, n_vocab=777, weight_dtype="f32", dense_dtype="f32",
     ring_dtype="bf16", n_seq=2, fill_lo=8, fill_hi=40, offset_hi=1000, seed=2003)
-TEST_CONFIGS: Dict[str, DraftConfig] = {c.name: c for c in (RAGGED, SMALL_FP8, MIXED_F32)}
+# batches of >= 128 block rows (the tcgen05 projection path): a ragged last
+# 128-row tile with FP8 weights, and bf16 weights
+DENSE_FP8 = SMALL_FP8.with_(name="dense_fp8", n_seq=9, seed=2004)
+DENSE_BF16 = SMALL_FP8.with_(name="dense_bf16", n_seq=8, weight_dtype="bf16", mismatch="uniform",
+                             seed=2005)
+TEST_CONFIGS: Dict[str, DraftConfig] = {c.name: c for c in (RAGGED, SMALL_FP8, MIXED_F32, DENSE_FP8,
+                                                            DENSE_BF16)}
 
 
 def get_config(name: str) -> DraftConfig:

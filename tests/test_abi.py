@@ -57,7 +57,7 @@ def test_config_validation():
     assert _bad(weight_dtype=7) == -1
     assert _bad(n_layer=17) == -2
     assert _bad(weight_dtype=2, n_embd=288) == -2   # FP8 needs multiples of 64
-    assert _bad(n_head=34, n_head_kv=2, head_dim=128) == -2   # more than 16 q heads per kv head
+    assert _bad(n_head=18, n_head_kv=2, head_dim=128) == -2   # more than 8 q heads per kv head
 
 
 def test_create_rejects_null_weights_without_gpu():

@@ -22,7 +22,7 @@ import oracle_bridge as OB
 
 pytestmark = pytest.mark.gpu
 
-SMALL = ["tiny_f32", "ragged_bf16", "mixed_f32w_bf16ring", "small_fp8"]
+SMALL = ["tiny_f32", "ragged_bf16", "mixed_f32w_bf16ring", "small_fp8", "dense_fp8", "dense_bf16"]
 
 
 @functools.lru_cache(maxsize=None)
