@@ -1,24 +1,31 @@
 // Sliding-window GQA attention of the noise block, one thread-block cluster per
-// (sequence, kv head).
+// (sequence, kv head, group of query heads).
 //
 // The block's 16 rows at positions n_past .. n_past + 15 attend (non-causally)
 // to every row of the block and to the ring slots holding positions p with
 // 0 <= p < n_past and (n_past + i) - p < window (dflash-ops model card, Method).
-// The ring of one kv head is split between the CL CTAs of a cluster; each CTA
-// walks its slots in 64-key sub-chunks (double-buffered async copies of the bf16
-// K/V rows) with an online softmax, one warp per query head of the kv group
-// (the G heads share every K/V tile).  Both products use the tensor cores with
-// fp32 accumulation: q and the probabilities are split into bf16 hi + lo, bf16
-// ring K/V are exact, fp32 K/V (an fp32 ring, the block's own keys) are split
-// too.  The CTAs then merge their (max, sum, O) partials through distributed
-// shared memory in rank order and write the o projection's input as a bf16
-// hi/lo pair.  Rank 0 also attends to the block's own keys.
+// The ring of one kv head is split between the CL CTAs of a cluster.  Inside a
+// CTA, warp (h, q) owns query head h of the CTA's head group and key lane q:
+// the CTA's slots are cut into 64-key sub-chunks, staged into shared memory
+// with async copies kq at a time (one round), and key lane q attends to
+// sub-chunk q of each round with an online softmax, so the heads of the kv
+// group share every K/V tile and the sub-chunks of a round run in parallel.
+// Both products use the tensor cores with fp32 accumulation: q and the
+// probabilities are split into bf16 hi + lo, bf16 ring K/V are exact, fp32 K/V
+// (an fp32 ring, the block's own keys) are split too.  The key lanes' partial
+// (max, sum, O) states are merged inside the CTA, then the CTAs of the cluster
+// merge theirs through distributed shared memory in rank order and write the o
+// projection's input as a bf16 hi/lo pair.  Rank 0 also attends to the
+// block's own keys.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "internal.h"
 
 #include <math_constants.h>
+
+#include <mutex>
+#include <vector>
 
 namespace cg = cooperative_groups;
 
@@ -28,13 +35,38 @@ constexpr int kSub = 64;       // keys per sub-chunk
 constexpr int kPad = 8;        // bf16 row padding (conflict-free fragment loads)
 constexpr int kMaxCluster = 8;
 
-DF_DEVICE void cp16(void* smem, const void* gmem) {
-  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+DF_DEVICE uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+DF_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(bar)), "r"(count) : "memory");
 }
-DF_DEVICE void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-DF_DEVICE void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+DF_DEVICE void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes)
+               : "memory");
+}
+// Wait for the phase with this parity to complete; false after ~2 s.
+DF_DEVICE bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(su32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > 4000000000LL) return false;
+  }
+}
+// One contiguous global -> shared copy by the bulk-copy engine (16-byte
+// aligned addresses, size a multiple of 16), completing on `bar`.
+DF_DEVICE void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          su32(dst)),
+      "l"(src), "r"(bytes), "r"(su32(bar))
+      : "memory");
+}
 
 DF_DEVICE void ldsm_x4_t(uint32_t (&r)[4], const void* smem) {
   const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
@@ -42,13 +74,33 @@ DF_DEVICE void ldsm_x4_t(uint32_t (&r)[4], const void* smem) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
 }
 
-// Ring sub-chunks in flight per CTA.  A bf16 ring keeps four in flight when the
-// grid is at most one CTA per SM (latency-bound single sequences) and two when
-// it is larger, so that two CTAs fit one SM; an fp32 ring's hi/lo tiles take
-// twice the room and always use two.
-constexpr int kMaxDepth = 4;
-inline int depth_for(bool f32, long long ctas, int n_sm) {
-  return f32 || ctas > n_sm ? 2 : kMaxDepth;
+// Launch plan: query heads per CTA (hpc, a divisor of the group size), key
+// lanes per head (kq: warps per head; warps = hpc * kq <= 8) and staging
+// buffers (nb 64-key sub-chunks in flight, a multiple of kq).
+struct AttnPlan {
+  int hpc, kq, nb;
+};
+// bf16 ring: four buffers stage a whole 256-key slice at once (one CTA per
+// SM); fp32 ring: two, whose hi/lo tiles take twice the room.  The throughput
+// plan of large batched grids stages two sub-chunks with four warps so that
+// two CTAs share an SM and overlap one another's copies and math.
+constexpr int kLatencyPlans = 4;
+inline int plans_for(bool f32, int G, AttnPlan (&out)[kLatencyPlans + 1]) {
+  const int nb = f32 ? 2 : 4;
+  int n = 0;
+  const int hpcs[3] = {4, 2, 1};
+  const int kqs[3] = {4, 2, 1};
+  for (int hpc : hpcs) {
+    if (G % hpc) continue;
+    for (int kq : kqs) {
+      if (hpc * kq > 8 || kq > nb || hpc * kq < 4 || n >= kLatencyPlans) continue;
+      out[n++] = AttnPlan{hpc, kq, nb};
+    }
+  }
+  if (n == 0) out[n++] = AttnPlan{1, nb, nb};  // groups of odd size
+  int h2 = G % 2 == 0 ? 2 : 1;
+  out[n++] = AttnPlan{h2, 2, 2};               // throughput plan (last)
+  return n;
 }
 
 template <int HD>
@@ -58,20 +110,21 @@ struct AttnSmem {
   // buffer b: K hi, V hi, K lo, V lo (lo only used by an fp32 ring)
   static constexpr int BUF = 4 * TILE;
   static constexpr int BLK = 4 * kBlock * KS;          // block keys: K hi/lo, V hi/lo [16][KS]
-  static size_t bytes(bool f32, int depth) {
-    const size_t bufs = depth * (size_t)(f32 ? BUF : 2 * TILE) * 2;
-    return bufs + (size_t)BLK * 2 + kMaxDepth * kSub * sizeof(int) + 256;
+  // staging: nb sub-chunk buffers, the block keys, nb x 64 slot positions
+  static size_t stage_bytes(bool f32, int nb) {
+    return (size_t)nb * (f32 ? BUF : 2 * TILE) * 2 + (size_t)BLK * 2 + (size_t)nb * kSub * 4;
+  }
+  // merge: per-warp fragments [warps][HD/8][32] float4 + (m, l) float4 per lane,
+  // then the CTA's partial [R][HD] + (m, l)
+  static size_t merge_bytes(int warps, int R) {
+    return (size_t)warps * (HD / 8) * 32 * 16 + (size_t)warps * 32 * 16 + (size_t)R * HD * 4 +
+           (size_t)R * 8;
+  }
+  static size_t bytes(bool f32, const AttnPlan& pl) {
+    const size_t a = stage_bytes(f32, pl.nb), b = merge_bytes(pl.kq * pl.hpc, kBlock * pl.hpc);
+    return (a > b ? a : b) + 256;
   }
 };
-
-DF_DEVICE void cp_wait_upto(int n) {
-  switch (n) {
-    case 0: cp_wait<0>(); break;
-    case 1: cp_wait<1>(); break;
-    case 2: cp_wait<2>(); break;
-    default: cp_wait<3>(); break;
-  }
-}
 
 // Online-softmax update of one warp's 16 rows with one tile of up to 64 keys.
 template <int HD, bool SPLIT>
@@ -199,22 +252,31 @@ template <int HD, bool RING_F32>
 __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant__ AttnParams p) {
   using SM = AttnSmem<HD>;
   constexpr int KS = SM::KS;
-  const int kDepth = p.depth;
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
-  const int kvh = blockIdx.y, seq = blockIdx.z;
-  const int G = p.n_head / p.n_head_kv, R = kBlock * G;
+  const int G = p.n_head / p.n_head_kv, hpc = p.hpc, kq = p.kq, nb = p.nb, n_hgrp = G / hpc;
+  const int kvh = blockIdx.y / n_hgrp, hgrp = blockIdx.y - kvh * n_hgrp, seq = blockIdx.z;
+  const int R = kBlock * hpc;                       // rows of this CTA (head-major)
+  const int head0 = kvh * G + hgrp * hpc;           // first query head of the CTA
   const int qd = p.n_head * HD, kvd = p.n_head_kv * HD;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int nwarps = (int)(blockDim.x >> 5);
+  const int hl = warp / kq, lk = warp - hl * kq;    // head within the CTA, key lane
   extern __shared__ __align__(16) uint8_t sm_raw[];
   uint16_t* bufs = reinterpret_cast<uint16_t*>(sm_raw);
   const int buf_elems = RING_F32 ? SM::BUF : 2 * SM::TILE;
-  uint16_t* blk_k_hi = bufs + kDepth * buf_elems;
+  uint16_t* blk_k_hi = bufs + nb * buf_elems;
   uint16_t* blk_k_lo = blk_k_hi + kBlock * KS;
   uint16_t* blk_v_hi = blk_k_lo + kBlock * KS;
   uint16_t* blk_v_lo = blk_v_hi + kBlock * KS;
-  int* kpos = reinterpret_cast<int*>(blk_v_lo + kBlock * KS);  // [kDepth][64]
+  int* kpos = reinterpret_cast<int*>(blk_v_lo + kBlock * KS);  // [nb][64]
+  __shared__ __align__(8) uint64_t s_bar[4];                    // one per staging buffer
 
+  if (!RING_F32 && tid == 0) {
+    for (int b = 0; b < nb; ++b) mbar_init(&s_bar[b], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
   pdl_trigger();
   pdl_wait();
   const int p0 = max(p.n_past[seq], 0);
@@ -225,119 +287,226 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
   const size_t kbase = ((((size_t)seq * p.n_layer + p.layer) * 2 + 0) * p.n_head_kv + kvh) * plane;
   const size_t vbase = kbase + (size_t)p.n_head_kv * plane;
 
-  // async copy (bf16 ring) or load + split (fp32 ring) of ring sub-chunk j
-  auto stage = [&](int j) {
-    uint16_t* kh = bufs + (j % kDepth) * buf_elems;
-    uint16_t* vh = kh + SM::TILE;
-    uint16_t* kl = vh + SM::TILE;
-    uint16_t* vl = kl + SM::TILE;
-    const int s0 = s_begin + j * kSub, nk = min(kSub, s_end - s0);
+  // Stage the ring rows of the round of sub-chunks j0 .. j0 + nb - 1 (buffer
+  // j % nb).  A bf16 ring row (hd bf16, 16-byte aligned in both spaces) is one
+  // bulk copy that completes on the buffer's mbarrier; rows past the CTA's
+  // slots are zeroed.  An fp32 ring is loaded and split into bf16 hi/lo by the
+  // threads.
+  auto stage_round = [&](int j0) {
+    const int jn = min(n_sub, j0 + nb);
     if (!RING_F32) {
+      if (tid == 0)
+        for (int j = j0; j < jn; ++j) {
+          const int nk = min(kSub, s_end - (s_begin + j * kSub));
+          mbar_expect_tx(&s_bar[j % nb], (uint32_t)nk * HD * 2 * 2);
+        }
+      __syncthreads();  // expectations first; earlier reads of the buffers are done
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       const uint16_t* r = reinterpret_cast<const uint16_t*>(p.ring);
-      for (int idx = tid; idx < kSub * (HD / 8); idx += blockDim.x) {
-        const int row = idx / (HD / 8), d = (idx - row * (HD / 8)) * 8;
+      for (int idx = tid; idx < (jn - j0) * 2 * kSub; idx += blockDim.x) {
+        const int jj = idx / (2 * kSub), rem = idx - jj * 2 * kSub;
+        const int kv = rem / kSub, row = rem - kv * kSub, j = j0 + jj;
+        const int s0 = s_begin + j * kSub, nk = min(kSub, s_end - s0);
+        uint16_t* dst = bufs + (j % nb) * buf_elems + kv * SM::TILE + row * KS;
         if (row < nk) {
-          cp16(kh + row * KS + d, r + kbase + (size_t)(s0 + row) * HD + d);
-          cp16(vh + row * KS + d, r + vbase + (size_t)(s0 + row) * HD + d);
+          bulk_copy(dst, r + (kv ? vbase : kbase) + (size_t)(s0 + row) * HD, HD * 2, &s_bar[j % nb]);
         } else {
-          *reinterpret_cast<uint4*>(kh + row * KS + d) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vh + row * KS + d) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int d = 0; d < HD; d += 8) *reinterpret_cast<uint4*>(dst + d) = make_uint4(0, 0, 0, 0);
         }
       }
     } else {
       const float* r = reinterpret_cast<const float*>(p.ring);
-      for (int idx = tid; idx < kSub * (HD / 4); idx += blockDim.x) {
-        const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
-        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-        if (row < nk) {
-          kv = *reinterpret_cast<const float4*>(r + kbase + (size_t)(s0 + row) * HD + d);
-          vv = *reinterpret_cast<const float4*>(r + vbase + (size_t)(s0 + row) * HD + d);
+      for (int j = j0; j < jn; ++j) {
+        uint16_t* kh = bufs + (j % nb) * buf_elems;
+        uint16_t* vh = kh + SM::TILE;
+        uint16_t* kl = vh + SM::TILE;
+        uint16_t* vl = kl + SM::TILE;
+        const int s0 = s_begin + j * kSub, nk = min(kSub, s_end - s0);
+        for (int idx = tid; idx < kSub * (HD / 4); idx += blockDim.x) {
+          const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+          float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+          if (row < nk) {
+            kv = *reinterpret_cast<const float4*>(r + kbase + (size_t)(s0 + row) * HD + d);
+            vv = *reinterpret_cast<const float4*>(r + vbase + (size_t)(s0 + row) * HD + d);
+          }
+          uint2 h, l;
+          split_bf16x2(kv.x, kv.y, h.x, l.x);
+          split_bf16x2(kv.z, kv.w, h.y, l.y);
+          *reinterpret_cast<uint2*>(kh + row * KS + d) = h;
+          *reinterpret_cast<uint2*>(kl + row * KS + d) = l;
+          split_bf16x2(vv.x, vv.y, h.x, l.x);
+          split_bf16x2(vv.z, vv.w, h.y, l.y);
+          *reinterpret_cast<uint2*>(vh + row * KS + d) = h;
+          *reinterpret_cast<uint2*>(vl + row * KS + d) = l;
         }
-        uint2 h, l;
-        split_bf16x2(kv.x, kv.y, h.x, l.x);
-        split_bf16x2(kv.z, kv.w, h.y, l.y);
-        *reinterpret_cast<uint2*>(kh + row * KS + d) = h;
-        *reinterpret_cast<uint2*>(kl + row * KS + d) = l;
-        split_bf16x2(vv.x, vv.y, h.x, l.x);
-        split_bf16x2(vv.z, vv.w, h.y, l.y);
-        *reinterpret_cast<uint2*>(vh + row * KS + d) = h;
-        *reinterpret_cast<uint2*>(vl + row * KS + d) = l;
       }
     }
-    int* kp = kpos + (j % kDepth) * kSub;
-    for (int row = tid; row < kSub; row += blockDim.x)
-      kp[row] = row < nk ? p.ring_pos[(size_t)seq * p.window + s0 + row] : -1;
-    cp_commit();
+  };
+  // slot positions of the round's sub-chunks (-1 past the CTA's slots), at
+  // most kPosPer per thread, all loads issued before the stores
+  constexpr int kPosPer = 4;
+  auto stage_kpos = [&](int j0) {
+    const int n = (min(n_sub, j0 + nb) - j0) * kSub;
+    for (int base = 0; base < n; base += kPosPer * (int)blockDim.x) {
+      int v[kPosPer];
+#pragma unroll
+      for (int u = 0; u < kPosPer; ++u) {
+        const int idx = base + u * (int)blockDim.x + tid;
+        const int jj = idx / kSub, row = idx - jj * kSub, s0 = s_begin + (j0 + jj) * kSub;
+        v[u] = idx < n && s0 + row < s_end ? p.ring_pos[(size_t)seq * p.window + s0 + row] : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < kPosPer; ++u) {
+        const int idx = base + u * (int)blockDim.x + tid;
+        const int jj = idx / kSub, row = idx - jj * kSub;
+        if (idx < n) kpos[((j0 + jj) % nb) * kSub + row] = v[u];
+      }
+    }
+  };
+  // wait for the bulk copies of sub-chunk j (round r is its buffer's r-th phase)
+  auto wait_sub = [&](int j, int r) {
+    if (RING_F32) return;
+    if (!mbar_wait(&s_bar[j % nb], (uint32_t)(r & 1))) {
+      if (lane == 0) atomicOr(p.status, 0x4u);
+      mbar_wait(&s_bar[j % nb], (uint32_t)(r & 1));  // a second bounded wait before moving on
+    }
   };
 
-  for (int j = 0; j < kDepth - 1 && j < n_sub; ++j) stage(j);
-  if (rank == 0) {  // the block's own 16 keys (fp32: split hi/lo)
-    for (int idx = tid; idx < kBlock * (HD / 4); idx += blockDim.x) {
-      const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
-      const size_t o = (size_t)(seq * kBlock + row) * kvd + kvh * HD + d;
-      const float4 kv = *reinterpret_cast<const float4*>(p.kblk + o);
-      const float4 vv = *reinterpret_cast<const float4*>(p.vblk + o);
-      uint2 h, l;
-      split_bf16x2(kv.x, kv.y, h.x, l.x);
-      split_bf16x2(kv.z, kv.w, h.y, l.y);
-      *reinterpret_cast<uint2*>(blk_k_hi + row * KS + d) = h;
-      *reinterpret_cast<uint2*>(blk_k_lo + row * KS + d) = l;
-      split_bf16x2(vv.x, vv.y, h.x, l.x);
-      split_bf16x2(vv.z, vv.w, h.y, l.y);
-      *reinterpret_cast<uint2*>(blk_v_hi + row * KS + d) = h;
-      *reinterpret_cast<uint2*>(blk_v_lo + row * KS + d) = l;
-    }
-  }
-
-  // this warp's head: q fragments (fp32 -> scaled hi/lo) straight from global
-  const bool active = warp < G;
-  uint32_t qh[HD / 16][4], ql[HD / 16][4];
+  // the first round's copies go out before anything else; then one batch of
+  // independent loads (q rows, the block's own keys, the round's slot
+  // positions) whose values are consumed only after all of them are issued
+  stage_round(0);
+  const bool active = hl < hpc;
+  float2 qraw[HD / 16][4];
   if (active) {
-    const int head = kvh * G + warp;
-    const float* qr0 = p.q + (size_t)(seq * kBlock + g) * qd + head * HD;
+    const float* qr0 = p.q + (size_t)(seq * kBlock + g) * qd + (head0 + hl) * HD;
     const float* qr1 = qr0 + (size_t)8 * qd;
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks) {
       const int k0 = ks * 16 + 2 * t;
-      const float2 a0 = *reinterpret_cast<const float2*>(qr0 + k0);
-      const float2 a1 = *reinterpret_cast<const float2*>(qr1 + k0);
-      const float2 a2 = *reinterpret_cast<const float2*>(qr0 + k0 + 8);
-      const float2 a3 = *reinterpret_cast<const float2*>(qr1 + k0 + 8);
-      split_bf16x2(a0.x * p.scale, a0.y * p.scale, qh[ks][0], ql[ks][0]);
-      split_bf16x2(a1.x * p.scale, a1.y * p.scale, qh[ks][1], ql[ks][1]);
-      split_bf16x2(a2.x * p.scale, a2.y * p.scale, qh[ks][2], ql[ks][2]);
-      split_bf16x2(a3.x * p.scale, a3.y * p.scale, qh[ks][3], ql[ks][3]);
+      qraw[ks][0] = *reinterpret_cast<const float2*>(qr0 + k0);
+      qraw[ks][1] = *reinterpret_cast<const float2*>(qr1 + k0);
+      qraw[ks][2] = *reinterpret_cast<const float2*>(qr0 + k0 + 8);
+      qraw[ks][3] = *reinterpret_cast<const float2*>(qr1 + k0 + 8);
     }
   }
+  if (rank == 0) {  // the block's own 16 keys (fp32: split hi/lo), <= 4 float4 per thread a pass
+    constexpr int kBlkPer = 4, n = kBlock * (HD / 4);
+    for (int base = 0; base < n; base += kBlkPer * (int)blockDim.x) {
+      float4 kr[kBlkPer], vr[kBlkPer];
+#pragma unroll
+      for (int u = 0; u < kBlkPer; ++u) {
+        const int idx = base + u * (int)blockDim.x + tid;
+        kr[u] = vr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < n) {
+          const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+          const size_t o = (size_t)(seq * kBlock + row) * kvd + kvh * HD + d;
+          kr[u] = *reinterpret_cast<const float4*>(p.kblk + o);
+          vr[u] = *reinterpret_cast<const float4*>(p.vblk + o);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBlkPer; ++u) {
+        const int idx = base + u * (int)blockDim.x + tid;
+        if (idx >= n) continue;
+        const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+        uint2 h, l;
+        split_bf16x2(kr[u].x, kr[u].y, h.x, l.x);
+        split_bf16x2(kr[u].z, kr[u].w, h.y, l.y);
+        *reinterpret_cast<uint2*>(blk_k_hi + row * KS + d) = h;
+        *reinterpret_cast<uint2*>(blk_k_lo + row * KS + d) = l;
+        split_bf16x2(vr[u].x, vr[u].y, h.x, l.x);
+        split_bf16x2(vr[u].z, vr[u].w, h.y, l.y);
+        *reinterpret_cast<uint2*>(blk_v_hi + row * KS + d) = h;
+        *reinterpret_cast<uint2*>(blk_v_lo + row * KS + d) = l;
+      }
+    }
+  }
+  stage_kpos(0);
+  // this warp's head: q fragments scaled by 1/sqrt(hd), split into bf16 hi/lo
+  uint32_t qh[HD / 16][4], ql[HD / 16][4];
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      split_bf16x2(qraw[ks][e].x * p.scale, qraw[ks][e].y * p.scale, qh[ks][e], ql[ks][e]);
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
   float O[HD / 8][4];
 #pragma unroll
   for (int jd = 0; jd < HD / 8; ++jd) O[jd][0] = O[jd][1] = O[jd][2] = O[jd][3] = 0.f;
+  // the block's own keys go to the key lane with the least ring work, first:
+  // their tile overlaps the wait for the ring copies
+  const bool blk_lane = rank == 0 && active && lk == n_sub % kq;
 
-  for (int j = 0; j < n_sub; ++j) {
-    // keep kDepth - 1 sub-chunks in flight: issue j + kDepth - 1, wait for j
-    if (j + kDepth - 1 < n_sub) stage(j + kDepth - 1);
-    cp_wait_upto(min(kDepth - 1, n_sub - 1 - j));
-    __syncthreads();
-    if (active) {
-      const uint16_t* kh = bufs + (j % kDepth) * buf_elems;
-      attend_tile<HD, RING_F32>(qh, ql, kh, kh + 2 * SM::TILE, kh + SM::TILE, kh + 3 * SM::TILE, KS,
-                                8, kpos + (j % kDepth) * kSub, false, p0, p.window, m0, m1, l0, l1, O,
-                                lane);
+  // rounds of nb sub-chunks; key lane q takes sub-chunks q, q + kq, ... of each
+  // round, each as soon as its own copies have landed
+  for (int j0 = 0, r = 0; j0 < n_sub; j0 += nb, ++r) {
+    if (j0 > 0) {
+      stage_round(j0);
+      stage_kpos(j0);
     }
-    __syncthreads();  // the buffer is refilled kDepth - 1 sub-chunks later
+    __syncthreads();  // zeroed rows, slot positions, fp32 tiles and the block keys
+    if (j0 == 0 && blk_lane)
+      attend_tile<HD, true>(qh, ql, blk_k_hi, blk_k_lo, blk_v_hi, blk_v_lo, KS, 2, nullptr, true,
+                            p0, p.window, m0, m1, l0, l1, O, lane);
+    for (int j = j0 + lk; j < min(n_sub, j0 + nb); j += kq) {
+      wait_sub(j, r);
+      if (active) {
+        const uint16_t* kh = bufs + (j % nb) * buf_elems;
+        attend_tile<HD, RING_F32>(qh, ql, kh, kh + 2 * SM::TILE, kh + SM::TILE, kh + 3 * SM::TILE,
+                                  KS, 8, kpos + (j % nb) * kSub, false, p0, p.window, m0, m1, l0,
+                                  l1, O, lane);
+      }
+    }
+    __syncthreads();  // the buffers are restaged by the next round
+  }
+  if (n_sub == 0) {   // a CTA with no ring slots
+    __syncthreads();
+    if (blk_lane)
+      attend_tile<HD, true>(qh, ql, blk_k_hi, blk_k_lo, blk_v_hi, blk_v_lo, KS, 2, nullptr, true,
+                            p0, p.window, m0, m1, l0, l1, O, lane);
+    __syncthreads();
+  }
+
+  // 1. key lanes 1.. of each head hand their (max, sum, O) fragments to key
+  //    lane 0 through shared memory (over the staging buffers), which merges
+  //    them into its registers in lane order
+  float4* frag_o = reinterpret_cast<float4*>(sm_raw);                     // [warps][HD/8][32]
+  float4* frag_ml = frag_o + (size_t)nwarps * (HD / 8) * 32;              // [warps][32]
+  float* part_o = reinterpret_cast<float*>(frag_ml + (size_t)nwarps * 32);  // [R][HD]
+  float2* part_ml = reinterpret_cast<float2*>(part_o + (size_t)R * HD);   // [R]
+  if (active && lk > 0) {
+#pragma unroll
+    for (int jd = 0; jd < HD / 8; ++jd)
+      frag_o[((size_t)warp * (HD / 8) + jd) * 32 + lane] = make_float4(O[jd][0], O[jd][1], O[jd][2], O[jd][3]);
+    frag_ml[warp * 32 + lane] = make_float4(m0, m1, l0, l1);
   }
   __syncthreads();
-  if (rank == 0 && active)
-    attend_tile<HD, true>(qh, ql, blk_k_hi, blk_k_lo, blk_v_hi, blk_v_lo, KS, 2, nullptr, true, p0,
-                          p.window, m0, m1, l0, l1, O, lane);
-  __syncthreads();
-
-  // partials into this CTA's shared memory (over the K/V buffers), then merge
-  float* part_o = reinterpret_cast<float*>(sm_raw);      // [R][HD]
-  float2* part_ml = reinterpret_cast<float2*>(part_o + (size_t)R * HD);
-  if (active) {
-    float* o0 = part_o + (size_t)(warp * kBlock + g) * HD;
+  if (active && lk == 0) {
+    for (int q = 1; q < kq; ++q) {
+      const int w = warp + q;
+      const float4 ml = frag_ml[w * 32 + lane];
+      const float n0 = fmaxf(m0, ml.x), n1 = fmaxf(m1, ml.y);
+      const float a0 = m0 == -CUDART_INF_F ? 0.f : expf(m0 - n0);
+      const float b0 = ml.x == -CUDART_INF_F ? 0.f : expf(ml.x - n0);
+      const float a1 = m1 == -CUDART_INF_F ? 0.f : expf(m1 - n1);
+      const float b1 = ml.y == -CUDART_INF_F ? 0.f : expf(ml.y - n1);
+      m0 = n0;
+      m1 = n1;
+      l0 = a0 * l0 + b0 * ml.z;
+      l1 = a1 * l1 + b1 * ml.w;
+#pragma unroll
+      for (int jd = 0; jd < HD / 8; ++jd) {
+        const float4 v = frag_o[((size_t)w * (HD / 8) + jd) * 32 + lane];
+        O[jd][0] = a0 * O[jd][0] + b0 * v.x;
+        O[jd][1] = a0 * O[jd][1] + b0 * v.y;
+        O[jd][2] = a1 * O[jd][2] + b1 * v.z;
+        O[jd][3] = a1 * O[jd][3] + b1 * v.w;
+      }
+    }
+    // 2. this CTA's partial of the head's 16 rows, row-major for the peers
+    float* o0 = part_o + (size_t)(hl * kBlock + g) * HD;
     float* o1 = o0 + (size_t)8 * HD;
 #pragma unroll
     for (int jd = 0; jd < HD / 8; ++jd) {
@@ -345,16 +514,24 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
       *reinterpret_cast<float2*>(o1 + 8 * jd + 2 * t) = make_float2(O[jd][2], O[jd][3]);
     }
     if (t == 0) {
-      part_ml[warp * kBlock + g] = make_float2(m0, l0);
-      part_ml[warp * kBlock + g + 8] = make_float2(m1, l1);
+      part_ml[hl * kBlock + g] = make_float2(m0, l0);
+      part_ml[hl * kBlock + g + 8] = make_float2(m1, l1);
     }
   }
+  // 3. merge the cluster's CTAs through distributed shared memory, rank order
   cluster.sync();
   const int rows_per = (R + CL - 1) / CL;
   const int r_lo = rank * rows_per, r_hi = min(R, r_lo + rows_per);
-  const int nw = blockDim.x >> 5;
-  for (int r = r_lo + warp; r < r_hi; r += nw) {
-    // lane c < CL fetches rank c's (max, sum); the row's weights via shuffles
+  for (int r = r_lo + warp; r < r_hi; r += nwarps) {
+    // remote loads first: lane c < CL fetches rank c's (max, sum), every lane
+    // the ranks' partial O at its four dims (one round trip for both)
+    const int d = lane * 4;
+    float4 v[kMaxCluster];
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c)
+      v[c] = c < CL && d < HD
+                 ? *reinterpret_cast<const float4*>(cluster.map_shared_rank(part_o, c) + (size_t)r * HD + d)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
     float2 ml = make_float2(-CUDART_INF_F, 0.f);
     if (lane < CL) ml = cluster.map_shared_rank(part_ml, lane)[r];
     float M = ml.x;
@@ -365,30 +542,22 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     L = __shfl_sync(0xffffffffu, L, 0);  // lanes 0..7 hold the total
-    float wc[kMaxCluster];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < kMaxCluster; ++c) wc[c] = __shfl_sync(0xffffffffu, wgt, c);
-    // lane-parallel over dims, ranks summed in rank order
-    for (int d = lane * 4; d < HD; d += 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < kMaxCluster; ++c) {
-        if (c < CL) {
-          const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part_o, c) +
-                                                             (size_t)r * HD + d);
-          acc.x += wc[c] * v.x;
-          acc.y += wc[c] * v.y;
-          acc.z += wc[c] * v.z;
-          acc.w += wc[c] * v.w;
-        }
-      }
+    for (int c = 0; c < kMaxCluster; ++c) {
+      const float wc = __shfl_sync(0xffffffffu, wgt, c);  // ranks summed in rank order
+      acc.x += wc * v[c].x;
+      acc.y += wc * v[c].y;
+      acc.z += wc * v[c].z;
+      acc.w += wc * v[c].w;
+    }
+    if (d < HD) {
+      const int h = r / kBlock, i = r - h * kBlock;
       const float inv = 1.f / L;
-      const float o4[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
-      const int hl = r / kBlock, i = r - hl * kBlock;
-      const size_t at = (size_t)(seq * kBlock + i) * qd + (kvh * G + hl) * HD + d;
+      const size_t at = (size_t)(seq * kBlock + i) * qd + (head0 + h) * HD + d;
       uint2 hi, lo;
-      split_bf16x2(o4[0], o4[1], hi.x, lo.x);
-      split_bf16x2(o4[2], o4[3], hi.y, lo.y);
+      split_bf16x2(acc.x * inv, acc.y * inv, hi.x, lo.x);
+      split_bf16x2(acc.z * inv, acc.w * inv, hi.y, lo.y);
       *reinterpret_cast<uint2*>(p.out_hi + at) = hi;
       *reinterpret_cast<uint2*>(p.out_lo + at) = lo;
     }
@@ -401,34 +570,125 @@ int attn_cluster_size(int window) {
   return cl < 1 ? 1 : (cl > kMaxCluster ? kMaxCluster : cl);
 }
 
-size_t attn_cluster_smem(int group, int hd, int ring_f32, int depth) {
-  if (depth <= 0) depth = ring_f32 ? 2 : kMaxDepth;  // the largest the launcher picks
-  size_t kv;
+template <int HD>
+static size_t smem_of(bool f32, const AttnPlan& pl) {
+  return AttnSmem<HD>::bytes(f32, pl);
+}
+static size_t smem_of_hd(int hd, bool f32, const AttnPlan& pl) {
   switch (hd) {
-    case 32: kv = AttnSmem<32>::bytes(ring_f32, depth); break;
-    case 64: kv = AttnSmem<64>::bytes(ring_f32, depth); break;
-    default: kv = AttnSmem<128>::bytes(ring_f32, depth); break;
+    case 32: return smem_of<32>(f32, pl);
+    case 64: return smem_of<64>(f32, pl);
+    default: return smem_of<128>(f32, pl);
   }
-  const size_t part = (size_t)kBlock * group * hd * 4 + (size_t)kBlock * group * 8;
-  return kv > part ? kv : part;
+}
+
+size_t attn_cluster_smem(int group, int hd, int ring_f32) {
+  AttnPlan pls[kLatencyPlans + 1];
+  const int n = plans_for(ring_f32 != 0, group, pls);
+  size_t best = 0;
+  for (int i = 0; i < n; ++i) {
+    const size_t b = smem_of_hd(hd, ring_f32 != 0, pls[i]);
+    if (b > best) best = b;
+  }
+  return best;
+}
+
+// Co-resident clusters of each plan, measured with the occupancy API once per
+// (kernel, plan, cluster size) when a handle is created, so that launches
+// (also under stream capture) only read the table.
+struct OccEntry {
+  const void* fn;
+  int threads, cl;
+  size_t smem;
+  int clusters;
+};
+static std::mutex g_occ_mu;
+static std::vector<OccEntry> g_occ;
+
+template <int HD, bool F32>
+static int active_clusters(const AttnPlan& pl, int CL, bool query) {
+  const void* fn = reinterpret_cast<const void*>(attn_cluster_kernel<HD, F32>);
+  const int threads = 32 * pl.hpc * pl.kq;
+  const size_t smem = smem_of<HD>(F32, pl);
+  std::lock_guard<std::mutex> lk(g_occ_mu);
+  for (const OccEntry& e : g_occ)
+    if (e.fn == fn && e.threads == threads && e.cl == CL && e.smem == smem) return e.clusters;
+  if (!query) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL, 1, 1);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_cluster_kernel<HD, F32>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  g_occ.push_back(OccEntry{fn, threads, CL, smem, n});
+  return n;
+}
+
+// The plan of a launch: the latency plan with the least estimated time when
+// the grid fits in a few waves of co-resident clusters, else the throughput
+// plan.  Estimated time = waves x (1 + tiles per warp x warps per SM
+// sub-partition), in units of one tile.
+template <int HD, bool F32>
+static AttnPlan choose_plan(int G, int CL, int n_head_kv, int n_seq, int window, bool query) {
+  AttnPlan pls[kLatencyPlans + 1];
+  const int n = plans_for(F32, G, pls);
+  const int per = (window + CL - 1) / CL, n_sub = (per + kSub - 1) / kSub;
+  AttnPlan best = pls[n - 1];
+  double best_cost = 1e30;
+  for (int i = 0; i < n - 1; ++i) {
+    const AttnPlan& pl = pls[i];
+    const int act = active_clusters<HD, F32>(pl, CL, query);
+    if (act <= 0) continue;
+    const long long clusters = (long long)n_head_kv * (G / pl.hpc) * n_seq;
+    const long long waves = (clusters + act - 1) / act;
+    if (waves > 2) continue;
+    const int tiles = (n_sub + pl.kq - 1) / pl.kq;
+    const int per_smsp = (pl.hpc * pl.kq + 3) / 4;
+    const double cost = (double)waves * (1.0 + (double)tiles * per_smsp);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = pl;
+    }
+  }
+  return best;
 }
 
 template <int HD, bool F32>
-static cudaError_t configure_cl(size_t smem) {
+static cudaError_t configure_cl(size_t smem, int G, int CL, int n_head_kv) {
   static size_t configured = 0;   // only ever raised, so every live handle still fits
-  if (smem <= configured) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<HD, F32>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e == cudaSuccess) configured = smem;
-  return e;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<HD, F32>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  AttnPlan pls[kLatencyPlans + 1];
+  const int n = plans_for(F32, G, pls);
+  for (int i = 0; i < n; ++i) (void)active_clusters<HD, F32>(pls[i], CL, true);
+  (void)n_head_kv;
+  return cudaSuccess;
 }
 
-cudaError_t configure_attention_cluster(int group, int hd, int ring_f32) {
-  const size_t smem = attn_cluster_smem(group, hd, ring_f32, 0);
+cudaError_t configure_attention_cluster(int group, int hd, int ring_f32, int window, int n_head_kv) {
+  const size_t smem = attn_cluster_smem(group, hd, ring_f32);
+  const int CL = attn_cluster_size(window);
   switch (hd) {
-    case 32: return ring_f32 ? configure_cl<32, true>(smem) : configure_cl<32, false>(smem);
-    case 64: return ring_f32 ? configure_cl<64, true>(smem) : configure_cl<64, false>(smem);
-    case 128: return ring_f32 ? configure_cl<128, true>(smem) : configure_cl<128, false>(smem);
+    case 32: return ring_f32 ? configure_cl<32, true>(smem, group, CL, n_head_kv)
+                             : configure_cl<32, false>(smem, group, CL, n_head_kv);
+    case 64: return ring_f32 ? configure_cl<64, true>(smem, group, CL, n_head_kv)
+                             : configure_cl<64, false>(smem, group, CL, n_head_kv);
+    case 128: return ring_f32 ? configure_cl<128, true>(smem, group, CL, n_head_kv)
+                              : configure_cl<128, false>(smem, group, CL, n_head_kv);
   }
   return cudaErrorInvalidValue;
 }
@@ -436,20 +696,15 @@ cudaError_t configure_attention_cluster(int group, int hd, int ring_f32) {
 template <int HD, bool F32>
 static cudaError_t launch_cl(const AttnParams& p_in, int n_seq, cudaStream_t st) {
   const int G = p_in.n_head / p_in.n_head_kv, CL = attn_cluster_size(p_in.window);
-  static int n_sm = 0;
-  if (!n_sm) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (n_sm <= 0) n_sm = 1;
-  }
+  const AttnPlan pl = choose_plan<HD, F32>(G, CL, p_in.n_head_kv, n_seq, p_in.window, false);
   AttnParams p = p_in;
-  p.depth = depth_for(F32, (long long)CL * p.n_head_kv * n_seq, n_sm);
-  const size_t smem = attn_cluster_smem(G, HD, F32, p.depth);
+  p.hpc = pl.hpc;
+  p.kq = pl.kq;
+  p.nb = pl.nb;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL, p.n_head_kv, n_seq);
-  cfg.blockDim = dim3(32 * G);
-  cfg.dynamicSmemBytes = smem;
+  cfg.gridDim = dim3(CL, p.n_head_kv * (G / pl.hpc), n_seq);
+  cfg.blockDim = dim3(32 * pl.kq * pl.hpc);
+  cfg.dynamicSmemBytes = smem_of<HD>(F32, pl);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -18,9 +18,10 @@ namespace {
 
 constexpr int kPlanSMs = 152;        // GB300: 2 dies x 76 SMs
 constexpr int kCtasPerSm = 2;        // projection CTAs resident per SM (registers bound it)
+// largest ring slice (all sequences of one layer) prefetched into L2 ahead of attention
+constexpr size_t kRingPrefetchMax = 32u << 20;
 constexpr int kGemmGrid = kPlanSMs * kCtasPerSm;
 constexpr int kXkMax = 960;          // activation stage width (3 CTAs of ~72 KB per SM)
-constexpr int kAttnChunk = 64;       // ring slots per attention CTA
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -99,10 +100,10 @@ void inject_shapes(const Geometry& g, GemmShape out[2]) {
 struct Layout {
   size_t status, inv_freq, counters, h, ss, qbuf, kblk, vblk, rope_step, am_part;
   size_t xn_hi, xn_lo, attn_hi, attn_lo, act_hi, act_lo;
-  size_t apart_acc, apart_ml, logits_int, drafts_int, idl_int, npast_int, partial;
+  size_t logits_int, drafts_int, idl_int, npast_int, partial;
   size_t inj_raw, inj_ss, inj_rope, total;
   size_t partial_floats;
-  int n_counters, ss_parts, ss_ld, lm_tiles, attn_chunks;
+  int n_counters, ss_parts, ss_ld, lm_tiles;
   size_t ring_seq_bytes, ring_kv_bytes, ring_total;
 };
 
@@ -122,9 +123,6 @@ Layout layout(const dflash_config& c) {
   L.ss_parts = cdiv(g.d, kTileRows);
   L.ss_ld = std::max(g.M_max, g.max_inject);
   L.lm_tiles = ss_[4].n_tiles;
-  L.attn_chunks = cdiv(g.W, kAttnChunk);
-  const int G = g.Hq / g.Hkv, R = 16 * G;
-  const size_t attn_slots = (size_t)g.max_seq * g.Hkv * (L.attn_chunks + 1);
 
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -148,8 +146,6 @@ Layout layout(const dflash_config& c) {
   L.act_lo = take(sizeof(uint16_t) * (size_t)g.M_max * g.F);
   L.rope_step = take(sizeof(float2) * g.M_max * (g.hd / 2));
   L.am_part = take(sizeof(float2) * (size_t)L.lm_tiles * g.M_max);
-  L.apart_acc = take(sizeof(float) * attn_slots * R * g.hd);
-  L.apart_ml = take(sizeof(float) * attn_slots * R * 2);
   L.logits_int = take(sizeof(float) * (size_t)g.M_max * g.V);
   L.drafts_int = take(sizeof(int32_t) * g.max_seq * (DFLASH_BLOCK - 1));
   L.idl_int = take(sizeof(int32_t) * g.max_seq);
@@ -188,9 +184,10 @@ int validate(const dflash_config* c) {
   if ((c->n_target_layers * c->target_embd) % 32) return DFLASH_ERR_UNSUPPORTED;
   // one warp per query head of a kv group in the attention CTA
   if (c->n_head / c->n_head_kv > 8) return DFLASH_ERR_UNSUPPORTED;
-  // the attention CTA's staging must fit one SM's shared memory (227 KB per block)
-  if (attn_cluster_smem(c->n_head / c->n_head_kv, c->head_dim, c->ring_dtype == DFLASH_DTYPE_F32, 0) >
-      232448)
+  // the attention CTA's staging must fit one SM's shared memory (227 KB per block,
+  // 1 KB kept for its static barriers)
+  if (attn_cluster_smem(c->n_head / c->n_head_kv, c->head_dim, c->ring_dtype == DFLASH_DTYPE_F32) >
+      232448 - 1024)
     return DFLASH_ERR_UNSUPPORTED;
   return DFLASH_OK;
 }
@@ -426,18 +423,26 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.epi = EPI_QKV; p.out = h->S<float>(L.qbuf); p.ldo = g.qd;
     p.kblk = h->S<float>(L.kblk); p.vblk = h->S<float>(L.vblk);
     p.q_norm = lw.q_norm; p.k_norm = lw.k_norm; p.rope_cs = rope;
+    {  // this layer's ring K/V of every sequence into L2 for the attention kernel
+      const size_t layer_bytes = L.ring_kv_bytes / g.L;
+      if ((size_t)n_seq * layer_bytes <= kRingPrefetchMax) {
+        p.pf_base = h->ring + (size_t)l * layer_bytes;
+        p.pf_bytes = layer_bytes;
+        p.pf_stride = L.ring_seq_bytes;
+        p.pf_count = n_seq;
+      }
+    }
     PROF(h, PC_QKV, st, launch_projection(h, p, l, {0, 1, 2}, XP_XN, st));
-    // attention over ring chunks + the block, then the chunk merge (-> attn pair)
+    // attention over the ring window + the block (-> attn pair)
     AttnParams a;
     std::memset(&a, 0, sizeof(a));
     a.q = h->S<float>(L.qbuf); a.kblk = h->S<float>(L.kblk); a.vblk = h->S<float>(L.vblk);
     a.ring = h->ring; a.ring_pos = h->ring_pos(0); a.n_past = n_past;
     a.ring_bf16 = g.ring_bf16; a.layer = l; a.n_layer = g.L;
     a.n_head = g.Hq; a.n_head_kv = g.Hkv; a.hd = g.hd; a.window = g.W;
-    a.n_chunks = L.attn_chunks;
     a.scale = (float)(1.0 / std::sqrt((double)g.hd));
-    a.part_acc = h->S<float>(L.apart_acc); a.part_ml = h->S<float>(L.apart_ml);
     a.out_hi = h->S<uint16_t>(L.attn_hi); a.out_lo = h->S<uint16_t>(L.attn_lo);
+    a.status = h->status();
     PROF(h, PC_ATTN, st, launch_attention_cluster(a, n_seq, st));
     // o projection + residual; next input xn = split(h * ffn_norm)
     p = base_params(h);
@@ -605,7 +610,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
   if (e == cudaSuccess && !build_maps(h)) e = cudaErrorNotSupported;
   if (e == cudaSuccess)
     e = configure_attention_cluster(cfg->n_head / cfg->n_head_kv, cfg->head_dim,
-                                    cfg->ring_dtype == DFLASH_DTYPE_F32);
+                                    cfg->ring_dtype == DFLASH_DTYPE_F32, cfg->window,
+                                    cfg->n_head_kv);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {

@@ -48,28 +48,63 @@ DF_DEVICE long long owner_of(long long u, long long U, int G) { return ((u + 1) 
 // CTA order.  Returns true when this CTA must run the tile's epilogue.
 DF_DEVICE bool segment_fixup(const GemmParams& p, float* acc_s, int item, int c0, int c1,
                              long long U, int G, int b, int* s_flag) {
+  constexpr int kVec = 16 * kTileRows / 4;            // float4 per partial tile
+  constexpr int kPer = kVec / kGemmThreads;           // float4 per thread
   const int tid = threadIdx.x;
   if (c0 == 0 && c1 == p.cpt) return true;
   const long long iu0 = (long long)item * p.cpt;
   const int first = (int)owner_of(iu0, U, G);
   const int last = (int)owner_of(iu0 + p.cpt - 1, U, G);
-  const size_t slot = 2 * (size_t)b + (b == first ? 1 : 0);
-  float* part = p.partial + slot * (16 * kTileRows);
-  for (int i = tid; i < 16 * kTileRows; i += kGemmThreads) part[i] = acc_s[i];
-  __threadfence();
+  float4* acc4 = reinterpret_cast<float4*>(acc_s);
+  auto part_of = [&](int c) {
+    const size_t sl = 2 * (size_t)c + (c == first ? 1 : 0);
+    return reinterpret_cast<float4*>(p.partial + sl * (16 * kTileRows));
+  };
+  float4* mine = part_of(b);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) __stcg(mine + tid + k * kGemmThreads, acc4[tid + k * kGemmThreads]);
+  // One thread takes the ticket with an acquire-release atomic after the CTA
+  // barrier: the release publishes every thread's partial (the barrier orders
+  // them before it), the acquire makes all earlier contributors' partials
+  // visible to the winner, whose threads read them after the next barrier.
   csync();
-  if (tid == 0) *s_flag = atomicAdd(p.counters + item, 1) == last - first;
+  if (tid == 0) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(p.counters + item)
+                 : "memory");
+    *s_flag = old == last - first;
+  }
   csync();
   if (!*s_flag) return false;
-  __threadfence();
-  for (int i = tid; i < 16 * kTileRows; i += kGemmThreads) {
-    float sum = 0.f;
-    for (int c = first; c <= last; ++c) {
-      const size_t sl = 2 * (size_t)c + (c == first ? 1 : 0);
-      sum += __ldcg(p.partial + sl * (16 * kTileRows) + i);
-    }
-    acc_s[i] = sum;
+  // Sum the partials in CTA order; the loads of a batch of contributors are all
+  // issued before the first add, so the fix-up costs about one L2 round trip
+  // per batch rather than one per contributor.
+  constexpr int kBatch = 4;
+  float4 sum[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) sum[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int cb = first; cb <= last; cb += kBatch) {
+    float4 v[kBatch][kPer];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+      for (int k = 0; k < kPer; ++k)
+        if (cb + j <= last) v[j][k] = __ldcg(part_of(cb + j) + tid + k * kGemmThreads);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+      for (int k = 0; k < kPer; ++k)
+        if (cb + j <= last) {
+          sum[k].x += v[j][k].x;
+          sum[k].y += v[j][k].y;
+          sum[k].z += v[j][k].z;
+          sum[k].w += v[j][k].w;
+        }
   }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc4[tid + k * kGemmThreads] = sum[k];
   if (tid == 0) p.counters[item] = 0;
   csync();
   return true;
@@ -95,18 +130,32 @@ DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* sca
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = mb * 16;
   const bool logits = p.epi == EPI_LOGITS;
-  for (int i = tid; i < 16 * kTileRows; i += kGemmThreads) {
+  constexpr int kPer = 16 * kTileRows / kGemmThreads;
+  const bool resid = p.epi == EPI_RESID_SS;
+  // the residual rows and next-norm weights this thread needs, all loads first
+  float res[kPer], nw[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = tid + k * kGemmThreads;
+    const int m = i / kTileRows, r = i - m * kTileRows;
+    const int n = tile * kTileRows + r, row = m0 + m;
+    const bool ok = n < p.N && row < p.M;
+    res[k] = resid && ok ? __ldcg(p.out + (size_t)row * p.ldo + n) : 0.f;
+    nw[k] = resid && ok && p.pair_hi ? load_dense(p.pair_norm, p.norm_bf16, n) : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int i = tid + k * kGemmThreads;
     const int m = i / kTileRows, r = i - m * kTileRows;
     const int n = tile * kTileRows + r, row = m0 + m;
     float y = acc_s[i] * scale_s[r];
     if (n < p.N && row < p.M) {
-      if (p.epi == EPI_RESID_SS) {
-        float* o = p.out + (size_t)row * p.ldo + n;
-        y += *o;
-        *o = y;
+      if (resid) {
+        y += res[k];
+        p.out[(size_t)row * p.ldo + n] = y;
         if (p.pair_hi) {
           // the next projection's input: split(h * next norm weight)
-          const float z = y * load_dense(p.pair_norm, p.norm_bf16, n);
+          const float z = y * nw[k];
           const uint16_t zh = f32_to_bf16_bits(z);
           p.pair_hi[(size_t)row * p.pair_ld + n] = zh;
           p.pair_lo[(size_t)row * p.pair_ld + n] = f32_to_bf16_bits(z - bf16_bits_to_f32(zh));
@@ -141,15 +190,18 @@ DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* sca
       p.am_part[(size_t)tile * p.M + m0 + m] = make_float2(v, __int_as_float(idx));
   }
   // the last finished tile of the whole launch reduces the argmax partials
-  __threadfence();
   csync();
-  if (tid == 0) {
+  if (tid == 0) {  // acquire-release ticket, as in segment_fixup
     const int total = p.n_tiles * p.n_mb;
-    *s_flag = atomicAdd(p.am_counter, 1) == total - 1;
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(p.am_counter)
+                 : "memory");
+    *s_flag = old == total - 1;
   }
   csync();
   if (!*s_flag) return;
-  __threadfence();
   for (int row = warp; row < p.M; row += kGemmThreads / 32) {
     const int i = row & 15;
     if (i == 0) continue;

@@ -221,6 +221,23 @@ DF_DEVICE void group_coord(const GemmParams& p, int tile, int grp, int& map, int
   row = vr - p.seg[s].row0;
 }
 
+// This CTA's 1/G share of the prefetch ranges (16-byte aligned pieces of at
+// most 32 KB): the next kernel's input moves into L2 while this kernel's last
+// weight stages are still streaming.
+DF_DEVICE void prefetch_share(const GemmParams& p, int b, int G) {
+  const unsigned long long total = p.pf_bytes * (unsigned long long)p.pf_count;
+  const unsigned long long x0 = (total * b / G) & ~15ull;
+  const unsigned long long x1 = b == G - 1 ? total : (total * (b + 1) / G) & ~15ull;
+  for (unsigned long long x = x0; x < x1;) {
+    const unsigned long long i = x / p.pf_bytes, off = x - i * p.pf_bytes;
+    unsigned long long n = p.pf_bytes - off;
+    if (n > x1 - x) n = x1 - x;
+    if (n > 32768) n = 32768;
+    prefetch_l2(p.pf_base + i * p.pf_stride + off, (uint32_t)n);
+    x += n;
+  }
+}
+
 template <int WT>
 __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __grid_constant__ GemmParams p) {
   using T = TT<WT>;
@@ -297,6 +314,7 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
         }
       }
     }
+    if (p.pf_count > 0) prefetch_share(p, b, G);
     // no copy may still be landing when the CTA exits: wait for the last stages
     for (long long j = it > T::S ? it - T::S : 0; j < it; ++j) {
       if (!mbar_wait(&full[j % T::S], (uint32_t)((j / T::S) & 1))) {

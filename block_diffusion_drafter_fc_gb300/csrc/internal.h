@@ -110,6 +110,11 @@ struct GemmParams {
   float2* am_part;        // [n_tiles][M] (value, index bits)
   int* am_counter;
   int32_t* drafts;        // [M/16][15]
+  // L2 prefetch of the next kernel's input (pf_count ranges of pf_bytes at
+  // pf_stride), shared out over the CTAs once their weight stream is issued
+  const char* pf_base;
+  unsigned long long pf_bytes, pf_stride;
+  int pf_count;
 };
 
 struct AttnParams {
@@ -122,13 +127,13 @@ struct AttnParams {
   int ring_bf16;
   int layer, n_layer;
   int n_head, n_head_kv, hd, window;
-  int n_chunks;           // 64-slot ring chunks (the block is chunk n_chunks)
   float scale;
-  int depth;              // ring sub-chunks in flight per CTA (set by the launcher)
-  float* part_acc;        // [n_seq][Hkv][n_chunks+1][R][hd]
-  float* part_ml;         // [n_seq][Hkv][n_chunks+1][R][2]
+  int hpc;                // query heads per CTA (set by the launcher)
+  int kq;                 // key lanes: warps per head
+  int nb;                 // 64-key sub-chunk staging buffers (a multiple of kq)
   uint16_t* out_hi;       // [M][qd] bf16 hi/lo pair (the o projection's input)
   uint16_t* out_lo;
+  unsigned* status;       // device status bits (DFLASH_DEV_TIMEOUT on a copy that never lands)
 };
 
 size_t gemm_smem_bytes(int wt, int xk);
@@ -145,16 +150,12 @@ size_t gemm_umma_smem_bytes();
 cudaError_t configure_gemm_umma();
 cudaError_t launch_gemm_umma(int wt, const GemmParams& p, cudaStream_t st);
 
-size_t attn_smem_bytes(int group, int hd, int ring_f32);
-cudaError_t configure_attention(size_t smem);
-cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st);
-cudaError_t launch_attn_combine(const AttnParams& p, int n_seq, cudaStream_t st);
 
 // one cluster per (sequence, kv head), partials merged in distributed shared memory
 int attn_cluster_size(int window);
-// depth 0: the largest pipeline depth the launcher may pick
-size_t attn_cluster_smem(int group, int hd, int ring_f32, int depth);
-cudaError_t configure_attention_cluster(int group, int hd, int ring_f32);
+// the largest dynamic shared memory any launch plan of this geometry uses
+size_t attn_cluster_smem(int group, int hd, int ring_f32);
+cudaError_t configure_attention_cluster(int group, int hd, int ring_f32, int window, int n_head_kv);
 cudaError_t launch_attention_cluster(const AttnParams& p, int n_seq, cudaStream_t st);
 
 cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
