@@ -24,11 +24,13 @@ enum Epi {
 };
 enum RowMap { MAP_SEGMENTS = 0, MAP_SWIGLU = 1 };
 
-// Programmatic dependent launch between the step's kernels.  Measured slower
-// than plain stream order inside the replayed graph (2.18 vs 1.78 ms per
-// real-dimension step), so launches do not request it; the kernels keep their
-// griddepcontrol points, which are no-ops without the launch attribute.
-constexpr bool kDependentLaunch = false;
+// Programmatic dependent launch between the step's kernels: a projection's
+// CTAs start (mbarrier set-up, first weight stages in flight) while the
+// previous kernel's last CTAs finish their fix-up and epilogue; everything
+// that reads an earlier kernel's output waits at griddepcontrol.wait, which
+// returns only once that kernel has completed and its writes are visible.
+// Measured 1.042 vs 1.065 ms per real-dimension step in the replayed graph.
+constexpr bool kDependentLaunch = true;
 
 constexpr int kTileRows = 128;     // output rows (weight rows) of one CTA tile
 constexpr int kGemmThreads = 256;  // 8 warps x 16 weight rows
@@ -151,7 +153,8 @@ cudaError_t configure_gemm_umma();
 cudaError_t launch_gemm_umma(int wt, const GemmParams& p, cudaStream_t st);
 
 
-// one cluster per (sequence, kv head), partials merged in distributed shared memory
+// one cluster per (sequence, kv head, query-head group), partials merged in
+// distributed shared memory
 int attn_cluster_size(int window);
 // the largest dynamic shared memory any launch plan of this geometry uses
 size_t attn_cluster_smem(int group, int hd, int ring_f32);
