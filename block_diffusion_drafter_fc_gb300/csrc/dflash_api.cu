@@ -101,7 +101,7 @@ struct Layout {
   size_t status, inv_freq, counters, h, ss, qbuf, kblk, vblk, rope_step, am_part;
   size_t xn_hi, xn_lo, attn_hi, attn_lo, act_hi, act_lo;
   size_t logits_int, drafts_int, idl_int, npast_int, partial;
-  size_t inj_raw, inj_ss, inj_rope, total;
+  size_t inj_raw, inj_ss, inj_rope, loop_pos, loop_cnt, loop_H, total;
   size_t partial_floats;
   int n_counters, ss_parts, ss_ld, lm_tiles;
   size_t ring_seq_bytes, ring_kv_bytes, ring_total;
@@ -154,6 +154,10 @@ Layout layout(const dflash_config& c) {
   L.inj_raw = take(sizeof(float) * (size_t)g.max_inject * g.d);
   L.inj_ss = take(sizeof(float) * (size_t)L.ss_parts * L.ss_ld);
   L.inj_rope = take(sizeof(float2) * (size_t)g.max_inject * (g.hd / 2));
+  // speculative-loop turn: block positions, accepted-row counts, encoded rows
+  L.loop_pos = take(sizeof(int32_t) * (size_t)g.max_seq * DFLASH_BLOCK);
+  L.loop_cnt = take(sizeof(int32_t) * (size_t)g.max_seq);
+  L.loop_H = take(sizeof(float) * (size_t)g.max_seq * DFLASH_BLOCK * g.d);
   L.total = off;
 
   L.ring_kv_bytes = (size_t)g.L * 2 * g.Hkv * g.W * g.hd * (g.ring_bf16 ? 2 : 4);
@@ -634,13 +638,10 @@ void dflash_destroy(dflash_handle* h) {
   delete h;
 }
 
-int dflash_encode(dflash_handle* h, const void* feats, int32_t T, float* H_t, void* stream) {
-  clear_stale_error();
-  if (!h || T < 0) return DFLASH_ERR_INVALID_ARG;
-  if (T > h->g.max_inject) return DFLASH_ERR_TOO_MANY_ROWS;
-  if (T == 0) return DFLASH_OK;
-  if (bad_ptr(feats) || bad_ptr(H_t)) return DFLASH_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+namespace {
+
+// encode T rows (validated by the caller)
+int run_encode(dflash_handle* h, const void* feats, int T, float* H_t, cudaStream_t st) {
   const Geometry& g = h->g;
   GemmShape sh[2];
   inject_shapes(g, sh);
@@ -661,22 +662,17 @@ int dflash_encode(dflash_handle* h, const void* feats, int32_t T, float* H_t, vo
   return DFLASH_OK;
 }
 
-int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, const int32_t* pos, int32_t T,
-                  void* stream) {
-  clear_stale_error();
-  if (!h || T < 0) return DFLASH_ERR_INVALID_ARG;
-  if (seq < 0 || seq >= h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
-  if (T > h->g.W || T > h->g.max_inject) return DFLASH_ERR_TOO_MANY_ROWS;
-  if (T == 0) return DFLASH_OK;
-  if (bad_ptr(H_t) || !pos) return DFLASH_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+// inject T rows: into sequence `seq`'s ring, or (rows_per_seq > 0) row t into
+// sequence t / rows_per_seq, only its first count[sequence] rows
+int run_inject(dflash_handle* h, int seq, const float* H_t, const int32_t* pos, int T,
+               int rows_per_seq, const int32_t* count, cudaStream_t st) {
   const Geometry& g = h->g;
   GemmShape sh[2];
   inject_shapes(g, sh);
   float2* rope = h->S<float2>(h->L.inj_rope);
   prof_begin(h, PC_INJECT, st);
   DF_CHECK(h, launch_rope_table(pos, T, h->S<double>(h->L.inv_freq), g.hd, rope, h->ring_pos(seq),
-                                g.W, h->status(), st));
+                                g.W, rows_per_seq, count, h->status(), st));
   const int n_mb = cdiv(T, 16);
   GemmParams p = base_params(h);
   set_plan(p, sh[1], n_mb);
@@ -689,9 +685,66 @@ int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, const int32_t
   }
   p.nseg = 2 * g.L; p.N = 2 * g.L * g.kvd; p.map = MAP_SEGMENTS;
   p.epi = EPI_INJECT; p.ring_seq = h->ring_seq(seq); p.pos = pos; p.rope_cs = rope;
+  p.rows_per_seq = rows_per_seq; p.row_count = count; p.ring_seq_stride = h->L.ring_seq_bytes;
   DF_CHECK(h, launch_gemm(g.wt, p, st));
   prof_end(h, st);
   return DFLASH_OK;
+}
+
+// accept + bonus token + position update, then encode and inject the accepted
+// rows of every sequence (validated by the caller)
+int run_advance(dflash_handle* h, int n_seq, const int32_t* drafts, const int32_t* targets,
+                const void* feats, int32_t* id_last, int32_t* n_past, int32_t* n_ok,
+                cudaStream_t st) {
+  int32_t* pos = h->S<int32_t>(h->L.loop_pos);
+  int32_t* cnt = h->S<int32_t>(h->L.loop_cnt);
+  float* H = h->S<float>(h->L.loop_H);
+  const int T = n_seq * DFLASH_BLOCK;
+  PROF(h, PC_ACCEPT, st, launch_advance(drafts, targets, n_seq, id_last, n_past, n_ok, pos, cnt, st));
+  int rc = run_encode(h, feats, T, H, st);
+  if (rc != DFLASH_OK) return rc;
+  return run_inject(h, 0, H, pos, T, DFLASH_BLOCK, cnt, st);
+}
+
+int check_advance(const dflash_handle* h, int n_seq) {
+  if (n_seq < 1 || n_seq > h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  if (n_seq * DFLASH_BLOCK > h->g.max_inject || h->g.W < DFLASH_BLOCK) return DFLASH_ERR_TOO_MANY_ROWS;
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+int dflash_encode(dflash_handle* h, const void* feats, int32_t T, float* H_t, void* stream) {
+  clear_stale_error();
+  if (!h || T < 0) return DFLASH_ERR_INVALID_ARG;
+  if (T > h->g.max_inject) return DFLASH_ERR_TOO_MANY_ROWS;
+  if (T == 0) return DFLASH_OK;
+  if (bad_ptr(feats) || bad_ptr(H_t)) return DFLASH_ERR_INVALID_ARG;
+  return run_encode(h, feats, T, H_t, static_cast<cudaStream_t>(stream));
+}
+
+int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, const int32_t* pos, int32_t T,
+                  void* stream) {
+  clear_stale_error();
+  if (!h || T < 0) return DFLASH_ERR_INVALID_ARG;
+  if (seq < 0 || seq >= h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  if (T > h->g.W || T > h->g.max_inject) return DFLASH_ERR_TOO_MANY_ROWS;
+  if (T == 0) return DFLASH_OK;
+  if (bad_ptr(H_t) || !pos) return DFLASH_ERR_INVALID_ARG;
+  return run_inject(h, seq, H_t, pos, T, 0, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int dflash_advance(dflash_handle* h, int32_t n_seq, const int32_t* drafts, const int32_t* targets,
+                   const void* feats, int32_t* id_last, int32_t* n_past, int32_t* n_ok,
+                   void* stream) {
+  clear_stale_error();
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  const int v = check_advance(h, n_seq);
+  if (v != DFLASH_OK) return v;
+  if (!drafts || !targets || bad_ptr(feats) || !id_last || !n_past || !n_ok)
+    return DFLASH_ERR_INVALID_ARG;
+  return run_advance(h, n_seq, drafts, targets, feats, id_last, n_past, n_ok,
+                     static_cast<cudaStream_t>(stream));
 }
 
 int dflash_step(dflash_handle* h, int32_t n_seq, const int32_t* id_last, const int32_t* n_past,
@@ -748,6 +801,35 @@ int dflash_replay(dflash_handle* h, void* stream) {
   if (!h) return DFLASH_ERR_INVALID_ARG;
   if (!h->exec) return DFLASH_ERR_NOT_CAPTURED;
   DF_CHECK(h, cudaGraphLaunch(h->exec, static_cast<cudaStream_t>(stream)));
+  return DFLASH_OK;
+}
+
+int dflash_capture_loop(dflash_handle* h, int32_t n_seq, const int32_t* targets, const void* feats,
+                        int32_t* id_last, int32_t* n_past, int32_t* n_ok, float* logits,
+                        int32_t* drafts, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  const int v = check_advance(h, n_seq);
+  if (v != DFLASH_OK) return v;
+  if (!targets || bad_ptr(feats) || !id_last || !n_past || !n_ok || !drafts)
+    return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DF_CHECK(h, cudaStreamSynchronize(st));
+  if (h->exec) { cudaGraphExecDestroy(h->exec); h->exec = nullptr; }
+  if (h->graph) { cudaGraphDestroy(h->graph); h->graph = nullptr; }
+  DF_CHECK(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  h->capturing = true;
+  int rc = run_advance(h, n_seq, drafts, targets, feats, id_last, n_past, n_ok, h->cap_stream);
+  if (rc == DFLASH_OK) rc = run_step(h, n_seq, id_last, n_past, logits, drafts, h->cap_stream);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
+  h->capturing = false;
+  if (rc != DFLASH_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
+  h->graph = graph;
+  DF_CHECK(h, cudaGraphInstantiate(&h->exec, h->graph, 0));
   return DFLASH_OK;
 }
 

@@ -296,6 +296,11 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
         }
       }
     } else {
+      int sq = 0;
+      if (p.rows_per_seq > 0) {
+        sq = row / p.rows_per_seq;
+        if (p.row_count && row - sq * p.rows_per_seq >= p.row_count[sq]) continue;
+      }
       const int pos = p.pos[row];
       if (pos < 0) {
         if (lane == 0) atomicOr(p.status, 0x2u);
@@ -304,16 +309,17 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
       const int slot = pos % p.window;
       const size_t off =
           ((((size_t)layer * 2 + (kind == 2)) * p.n_head_kv + head) * p.window + slot) * hd;
+      void* ring_base = static_cast<char*>(p.ring_seq) + (size_t)sq * p.ring_seq_stride;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int j = lane + 32 * u;
         if (j >= half) continue;
         if (p.ring_bf16) {
-          uint16_t* d = reinterpret_cast<uint16_t*>(p.ring_seq) + off;
+          uint16_t* d = reinterpret_cast<uint16_t*>(ring_base) + off;
           d[j] = f32_to_bf16_bits(x1[u]);
           d[j + half] = f32_to_bf16_bits(x2[u]);
         } else {
-          float* d = reinterpret_cast<float*>(p.ring_seq) + off;
+          float* d = reinterpret_cast<float*>(ring_base) + off;
           d[j] = x1[u];
           d[j + half] = x2[u];
         }

@@ -106,6 +106,12 @@ struct GemmParams {
   int window;
   int n_head_kv;
   const int32_t* pos;     // [T]
+  // batched injection: row t belongs to sequence t / rows_per_seq (ring at
+  // ring_seq + sequence x ring_seq_stride bytes); rows at or past
+  // row_count[sequence] within their sequence are not written
+  int rows_per_seq;
+  const int32_t* row_count;
+  unsigned long long ring_seq_stride;
   const void* k_norm_l[kMaxLayers];
   unsigned* status;
   // logits epilogue
@@ -167,8 +173,11 @@ cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n
                          const void* norm0, uint16_t* x_hi, uint16_t* x_lo, unsigned* status,
                          cudaStream_t st);
 cudaError_t launch_rope_table(const int32_t* pos, int T, const double* inv_freq, int hd,
-                              float2* rope_cs, int32_t* ring_pos, int window, unsigned* status,
-                              cudaStream_t st);
+                              float2* rope_cs, int32_t* ring_pos, int window, int rows_per_seq,
+                              const int32_t* count, unsigned* status, cudaStream_t st);
+cudaError_t launch_advance(const int32_t* drafts, const int32_t* targets, int n_seq,
+                           int32_t* id_last, int32_t* n_past, int32_t* n_ok, int32_t* pos,
+                           int32_t* count, cudaStream_t st);
 cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss_ld, int T,
                              int n, const void* normw, int norm_bf16, float eps, float* out,
                              cudaStream_t st);

@@ -117,10 +117,13 @@ cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n
   return cudaGetLastError();
 }
 
-// Rope table of injected positions + ring_pos of their slots.
+// Rope table of injected positions + ring_pos of their slots.  With
+// rows_per_seq > 0 the rows belong to consecutive sequences (row t to sequence
+// t / rows_per_seq) and, with a count array, only each sequence's first
+// count[seq] rows claim their slot.
 __global__ void rope_table_kernel(const int32_t* pos, int T, const double* inv_freq, int half,
-                                  float2* rope_cs, int32_t* ring_pos, int window,
-                                  unsigned* status) {
+                                  float2* rope_cs, int32_t* ring_pos, int window, int rows_per_seq,
+                                  const int32_t* count, unsigned* status) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= T * half) return;
   const int t = e / half, j = e - t * half;
@@ -129,7 +132,13 @@ __global__ void rope_table_kernel(const int32_t* pos, int T, const double* inv_f
     if (j == 0) atomicOr(status, 0x2u);
     p = 0;
   } else if (j == 0) {
-    ring_pos[p % window] = p;
+    int sq = 0;
+    bool claim = true;
+    if (rows_per_seq > 0) {
+      sq = t / rows_per_seq;
+      claim = !count || t - sq * rows_per_seq < count[sq];
+    }
+    if (claim) ring_pos[(size_t)sq * window + p % window] = p;
   }
   double sn, cs;
   sincos((double)p * inv_freq[j], &sn, &cs);
@@ -137,12 +146,13 @@ __global__ void rope_table_kernel(const int32_t* pos, int T, const double* inv_f
 }
 
 cudaError_t launch_rope_table(const int32_t* pos, int T, const double* inv_freq, int hd,
-                              float2* rope_cs, int32_t* ring_pos, int window, unsigned* status,
-                              cudaStream_t st) {
+                              float2* rope_cs, int32_t* ring_pos, int window, int rows_per_seq,
+                              const int32_t* count, unsigned* status, cudaStream_t st) {
   const int half = hd / 2;
   if (T <= 0) return cudaSuccess;
   rope_table_kernel<<<(T * half + 255) / 256, 256, 0, st>>>(pos, T, inv_freq, half, rope_cs,
-                                                            ring_pos, window, status);
+                                                            ring_pos, window, rows_per_seq, count,
+                                                            status);
   return cudaGetLastError();
 }
 
@@ -191,6 +201,42 @@ __global__ void accept_kernel(const int32_t* drafts, const int32_t* targets, int
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t* n_ok, int n_seq,
                           cudaStream_t st) {
   accept_kernel<<<(n_seq + 7) / 8, 256, 0, st>>>(drafts, targets, n_ok, n_seq);
+  return cudaGetLastError();
+}
+
+// One turn of the speculative loop after the target's verification, one warp
+// per sequence (dflash_engine.py, DFlashSpeculativeVerifier.verify_block;
+// dflash-ops model card, Usage): m = number of leading drafts equal to the
+// target's tokens; the accepted block rows 0..m (positions n_past .. n_past + m)
+// are the rows to inject, the target's token m becomes the next id_last, and
+// n_past advances by m + 1.  Writes pos[16 s + i] = n_past + i for all 16 rows
+// and count[s] = m + 1.
+__global__ void advance_kernel(const int32_t* drafts, const int32_t* targets, int n_seq,
+                               int32_t* id_last, int32_t* n_past, int32_t* n_ok, int32_t* pos,
+                               int32_t* count) {
+  const int seq = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (seq >= n_seq) return;
+  bool miss = false;
+  if (lane < kBlock - 1) miss = drafts[seq * (kBlock - 1) + lane] != targets[seq * kBlock + lane];
+  const unsigned mask = __ballot_sync(0xffffffffu, miss);
+  const int m = mask ? __ffs(mask) - 1 : kBlock - 1;
+  const int p0 = n_past[seq];
+  __syncwarp();
+  if (lane < kBlock) pos[seq * kBlock + lane] = p0 + lane;
+  if (lane == 0) {
+    n_ok[seq] = m;
+    count[seq] = m + 1;
+    id_last[seq] = targets[seq * kBlock + m];
+    n_past[seq] = p0 + m + 1;
+  }
+}
+
+cudaError_t launch_advance(const int32_t* drafts, const int32_t* targets, int n_seq,
+                           int32_t* id_last, int32_t* n_past, int32_t* n_ok, int32_t* pos,
+                           int32_t* count, cudaStream_t st) {
+  advance_kernel<<<(n_seq + 7) / 8, 256, 0, st>>>(drafts, targets, n_seq, id_last, n_past, n_ok,
+                                                  pos, count);
   return cudaGetLastError();
 }
 

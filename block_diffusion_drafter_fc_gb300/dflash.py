@@ -73,6 +73,8 @@ def _load() -> C.CDLL:
         "dflash_accept": (C.c_int, [vp, i32, vp, vp, vp, vp]),
         "dflash_capture": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_replay": (C.c_int, [vp, vp]),
+        "dflash_advance": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "dflash_capture_loop": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_step_host": (C.c_int, [vp, i32, vp, vp, vp, vp, vp]),
         "dflash_ring_reset": (C.c_int, [vp, i32, vp]),
         "dflash_read_status": (C.c_int, [vp, C.POINTER(C.c_uint32), vp]),
@@ -225,6 +227,16 @@ class Drafter:
 
     def dflash_replay(self, stream=None):
         _check(LIB.dflash_replay(self.h, _stream(stream)), self.h, "replay")
+
+    def dflash_advance(self, drafts, targets, feats, id_last, n_past, n_ok, stream=None):
+        _check(LIB.dflash_advance(self.h, drafts.shape[0], _ptr(drafts), _ptr(targets), _ptr(feats),
+                                  _ptr(id_last), _ptr(n_past), _ptr(n_ok), _stream(stream)),
+               self.h, "advance")
+
+    def dflash_capture_loop(self, targets, feats, id_last, n_past, n_ok, logits, drafts, stream=None):
+        _check(LIB.dflash_capture_loop(self.h, targets.shape[0], _ptr(targets), _ptr(feats),
+                                       _ptr(id_last), _ptr(n_past), _ptr(n_ok), _ptr(logits),
+                                       _ptr(drafts), _stream(stream)), self.h, "capture_loop")
 
     def dflash_step_host(self, id_last: torch.Tensor, n_past: torch.Tensor, drafts: torch.Tensor,
                          logits: Optional[torch.Tensor] = None, stream=None):

@@ -278,6 +278,47 @@ DFLASH_API int dflash_capture(dflash_handle* h, int32_t n_seq, const int32_t* id
 DFLASH_API int dflash_replay(dflash_handle* h, void* stream);
 
 /*
+ * One turn of the speculative loop on the device, after the target model has
+ * verified the block that the last dflash_step drafted (dflash_engine.py,
+ * DFlashSpeculativeVerifier.verify_block: accepted prefix + one bonus token;
+ * dflash-ops model card, Usage: inject(encode(features), positions) of the
+ * verified positions, then the next step(id_last, n_past)).  Per sequence s:
+ *   m = number of leading j in 0..14 with drafts[s][j] == targets[s][j];
+ *   the target features of block rows 0..m (positions n_past[s] .. n_past[s]+m)
+ *   are encoded and injected into sequence s's ring (rows m+1..15 are encoded
+ *   but not written: their slots may still hold keys inside the window);
+ *   n_ok[s] = m; id_last[s] = targets[s][m] (the target's own token after the
+ *   accepted drafts: the correction, or the bonus token when m = 15);
+ *   n_past[s] += m + 1.
+ *   drafts:  device int32 [n_seq][15] (the previous step's drafts);
+ *   targets: device int32 [n_seq][16], the target's greedy token at block rows
+ *            0..15 (row j predicts position n_past + j + 1);
+ *   feats:   device [n_seq][16][n_target_layers*target_embd] in dense_dtype,
+ *            the target's features at block rows 0..15;
+ *   id_last, n_past: device int32 [n_seq], read and updated in place;
+ *   n_ok:    device int32 [n_seq], written.
+ * Requires 16 * n_seq <= max_inject and window >= 16 (TOO_MANY_ROWS
+ * otherwise).  Nothing is read back to the host, so the call can be captured
+ * (dflash_capture_loop).  Asynchronous on `stream`.
+ */
+DFLASH_API int dflash_advance(dflash_handle* h, int32_t n_seq, const int32_t* drafts,
+                              const int32_t* targets, const void* feats, int32_t* id_last,
+                              int32_t* n_past, int32_t* n_ok, void* stream);
+
+/*
+ * Capture one whole loop turn - dflash_advance followed by dflash_step with
+ * the updated id_last / n_past - into the handle's graph (replacing any
+ * previous capture; dflash_replay launches it).  With these exact pointers,
+ * each replay consumes the target's tokens and features for the block drafted
+ * by the previous replay (or step) and leaves the next block's logits and
+ * drafts in `logits` / `drafts`.  Capture runs on an internal stream; nothing
+ * is launched; `stream` orders the capture after earlier work on it.
+ */
+DFLASH_API int dflash_capture_loop(dflash_handle* h, int32_t n_seq, const int32_t* targets,
+                                   const void* feats, int32_t* id_last, int32_t* n_past,
+                                   int32_t* n_ok, float* logits, int32_t* drafts, void* stream);
+
+/*
  * The same step as dflash_step, driven from host memory: copies id_last and
  * n_past (host int32 [n_seq]) to the device, runs the step into internal
  * scratch buffers, copies the drafts back to host int32 [n_seq][15] (and the

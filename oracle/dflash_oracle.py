@@ -390,6 +390,34 @@ def accept(drafts: np.ndarray, targets: np.ndarray) -> np.ndarray:
     return out
 
 
+def advance(w: OracleWeights, rings: List[OracleRing], drafts: np.ndarray, targets: np.ndarray,
+            feats: np.ndarray, id_last: Sequence[int], n_past: Sequence[int]):
+    """One turn of the speculative loop after the target has verified the drafted
+    block (dflash_engine.py, DFlashSpeculativeVerifier.verify_block: the accepted
+    drafts plus one token of the target; dflash-ops model card, Usage: the target's
+    features of the verified positions are encoded and injected before the next
+    step(id_last, n_past)).
+
+    targets[s] holds the target's token at each of the 16 block rows (row j
+    predicts position n_past + j + 1) and feats[s] its features at the 16 block
+    rows.  With m = accept(drafts, targets[:, :15])[s]: block rows 0..m (positions
+    n_past .. n_past + m) are the verified context and are injected; the next
+    anchor is the target's token m; n_past grows by m + 1.  Rings change in place;
+    returns (n_ok, id_last, n_past) as new arrays."""
+    targets = np.asarray(targets)
+    n_ok = accept(drafts, targets[:, :15])
+    new_id = np.zeros((len(rings),), dtype=np.int32)
+    new_np = np.zeros((len(rings),), dtype=np.int32)
+    for s, ring in enumerate(rings):
+        m = int(n_ok[s])
+        p0 = int(n_past[s])
+        H_t = encode(w, np.asarray(feats[s])[:m + 1])
+        inject(w, ring, H_t, np.arange(p0, p0 + m + 1))
+        new_id[s] = targets[s, m]
+        new_np[s] = p0 + m + 1
+    return n_ok, new_id, new_np
+
+
 def _causal_attention(q, k_blk, v_blk, k_ring, v_ring, valid):
     """Comparison variant for the non-causality pin: block key j visible to row i
     only when j <= i.  Not part of the method."""

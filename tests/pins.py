@@ -284,6 +284,67 @@ def _torch_rope(x, pos, inv):
     return torch.cat([zr.real, zr.imag], dim=-1)
 
 
+# ---------------------------------------------------------------- speculative loop turn
+
+def _advance_case(mismatch, seed=31):
+    """tiny_f32 after its prefill: synthetic drafts / targets with the first
+    mismatch at `mismatch` (15 = none) and random target features."""
+    wl = _tiny()
+    cfg = wl.cfg
+    w, rings, _ = OB.oracle_prefill(wl)
+    g = np.random.default_rng(seed)
+    drafts = g.integers(0, cfg.n_vocab, size=(1, 15)).astype(np.int32)
+    targets = g.integers(0, cfg.n_vocab, size=(1, 16)).astype(np.int32)
+    targets[0, :15] = drafts[0]
+    if mismatch < 15:
+        targets[0, mismatch] = (drafts[0, mismatch] + 1) % cfg.n_vocab
+    fdim = cfg.feat_dim
+    feats = O.store(g.standard_normal((1, 16, fdim)), cfg.dense_dtype)
+    return w, rings, drafts, targets, feats, wl.id_last.numpy()[:1], wl.n_past.numpy()[:1]
+
+
+def pin_advance_example():
+    """The verifier example of dflash_engine.py (block 8: 3 drafts accepted, then
+    a mismatch; tau = 4, the last accepted token is the target's token at index 3)
+    carried into the 16-row block: n_ok 3, n_past grows by tau, and the next
+    anchor is the target's token at index 3; targets after index 3 do not matter."""
+    ex = json.loads((GOLDEN / "verify_block_example.json").read_text())
+    w, rings, d, t, f, idl, npast = _advance_case(15)
+    k = len(ex["drafts"])
+    d[0, :k] = ex["drafts"]
+    t[0, :k] = ex["targets"]
+    t[0, k:] = (d[0, k:15].tolist() + [0])[:16 - k]
+    t[0, 5:] = (t[0, 5:] + 7) % 256      # arbitrary after the mismatch
+    n_ok, nid, nnp = O.advance(w, rings, d, t, f, idl, npast)
+    assert int(n_ok[0]) == ex["expect_n_ok"]
+    assert int(nnp[0]) - int(npast[0]) == ex["expect_tau"]
+    assert int(nid[0]) == ex["expect_bonus"]
+
+
+def pin_advance_injects_verified_rows_only():
+    """Only block rows 0..m enter the ring, at positions n_past .. n_past + m: the
+    ring's positions become the old ones plus exactly those, and perturbing the
+    features of rows m+1..15 changes nothing (they are not verified context)."""
+    for m in (0, 4, 15):
+        w, rings, d, t, f, idl, npast = _advance_case(m)
+        before = rings[0].pos.copy()
+        _, nid, nnp = O.advance(w, rings, d, t, f, idl, npast)
+        p0 = int(npast[0])
+        want = before.copy()
+        for p in range(p0, p0 + m + 1):
+            want[p % w.cfg.window] = p
+        assert np.array_equal(rings[0].pos, want), m
+        assert int(nnp[0]) == p0 + m + 1 and int(nid[0]) == int(t[0, m])
+        w2, rings2, d2, t2, f2, _, _ = _advance_case(m)
+        f2 = f2.copy()
+        if m < 15:
+            f2[0, m + 1:] = O.store(np.asarray(O.decode(f2[0, m + 1:], w2.cfg.dense_dtype)) * -3.0 + 1.0,
+                                    w2.cfg.dense_dtype)
+        O.advance(w2, rings2, d2, t2, f2, idl, npast)
+        for l in range(w.cfg.n_layer):
+            assert np.array_equal(rings[0].k[l], rings2[0].k[l]) and np.array_equal(rings[0].v[l], rings2[0].v[l])
+
+
 def pin_encode_inject_vs_torch():
     """H_t and one layer's stored K/V against a torch float64 composition of
     library ops (linear, rms_norm) and rope as a complex rotation."""

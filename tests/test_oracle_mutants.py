@@ -132,6 +132,24 @@ def _silu_on_identity(z):
     return z
 
 
+def _advance_variant(inject_rows, bonus_shift, past_shift):
+    def adv(w, rings, drafts, targets, feats, id_last, n_past):
+        targets = np.asarray(targets)
+        n_ok = _orig["accept"](drafts, targets[:, :15])
+        new_id = np.zeros((len(rings),), dtype=np.int32)
+        new_np = np.zeros((len(rings),), dtype=np.int32)
+        for s, ring in enumerate(rings):
+            m = int(n_ok[s])
+            p0 = int(n_past[s])
+            rows = inject_rows(m)
+            H_t = O.encode(w, np.asarray(feats[s])[:rows])
+            O.inject(w, ring, H_t, np.arange(p0, p0 + rows))
+            new_id[s] = targets[s, min(15, m + bonus_shift)]
+            new_np[s] = p0 + m + 1 + past_shift
+        return n_ok, new_id, new_np
+    return adv
+
+
 MUTANTS = {
     "rmsnorm drops eps": ("rmsnorm", _rms_no_eps),
     "rmsnorm sums instead of mean": ("rmsnorm", _rms_sum),
@@ -157,6 +175,10 @@ MUTANTS = {
     "drafts read rows 0..14": ("greedy_drafts", _drafts_rows_0_14),
     "anchor in the last row": ("block_tokens", _block_tokens_anchor_last),
     "output norm dropped": ("logits_from_hidden", _logits_no_norm),
+    "advance injects all 16 block rows": ("advance", _advance_variant(lambda m: 16, 0, 0)),
+    "advance bonus from the next row": ("advance", _advance_variant(lambda m: m + 1, 1, 0)),
+    "advance n_past grows by n_ok": ("advance", _advance_variant(lambda m: m + 1, 0, -1)),
+    "advance drops the anchor row": ("advance", _advance_variant(lambda m: m, 0, 0)),
 }
 
 
