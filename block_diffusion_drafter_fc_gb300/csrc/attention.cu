@@ -34,6 +34,7 @@ namespace dflash {
 constexpr int kSub = 64;       // keys per sub-chunk
 constexpr int kPad = 8;        // bf16 row padding (conflict-free fragment loads)
 constexpr int kMaxCluster = 8;
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = exp2(x log2 e)
 
 DF_DEVICE uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 DF_DEVICE void mbar_init(uint64_t* bar, uint32_t count) {
@@ -68,6 +69,11 @@ DF_DEVICE void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* b
       : "memory");
 }
 
+DF_DEVICE void ldsm_x4(uint32_t (&r)[4], const void* smem) {
+  const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a));
+}
 DF_DEVICE void ldsm_x4_t(uint32_t (&r)[4], const void* smem) {
   const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -140,17 +146,22 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
 #pragma unroll
   for (int ks = 0; ks < HD / 16; ++ks) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 8; j += 2) {
       if (j < nt) {
-        const uint16_t* kr = k_hi + (8 * j + g) * KS + ks * 16 + 2 * t;
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 8);
-        mma_bf16_16816(S[j], qh[ks], b0, b1);
-        mma_bf16_16816(S[j], ql[ks], b0, b1);
+        // B fragments of key tiles j and j + 1 (k = dims ks*16 .. +15) in one
+        // ldmatrix: lane i addresses key 8 (j + i/16) + i%8, dims + 8 ((i/8)%2)
+        const int lm = lane >> 3;
+        const int off = (8 * (j + (lm >> 1)) + (lane & 7)) * KS + ks * 16 + (lm & 1) * 8;
+        uint32_t b[4];
+        ldsm_x4(b, k_hi + off);
+        mma_bf16_16816(S[j], qh[ks], b[0], b[1]);
+        mma_bf16_16816(S[j], ql[ks], b[0], b[1]);
+        mma_bf16_16816(S[j + 1], qh[ks], b[2], b[3]);
+        mma_bf16_16816(S[j + 1], ql[ks], b[2], b[3]);
         if (SPLIT) {
-          const uint16_t* kl = k_lo + (8 * j + g) * KS + ks * 16 + 2 * t;
-          mma_bf16_16816(S[j], qh[ks], *reinterpret_cast<const uint32_t*>(kl),
-                         *reinterpret_cast<const uint32_t*>(kl + 8));
+          ldsm_x4(b, k_lo + off);
+          mma_bf16_16816(S[j], qh[ks], b[0], b[1]);
+          mma_bf16_16816(S[j + 1], qh[ks], b[2], b[3]);
         }
       }
     }
@@ -183,8 +194,8 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
   t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, 2));
   const float n0 = fmaxf(m0, t0), n1 = fmaxf(m1, t1);
   // rescale the running sums to the new maxima (nothing to rescale while -inf)
-  const float c0 = m0 == -CUDART_INF_F ? 0.f : expf(m0 - n0);
-  const float c1 = m1 == -CUDART_INF_F ? 0.f : expf(m1 - n1);
+  const float c0 = m0 == -CUDART_INF_F ? 0.f : exp2f(m0 - n0);
+  const float c1 = m1 == -CUDART_INF_F ? 0.f : exp2f(m1 - n1);
   m0 = n0;
   m1 = n1;
   float s0 = 0.f, s1 = 0.f;
@@ -193,8 +204,8 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
     if (j < nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        S[j][e] = n0 == -CUDART_INF_F ? 0.f : expf(S[j][e] - n0);
-        S[j][2 + e] = n1 == -CUDART_INF_F ? 0.f : expf(S[j][2 + e] - n1);
+        S[j][e] = n0 == -CUDART_INF_F ? 0.f : exp2f(S[j][e] - n0);
+        S[j][2 + e] = n1 == -CUDART_INF_F ? 0.f : exp2f(S[j][2 + e] - n1);
         s0 += S[j][e];
         s1 += S[j][2 + e];
       }
@@ -424,13 +435,15 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
     }
   }
   stage_kpos(0);
-  // this warp's head: q fragments scaled by 1/sqrt(hd), split into bf16 hi/lo
+  // this warp's head: q fragments scaled by log2(e)/sqrt(hd) (scores in base-2
+  // units: softmax weights are exp2(s - max)), split into bf16 hi/lo
   uint32_t qh[HD / 16][4], ql[HD / 16][4];
+  const float qscale = p.scale * kLog2e;
 #pragma unroll
   for (int ks = 0; ks < HD / 16; ++ks)
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      split_bf16x2(qraw[ks][e].x * p.scale, qraw[ks][e].y * p.scale, qh[ks][e], ql[ks][e]);
+      split_bf16x2(qraw[ks][e].x * qscale, qraw[ks][e].y * qscale, qh[ks][e], ql[ks][e]);
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
   float O[HD / 8][4];
 #pragma unroll
@@ -488,10 +501,10 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
       const int w = warp + q;
       const float4 ml = frag_ml[w * 32 + lane];
       const float n0 = fmaxf(m0, ml.x), n1 = fmaxf(m1, ml.y);
-      const float a0 = m0 == -CUDART_INF_F ? 0.f : expf(m0 - n0);
-      const float b0 = ml.x == -CUDART_INF_F ? 0.f : expf(ml.x - n0);
-      const float a1 = m1 == -CUDART_INF_F ? 0.f : expf(m1 - n1);
-      const float b1 = ml.y == -CUDART_INF_F ? 0.f : expf(ml.y - n1);
+      const float a0 = m0 == -CUDART_INF_F ? 0.f : exp2f(m0 - n0);
+      const float b0 = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - n0);
+      const float a1 = m1 == -CUDART_INF_F ? 0.f : exp2f(m1 - n1);
+      const float b1 = ml.y == -CUDART_INF_F ? 0.f : exp2f(ml.y - n1);
       m0 = n0;
       m1 = n1;
       l0 = a0 * l0 + b0 * ml.z;
@@ -537,7 +550,7 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
     float M = ml.x;
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float wgt = (lane < CL && ml.x != -CUDART_INF_F) ? expf(ml.x - M) : 0.f;
+    const float wgt = (lane < CL && ml.x != -CUDART_INF_F) ? exp2f(ml.x - M) : 0.f;
     float L = wgt * ml.y;
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);

@@ -34,9 +34,11 @@ constexpr int kTile = 128 * 128;       // bytes of one [128 rows x 128 B] swizzl
 constexpr int kRaw = 128 * 64;         // bytes of one raw [128 x 64] E4M3 tile
 constexpr long long kWait = 4000000000LL;
 constexpr int kThreads = 320;          // warps 0-7 epilogue/convert, 8 TMA, 9 MMA
+constexpr int kDRow = kTileRows + 4;   // row stride (floats) of the accumulator copy in smem
 
 // stage: A hi | A lo | B (bf16) | B raw (E4M3 only)
 constexpr int kStage = 3 * kTile + kRaw;
+static_assert(128 * kDRow * 4 <= kS * kStage, "the accumulator copy reuses the stages");
 constexpr int kOffAcc = kS * kStage;                  // 16 x 128 fp32 epilogue tile
 constexpr int kOffInv = kOffAcc + 16 * kTileRows * 4;
 constexpr int kOffScale = kOffInv + 16 * 4;
@@ -266,9 +268,10 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
     const bool ok = s_abort || bar_wait(accb, 0);
     if (!ok && lane == 0) atomicOr(p.status, 0x4u);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    // accumulator -> shared memory tile [128 rows][128 cols] over the pipeline
-    // stages (all MMAs have completed); warp w reads lanes 32(w%4).. and the
-    // column half w/4
+    // accumulator -> shared memory tile [128 rows][128 cols] (row stride
+    // kDRow: the padding spreads the rows of one tcgen05.ld over the banks) over
+    // the pipeline stages (all MMAs have completed); warp w reads lanes
+    // 32(w%4).. and the column half w/4
     float* dtile = reinterpret_cast<float*>(sm);
     {
       const int quad = warp & 3, half = warp >> 2;
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
               "=r"(r[31])
             : "r"(taddr));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        float* drow = dtile + (size_t)row * kTileRows + half * 64 + c * 32;
+        float* drow = dtile + (size_t)row * kDRow + half * 64 + c * 32;
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(drow + e) =
@@ -301,8 +304,10 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
     for (int b = 0; b < 8; ++b) {
       const int mb = mt * 8 + b;
       if (mb * 16 >= p.M) break;
-      for (int i = tid; i < 16 * kTileRows; i += kGemmThreads)
-        acc_s[i] = dtile[(size_t)b * 16 * kTileRows + i];
+      for (int i = tid; i < 16 * kTileRows; i += kGemmThreads) {
+        const int m = i / kTileRows, r = i - m * kTileRows;
+        acc_s[i] = dtile[(size_t)(b * 16 + m) * kDRow + r];
+      }
       if (p.row_scale) compute_inv_rms(p, inv_rms, mb * 16);
       csync();
       run_epilogue(p, acc_s, scale_s, inv_rms, mb, nt, &s_flag);
