@@ -99,6 +99,22 @@ DF_DEVICE void tma_load(void* dst, const CUtensorMap* map, int x, int y, uint64_
       : "memory");
 }
 
+// The same load with an L2 eviction-priority hint (weights: read once per step,
+// so they should not push the activations, partials and ring out of L2).
+DF_DEVICE void tma_load_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                             uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(su32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(su32(bar)), "l"(policy)
+      : "memory");
+}
+DF_DEVICE uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 DF_DEVICE void ldsm_x4(uint32_t (&r)[4], const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -273,6 +289,7 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
+    const uint64_t w_policy = policy_evict_first();
     long long it = 0;
     bool waited = false;
     for (long long u = ub0; u < ub1 && !s_abort;) {
@@ -299,8 +316,8 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
         for (int grp = 0; grp < 8; ++grp)
 #pragma unroll
           for (int wb = 0; wb < T::WBOXES; ++wb)
-            tma_load(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]], k + wb * T::WBOX_K,
-                     grow[grp], &full[st]);
+            tma_load_hint(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]],
+                          k + wb * T::WBOX_K, grow[grp], &full[st], w_policy);
         if (!waited) {  // activations may come from the previous kernel
           pdl_wait();
           waited = true;
