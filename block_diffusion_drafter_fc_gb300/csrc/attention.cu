@@ -137,7 +137,7 @@ template <int HD, bool SPLIT>
 DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql)[HD / 16][4],
                            const uint16_t* k_hi, const uint16_t* k_lo, const uint16_t* v_hi,
                            const uint16_t* v_lo, int KS, int nt, const int* kpos, bool blk, int p0,
-                           int window, float& m0, float& m1, float& l0, float& l1,
+                           int window, int bw, float& m0, float& m1, float& l0, float& l1,
                            float (&O)[HD / 8][4], int lane) {
   const int g = lane >> 2, t = lane & 3;
   float S[8][4];
@@ -175,7 +175,9 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         bool ok0 = true, ok1 = true;
-        if (!blk) {
+        if (blk) {  // block keys past the block's width do not exist
+          ok0 = ok1 = 8 * j + 2 * t + e < bw;
+        } else {
           const int kp = kpos[8 * j + 2 * t + e];
           const bool past = kp >= 0 && kp < p0;
           ok0 = past && q0 - kp < window;
@@ -462,13 +464,13 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
     __syncthreads();  // zeroed rows, slot positions, fp32 tiles and the block keys
     if (j0 == 0 && blk_lane)
       attend_tile<HD, true>(qh, ql, blk_k_hi, blk_k_lo, blk_v_hi, blk_v_lo, KS, 2, nullptr, true,
-                            p0, p.window, m0, m1, l0, l1, O, lane);
+                            p0, p.window, p.block_width, m0, m1, l0, l1, O, lane);
     for (int j = j0 + lk; j < min(n_sub, j0 + nb); j += kq) {
       wait_sub(j, r);
       if (active) {
         const uint16_t* kh = bufs + (j % nb) * buf_elems;
         attend_tile<HD, RING_F32>(qh, ql, kh, kh + 2 * SM::TILE, kh + SM::TILE, kh + 3 * SM::TILE,
-                                  KS, 8, kpos + (j % nb) * kSub, false, p0, p.window, m0, m1, l0,
+                                  KS, 8, kpos + (j % nb) * kSub, false, p0, p.window, 16, m0, m1, l0,
                                   l1, O, lane);
       }
     }
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
     __syncthreads();
     if (blk_lane)
       attend_tile<HD, true>(qh, ql, blk_k_hi, blk_k_lo, blk_v_hi, blk_v_lo, KS, 2, nullptr, true,
-                            p0, p.window, m0, m1, l0, l1, O, lane);
+                            p0, p.window, p.block_width, m0, m1, l0, l1, O, lane);
     __syncthreads();
   }
 

@@ -216,8 +216,10 @@ struct dflash_handle {
   CUtensorMap td_lm;
   CUtensorMap td_xn[2], td_attn[2], td_act[2];
   cudaStream_t cap_stream = nullptr;
-  cudaGraph_t graph = nullptr;
-  cudaGraphExec_t exec = nullptr;
+  // captured graphs, one per block width (a capture bakes its row count)
+  cudaGraph_t graphs[DFLASH_BLOCK + 1] = {};
+  cudaGraphExec_t execs[DFLASH_BLOCK + 1] = {};
+  int width = DFLASH_BLOCK;   // block rows of step / accept / advance / capture
   char err[512];
   // launch-class profiling (eager calls only)
   bool prof = false;
@@ -447,6 +449,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.scale = (float)(1.0 / std::sqrt((double)g.hd));
     a.out_hi = h->S<uint16_t>(L.attn_hi); a.out_lo = h->S<uint16_t>(L.attn_lo);
     a.status = h->status();
+    a.block_width = h->width;
     PROF(h, PC_ATTN, st, launch_attention_cluster(a, n_seq, st));
     // o projection + residual; next input xn = split(h * ffn_norm)
     p = base_params(h);
@@ -492,6 +495,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   p.am_part = h->S<float2>(L.am_part);
   p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
   p.drafts = drafts;
+  p.block_width = h->width;
   PROF(h, PC_LM, st, launch_projection(h, p, -1, {0}, XP_XN, st));
   return DFLASH_OK;
 }
@@ -632,8 +636,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
 void dflash_destroy(dflash_handle* h) {
   if (!h) return;
   for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
-  if (h->exec) cudaGraphExecDestroy(h->exec);
-  if (h->graph) cudaGraphDestroy(h->graph);
+  for (int w = 0; w <= DFLASH_BLOCK; ++w) {
+    if (h->execs[w]) cudaGraphExecDestroy(h->execs[w]);
+    if (h->graphs[w]) cudaGraphDestroy(h->graphs[w]);
+  }
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   delete h;
 }
@@ -700,7 +706,7 @@ int run_advance(dflash_handle* h, int n_seq, const int32_t* drafts, const int32_
   int32_t* cnt = h->S<int32_t>(h->L.loop_cnt);
   float* H = h->S<float>(h->L.loop_H);
   const int T = n_seq * DFLASH_BLOCK;
-  PROF(h, PC_ACCEPT, st, launch_advance(drafts, targets, n_seq, id_last, n_past, n_ok, pos, cnt, st));
+  PROF(h, PC_ACCEPT, st, launch_advance(drafts, targets, n_seq, h->width, id_last, n_past, n_ok, pos, cnt, st));
   int rc = run_encode(h, feats, T, H, st);
   if (rc != DFLASH_OK) return rc;
   return run_inject(h, 0, H, pos, T, DFLASH_BLOCK, cnt, st);
@@ -747,6 +753,13 @@ int dflash_advance(dflash_handle* h, int32_t n_seq, const int32_t* drafts, const
                      static_cast<cudaStream_t>(stream));
 }
 
+int dflash_set_block_width(dflash_handle* h, int32_t width) {
+  if (!h || width < 2 || width > DFLASH_BLOCK) return DFLASH_ERR_INVALID_ARG;
+  if (h->capturing) return DFLASH_ERR_INVALID_ARG;
+  h->width = width;
+  return DFLASH_OK;
+}
+
 int dflash_step(dflash_handle* h, int32_t n_seq, const int32_t* id_last, const int32_t* n_past,
                 float* logits, int32_t* drafts, void* stream) {
   if (!h) return DFLASH_ERR_INVALID_ARG;
@@ -762,7 +775,7 @@ int dflash_accept(dflash_handle* h, int32_t n_seq, const int32_t* drafts, const 
   if (!drafts || !targets || !n_ok) return DFLASH_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   clear_stale_error();
-  PROF(h, PC_ACCEPT, st, launch_accept(drafts, targets, n_ok, n_seq, st));
+  PROF(h, PC_ACCEPT, st, launch_accept(drafts, targets, n_ok, n_seq, h->width, st));
   return DFLASH_OK;
 }
 
@@ -775,13 +788,16 @@ int dflash_capture(dflash_handle* h, int32_t n_seq, const int32_t* id_last, cons
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // order the capture after the caller's queued work (nothing is launched here)
   DF_CHECK(h, cudaStreamSynchronize(st));
-  if (h->exec) { cudaGraphExecDestroy(h->exec); h->exec = nullptr; }
-  if (h->graph) { cudaGraphDestroy(h->graph); h->graph = nullptr; }
+  {
+    const int w = h->width;
+    if (h->execs[w]) { cudaGraphExecDestroy(h->execs[w]); h->execs[w] = nullptr; }
+    if (h->graphs[w]) { cudaGraphDestroy(h->graphs[w]); h->graphs[w] = nullptr; }
+  }
   DF_CHECK(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
   h->capturing = true;
   int rc = run_step(h, n_seq, id_last, n_past, logits, drafts, h->cap_stream);
   if (rc == DFLASH_OK && targets) {
-    cudaError_t e = launch_accept(drafts, targets, n_ok, n_seq, h->cap_stream);
+    cudaError_t e = launch_accept(drafts, targets, n_ok, n_seq, h->width, h->cap_stream);
     if (e != cudaSuccess) rc = cuda_fail(h, e, "accept (capture)");
   }
   cudaGraph_t graph = nullptr;
@@ -792,15 +808,15 @@ int dflash_capture(dflash_handle* h, int32_t n_seq, const int32_t* id_last, cons
     return rc;
   }
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
-  h->graph = graph;
-  DF_CHECK(h, cudaGraphInstantiate(&h->exec, h->graph, 0));
+  h->graphs[h->width] = graph;
+  DF_CHECK(h, cudaGraphInstantiate(&h->execs[h->width], graph, 0));
   return DFLASH_OK;
 }
 
 int dflash_replay(dflash_handle* h, void* stream) {
   if (!h) return DFLASH_ERR_INVALID_ARG;
-  if (!h->exec) return DFLASH_ERR_NOT_CAPTURED;
-  DF_CHECK(h, cudaGraphLaunch(h->exec, static_cast<cudaStream_t>(stream)));
+  if (!h->execs[h->width]) return DFLASH_ERR_NOT_CAPTURED;
+  DF_CHECK(h, cudaGraphLaunch(h->execs[h->width], static_cast<cudaStream_t>(stream)));
   return DFLASH_OK;
 }
 
@@ -814,8 +830,11 @@ int dflash_capture_loop(dflash_handle* h, int32_t n_seq, const int32_t* targets,
     return DFLASH_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   DF_CHECK(h, cudaStreamSynchronize(st));
-  if (h->exec) { cudaGraphExecDestroy(h->exec); h->exec = nullptr; }
-  if (h->graph) { cudaGraphDestroy(h->graph); h->graph = nullptr; }
+  {
+    const int w = h->width;
+    if (h->execs[w]) { cudaGraphExecDestroy(h->execs[w]); h->execs[w] = nullptr; }
+    if (h->graphs[w]) { cudaGraphDestroy(h->graphs[w]); h->graphs[w] = nullptr; }
+  }
   DF_CHECK(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
   h->capturing = true;
   int rc = run_advance(h, n_seq, drafts, targets, feats, id_last, n_past, n_ok, h->cap_stream);
@@ -828,8 +847,8 @@ int dflash_capture_loop(dflash_handle* h, int32_t n_seq, const int32_t* targets,
     return rc;
   }
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
-  h->graph = graph;
-  DF_CHECK(h, cudaGraphInstantiate(&h->exec, h->graph, 0));
+  h->graphs[h->width] = graph;
+  DF_CHECK(h, cudaGraphInstantiate(&h->execs[h->width], graph, 0));
   return DFLASH_OK;
 }
 

@@ -212,7 +212,7 @@ DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* sca
       argmax_merge(v, idx, e.x, __float_as_int(e.y));
     }
     warp_argmax(v, idx);
-    if (lane == 0) p.drafts[(row >> 4) * 15 + i - 1] = idx;
+    if (lane == 0) p.drafts[(row >> 4) * 15 + i - 1] = i < p.block_width ? idx : -1;
   }
   if (tid == 0) *p.am_counter = 0;
 }

@@ -117,7 +117,8 @@ struct GemmParams {
   // logits epilogue
   float2* am_part;        // [n_tiles][M] (value, index bits)
   int* am_counter;
-  int32_t* drafts;        // [M/16][15]
+  int32_t* drafts;        // [M/16][15]; rows at or past block_width draft -1
+  int block_width;
   // L2 prefetch of the next kernel's input (pf_count ranges of pf_bytes at
   // pf_stride), shared out over the CTAs once their weight stream is issued
   const char* pf_base;
@@ -142,6 +143,7 @@ struct AttnParams {
   uint16_t* out_hi;       // [M][qd] bf16 hi/lo pair (the o projection's input)
   uint16_t* out_lo;
   unsigned* status;       // device status bits (DFLASH_DEV_TIMEOUT on a copy that never lands)
+  int block_width;        // block rows that exist (2..16): block keys at or past it are masked
 };
 
 size_t gemm_smem_bytes(int wt, int xk);
@@ -175,14 +177,14 @@ cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n
 cudaError_t launch_rope_table(const int32_t* pos, int T, const double* inv_freq, int hd,
                               float2* rope_cs, int32_t* ring_pos, int window, int rows_per_seq,
                               const int32_t* count, unsigned* status, cudaStream_t st);
-cudaError_t launch_advance(const int32_t* drafts, const int32_t* targets, int n_seq,
+cudaError_t launch_advance(const int32_t* drafts, const int32_t* targets, int n_seq, int width,
                            int32_t* id_last, int32_t* n_past, int32_t* n_ok, int32_t* pos,
                            int32_t* count, cudaStream_t st);
 cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss_ld, int T,
                              int n, const void* normw, int norm_bf16, float eps, float* out,
                              cudaStream_t st);
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t* n_ok, int n_seq,
-                          cudaStream_t st);
+                          int width, cudaStream_t st);
 cudaError_t launch_fill_i32(int32_t* p, int n, int32_t v, cudaStream_t st);
 
 }  // namespace dflash

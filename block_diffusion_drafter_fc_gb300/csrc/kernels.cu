@@ -188,19 +188,20 @@ cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss
 // matches (15 when none): dflash-ops model card, Usage (device-side accept) and
 // dflash_engine.py, DFlashSpeculativeVerifier.verify_block.
 __global__ void accept_kernel(const int32_t* drafts, const int32_t* targets, int32_t* n_ok,
-                              int n_seq) {
+                              int n_seq, int width) {
   const int seq = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (seq >= n_seq) return;
   bool miss = false;
-  if (lane < kBlock - 1) miss = drafts[seq * (kBlock - 1) + lane] != targets[seq * (kBlock - 1) + lane];
+  if (lane < kBlock - 1)
+    miss = lane >= width - 1 || drafts[seq * (kBlock - 1) + lane] != targets[seq * (kBlock - 1) + lane];
   const unsigned mask = __ballot_sync(0xffffffffu, miss);
   if (lane == 0) n_ok[seq] = mask ? __ffs(mask) - 1 : kBlock - 1;
 }
 
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t* n_ok, int n_seq,
-                          cudaStream_t st) {
-  accept_kernel<<<(n_seq + 7) / 8, 256, 0, st>>>(drafts, targets, n_ok, n_seq);
+                          int width, cudaStream_t st) {
+  accept_kernel<<<(n_seq + 7) / 8, 256, 0, st>>>(drafts, targets, n_ok, n_seq, width);
   return cudaGetLastError();
 }
 
@@ -211,14 +212,15 @@ cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t
 // are the rows to inject, the target's token m becomes the next id_last, and
 // n_past advances by m + 1.  Writes pos[16 s + i] = n_past + i for all 16 rows
 // and count[s] = m + 1.
-__global__ void advance_kernel(const int32_t* drafts, const int32_t* targets, int n_seq,
+__global__ void advance_kernel(const int32_t* drafts, const int32_t* targets, int n_seq, int width,
                                int32_t* id_last, int32_t* n_past, int32_t* n_ok, int32_t* pos,
                                int32_t* count) {
   const int seq = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (seq >= n_seq) return;
   bool miss = false;
-  if (lane < kBlock - 1) miss = drafts[seq * (kBlock - 1) + lane] != targets[seq * kBlock + lane];
+  if (lane < kBlock - 1)
+    miss = lane >= width - 1 || drafts[seq * (kBlock - 1) + lane] != targets[seq * kBlock + lane];
   const unsigned mask = __ballot_sync(0xffffffffu, miss);
   const int m = mask ? __ffs(mask) - 1 : kBlock - 1;
   const int p0 = n_past[seq];
@@ -232,11 +234,11 @@ __global__ void advance_kernel(const int32_t* drafts, const int32_t* targets, in
   }
 }
 
-cudaError_t launch_advance(const int32_t* drafts, const int32_t* targets, int n_seq,
+cudaError_t launch_advance(const int32_t* drafts, const int32_t* targets, int n_seq, int width,
                            int32_t* id_last, int32_t* n_past, int32_t* n_ok, int32_t* pos,
                            int32_t* count, cudaStream_t st) {
-  advance_kernel<<<(n_seq + 7) / 8, 256, 0, st>>>(drafts, targets, n_seq, id_last, n_past, n_ok,
-                                                  pos, count);
+  advance_kernel<<<(n_seq + 7) / 8, 256, 0, st>>>(drafts, targets, n_seq, width, id_last, n_past,
+                                                  n_ok, pos, count);
   return cudaGetLastError();
 }
 

@@ -74,6 +74,7 @@ def _load() -> C.CDLL:
         "dflash_capture": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_replay": (C.c_int, [vp, vp]),
         "dflash_advance": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
+        "dflash_set_block_width": (C.c_int, [vp, i32]),
         "dflash_capture_loop": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_step_host": (C.c_int, [vp, i32, vp, vp, vp, vp, vp]),
         "dflash_ring_reset": (C.c_int, [vp, i32, vp]),
@@ -227,6 +228,9 @@ class Drafter:
 
     def dflash_replay(self, stream=None):
         _check(LIB.dflash_replay(self.h, _stream(stream)), self.h, "replay")
+
+    def dflash_set_block_width(self, width: int):
+        _check(LIB.dflash_set_block_width(self.h, int(width)), self.h, "set_block_width")
 
     def dflash_advance(self, drafts, targets, feats, id_last, n_past, n_ok, stream=None):
         _check(LIB.dflash_advance(self.h, drafts.shape[0], _ptr(drafts), _ptr(targets), _ptr(feats),

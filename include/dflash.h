@@ -235,6 +235,21 @@ DFLASH_API int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, co
                   int32_t T, void* stream);
 
 /*
+ * Block width of the following steps, accepts, loop turns and captures
+ * (dflash_head.rs, set_block_g: the scheduler's narrower block of the anchor
+ * plus num_drafts mask rows, clamped to 2..16; its propose graphs are keyed by
+ * width because a capture bakes its row count).  With width B the block holds
+ * rows 0..B-1 at positions n_past .. n_past+B-1 ([id_last, mask x (B-1)]),
+ * every row attends to the B block keys (and the ring); drafts j >= B-1 are
+ * written as -1; logits rows >= B are computed but are not part of the result;
+ * accept and advance count at most B-1 drafts.  dflash_capture and
+ * dflash_capture_loop store one graph per width, and dflash_replay launches
+ * the current width's graph.  2 <= width <= 16 (INVALID_ARG otherwise, or
+ * while a capture is running).  Default 16.
+ */
+DFLASH_API int dflash_set_block_width(dflash_handle* h, int32_t width);
+
+/*
  * One block step for sequences 0..n_seq-1 (dflash-ops model card, Usage:
  * step(id_last, n_past) -> logits [16, n_vocab]; drafts = argmax of rows 1..15).
  *   id_last: device int32 [n_seq], the anchor token of each block;

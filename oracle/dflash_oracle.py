@@ -275,12 +275,12 @@ def inject(w: OracleWeights, ring: OracleRing, H_t: np.ndarray, positions: Seque
 # the block step
 # ---------------------------------------------------------------------------
 
-def ring_mask(ring_pos: np.ndarray, n_past: int, window: int) -> np.ndarray:
-    """valid[i, s] for block row i (position n_past + i) and ring slot s: the slot
-    holds a past position p (0 <= p < n_past) within the window,
+def ring_mask(ring_pos: np.ndarray, n_past: int, window: int, rows: int = BLOCK) -> np.ndarray:
+    """valid[i, s] for block row i (position n_past + i, i < rows) and ring slot
+    s: the slot holds a past position p (0 <= p < n_past) within the window,
     (n_past + i) - p < window (dflash-ops model card, Method)."""
     p = np.asarray(ring_pos, dtype=np.int64)[None, :]
-    q = n_past + np.arange(BLOCK, dtype=np.int64)[:, None]
+    q = n_past + np.arange(rows, dtype=np.int64)[:, None]
     return (p >= 0) & (p < n_past) & (q - p < window)
 
 
@@ -309,10 +309,12 @@ def attention(q: np.ndarray, k_blk: np.ndarray, v_blk: np.ndarray,
     return out
 
 
-def block_tokens(cfg: OracleConfig, id_last: int) -> np.ndarray:
-    """[id_last, mask x 15]: the anchor then the mask tokens (dflash-ops model
-    card, Method; dflash_head.rs field mask_token_id)."""
-    t = np.full((BLOCK,), cfg.mask_token_id, dtype=np.int64)
+def block_tokens(cfg: OracleConfig, id_last: int, width: int = BLOCK) -> np.ndarray:
+    """[id_last, mask x (width - 1)]: the anchor then the mask tokens (dflash-ops
+    model card, Method; dflash_head.rs field mask_token_id).  The block holds
+    width rows: 16 by default, or the scheduler's narrower block_g
+    (dflash_head.rs, set_block_g: the anchor plus num_drafts mask rows)."""
+    t = np.full((width,), cfg.mask_token_id, dtype=np.int64)
     t[0] = id_last
     return t
 
@@ -320,31 +322,32 @@ def block_tokens(cfg: OracleConfig, id_last: int) -> np.ndarray:
 def step_hidden(w: OracleWeights, rings: List[OracleRing], tokens: np.ndarray,
                 n_past: Sequence[int], causal: bool = False) -> np.ndarray:
     """Final hidden state (before the output norm) of every block row.
-    tokens [n_seq, 16]; returns float64 [n_seq, 16, n_embd].  `causal=True` is a
-    comparison variant used only by the tests (block keys j <= i)."""
+    tokens [n_seq, B] (B = block width, 16 by default); returns float64
+    [n_seq, B, n_embd].  `causal=True` is a comparison variant used only by the
+    tests (block keys j <= i)."""
     cfg = w.cfg
-    n_seq = tokens.shape[0]
+    n_seq, B = tokens.shape
     inv_freq = inv_freq_table(cfg.rope_theta, cfg.head_dim)
     hd, hq, hkv = cfg.head_dim, cfg.n_head, cfg.n_head_kv
-    h = w.rows("tok_embd", tokens.reshape(-1)).reshape(n_seq, BLOCK, cfg.n_embd)
-    pos = np.asarray(n_past, dtype=np.int64)[:, None] + np.arange(BLOCK)[None, :]
+    h = w.rows("tok_embd", tokens.reshape(-1)).reshape(n_seq, B, cfg.n_embd)
+    pos = np.asarray(n_past, dtype=np.int64)[:, None] + np.arange(B)[None, :]
     for layer in range(cfg.n_layer):
         L = f"l{layer}."
         x = rmsnorm(h, w.get(L + "attn_norm"), cfg.eps)
-        q = linear(x, w.get(L + "wq")).reshape(n_seq, BLOCK, hq, hd)
-        k = linear(x, w.get(L + "wk")).reshape(n_seq, BLOCK, hkv, hd)
-        v = linear(x, w.get(L + "wv")).reshape(n_seq, BLOCK, hkv, hd)
+        q = linear(x, w.get(L + "wq")).reshape(n_seq, B, hq, hd)
+        k = linear(x, w.get(L + "wk")).reshape(n_seq, B, hkv, hd)
+        v = linear(x, w.get(L + "wv")).reshape(n_seq, B, hkv, hd)
         q = rope_neox(rmsnorm(q, w.get(L + "q_norm"), cfg.eps), pos, inv_freq)
         k = rope_neox(rmsnorm(k, w.get(L + "k_norm"), cfg.eps), pos, inv_freq)
-        att = np.zeros((n_seq, BLOCK, hq, hd))
+        att = np.zeros((n_seq, B, hq, hd))
         for s in range(n_seq):
             kr, vr = rings[s].values(layer)
-            valid = ring_mask(rings[s].pos, int(n_past[s]), cfg.window)
+            valid = ring_mask(rings[s].pos, int(n_past[s]), cfg.window, B)
             if causal:
                 att[s] = _causal_attention(q[s], k[s], v[s], kr, vr, valid)
             else:
                 att[s] = attention(q[s], k[s], v[s], kr, vr, valid)
-        h = h + linear(att.reshape(n_seq, BLOCK, hq * hd), w.get(L + "wo"))
+        h = h + linear(att.reshape(n_seq, B, hq * hd), w.get(L + "wo"))
         x2 = rmsnorm(h, w.get(L + "ffn_norm"), cfg.eps)
         mlp = silu(linear(x2, w.get(L + "gate"))) * linear(x2, w.get(L + "up"))
         h = h + linear(mlp, w.get(L + "down"))
@@ -366,10 +369,10 @@ def greedy_drafts(logits: np.ndarray) -> np.ndarray:
 
 
 def step(w: OracleWeights, rings: List[OracleRing], id_last: Sequence[int],
-         n_past: Sequence[int]):
-    """One block step for n_seq sequences: (logits float64 [n_seq, 16, V],
-    drafts int32 [n_seq, 15])."""
-    tokens = np.stack([block_tokens(w.cfg, int(t)) for t in id_last])
+         n_past: Sequence[int], width: int = BLOCK):
+    """One block step of `width` rows for n_seq sequences: (logits float64
+    [n_seq, width, V], drafts int32 [n_seq, width - 1])."""
+    tokens = np.stack([block_tokens(w.cfg, int(t), width) for t in id_last])
     h = step_hidden(w, rings, tokens, n_past)
     logits = logits_from_hidden(w, h)
     return logits, greedy_drafts(logits)
@@ -398,14 +401,15 @@ def advance(w: OracleWeights, rings: List[OracleRing], drafts: np.ndarray, targe
     features of the verified positions are encoded and injected before the next
     step(id_last, n_past)).
 
-    targets[s] holds the target's token at each of the 16 block rows (row j
-    predicts position n_past + j + 1) and feats[s] its features at the 16 block
-    rows.  With m = accept(drafts, targets[:, :15])[s]: block rows 0..m (positions
+    targets[s] holds the target's token at each block row (row j predicts
+    position n_past + j + 1) and feats[s] its features at the block rows; drafts
+    has one column per drafted row (15 for a 16-row block).  With
+    m = accept(drafts, targets[:, :drafts.shape[1]])[s]: block rows 0..m (positions
     n_past .. n_past + m) are the verified context and are injected; the next
     anchor is the target's token m; n_past grows by m + 1.  Rings change in place;
     returns (n_ok, id_last, n_past) as new arrays."""
     targets = np.asarray(targets)
-    n_ok = accept(drafts, targets[:, :15])
+    n_ok = accept(drafts, targets[:, :np.asarray(drafts).shape[1]])
     new_id = np.zeros((len(rings),), dtype=np.int32)
     new_np = np.zeros((len(rings),), dtype=np.int32)
     for s, ring in enumerate(rings):

@@ -381,35 +381,37 @@ def pin_encode_inject_vs_torch():
 
 # ---------------------------------------------------------------- whole step
 
-def _torch_step(w, rings, id_last, n_past):
+def _torch_step(w, rings, id_last, n_past, B=BLOCK):
     """The block step composed from torch float64 library ops: embedding,
     rms_norm, linear, SDPA with an explicit mask and grouped kv heads, silu."""
     cfg = w.cfg
     n_seq = len(id_last)
     T = lambda a: torch.from_numpy(np.ascontiguousarray(a))
     inv = T(O.inv_freq_table(cfg.rope_theta, cfg.head_dim))
-    tok = torch.full((n_seq, BLOCK), cfg.mask_token_id, dtype=torch.int64)
+    tok = torch.full((n_seq, B), cfg.mask_token_id, dtype=torch.int64)
     tok[:, 0] = torch.as_tensor(np.asarray(id_last, dtype=np.int64))
     h = F.embedding(tok, T(w.get("tok_embd")))
     hd, hq, hkv = cfg.head_dim, cfg.n_head, cfg.n_head_kv
     for layer in range(cfg.n_layer):
         L = f"l{layer}."
         x = F.rms_norm(h, (cfg.n_embd,), T(w.get(L + "attn_norm")), eps=cfg.eps)
-        q = F.linear(x, T(w.get(L + "wq"))).view(n_seq, BLOCK, hq, hd)
-        k = F.linear(x, T(w.get(L + "wk"))).view(n_seq, BLOCK, hkv, hd)
-        v = F.linear(x, T(w.get(L + "wv"))).view(n_seq, BLOCK, hkv, hd)
+        q = F.linear(x, T(w.get(L + "wq"))).view(n_seq, B, hq, hd)
+        k = F.linear(x, T(w.get(L + "wk"))).view(n_seq, B, hkv, hd)
+        v = F.linear(x, T(w.get(L + "wv"))).view(n_seq, B, hkv, hd)
         q = F.rms_norm(q, (hd,), T(w.get(L + "q_norm")), eps=cfg.eps)
         k = F.rms_norm(k, (hd,), T(w.get(L + "k_norm")), eps=cfg.eps)
         outs = []
         for s in range(n_seq):
-            pos = torch.arange(BLOCK) + int(n_past[s])
+            pos = torch.arange(B) + int(n_past[s])
             qs = _torch_rope(q[s], pos, inv)
             ks = _torch_rope(k[s], pos, inv)
             kr, vr = rings[s].values(layer)
-            valid = O.ring_mask(rings[s].pos, int(n_past[s]), cfg.window)
+            p_ = np.asarray(rings[s].pos, dtype=np.int64)[None, :]
+            q_ = int(n_past[s]) + np.arange(B)[:, None]
+            valid = (p_ >= 0) & (p_ < int(n_past[s])) & (q_ - p_ < cfg.window)
             outs.append(torch.from_numpy(_sdpa_reference(qs.numpy(), ks.numpy(), v[s].numpy(),
                                                          kr, vr, valid)))
-        att = torch.stack(outs).reshape(n_seq, BLOCK, hq * hd)
+        att = torch.stack(outs).reshape(n_seq, B, hq * hd)
         h = h + F.linear(att, T(w.get(L + "wo")))
         x2 = F.rms_norm(h, (cfg.n_embd,), T(w.get(L + "ffn_norm")), eps=cfg.eps)
         h = h + F.linear(F.silu(F.linear(x2, T(w.get(L + "gate")))) * F.linear(x2, T(w.get(L + "up"))),
@@ -425,6 +427,20 @@ def pin_step_vs_torch():
     ref = _torch_step(w, rings, wl.id_last.numpy(), wl.n_past.numpy())
     _close(logits, ref, 1e-10, "step vs torch composition")
     assert np.array_equal(drafts, np.argmax(ref.astype(np.float32)[:, 1:], axis=-1))
+
+
+def pin_step_width_vs_torch():
+    """Narrow blocks (dflash_head.rs, set_block_g: the anchor plus num_drafts
+    mask rows, at least 2): the torch composition over B rows, with the window
+    rule written out here rather than taken from the oracle."""
+    wl = _ragged()
+    w, rings, _ = OB.oracle_prefill(wl)
+    for B in (2, 5):
+        logits, drafts = O.step(w, rings, wl.id_last.numpy(), wl.n_past.numpy(), width=B)
+        assert logits.shape[1] == B and drafts.shape[1] == B - 1
+        ref = _torch_step(w, rings, wl.id_last.numpy(), wl.n_past.numpy(), B=B)
+        _close(logits, ref, 1e-10, f"width {B} step vs torch composition")
+        assert np.array_equal(drafts, np.argmax(ref.astype(np.float32)[:, 1:], axis=-1))
 
 
 def pin_ring_wraparound():
