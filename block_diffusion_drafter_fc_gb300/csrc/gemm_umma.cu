@@ -2,25 +2,29 @@
 // steps with at least 128 activation rows (the cross-sequence batch of
 // dflash_head.rs, struct DflashBatch: 16 rows per sequence).
 //
-// One CTA computes one 128 x 128 output tile D[act row][weight row] over the
-// whole k range, accumulating in tensor memory:
-//   warp 8 (one lane)  TMA producer: per 64-wide k chunk, the activation hi and
-//                      lo boxes [128 rows x 128 B] and the weight box(es) into a
-//                      3-stage shared-memory ring (128-byte swizzle, the UMMA
-//                      K-major canonical layout);
-//   warps 0..7         E4M3 weights only: widen the raw [128 x 64] byte tile to
-//                      the bf16 swizzled tile the MMA reads (exact), then fence
-//                      the generic-proxy writes for the async proxy;
-//   warp 9 (one lane)  allocates 128 TMEM columns and issues, per k16 step,
-//                      tcgen05.mma kind::f16 (bf16 x bf16, fp32 accumulate) for
-//                      the activation hi part and again for the lo part (the
-//                      fp32 activations are split into bf16 hi + lo); commits
-//                      each stage back to the producer and the tile to the
-//                      epilogue;
-//   warps 0..7         read the accumulator with tcgen05.ld into shared memory
-//                      and run the fused epilogues of the 16-row kernels on each
-//                      16-row block (RMS row scale, per-head q/k norm + rope,
-//                      residual + next input, SwiGLU, logits + argmax).
+// Persistent: one CTA per SM walks output tiles D[128 activation rows][128
+// weight rows] (tile t = CTA, CTA + grid, ...; consecutive tiles share a weight
+// tile across the activation row blocks, so weights come from HBM once), each
+// over the whole k range, with the accumulator double-buffered in tensor memory
+// so that a tile's epilogue overlaps the next tile's MMAs:
+//   warp 12 (one lane)  TMA producer: per 64-wide k chunk, the activation hi and
+//                       lo boxes [128 rows x 128 B] and the weight box(es) into
+//                       a 3-stage shared-memory ring (128-byte swizzle, the UMMA
+//                       K-major canonical layout), across tile boundaries;
+//   warps 8..11         E4M3 weights only: widen the raw [128 x 64] byte tile to
+//                       the bf16 swizzled tile the MMA reads (exact), then fence
+//                       the generic-proxy writes for the async proxy;
+//   warp 13 (one lane)  allocates 2 x 128 TMEM columns and issues, per k16 step,
+//                       tcgen05.mma kind::f16 (bf16 x bf16, fp32 accumulate) for
+//                       the activation hi part and again for the lo part (the
+//                       fp32 activations are split into bf16 hi + lo) into the
+//                       tile's accumulator buffer; commits each stage back to
+//                       the producer and each finished tile to the epilogue;
+//   warps 0..7          per 32-lane quadrant of the accumulator, tcgen05.ld into
+//                       two 16-row blocks in shared memory and the fused
+//                       epilogues of the 16-row kernels on each (RMS row scale,
+//                       per-head q/k norm + rope, residual + next input, SwiGLU,
+//                       logits + argmax); then hand the buffer back to the MMA.
 // Every mbarrier wait gives up after ~2 s with DFLASH_DEV_TIMEOUT; tensor memory
 // is always released before exit.
 #include "gemm_common.cuh"
@@ -33,17 +37,19 @@ constexpr int kS = 3;                  // pipeline stages
 constexpr int kTile = 128 * 128;       // bytes of one [128 rows x 128 B] swizzled tile
 constexpr int kRaw = 128 * 64;         // bytes of one raw [128 x 64] E4M3 tile
 constexpr long long kWait = 4000000000LL;
-constexpr int kThreads = 320;          // warps 0-7 epilogue/convert, 8 TMA, 9 MMA
-constexpr int kDRow = kTileRows + 4;   // row stride (floats) of the accumulator copy in smem
+constexpr int kThreads = 448;          // warps 0-7 epilogue, 8-11 E4M3 widening, 12 TMA, 13 MMA
+constexpr int kWiden = 4;              // widening warps
+constexpr int kAccCols = 128;          // TMEM columns of one accumulator buffer
 
 // stage: A hi | A lo | B (bf16) | B raw (E4M3 only)
 constexpr int kStage = 3 * kTile + kRaw;
-static_assert(128 * kDRow * 4 <= kS * kStage, "the accumulator copy reuses the stages");
-constexpr int kOffAcc = kS * kStage;                  // 16 x 128 fp32 epilogue tile
+constexpr int kBRow = kTileRows + 4;                  // padded row (floats) of a read-out block
+constexpr int kOffBlk = kS * kStage;                  // two 16-row read-out blocks, padded rows
+constexpr int kOffAcc = kOffBlk + 2 * 16 * kBRow * 4; // one 16 x 128 fp32 epilogue tile
 constexpr int kOffInv = kOffAcc + 16 * kTileRows * 4;
 constexpr int kOffScale = kOffInv + 16 * 4;
-constexpr int kOffBars = kOffScale + kTileRows * 4;   // full[S], conv[S], empty[S], acc
-constexpr int kOffTmem = kOffBars + (3 * kS + 1) * 8;
+constexpr int kOffBars = kOffScale + kTileRows * 4;   // full[S], conv[S], empty[S], accf[2], acce[2]
+constexpr int kOffTmem = kOffBars + (3 * kS + 4) * 8;
 constexpr int kSmem = kOffTmem + 16 + 1024;           // + alignment slack
 
 DF_DEVICE uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -117,33 +123,40 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
   using namespace umma;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* blk = reinterpret_cast<float*>(sm + kOffBlk);
   float* acc_s = reinterpret_cast<float*>(sm + kOffAcc);
   float* inv_rms = reinterpret_cast<float*>(sm + kOffInv);
   float* scale_s = reinterpret_cast<float*>(sm + kOffScale);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOffBars);
   uint64_t* conv = full + kS;
   uint64_t* empty = conv + kS;
-  uint64_t* accb = empty + kS;
+  uint64_t* accf = empty + kS;   // accumulator buffer b holds a finished tile
+  uint64_t* acce = accf + 2;     // accumulator buffer b has been read out
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
   __shared__ int s_flag;
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool fp8 = WT == W_FP8;
-  const int mt = blockIdx.x, nt = blockIdx.y;      // 128 activation rows, 128 weight rows
+  const int m_tiles = (p.M + 127) / 128;
+  const int n_items = m_tiles * p.n_tiles;
   const int nk = p.cpt;                            // 64-wide k chunks
+  const int G = gridDim.x;
   if (tid == 0) {
     for (int s = 0; s < kS; ++s) {
       bar_init(&full[s], 1);
-      bar_init(&conv[s], 8);
+      bar_init(&conv[s], kWiden);
       bar_init(&empty[s], 1);
     }
-    bar_init(accb, 1);
+    for (int b = 0; b < 2; ++b) {
+      bar_init(&accf[b], 1);
+      bar_init(&acce[b], 8);
+    }
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 9) {  // 128 fp32 columns of tensor memory for the accumulator
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
+  if (warp == 13) {  // two accumulator buffers of 128 fp32 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(
                      su32(tmem_slot))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -154,171 +167,202 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
   const uint32_t tmem = *tmem_slot;
   pdl_trigger();
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       pdl_wait();
       const uint32_t bytes = kTile * (p.has_lo ? 2 : 1) + (fp8 ? kRaw : kTile);
-      int issued = 0;
-      for (int k = 0; k < nk && !s_abort; ++k) {
-        const int st = k % kS;
-        if (!bar_wait(&empty[st], ((k / kS) & 1) ^ 1)) {
-          atomicOr(p.status, 0x4u);
-          s_abort = 1;
-          break;
-        }
-        uint8_t* base = sm + st * kStage;
-        bar_expect(&full[st], bytes);
-        tma2d(base, &p.tm_xh, k * 64, mt * 128, &full[st]);
-        if (p.has_lo) tma2d(base + kTile, &p.tm_xl, k * 64, mt * 128, &full[st]);
-        // weight rows of this tile in 32-row boxes, each from its own segment map
-        uint8_t* bdst = fp8 ? base + 3 * kTile : base + 2 * kTile;
-        const int box_bytes = fp8 ? 32 * 64 : 32 * 128;
+      long long it = 0;
+      for (int t = blockIdx.x; t < n_items && !s_abort; t += G) {
+        const int mt = t % m_tiles, nt = t / m_tiles;
+        int maps[4], rows[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          int map, row;
+        for (int q = 0; q < 4; ++q) {  // weight rows of this tile in 32-row boxes, per segment map
           if (p.map == MAP_SWIGLU) {
-            map = q < 2 ? 0 : 1;
-            row = nt * (kTileRows / 2) + (q & 1) * 32;
+            maps[q] = q < 2 ? 0 : 1;
+            rows[q] = nt * (kTileRows / 2) + (q & 1) * 32;
           } else {
             const int vr = nt * kTileRows + q * 32;
             int s = 0;
             while (s + 1 < p.nseg && vr >= p.seg[s + 1].row0) ++s;
-            map = s;
-            row = vr - p.seg[s].row0;
+            maps[q] = s;
+            rows[q] = vr - p.seg[s].row0;
           }
-          tma2d(bdst + q * box_bytes, &p.tm_w[map], k * 64, row, &full[st]);
         }
-        issued = k + 1;
+        for (int k = 0; k < nk; ++k, ++it) {
+          const int st = (int)(it % kS);
+          if (!bar_wait(&empty[st], (uint32_t)((it / kS) & 1) ^ 1)) {
+            atomicOr(p.status, 0x4u);
+            s_abort = 1;
+            break;
+          }
+          uint8_t* base = sm + st * kStage;
+          bar_expect(&full[st], bytes);
+          tma2d(base, &p.tm_xh, k * 64, mt * 128, &full[st]);
+          if (p.has_lo) tma2d(base + kTile, &p.tm_xl, k * 64, mt * 128, &full[st]);
+          uint8_t* bdst = fp8 ? base + 3 * kTile : base + 2 * kTile;
+          const int box_bytes = fp8 ? 32 * 64 : 32 * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tma2d(bdst + q * box_bytes, &p.tm_w[maps[q]], k * 64, rows[q], &full[st]);
+        }
       }
       // no copy may still be landing when the CTA exits
-      for (int k = issued > kS ? issued - kS : 0; k < issued; ++k)
-        if (!bar_wait(&full[k % kS], (k / kS) & 1)) {
+      for (long long j = it > kS ? it - kS : 0; j < it; ++j)
+        if (!bar_wait(&full[j % kS], (uint32_t)((j / kS) & 1))) {
           atomicOr(p.status, 0x4u);
           break;
         }
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, 128);
-      for (int k = 0; k < nk && !s_abort; ++k) {
-        const int st = k % kS;
-        uint64_t* ready = fp8 ? &conv[st] : &full[st];
-        if (!bar_wait(ready, (k / kS) & 1)) {
+      long long it = 0;
+      int i = 0;
+      for (int t = blockIdx.x; t < n_items && !s_abort; t += G, ++i) {
+        const int buf = i & 1;
+        if (!bar_wait(&acce[buf], (uint32_t)((i >> 1) & 1) ^ 1)) {  // epilogue done with it
           atomicOr(p.status, 0x4u);
           s_abort = 1;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        uint8_t* base = sm + st * kStage;
-        const uint64_t da = desc_sw128(base), dl = desc_sw128(base + kTile),
-                       db = desc_sw128(base + 2 * kTile);
+        const uint32_t acc = tmem + buf * kAccCols;
+        for (int k = 0; k < nk; ++k, ++it) {
+          const int st = (int)(it % kS);
+          uint64_t* ready = fp8 ? &conv[st] : &full[st];
+          if (!bar_wait(ready, (uint32_t)((it / kS) & 1))) {
+            atomicOr(p.status, 0x4u);
+            s_abort = 1;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          uint8_t* base = sm + st * kStage;
+          const uint64_t da = desc_sw128(base), dl = desc_sw128(base + kTile),
+                         db = desc_sw128(base + 2 * kTile);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // 16 k per MMA: +32 bytes inside the swizzled rows
-          const uint64_t adv = (uint64_t)(j * 32) >> 4;
-          mma_f16(tmem, da + adv, db + adv, idesc, (k | j) != 0);
-          if (p.has_lo) mma_f16(tmem, dl + adv, db + adv, idesc, 1);
+          for (int j = 0; j < 4; ++j) {  // 16 k per MMA: +32 bytes inside the swizzled rows
+            const uint64_t adv = (uint64_t)(j * 32) >> 4;
+            mma_f16(acc, da + adv, db + adv, idesc, (k | j) != 0);
+            if (p.has_lo) mma_f16(acc, dl + adv, db + adv, idesc, 1);
+          }
+          mma_commit(&empty[st]);
         }
-        mma_commit(&empty[st]);
+        mma_commit(&accf[buf]);
       }
-      mma_commit(accb);
+    }
+  } else if (warp >= 8) {
+    // ---------------------------------------------------------------- E4M3 widening
+    if (fp8) {
+      const int wt = tid - 256;  // 0..127
+      long long it = 0;
+      for (int t = blockIdx.x; t < n_items; t += G) {
+        for (int k = 0; k < nk; ++k, ++it) {
+          const int st = (int)(it % kS);
+          if (!s_abort && !bar_wait(&full[st], (uint32_t)((it / kS) & 1))) {
+            if (lane == 0) atomicOr(p.status, 0x4u);
+            s_abort = 1;
+          }
+          uint8_t* base = sm + st * kStage;
+          const uint8_t* raw = base + 3 * kTile;   // [128 rows][64 B], 32-row boxes, unswizzled
+          uint8_t* dst = base + 2 * kTile;         // [128 rows][128 B] bf16, 128-byte swizzle
+          // 128 rows x 4 (16-byte raw pieces) = 512 pieces over 128 threads
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int pc = wt + u * 128;
+            const int row = pc >> 2, q = pc & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + row * 64 + q * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              o[2 * e] = e4m3x2_to_bf16x2((uint16_t)(w[e] & 0xffffu));
+              o[2 * e + 1] = e4m3x2_to_bf16x2((uint16_t)(w[e] >> 16));
+            }
+            // 16 E4M3 = 32 bf16 bytes = chunks 2q and 2q + 1 of the bf16 row
+            *reinterpret_cast<uint4*>(dst + row * 128 + (((2 * q) ^ (row & 7)) << 4)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + row * 128 + (((2 * q + 1) ^ (row & 7)) << 4)) =
+                make_uint4(o[4], o[5], o[6], o[7]);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) bar_arrive(&conv[st]);
+        }
+      }
     }
   } else {
-    // ---------------------------------------------------------------- warps 0..7
-    if (fp8) {  // widen E4M3 weight tiles to the swizzled bf16 tile
-      for (int k = 0; k < nk; ++k) {
-        const int st = k % kS;
-        if (!s_abort && !bar_wait(&full[st], (k / kS) & 1)) {
-          if (lane == 0) atomicOr(p.status, 0x4u);
-          s_abort = 1;
-        }
-        uint8_t* base = sm + st * kStage;
-        const uint8_t* raw = base + 3 * kTile;   // [128 rows][64 B], 32-row boxes, unswizzled
-        uint8_t* dst = base + 2 * kTile;         // [128 rows][128 B] bf16, 128-byte swizzle
-        // 128 rows x 4 (16-byte raw pieces) = 512 pieces over 256 threads
-        for (int pc = tid; pc < 512; pc += 256) {
-          const int row = pc >> 2, q = pc & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(raw + row * 64 + q * 16);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[8];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            o[2 * e] = e4m3x2_to_bf16x2((uint16_t)(w[e] & 0xffffu));
-            o[2 * e + 1] = e4m3x2_to_bf16x2((uint16_t)(w[e] >> 16));
-          }
-          // 16 E4M3 = 32 bf16 bytes = chunks 2q and 2q + 1 of the bf16 row
-          *reinterpret_cast<uint4*>(dst + row * 128 + (((2 * q) ^ (row & 7)) << 4)) =
-              make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(dst + row * 128 + (((2 * q + 1) ^ (row & 7)) << 4)) =
-              make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) bar_arrive(&conv[st]);
-      }
-    }
+    // ---------------------------------------------------------------- epilogue warps 0..7
     pdl_wait();
-    // scales of this tile's weight rows
-    if (tid < kTileRows) {
-      const float* sc = nullptr;
-      const uint8_t* r = map_row(p, nt, tid, 1, &sc);
-      scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
-    }
-    const bool ok = s_abort || bar_wait(accb, 0);
-    if (!ok && lane == 0) atomicOr(p.status, 0x4u);
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    // accumulator -> shared memory tile [128 rows][128 cols] (row stride
-    // kDRow: the padding spreads the rows of one tcgen05.ld over the banks) over
-    // the pipeline stages (all MMAs have completed); warp w reads lanes
-    // 32(w%4).. and the column half w/4
-    float* dtile = reinterpret_cast<float*>(sm);
-    {
-      const int quad = warp & 3, half = warp >> 2;
-      const int row = quad * 32 + lane;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + half * 64 + c * 32;
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-            "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-              "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-              "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-              "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-              "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-              "=r"(r[31])
-            : "r"(taddr));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        float* drow = dtile + (size_t)row * kDRow + half * 64 + c * 32;
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(drow + e) =
-              make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                          __uint_as_float(r[e + 3]));
+    const int quad = warp & 3, half = warp >> 2;
+    int i = 0;
+    for (int t = blockIdx.x; t < n_items; t += G, ++i) {
+      const int mt = t % m_tiles, nt = t / m_tiles;
+      const int buf = i & 1;
+      // scales of this tile's weight rows
+      if (tid < kTileRows) {
+        const float* sc = nullptr;
+        const uint8_t* r = map_row(p, nt, tid, 1, &sc);
+        scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
       }
-    }
-    csync();
-    // fused epilogues, 16 activation rows at a time
-    for (int b = 0; b < 8; ++b) {
-      const int mb = mt * 8 + b;
-      if (mb * 16 >= p.M) break;
-      for (int i = tid; i < 16 * kTileRows; i += kGemmThreads) {
-        const int m = i / kTileRows, r = i - m * kTileRows;
-        acc_s[i] = dtile[(size_t)(b * 16 + m) * kDRow + r];
+      const bool ok = s_abort || bar_wait(&accf[buf], (uint32_t)((i >> 1) & 1));
+      if (!ok && lane == 0) atomicOr(p.status, 0x4u);
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      for (int q = 0; q < 4; ++q) {
+        const int mb0 = mt * 8 + 2 * q;    // the quadrant's two 16-row blocks
+        if (mb0 * 16 >= p.M) break;
+        if (quad == q) {
+          // lanes 32q..32q+31 of the accumulator, this warp's half of the columns,
+          // into block (lane / 16) row (lane % 16) (padded rows: the 32 lanes'
+          // rows do not share banks)
+          float* row = blk + (size_t)(lane >> 4) * 16 * kBRow + (size_t)(lane & 15) * kBRow;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t r[32];
+            const uint32_t taddr = tmem + buf * kAccCols + ((uint32_t)(q * 32) << 16) + half * 64 + c * 32;
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+                "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                  "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+                  "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+                  "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+                  "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+                  "=r"(r[31])
+                : "r"(taddr));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(row + half * 64 + c * 32 + e) =
+                  make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                              __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+          }
+        }
+        csync();
+        for (int b2 = 0; b2 < 2; ++b2) {
+          const int mb = mb0 + b2;
+          if (mb * 16 >= p.M) break;
+          for (int e = tid; e < 16 * kTileRows; e += kGemmThreads) {
+            const int m = e / kTileRows, c = e - m * kTileRows;
+            acc_s[e] = blk[(size_t)(b2 * 16 + m) * kBRow + c];
+          }
+          if (p.row_scale) compute_inv_rms(p, inv_rms, mb * 16);
+          csync();
+          run_epilogue(p, acc_s, scale_s, inv_rms, mb, nt, &s_flag);
+          csync();
+        }
       }
-      if (p.row_scale) compute_inv_rms(p, inv_rms, mb * 16);
-      csync();
-      run_epilogue(p, acc_s, scale_s, inv_rms, mb, nt, &s_flag);
-      csync();
+      // the accumulator buffer may be overwritten by the next tile's MMAs
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) bar_arrive(&acce[buf]);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem) : "memory");
   }
 }
 
@@ -334,8 +378,16 @@ cudaError_t configure_gemm_umma() {
 }
 
 cudaError_t launch_gemm_umma(int wt, const GemmParams& p, cudaStream_t st) {
+  static int n_sm = 0;
+  if (!n_sm) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (n_sm <= 0) n_sm = 1;
+  }
+  const int items = (p.M + 127) / 128 * p.n_tiles;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.M + 127) / 128, p.n_tiles);
+  cfg.gridDim = dim3(items < n_sm ? items : n_sm);   // persistent: one CTA per SM
   cfg.blockDim = dim3(umma::kThreads);
   cfg.dynamicSmemBytes = umma::kSmem;
   cfg.stream = st;
