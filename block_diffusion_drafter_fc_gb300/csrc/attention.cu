@@ -467,7 +467,13 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
                             p0, p.window, p.block_width, m0, m1, l0, l1, O, lane);
     for (int j = j0 + lk; j < min(n_sub, j0 + nb); j += kq) {
       wait_sub(j, r);
-      if (active) {
+      // row 0 has the widest window: a sub-chunk with no key for it has none
+      // for any row (empty slots of a partly filled ring, or out of window)
+      const int* kp = kpos + (j % nb) * kSub;
+      const int ka = kp[lane], kb = kp[lane + 32];
+      const bool any = __any_sync(0xffffffffu, (ka >= 0 && ka < p0 && p0 - ka < p.window) ||
+                                                   (kb >= 0 && kb < p0 && p0 - kb < p.window));
+      if (active && any) {
         const uint16_t* kh = bufs + (j % nb) * buf_elems;
         attend_tile<HD, RING_F32>(qh, ql, kh, kh + 2 * SM::TILE, kh + SM::TILE, kh + 3 * SM::TILE,
                                   KS, 8, kpos + (j % nb) * kSub, false, p0, p.window, 16, m0, m1, l0,
@@ -710,8 +716,20 @@ cudaError_t configure_attention_cluster(int group, int hd, int ring_f32, int win
 
 template <int HD, bool F32>
 static cudaError_t launch_cl(const AttnParams& p_in, int n_seq, cudaStream_t st) {
-  const int G = p_in.n_head / p_in.n_head_kv, CL = attn_cluster_size(p_in.window);
+  const int G = p_in.n_head / p_in.n_head_kv;
+  int CL = attn_cluster_size(p_in.window);
   const AttnPlan pl = choose_plan<HD, F32>(G, CL, p_in.n_head_kv, n_seq, p_in.window, false);
+  // a batch large enough to fill the GPU twice without splitting windows gives
+  // each CTA a whole window: no cluster merge, and the prologue and merge are
+  // paid once per window instead of once per slice
+  static int n_sm = 0;
+  if (!n_sm) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (n_sm <= 0) n_sm = 1;
+  }
+  if ((long long)p_in.n_head_kv * (G / pl.hpc) * n_seq >= 2LL * n_sm) CL = 1;
   AttnParams p = p_in;
   p.hpc = pl.hpc;
   p.kq = pl.kq;

@@ -35,22 +35,29 @@ namespace umma {
 
 constexpr int kS = 3;                  // pipeline stages
 constexpr int kTile = 128 * 128;       // bytes of one [128 rows x 128 B] swizzled tile
-constexpr int kRaw = 128 * 64;         // bytes of one raw [128 x 64] E4M3 tile
 constexpr long long kWait = 4000000000LL;
 constexpr int kThreads = 448;          // warps 0-7 epilogue, 8-11 E4M3 widening, 12 TMA, 13 MMA
 constexpr int kWiden = 4;              // widening warps
-constexpr int kAccCols = 128;          // TMEM columns of one accumulator buffer
+constexpr int kBRow = kTileRows + 4;   // padded row (floats) of a read-out block
 
-// stage: A hi | A lo | B (bf16) | B raw (E4M3 only)
-constexpr int kStage = 3 * kTile + kRaw;
-constexpr int kBRow = kTileRows + 4;                  // padded row (floats) of a read-out block
-constexpr int kOffBlk = kS * kStage;                  // two 16-row read-out blocks, padded rows
-constexpr int kOffAcc = kOffBlk + 2 * 16 * kBRow * 4; // one 16 x 128 fp32 epilogue tile
-constexpr int kOffInv = kOffAcc + 16 * kTileRows * 4;
-constexpr int kOffScale = kOffInv + 16 * 4;
-constexpr int kOffBars = kOffScale + kTileRows * 4;   // full[S], conv[S], empty[S], accf[2], acce[2]
-constexpr int kOffTmem = kOffBars + (3 * kS + 4) * 8;
-constexpr int kSmem = kOffTmem + 16 + 1024;           // + alignment slack
+// Shared-memory layout for output tiles of 128 activation rows x WR weight rows
+// (WR = 128, or 256 = two 128-row n-tiles sharing every activation chunk).
+template <int WR>
+struct L {
+  static constexpr int kWTile = WR * 128;   // bf16 [WR x 64] swizzled weight tile
+  static constexpr int kWRaw = WR * 64;     // raw [WR x 64] E4M3 (upper half of kWTile)
+  static constexpr int kAccCols = WR;       // TMEM columns of one accumulator buffer (fp32)
+  // stage: A hi | A lo | B (bf16; E4M3 lands raw in its upper half, widened in place)
+  static constexpr int kStage = 2 * kTile + kWTile;
+  static constexpr int kOffBlk = kS * kStage;                  // two 16-row read-out blocks
+  static constexpr int kOffAcc = kOffBlk + 2 * 16 * kBRow * 4; // one 16 x 128 fp32 epilogue tile
+  static constexpr int kOffInv = kOffAcc + 16 * kTileRows * 4;
+  static constexpr int kOffScale = kOffInv + 16 * 4;
+  static constexpr int kOffBars = kOffScale + kTileRows * 4;   // full, conv, empty [S], accf, acce [2]
+  static constexpr int kOffTmem = kOffBars + (3 * kS + 4) * 8;
+  static constexpr int kSmem = kOffTmem + 16 + 1024;           // + alignment slack
+  static_assert(kSmem <= 227 * 1024, "shared memory of the tcgen05 projection");
+};
 
 DF_DEVICE uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -118,9 +125,14 @@ DF_DEVICE void mma_commit(uint64_t* b) {
 
 }  // namespace umma
 
-template <int WT>
+template <int WT, int WR>
 __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __grid_constant__ GemmParams p) {
   using namespace umma;
+  using Lt = L<WR>;
+  constexpr int kWTile = Lt::kWTile, kWRaw = Lt::kWRaw, kAccCols = Lt::kAccCols, kStage = Lt::kStage;
+  constexpr int kOffBlk = Lt::kOffBlk, kOffAcc = Lt::kOffAcc, kOffInv = Lt::kOffInv;
+  constexpr int kOffScale = Lt::kOffScale, kOffBars = Lt::kOffBars, kOffTmem = Lt::kOffTmem;
+  constexpr int kNsub = WR / 128;   // 128-row n-tiles per output tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* blk = reinterpret_cast<float*>(sm + kOffBlk);
@@ -139,7 +151,7 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool fp8 = WT == W_FP8;
   const int m_tiles = (p.M + 127) / 128;
-  const int n_items = m_tiles * p.n_tiles;
+  const int n_items = m_tiles * ((p.n_tiles + kNsub - 1) / kNsub);   // 128 act rows x WR weight rows
   const int nk = p.cpt;                            // 64-wide k chunks
   const int G = gridDim.x;
   if (tid == 0) {
@@ -155,9 +167,9 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 13) {  // two accumulator buffers of 128 fp32 columns
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(
-                     su32(tmem_slot))
+  if (warp == 13) {  // two accumulator buffers of WR fp32 columns
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(tmem_slot)), "n"(2 * WR)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -171,18 +183,19 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       pdl_wait();
-      const uint32_t bytes = kTile * (p.has_lo ? 2 : 1) + (fp8 ? kRaw : kTile);
+      const uint32_t bytes = kTile * (p.has_lo ? 2 : 1) + (fp8 ? kWRaw : kWTile);
       long long it = 0;
       for (int t = blockIdx.x; t < n_items && !s_abort; t += G) {
-        const int mt = t % m_tiles, nt = t / m_tiles;
-        int maps[4], rows[4];
+        const int mt = t % m_tiles, wt2 = t / m_tiles;
+        int maps[WR / 32], rows[WR / 32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // weight rows of this tile in 32-row boxes, per segment map
+        for (int q = 0; q < WR / 32; ++q) {  // the WR weight rows in 32-row boxes, per segment map
+          const int nt = kNsub * wt2 + (q >> 2), qq = q & 3;
           if (p.map == MAP_SWIGLU) {
-            maps[q] = q < 2 ? 0 : 1;
-            rows[q] = nt * (kTileRows / 2) + (q & 1) * 32;
+            maps[q] = qq < 2 ? 0 : 1;
+            rows[q] = nt * (kTileRows / 2) + (qq & 1) * 32;
           } else {
-            const int vr = nt * kTileRows + q * 32;
+            const int vr = nt * kTileRows + qq * 32;   // past N: read as zeros
             int s = 0;
             while (s + 1 < p.nseg && vr >= p.seg[s + 1].row0) ++s;
             maps[q] = s;
@@ -200,10 +213,10 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
           bar_expect(&full[st], bytes);
           tma2d(base, &p.tm_xh, k * 64, mt * 128, &full[st]);
           if (p.has_lo) tma2d(base + kTile, &p.tm_xl, k * 64, mt * 128, &full[st]);
-          uint8_t* bdst = fp8 ? base + 3 * kTile : base + 2 * kTile;
+          uint8_t* bdst = fp8 ? base + 2 * kTile + kWRaw : base + 2 * kTile;
           const int box_bytes = fp8 ? 32 * 64 : 32 * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) tma2d(bdst + q * box_bytes, &p.tm_w[maps[q]], k * 64, rows[q], &full[st]);
+          for (int q = 0; q < WR / 32; ++q) tma2d(bdst + q * box_bytes, &p.tm_w[maps[q]], k * 64, rows[q], &full[st]);
         }
       }
       // no copy may still be landing when the CTA exits
@@ -216,7 +229,7 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
   } else if (warp == 13) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, 128);
+      const uint32_t idesc = idesc_bf16(128, WR);
       long long it = 0;
       int i = 0;
       for (int t = blockIdx.x; t < n_items && !s_abort; t += G, ++i) {
@@ -264,15 +277,22 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
             s_abort = 1;
           }
           uint8_t* base = sm + st * kStage;
-          const uint8_t* raw = base + 3 * kTile;   // [128 rows][64 B], 32-row boxes, unswizzled
-          uint8_t* dst = base + 2 * kTile;         // [128 rows][128 B] bf16, 128-byte swizzle
-          // 128 rows x 4 (16-byte raw pieces) = 512 pieces over 128 threads
+          uint8_t* dst = base + 2 * kTile;          // [WR rows][128 B] bf16, 128-byte swizzle
+          const uint8_t* raw = dst + kWRaw;         // [WR rows][64 B] E4M3, unswizzled
+          // WR rows x 4 (16-byte raw pieces) over 128 threads: all read before any
+          // write (the raw bytes sit in the widened tile's upper half)
+          uint4 v[WR / 32];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < WR / 32; ++u) {
+            const int pc = wt + u * 128;
+            v[u] = *reinterpret_cast<const uint4*>(raw + (pc >> 2) * 64 + (pc & 3) * 16);
+          }
+          asm volatile("bar.sync 2, %0;" ::"n"(32 * kWiden) : "memory");
+#pragma unroll
+          for (int u = 0; u < WR / 32; ++u) {
             const int pc = wt + u * 128;
             const int row = pc >> 2, q = pc & 3;
-            const uint4 v = *reinterpret_cast<const uint4*>(raw + row * 64 + q * 16);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
             uint32_t o[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -286,6 +306,8 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
                 make_uint4(o[4], o[5], o[6], o[7]);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          // every widening warp is done reading this stage's raw bytes before the
+          // next use of the buffer can be refilled (it follows the MMA's commit)
           __syncwarp();
           if (lane == 0) bar_arrive(&conv[st]);
         }
@@ -297,59 +319,64 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
     const int quad = warp & 3, half = warp >> 2;
     int i = 0;
     for (int t = blockIdx.x; t < n_items; t += G, ++i) {
-      const int mt = t % m_tiles, nt = t / m_tiles;
+      const int mt = t % m_tiles, wt2 = t / m_tiles;
       const int buf = i & 1;
-      // scales of this tile's weight rows
-      if (tid < kTileRows) {
-        const float* sc = nullptr;
-        const uint8_t* r = map_row(p, nt, tid, 1, &sc);
-        scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
-      }
       const bool ok = s_abort || bar_wait(&accf[buf], (uint32_t)((i >> 1) & 1));
       if (!ok && lane == 0) atomicOr(p.status, 0x4u);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      for (int q = 0; q < 4; ++q) {
-        const int mb0 = mt * 8 + 2 * q;    // the quadrant's two 16-row blocks
-        if (mb0 * 16 >= p.M) break;
-        if (quad == q) {
-          // lanes 32q..32q+31 of the accumulator, this warp's half of the columns,
-          // into block (lane / 16) row (lane % 16) (padded rows: the 32 lanes'
-          // rows do not share banks)
-          float* row = blk + (size_t)(lane >> 4) * 16 * kBRow + (size_t)(lane & 15) * kBRow;
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t r[32];
-            const uint32_t taddr = tmem + buf * kAccCols + ((uint32_t)(q * 32) << 16) + half * 64 + c * 32;
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-                "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                  "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-                  "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-                  "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-                  "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-                  "=r"(r[31])
-                : "r"(taddr));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(row + half * 64 + c * 32 + e) =
-                  make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                              __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-          }
+      for (int sub = 0; sub < kNsub; ++sub) {
+        const int nt = kNsub * wt2 + sub;
+        if (nt >= p.n_tiles) break;
+        csync();  // the previous n-tile's epilogues are done with scale_s
+        if (tid < kTileRows) {  // scales of this n-tile's weight rows
+          const float* sc = nullptr;
+          const uint8_t* r = map_row(p, nt, tid, 1, &sc);
+          scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
         }
-        csync();
-        for (int b2 = 0; b2 < 2; ++b2) {
-          const int mb = mb0 + b2;
-          if (mb * 16 >= p.M) break;
-          for (int e = tid; e < 16 * kTileRows; e += kGemmThreads) {
-            const int m = e / kTileRows, c = e - m * kTileRows;
-            acc_s[e] = blk[(size_t)(b2 * 16 + m) * kBRow + c];
+        for (int q = 0; q < 4; ++q) {
+          const int mb0 = mt * 8 + 2 * q;    // the quadrant's two 16-row blocks
+          if (mb0 * 16 >= p.M) break;
+          if (quad == q) {
+            // lanes 32q..32q+31 of the accumulator, this warp's half of the
+            // n-tile's columns, into block (lane / 16) row (lane % 16) (padded
+            // rows: the 32 lanes' rows do not share banks)
+            float* row = blk + (size_t)(lane >> 4) * 16 * kBRow + (size_t)(lane & 15) * kBRow;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t r[32];
+              const uint32_t taddr = tmem + buf * kAccCols + ((uint32_t)(q * 32) << 16) + sub * 128 +
+                                     half * 64 + c * 32;
+              asm volatile(
+                  "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+                  "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                    "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+                    "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+                    "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+                    "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+                    "=r"(r[31])
+                  : "r"(taddr));
+              asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(row + half * 64 + c * 32 + e) =
+                    make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+            }
           }
-          if (p.row_scale) compute_inv_rms(p, inv_rms, mb * 16);
           csync();
-          run_epilogue(p, acc_s, scale_s, inv_rms, mb, nt, &s_flag);
-          csync();
+          for (int b2 = 0; b2 < 2; ++b2) {
+            const int mb = mb0 + b2;
+            if (mb * 16 >= p.M) break;
+            for (int e = tid; e < 16 * kTileRows; e += kGemmThreads) {
+              const int m = e / kTileRows, c = e - m * kTileRows;
+              acc_s[e] = blk[(size_t)(b2 * 16 + m) * kBRow + c];
+            }
+            if (p.row_scale) compute_inv_rms(p, inv_rms, mb * 16);
+            csync();
+            run_epilogue(p, acc_s, scale_s, inv_rms, mb, nt, &s_flag);
+            csync();
+          }
         }
       }
       // the accumulator buffer may be overwritten by the next tile's MMAs
@@ -362,21 +389,44 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
   __syncthreads();
   if (warp == 13) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(2 * WR) : "memory");
   }
 }
 
-size_t gemm_umma_smem_bytes() { return umma::kSmem; }
+size_t gemm_umma_smem_bytes() { return umma::L<256>::kSmem; }
 
 cudaError_t configure_gemm_umma() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_umma_kernel<W_BF16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, umma::kSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_umma_kernel<W_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             umma::kSmem);
+  cudaError_t e = cudaSuccess;
+  auto set = [&](const void* fn, int bytes) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  };
+  set(reinterpret_cast<const void*>(gemm_umma_kernel<W_BF16, 128>), umma::L<128>::kSmem);
+  set(reinterpret_cast<const void*>(gemm_umma_kernel<W_BF16, 256>), umma::L<256>::kSmem);
+  set(reinterpret_cast<const void*>(gemm_umma_kernel<W_FP8, 128>), umma::L<128>::kSmem);
+  set(reinterpret_cast<const void*>(gemm_umma_kernel<W_FP8, 256>), umma::L<256>::kSmem);
   return e;
 }
 
+template <int WT, int WR>
+static cudaError_t launch_umma_t(const GemmParams& p, int n_sm, cudaStream_t st) {
+  const int items = (p.M + 127) / 128 * ((p.n_tiles + WR / 128 - 1) / (WR / 128));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(items < n_sm ? items : n_sm);   // persistent: one CTA per SM
+  cfg.blockDim = dim3(umma::kThreads);
+  cfg.dynamicSmemBytes = umma::L<WR>::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_umma_kernel<WT, WR>, p);
+}
+
+// 256-row weight tiles (half the activation traffic per flop) when they still
+// give every SM a tile, else 128-row tiles for more parallelism.  The logits
+// epilogue (an fp32 store of every output plus the argmax partials) is the
+// heaviest; its tiles stay 128 rows so that it keeps pace with the MMAs.
 cudaError_t launch_gemm_umma(int wt, const GemmParams& p, cudaStream_t st) {
   static int n_sm = 0;
   if (!n_sm) {
@@ -385,19 +435,9 @@ cudaError_t launch_gemm_umma(int wt, const GemmParams& p, cudaStream_t st) {
     cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (n_sm <= 0) n_sm = 1;
   }
-  const int items = (p.M + 127) / 128 * p.n_tiles;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(items < n_sm ? items : n_sm);   // persistent: one CTA per SM
-  cfg.blockDim = dim3(umma::kThreads);
-  cfg.dynamicSmemBytes = umma::kSmem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (wt == W_BF16) return cudaLaunchKernelEx(&cfg, gemm_umma_kernel<W_BF16>, p);
-  if (wt == W_FP8) return cudaLaunchKernelEx(&cfg, gemm_umma_kernel<W_FP8>, p);
+  const bool wide = p.epi != EPI_LOGITS && (p.M + 127) / 128 * ((p.n_tiles + 1) / 2) >= n_sm;
+  if (wt == W_BF16) return wide ? launch_umma_t<W_BF16, 256>(p, n_sm, st) : launch_umma_t<W_BF16, 128>(p, n_sm, st);
+  if (wt == W_FP8) return wide ? launch_umma_t<W_FP8, 256>(p, n_sm, st) : launch_umma_t<W_FP8, 128>(p, n_sm, st);
   return cudaErrorInvalidValue;
 }
 

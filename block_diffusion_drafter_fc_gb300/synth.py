@@ -143,8 +143,20 @@ MIXED_F32 = DraftConfig(
 DENSE_FP8 = SMALL_FP8.with_(name="dense_fp8", n_seq=9, seed=2004)
 DENSE_BF16 = SMALL_FP8.with_(name="dense_bf16", n_seq=8, weight_dtype="bf16", mismatch="uniform",
                              seed=2005)
+# wide gate/up and LM head (> 2 x 152 n-tiles of 128 rows): the tcgen05 path's
+# 256-row weight tiles, FP8 with a ragged row tile and bf16
+WIDE_FP8 = SMALL_FP8.with_(name="wide_fp8", n_layer=1, n_embd=256, n_head=4, n_head_kv=2,
+                           n_ff=20480, n_vocab=40000, n_seq=9, seed=2006)
+WIDE_BF16 = WIDE_FP8.with_(name="wide_bf16", weight_dtype="bf16", mismatch="uniform", n_seq=8,
+                           seed=2007)
+# enough sequences that attention gives every CTA a whole window (no cluster
+# split: > 2 x 152 CTAs without one)
+MANY_SEQ = DraftConfig(
+    name="many_seq_bf16", n_layer=1, n_embd=256, n_head=8, n_head_kv=4, head_dim=64,
+    n_ff=512, window=128, n_vocab=512, weight_dtype="bf16", dense_dtype="bf16",
+    ring_dtype="bf16", n_seq=80, fill_lo=16, fill_hi=128, offset_hi=4000, seed=2008)
 TEST_CONFIGS: Dict[str, DraftConfig] = {c.name: c for c in (RAGGED, SMALL_FP8, MIXED_F32, DENSE_FP8,
-                                                            DENSE_BF16)}
+                                                            DENSE_BF16, WIDE_FP8, WIDE_BF16, MANY_SEQ)}
 
 
 def get_config(name: str) -> DraftConfig:
