@@ -101,7 +101,7 @@ struct Layout {
   size_t status, inv_freq, counters, h, ss, qbuf, kblk, vblk, rope_step, am_part;
   size_t xn_hi, xn_lo, attn_hi, attn_lo, act_hi, act_lo;
   size_t logits_int, drafts_int, idl_int, npast_int, partial;
-  size_t inj_raw, inj_ss, inj_rope, loop_pos, loop_cnt, loop_H, total;
+  size_t inj_raw, inj_ss, inj_rope, inj_hi, inj_lo, loop_pos, loop_cnt, loop_H, total;
   size_t partial_floats;
   int n_counters, ss_parts, ss_ld, lm_tiles;
   size_t ring_seq_bytes, ring_kv_bytes, ring_total;
@@ -154,6 +154,10 @@ Layout layout(const dflash_config& c) {
   L.inj_raw = take(sizeof(float) * (size_t)g.max_inject * g.d);
   L.inj_ss = take(sizeof(float) * (size_t)L.ss_parts * L.ss_ld);
   L.inj_rope = take(sizeof(float2) * (size_t)g.max_inject * (g.hd / 2));
+  // H_t as a bf16 hi/lo pair for injections of >= 128 rows on the tcgen05 path
+  const bool inj_dense = g.max_inject >= 128 && (g.wt == W_BF16 || g.wt == W_FP8);
+  L.inj_hi = take(inj_dense ? sizeof(uint16_t) * (size_t)g.max_inject * g.d : 0);
+  L.inj_lo = take(inj_dense ? sizeof(uint16_t) * (size_t)g.max_inject * g.d : 0);
   // speculative-loop turn: block positions, accepted-row counts, encoded rows
   L.loop_pos = take(sizeof(int32_t) * (size_t)g.max_seq * DFLASH_BLOCK);
   L.loop_cnt = take(sizeof(int32_t) * (size_t)g.max_seq);
@@ -215,6 +219,12 @@ struct dflash_handle {
   CUtensorMap td_layer[DFLASH_MAX_LAYERS][7];
   CUtensorMap td_lm;
   CUtensorMap td_xn[2], td_attn[2], td_act[2];
+  // prefill on the tcgen05 path (>= 128 rows): fc (bf16 features), all-layer
+  // wk / wv, and the injection input pair
+  bool enc_dense = false, inj_dense = false;
+  CUtensorMap td_fc;
+  CUtensorMap td_kv[DFLASH_MAX_LAYERS][2];
+  CUtensorMap td_inj[2];
   cudaStream_t cap_stream = nullptr;
   // captured graphs, one per block width (a capture bakes its row count)
   cudaGraph_t graphs[DFLASH_BLOCK + 1] = {};
@@ -519,6 +529,21 @@ bool build_maps(dflash_handle* h) {
   for (int i = 0; i < 3; ++i)
     for (int j = 0; j < 2; ++j)
       if (!make_map(&dst[i][j], h->scratch + pairs[i][j], W_BF16, kdim[i], g.M_max)) return false;
+  // prefill on the tcgen05 path: encode when features and fc are bf16, injection
+  // when the weights are bf16 or E4M3, for calls of >= 128 rows
+  h->enc_dense = g.max_inject >= 128 && g.dense_bf16;
+  if (h->enc_dense && !make_map(&h->td_fc, h->w.fc, W_BF16, g.fdim, g.d, 64, 32, true)) return false;
+  h->inj_dense = g.max_inject >= 128 && (g.wt == W_BF16 || g.wt == W_FP8);
+  if (h->inj_dense) {
+    const bool swk = g.wt == W_BF16;
+    for (int l = 0; l < g.L; ++l) {
+      if (!make_map(&h->td_kv[l][0], h->w.layers[l].wk, g.wt, g.d, g.kvd, 64, 32, swk)) return false;
+      if (!make_map(&h->td_kv[l][1], h->w.layers[l].wv, g.wt, g.d, g.kvd, 64, 32, swk)) return false;
+    }
+    if (!make_map(&h->td_inj[0], h->scratch + L.inj_hi, W_BF16, g.d, g.max_inject, 64, 128, true) ||
+        !make_map(&h->td_inj[1], h->scratch + L.inj_lo, W_BF16, g.d, g.max_inject, 64, 128, true))
+      return false;
+  }
   // tcgen05 path: batches of >= 128 activation rows with bf16 or E4M3 weights
   h->dense = g.M_max >= 128 && (g.wt == W_BF16 || g.wt == W_FP8);
   if (!h->dense) return true;
@@ -653,6 +678,27 @@ int run_encode(dflash_handle* h, const void* feats, int T, float* H_t, cudaStrea
   inject_shapes(g, sh);
   const int n_mb = cdiv(T, 16);
   GemmParams p = base_params(h);
+  CUtensorMap fm;
+  if (h->enc_dense && T >= 128 && make_map(&fm, feats, W_BF16, g.fdim, T, 64, 128, true)) {
+    // >= 128 rows: a dense contraction on the tcgen05 kernel (bf16 features
+    // are exact in bf16: no lo part)
+    p.tm_xh = fm;
+    p.tm_xl = fm;
+    p.has_lo = 0;
+    p.tm_w[0] = h->td_fc;
+    p.seg[0] = {h->w.fc, nullptr, 0, g.d};
+    p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS; p.M = T; p.K = g.fdim;
+    p.n_tiles = cdiv(g.d, kTileRows); p.n_mb = n_mb; p.cpt = cdiv(g.fdim, 64);
+    p.epi = EPI_STORE_SS; p.out = h->S<float>(h->L.inj_raw); p.ldo = g.d;
+    p.ss_out = h->S<float>(h->L.inj_ss); p.ss_out_ld = h->L.ss_ld;
+    prof_begin(h, PC_ENCODE, st);
+    DF_CHECK(h, launch_gemm_umma(W_BF16, p, st));
+    DF_CHECK(h, launch_rms_apply(h->S<float>(h->L.inj_raw), h->S<float>(h->L.inj_ss), p.n_tiles,
+                                 h->L.ss_ld, T, g.d, h->w.hidden_norm, g.dense_bf16, h->cfg.eps, H_t,
+                                 st));
+    prof_end(h, st);
+    return DFLASH_OK;
+  }
   set_plan(p, sh[0], n_mb);
   p.x = feats; p.x_mode = g.dense_bf16 ? X_BF16 : X_F32; p.ldx = g.fdim; p.M = T;
   p.seg[0] = {h->w.fc, nullptr, 0, g.d};
@@ -681,6 +727,34 @@ int run_inject(dflash_handle* h, int seq, const float* H_t, const int32_t* pos, 
                                 g.W, rows_per_seq, count, h->status(), st));
   const int n_mb = cdiv(T, 16);
   GemmParams p = base_params(h);
+  if (h->inj_dense && T >= 128) {
+    // >= 128 rows: H_t as a bf16 hi/lo pair, then per layer its wk / wv
+    // projection on the tcgen05 kernel with the ring scatter in the epilogue
+    // (the ring pointer moved to the layer's planes: the epilogue's layer 0)
+    DF_CHECK(h, launch_split_pair(H_t, T * g.d, h->S<uint16_t>(h->L.inj_hi),
+                                  h->S<uint16_t>(h->L.inj_lo), st));
+    const size_t layer_bytes = h->L.ring_kv_bytes / g.L;
+    for (int l = 0; l < g.L; ++l) {
+      const dflash_layer_weights& lw = h->w.layers[l];
+      GemmParams q = base_params(h);
+      q.tm_xh = h->td_inj[0];
+      q.tm_xl = h->td_inj[1];
+      q.has_lo = 1;
+      q.tm_w[0] = h->td_kv[l][0];
+      q.tm_w[1] = h->td_kv[l][1];
+      q.seg[0] = {lw.wk, lw.wk_scale, 0, g.kvd};
+      q.seg[1] = {lw.wv, lw.wv_scale, g.kvd, g.kvd};
+      q.k_norm_l[0] = lw.k_norm;
+      q.nseg = 2; q.N = 2 * g.kvd; q.map = MAP_SEGMENTS; q.M = T; q.K = g.d;
+      q.n_tiles = cdiv(2 * g.kvd, kTileRows); q.n_mb = n_mb; q.cpt = cdiv(g.d, 64);
+      q.epi = EPI_INJECT; q.ring_seq = h->ring_seq(seq) + (size_t)l * layer_bytes; q.pos = pos;
+      q.rope_cs = rope;
+      q.rows_per_seq = rows_per_seq; q.row_count = count; q.ring_seq_stride = h->L.ring_seq_bytes;
+      DF_CHECK(h, launch_gemm_umma(g.wt, q, st));
+    }
+    prof_end(h, st);
+    return DFLASH_OK;
+  }
   set_plan(p, sh[1], n_mb);
   p.x = H_t; p.x_mode = X_F32; p.ldx = g.d; p.M = T;
   for (int l = 0; l < g.L; ++l) {

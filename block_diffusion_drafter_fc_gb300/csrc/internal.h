@@ -186,5 +186,7 @@ cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t* n_ok, int n_seq,
                           int width, cudaStream_t st);
 cudaError_t launch_fill_i32(int32_t* p, int n, int32_t v, cudaStream_t st);
+// x (fp32, n values) -> bf16 hi + lo with x = hi + lo + O(2^-17 |x|)
+cudaError_t launch_split_pair(const float* x, int n, uint16_t* hi, uint16_t* lo, cudaStream_t st);
 
 }  // namespace dflash

@@ -242,6 +242,30 @@ cudaError_t launch_advance(const int32_t* drafts, const int32_t* targets, int n_
   return cudaGetLastError();
 }
 
+// fp32 rows -> the bf16 hi / lo pair the tcgen05 projection reads (two values
+// per thread)
+__global__ void split_pair_kernel(const float* x, int n, uint16_t* hi, uint16_t* lo) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float2 v = i + 1 < n ? *reinterpret_cast<const float2*>(x + i) : make_float2(x[i], 0.f);
+  uint32_t h, l;
+  split_bf16x2(v.x, v.y, h, l);
+  if (i + 1 < n) {
+    *reinterpret_cast<uint32_t*>(hi + i) = h;
+    *reinterpret_cast<uint32_t*>(lo + i) = l;
+  } else {
+    hi[i] = (uint16_t)(h & 0xffffu);
+    lo[i] = (uint16_t)(l & 0xffffu);
+  }
+}
+
+cudaError_t launch_split_pair(const float* x, int n, uint16_t* hi, uint16_t* lo, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int pairs = (n + 1) / 2;
+  split_pair_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(x, n, hi, lo);
+  return cudaGetLastError();
+}
+
 __global__ void fill_i32_kernel(int32_t* p, int n, int32_t v) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = v;
