@@ -143,25 +143,45 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
   float S[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j) S[j][0] = S[j][1] = S[j][2] = S[j][3] = 0.f;
+  // Key tiles in groups of four: the hi-q products of the group, then its lo-q
+  // products, so that the two updates of an accumulator are four MMAs apart
+  const int lm = lane >> 3;
 #pragma unroll
   for (int ks = 0; ks < HD / 16; ++ks) {
 #pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      if (j < nt) {
+    for (int j0 = 0; j0 < 8; j0 += 4) {
+      if (j0 < nt) {
         // B fragments of key tiles j and j + 1 (k = dims ks*16 .. +15) in one
         // ldmatrix: lane i addresses key 8 (j + i/16) + i%8, dims + 8 ((i/8)%2)
-        const int lm = lane >> 3;
-        const int off = (8 * (j + (lm >> 1)) + (lane & 7)) * KS + ks * 16 + (lm & 1) * 8;
-        uint32_t b[4];
-        ldsm_x4(b, k_hi + off);
-        mma_bf16_16816(S[j], qh[ks], b[0], b[1]);
-        mma_bf16_16816(S[j], ql[ks], b[0], b[1]);
-        mma_bf16_16816(S[j + 1], qh[ks], b[2], b[3]);
-        mma_bf16_16816(S[j + 1], ql[ks], b[2], b[3]);
+        uint32_t b[2][4];
+        int off[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          off[u] = (8 * (j0 + 2 * u + (lm >> 1)) + (lane & 7)) * KS + ks * 16 + (lm & 1) * 8;
+          if (j0 + 2 * u < nt) ldsm_x4(b[u], k_hi + off[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          if (j0 + 2 * u < nt) {
+            mma_bf16_16816(S[j0 + 2 * u], qh[ks], b[u][0], b[u][1]);
+            mma_bf16_16816(S[j0 + 2 * u + 1], qh[ks], b[u][2], b[u][3]);
+          }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          if (j0 + 2 * u < nt) {
+            mma_bf16_16816(S[j0 + 2 * u], ql[ks], b[u][0], b[u][1]);
+            mma_bf16_16816(S[j0 + 2 * u + 1], ql[ks], b[u][2], b[u][3]);
+          }
         if (SPLIT) {
-          ldsm_x4(b, k_lo + off);
-          mma_bf16_16816(S[j], qh[ks], b[0], b[1]);
-          mma_bf16_16816(S[j + 1], qh[ks], b[2], b[3]);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (j0 + 2 * u < nt) ldsm_x4(b[u], k_lo + off[u]);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (j0 + 2 * u < nt) {
+              mma_bf16_16816(S[j0 + 2 * u], qh[ks], b[u][0], b[u][1]);
+              mma_bf16_16816(S[j0 + 2 * u + 1], qh[ks], b[u][2], b[u][3]);
+            }
         }
       }
     }
@@ -236,25 +256,37 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
     split_bf16x2(S[2 * kk + 1][0], S[2 * kk + 1][1], ph[kk][2], pl[kk][2]);
     split_bf16x2(S[2 * kk + 1][2], S[2 * kk + 1][3], ph[kk][3], pl[kk][3]);
   }
+  // output dims in groups of four n8 tiles: per 16-key step the hi-p products
+  // of the group, then its lo-p products (accumulator updates four MMAs apart)
   const int lrow = lane & 7, lmat = lane >> 3;
 #pragma unroll
-  for (int jd = 0; jd < HD / 8; jd += 2) {
+  for (int jd = 0; jd < HD / 8; jd += 4) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       if (2 * kk < nt) {
         const int key = 16 * kk + (lmat & 1) * 8 + lrow;
-        const int dim = 8 * jd + (lmat >> 1) * 8;
-        uint32_t b[4];
-        ldsm_x4_t(b, v_hi + key * KS + dim);
-        mma_bf16_16816(O[jd], ph[kk], b[0], b[1]);
-        mma_bf16_16816(O[jd], pl[kk], b[0], b[1]);
-        mma_bf16_16816(O[jd + 1], ph[kk], b[2], b[3]);
-        mma_bf16_16816(O[jd + 1], pl[kk], b[2], b[3]);
+        uint32_t b[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) ldsm_x4_t(b[u], v_hi + key * KS + 8 * (jd + 2 * u) + (lmat >> 1) * 8);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          mma_bf16_16816(O[jd + 2 * u], ph[kk], b[u][0], b[u][1]);
+          mma_bf16_16816(O[jd + 2 * u + 1], ph[kk], b[u][2], b[u][3]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          mma_bf16_16816(O[jd + 2 * u], pl[kk], b[u][0], b[u][1]);
+          mma_bf16_16816(O[jd + 2 * u + 1], pl[kk], b[u][2], b[u][3]);
+        }
         if (SPLIT) {
-          uint32_t bl[4];
-          ldsm_x4_t(bl, v_lo + key * KS + dim);
-          mma_bf16_16816(O[jd], ph[kk], bl[0], bl[1]);
-          mma_bf16_16816(O[jd + 1], ph[kk], bl[2], bl[3]);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            ldsm_x4_t(b[u], v_lo + key * KS + 8 * (jd + 2 * u) + (lmat >> 1) * 8);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            mma_bf16_16816(O[jd + 2 * u], ph[kk], b[u][0], b[u][1]);
+            mma_bf16_16816(O[jd + 2 * u + 1], ph[kk], b[u][2], b[u][3]);
+          }
         }
       }
     }
@@ -577,8 +609,8 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
       const float inv = 1.f / L;
       const size_t at = (size_t)(seq * kBlock + i) * qd + (head0 + h) * HD + d;
       uint2 hi, lo;
-      split_bf16x2(acc.x * inv, acc.y * inv, hi.x, lo.x);
-      split_bf16x2(acc.z * inv, acc.w * inv, hi.y, lo.y);
+      split_pair16x2(acc.x * inv, acc.y * inv, p.pair_f16 != 0, hi.x, lo.x);
+      split_pair16x2(acc.z * inv, acc.w * inv, p.pair_f16 != 0, hi.y, lo.y);
       *reinterpret_cast<uint2*>(p.out_hi + at) = hi;
       *reinterpret_cast<uint2*>(p.out_lo + at) = lo;
     }

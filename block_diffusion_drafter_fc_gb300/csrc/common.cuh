@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
+#include <cuda_fp4.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,6 +38,31 @@ DF_DEVICE void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
   __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
   hi = *reinterpret_cast<uint32_t*>(&h);
   lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+// Split fp32 pairs into fp16 hi + fp16 lo parts (the activation pair of FP4
+// weights, whose products run in fp16): x = hi + lo to 2^-22 |x| (2^-25 absolute
+// below 2^-3); |x| must stay below 65504.
+DF_DEVICE void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// The 16-bit activation pair of a projection input: bf16, or fp16 with FP4 weights.
+DF_DEVICE void split_pair16x2(float a, float b, bool f16, uint32_t& hi, uint32_t& lo) {
+  if (f16)
+    split_f16x2(a, b, hi, lo);
+  else
+    split_bf16x2(a, b, hi, lo);
+}
+DF_DEVICE void split_pair16(float x, bool f16, uint16_t& hi, uint16_t& lo) {
+  uint32_t h, l;
+  split_pair16x2(x, 0.f, f16, h, l);
+  hi = (uint16_t)(h & 0xffffu);
+  lo = (uint16_t)(l & 0xffffu);
 }
 
 // Two E4M3 codes (low byte = first element) -> bf16x2.  Every E4M3 value is
@@ -116,6 +142,14 @@ DF_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // ---------------------------------------------------------------- tensor cores
 
 // D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.
+DF_DEVICE void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 DF_DEVICE void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "

@@ -28,7 +28,8 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 int wtype_of(int dtype) {
-  return dtype == DFLASH_DTYPE_F32 ? W_F32 : dtype == DFLASH_DTYPE_BF16 ? W_BF16 : W_FP8;
+  return dtype == DFLASH_DTYPE_F32 ? W_F32 : dtype == DFLASH_DTYPE_BF16 ? W_BF16
+         : dtype == DFLASH_DTYPE_FP8_E4M3 ? W_FP8 : W_FP4;
 }
 int chunk_of(int wt) { return wt == W_FP8 ? 64 : 32; }
 
@@ -155,9 +156,10 @@ Layout layout(const dflash_config& c) {
   L.inj_ss = take(sizeof(float) * (size_t)L.ss_parts * L.ss_ld);
   L.inj_rope = take(sizeof(float2) * (size_t)g.max_inject * (g.hd / 2));
   // H_t as a bf16 hi/lo pair for injections of >= 128 rows on the tcgen05 path
-  const bool inj_dense = g.max_inject >= 128 && (g.wt == W_BF16 || g.wt == W_FP8);
-  L.inj_hi = take(inj_dense ? sizeof(uint16_t) * (size_t)g.max_inject * g.d : 0);
-  L.inj_lo = take(inj_dense ? sizeof(uint16_t) * (size_t)g.max_inject * g.d : 0);
+  // (and for every injection with FP4 weights, which runs on the 16-row TMA kernel)
+  const bool inj_pair = (g.max_inject >= 128 && (g.wt == W_BF16 || g.wt == W_FP8)) || g.wt == W_FP4;
+  L.inj_hi = take(inj_pair ? sizeof(uint16_t) * (size_t)std::max(g.max_inject, 1) * g.d : 0);
+  L.inj_lo = take(inj_pair ? sizeof(uint16_t) * (size_t)std::max(g.max_inject, 1) * g.d : 0);
   // speculative-loop turn: block positions, accepted-row counts, encoded rows
   L.loop_pos = take(sizeof(int32_t) * (size_t)g.max_seq * DFLASH_BLOCK);
   L.loop_cnt = take(sizeof(int32_t) * (size_t)g.max_seq);
@@ -178,7 +180,7 @@ int validate(const dflash_config* c) {
     return DFLASH_ERR_INVALID_ARG;
   if (c->mask_token_id < 0 || c->mask_token_id >= c->n_vocab) return DFLASH_ERR_INVALID_ARG;
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.0)) return DFLASH_ERR_INVALID_ARG;
-  if (c->weight_dtype < DFLASH_DTYPE_F32 || c->weight_dtype > DFLASH_DTYPE_FP8_E4M3)
+  if (c->weight_dtype < DFLASH_DTYPE_F32 || c->weight_dtype > DFLASH_DTYPE_FP4_E2M1)
     return DFLASH_ERR_INVALID_ARG;
   if ((c->dense_dtype != DFLASH_DTYPE_F32 && c->dense_dtype != DFLASH_DTYPE_BF16) ||
       (c->ring_dtype != DFLASH_DTYPE_F32 && c->ring_dtype != DFLASH_DTYPE_BF16))
@@ -186,7 +188,8 @@ int validate(const dflash_config* c) {
   if (c->n_layer > DFLASH_MAX_LAYERS) return DFLASH_ERR_UNSUPPORTED;
   if (c->n_head % c->n_head_kv) return DFLASH_ERR_UNSUPPORTED;
   if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128) return DFLASH_ERR_UNSUPPORTED;
-  const int kc = c->weight_dtype == DFLASH_DTYPE_FP8_E4M3 ? 64 : 32;
+  const int kc = c->weight_dtype == DFLASH_DTYPE_FP4_E2M1 ? 256
+                 : c->weight_dtype == DFLASH_DTYPE_FP8_E4M3 ? 64 : 32;
   const int qd = c->n_head * c->head_dim;
   if (c->n_embd % kc || qd % kc || c->n_ff % kc) return DFLASH_ERR_UNSUPPORTED;
   if ((c->n_target_layers * c->target_embd) % 32) return DFLASH_ERR_UNSUPPORTED;
@@ -219,6 +222,8 @@ struct dflash_handle {
   CUtensorMap td_layer[DFLASH_MAX_LAYERS][7];
   CUtensorMap td_lm;
   CUtensorMap td_xn[2], td_attn[2], td_act[2];
+  // FP4: the injection input pair for the 16-row kernel
+  CUtensorMap tm_inj[2];
   // prefill on the tcgen05 path (>= 128 rows): fc (bf16 features), all-layer
   // wk / wv, and the injection input pair
   bool enc_dense = false, inj_dense = false;
@@ -365,6 +370,8 @@ GemmParams base_params(const dflash_handle* h) {
   p.window = h->g.W;
   p.n_head_kv = h->g.Hkv;
   p.ring_bf16 = h->g.ring_bf16;
+  // FP4 weights multiply in fp16: their projections' activation pairs are fp16
+  p.pair_f16 = h->g.wt == W_FP4;
   return p;
 }
 
@@ -398,9 +405,10 @@ cudaError_t launch_projection(const dflash_handle* h, GemmParams& p, int l,
                               dense ? h->td_act : h->tm_act};
   set_tma_inputs(p, xs[xi]);
   int i = 0;
-  for (int w : wi)
+  for (int w : wi) {
     p.tm_w[i++] = l < 0 ? (dense ? h->td_lm : h->tm_lm)
                         : (dense ? h->td_layer[l][w] : h->tm_layer[l][w]);
+  }
   if (!dense) return launch_gemm_tma(h->g.wt, p, st);
   p.cpt = cdiv(p.K, 64);
   return launch_gemm_umma(h->g.wt, p, st);
@@ -422,7 +430,8 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   // h = embeddings; xn = split(h * attn_norm_0); ss = row sums of squares
   PROF(h, PC_EMBED, st, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id,
                                      id_last, n_past, n_seq, h->S<double>(L.inv_freq), g.hd, hbuf, ss,
-                                     rope, h->w.layers[0].attn_norm, xn_hi, xn_lo, h->status(), st));
+                                     rope, h->w.layers[0].attn_norm, xn_hi, xn_lo, g.wt == W_FP4,
+                                     h->status(), st));
   int n_ss = 1;
   for (int l = 0; l < g.L; ++l) {
     const dflash_layer_weights& lw = h->w.layers[l];
@@ -458,6 +467,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.n_head = g.Hq; a.n_head_kv = g.Hkv; a.hd = g.hd; a.window = g.W;
     a.scale = (float)(1.0 / std::sqrt((double)g.hd));
     a.out_hi = h->S<uint16_t>(L.attn_hi); a.out_lo = h->S<uint16_t>(L.attn_lo);
+    a.pair_f16 = g.wt == W_FP4;
     a.status = h->status();
     a.block_width = h->width;
     PROF(h, PC_ATTN, st, launch_attention_cluster(a, n_seq, st));
@@ -511,6 +521,12 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
 }
 
 // Tensor maps of every weight the step streams and of the activation pairs.
+// FP4 matrix [rows][cols]: its code bytes as [rows][cols/2] (16-row x 128-byte
+// swizzled boxes); the kernel reads the block scales behind them by bulk copies
+bool make_fp4_map(CUtensorMap* codes, const void* base, uint64_t cols, uint64_t rows) {
+  return make_map(codes, base, W_FP8, cols / 2, rows, 128, 16, true);
+}
+
 bool build_maps(dflash_handle* h) {
   const Geometry& g = h->g;
   const Layout& L = h->L;
@@ -519,10 +535,15 @@ bool build_maps(dflash_handle* h) {
     const void* mats[7] = {w.wq, w.wk, w.wv, w.wo, w.gate, w.up, w.down};
     const int rows[7] = {g.qd, g.kvd, g.kvd, g.d, g.F, g.F, g.d};
     const int cols[7] = {g.d, g.d, g.d, g.qd, g.d, g.d, g.F};
-    for (int i = 0; i < 7; ++i)
-      if (!make_map(&h->tm_layer[l][i], mats[i], g.wt, cols[i], rows[i])) return false;
+    for (int i = 0; i < 7; ++i) {
+      const bool ok = g.wt == W_FP4 ? make_fp4_map(&h->tm_layer[l][i], mats[i], cols[i], rows[i])
+                                    : make_map(&h->tm_layer[l][i], mats[i], g.wt, cols[i], rows[i]);
+      if (!ok) return false;
+    }
   }
-  if (!make_map(&h->tm_lm, h->w.lm_head, g.wt, g.d, g.V)) return false;
+  if (g.wt == W_FP4 ? !make_fp4_map(&h->tm_lm, h->w.lm_head, g.d, g.V)
+                    : !make_map(&h->tm_lm, h->w.lm_head, g.wt, g.d, g.V))
+    return false;
   const size_t pairs[3][2] = {{L.xn_hi, L.xn_lo}, {L.attn_hi, L.attn_lo}, {L.act_hi, L.act_lo}};
   const int kdim[3] = {g.d, g.qd, g.F};
   CUtensorMap* dst[3] = {h->tm_xn, h->tm_attn, h->tm_act};
@@ -544,6 +565,10 @@ bool build_maps(dflash_handle* h) {
         !make_map(&h->td_inj[1], h->scratch + L.inj_lo, W_BF16, g.d, g.max_inject, 64, 128, true))
       return false;
   }
+  if (g.wt == W_FP4 && g.max_inject > 0 &&
+      (!make_map(&h->tm_inj[0], h->scratch + L.inj_hi, W_BF16, g.d, g.max_inject) ||
+       !make_map(&h->tm_inj[1], h->scratch + L.inj_lo, W_BF16, g.d, g.max_inject)))
+    return false;
   // tcgen05 path: batches of >= 128 activation rows with bf16 or E4M3 weights
   h->dense = g.M_max >= 128 && (g.wt == W_BF16 || g.wt == W_FP8);
   if (!h->dense) return true;
@@ -569,7 +594,7 @@ bool bad_ptr(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t
 
 int check_weights(const dflash_config* c, const dflash_weights* w) {
   if (!w) return DFLASH_ERR_INVALID_ARG;
-  const bool fp8 = c->weight_dtype == DFLASH_DTYPE_FP8_E4M3;
+  const bool fp8 = c->weight_dtype == DFLASH_DTYPE_FP8_E4M3 || c->weight_dtype == DFLASH_DTYPE_FP4_E2M1;
   if (bad_ptr(w->tok_embd) || bad_ptr(w->lm_head) || bad_ptr(w->fc) || bad_ptr(w->hidden_norm) ||
       bad_ptr(w->out_norm))
     return DFLASH_ERR_INVALID_ARG;
@@ -727,12 +752,41 @@ int run_inject(dflash_handle* h, int seq, const float* H_t, const int32_t* pos, 
                                 g.W, rows_per_seq, count, h->status(), st));
   const int n_mb = cdiv(T, 16);
   GemmParams p = base_params(h);
+  if (g.wt == W_FP4) {
+    // FP4 weights: H_t as a bf16 pair, then per layer its wk / wv projection on
+    // the 16-row TMA kernel with the ring scatter in the epilogue (the ring
+    // pointer moved to the layer's planes: the epilogue's layer 0)
+    DF_CHECK(h, launch_split_pair(H_t, T * g.d, h->S<uint16_t>(h->L.inj_hi),
+                                  h->S<uint16_t>(h->L.inj_lo), g.wt == W_FP4, st));
+    const size_t layer_bytes = h->L.ring_kv_bytes / g.L;
+    const GemmShape kv = {cdiv(2 * g.kvd, kTileRows), g.d, tma_chunk_k(g.wt)};
+    for (int l = 0; l < g.L; ++l) {
+      const dflash_layer_weights& lw = h->w.layers[l];
+      GemmParams q = base_params(h);
+      set_plan(q, kv, n_mb);
+      q.tm_xh = h->tm_inj[0];
+      q.tm_xl = h->tm_inj[1];
+      q.has_lo = 1;
+      q.tm_w[0] = h->tm_layer[l][1];
+      q.tm_w[1] = h->tm_layer[l][2];
+      q.seg[0] = {lw.wk, lw.wk_scale, 0, g.kvd};
+      q.seg[1] = {lw.wv, lw.wv_scale, g.kvd, g.kvd};
+      q.k_norm_l[0] = lw.k_norm;
+      q.nseg = 2; q.N = 2 * g.kvd; q.map = MAP_SEGMENTS; q.M = T;
+      q.epi = EPI_INJECT; q.ring_seq = h->ring_seq(seq) + (size_t)l * layer_bytes; q.pos = pos;
+      q.rope_cs = rope;
+      q.rows_per_seq = rows_per_seq; q.row_count = count; q.ring_seq_stride = h->L.ring_seq_bytes;
+      DF_CHECK(h, launch_gemm_tma(g.wt, q, st));
+    }
+    prof_end(h, st);
+    return DFLASH_OK;
+  }
   if (h->inj_dense && T >= 128) {
     // >= 128 rows: H_t as a bf16 hi/lo pair, then per layer its wk / wv
     // projection on the tcgen05 kernel with the ring scatter in the epilogue
     // (the ring pointer moved to the layer's planes: the epilogue's layer 0)
     DF_CHECK(h, launch_split_pair(H_t, T * g.d, h->S<uint16_t>(h->L.inj_hi),
-                                  h->S<uint16_t>(h->L.inj_lo), st));
+                                  h->S<uint16_t>(h->L.inj_lo), g.wt == W_FP4, st));
     const size_t layer_bytes = h->L.ring_kv_bytes / g.L;
     for (int l = 0; l < g.L; ++l) {
       const dflash_layer_weights& lw = h->w.layers[l];

@@ -155,10 +155,10 @@ DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* sca
         p.out[(size_t)row * p.ldo + n] = y;
         if (p.pair_hi) {
           // the next projection's input: split(h * next norm weight)
-          const float z = y * nw[k];
-          const uint16_t zh = f32_to_bf16_bits(z);
+          uint16_t zh, zl;
+          split_pair16(y * nw[k], p.pair_f16 != 0, zh, zl);
           p.pair_hi[(size_t)row * p.pair_ld + n] = zh;
-          p.pair_lo[(size_t)row * p.pair_ld + n] = f32_to_bf16_bits(z - bf16_bits_to_f32(zh));
+          p.pair_lo[(size_t)row * p.pair_ld + n] = zl;
         }
       } else if (p.out) {
         p.out[(size_t)row * p.ldo + n] = y;
@@ -229,9 +229,10 @@ DF_DEVICE void epilogue_swiglu(const GemmParams& p, const float* acc_s, const fl
     const float a = gv / (1.f + expf(-gv)) * uv;
     if (p.out) p.out[(size_t)row * p.ldo + f] = a;
     if (p.pair_hi) {
-      const uint16_t ah = f32_to_bf16_bits(a);
+      uint16_t ah, al;
+      split_pair16(a, p.pair_f16 != 0, ah, al);
       p.pair_hi[(size_t)row * p.pair_ld + f] = ah;
-      p.pair_lo[(size_t)row * p.pair_ld + f] = f32_to_bf16_bits(a - bf16_bits_to_f32(ah));
+      p.pair_lo[(size_t)row * p.pair_ld + f] = al;
     }
   }
 }

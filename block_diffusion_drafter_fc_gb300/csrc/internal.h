@@ -9,7 +9,7 @@
 namespace dflash {
 
 // weight storage of a projection matrix
-enum WType { W_F32 = 0, W_BF16 = 1, W_FP8 = 2 };
+enum WType { W_F32 = 0, W_BF16 = 1, W_FP8 = 2, W_FP4 = 3 };
 // activation storage fed to a projection kernel
 enum XMode { X_F32 = 0, X_BF16 = 1, X_F32_DENSE = 2 };
 // what the split-K fix-up does with a finished 16 x 128 output tile
@@ -92,6 +92,7 @@ struct GemmParams {
   uint16_t* pair_hi;
   uint16_t* pair_lo;
   int pair_ld;
+  int pair_f16;           // the pair is fp16 (FP4 weights), else bf16
   const void* pair_norm;
   // q/k/v epilogues
   float* kblk;
@@ -140,8 +141,9 @@ struct AttnParams {
   int hpc;                // query heads per CTA (set by the launcher)
   int kq;                 // key lanes: warps per head
   int nb;                 // 64-key sub-chunk staging buffers (a multiple of kq)
-  uint16_t* out_hi;       // [M][qd] bf16 hi/lo pair (the o projection's input)
+  uint16_t* out_hi;       // [M][qd] hi/lo pair (the o projection's input)
   uint16_t* out_lo;
+  int pair_f16;           // fp16 pair (FP4 weights), else bf16
   unsigned* status;       // device status bits (DFLASH_DEV_TIMEOUT on a copy that never lands)
   int block_width;        // block rows that exist (2..16): block keys at or past it are masked
 };
@@ -172,8 +174,8 @@ cudaError_t launch_attention_cluster(const AttnParams& p, int n_seq, cudaStream_
 cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
                          const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
-                         const void* norm0, uint16_t* x_hi, uint16_t* x_lo, unsigned* status,
-                         cudaStream_t st);
+                         const void* norm0, uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
+                         unsigned* status, cudaStream_t st);
 cudaError_t launch_rope_table(const int32_t* pos, int T, const double* inv_freq, int hd,
                               float2* rope_cs, int32_t* ring_pos, int window, int rows_per_seq,
                               const int32_t* count, unsigned* status, cudaStream_t st);
@@ -186,7 +188,9 @@ cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t* n_ok, int n_seq,
                           int width, cudaStream_t st);
 cudaError_t launch_fill_i32(int32_t* p, int n, int32_t v, cudaStream_t st);
-// x (fp32, n values) -> bf16 hi + lo with x = hi + lo + O(2^-17 |x|)
-cudaError_t launch_split_pair(const float* x, int n, uint16_t* hi, uint16_t* lo, cudaStream_t st);
+// x (fp32, n values) -> bf16 hi + lo with x = hi + lo + O(2^-17 |x|) (pair_f16:
+// fp16 hi + lo)
+cudaError_t launch_split_pair(const float* x, int n, uint16_t* hi, uint16_t* lo, int pair_f16,
+                              cudaStream_t st);
 
 }  // namespace dflash

@@ -20,7 +20,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
                                                     const int32_t* n_past, int n_seq,
                                                     const double* inv_freq, int half, float* h,
                                                     float* ss, float2* rope_cs, const void* norm0,
-                                                    uint16_t* x_hi, uint16_t* x_lo,
+                                                    uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
                                                     unsigned* status) {
   const int M = n_seq * kBlock;
   if ((int)blockIdx.x < M) {
@@ -66,13 +66,13 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
         float4* dst = reinterpret_cast<float4*>(h + (size_t)m * d + k);
         dst[0] = make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
         dst[1] = make_float4(v[r][4], v[r][5], v[r][6], v[r][7]);
-        // first layer's projection input: h * attn_norm, split into bf16 hi + lo
+        // first layer's projection input: h * attn_norm, split into a hi + lo pair
         uint32_t hh[4], ll[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float z0 = v[r][2 * e] * load_dense(norm0, dense_bf16, k + 2 * e);
           const float z1 = v[r][2 * e + 1] * load_dense(norm0, dense_bf16, k + 2 * e + 1);
-          split_bf16x2(z0, z1, hh[e], ll[e]);
+          split_pair16x2(z0, z1, pair_f16 != 0, hh[e], ll[e]);
         }
         *reinterpret_cast<uint4*>(x_hi + (size_t)m * d + k) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
         *reinterpret_cast<uint4*>(x_lo + (size_t)m * d + k) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
@@ -107,13 +107,13 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
 cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
                          const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
-                         const void* norm0, uint16_t* x_hi, uint16_t* x_lo, unsigned* status,
-                         cudaStream_t st) {
+                         const void* norm0, uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
+                         unsigned* status, cudaStream_t st) {
   const int M = n_seq * kBlock, half = hd / 2;
   const int tb = (M * half + 255) / 256;
   embed_kernel<<<M + tb, 256, 0, st>>>(tok_embd, dense_bf16, n_embd, n_vocab, mask_token, id_last,
                                        n_past, n_seq, inv_freq, half, h, ss, rope_cs, norm0, x_hi,
-                                       x_lo, status);
+                                       x_lo, pair_f16, status);
   return cudaGetLastError();
 }
 
@@ -242,14 +242,14 @@ cudaError_t launch_advance(const int32_t* drafts, const int32_t* targets, int n_
   return cudaGetLastError();
 }
 
-// fp32 rows -> the bf16 hi / lo pair the tcgen05 projection reads (two values
-// per thread)
-__global__ void split_pair_kernel(const float* x, int n, uint16_t* hi, uint16_t* lo) {
+// fp32 rows -> the hi / lo pair a projection reads (bf16, or fp16 with FP4
+// weights; two values per thread)
+__global__ void split_pair_kernel(const float* x, int n, uint16_t* hi, uint16_t* lo, int pair_f16) {
   const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (i >= n) return;
   const float2 v = i + 1 < n ? *reinterpret_cast<const float2*>(x + i) : make_float2(x[i], 0.f);
   uint32_t h, l;
-  split_bf16x2(v.x, v.y, h, l);
+  split_pair16x2(v.x, v.y, pair_f16 != 0, h, l);
   if (i + 1 < n) {
     *reinterpret_cast<uint32_t*>(hi + i) = h;
     *reinterpret_cast<uint32_t*>(lo + i) = l;
@@ -259,10 +259,11 @@ __global__ void split_pair_kernel(const float* x, int n, uint16_t* hi, uint16_t*
   }
 }
 
-cudaError_t launch_split_pair(const float* x, int n, uint16_t* hi, uint16_t* lo, cudaStream_t st) {
+cudaError_t launch_split_pair(const float* x, int n, uint16_t* hi, uint16_t* lo, int pair_f16,
+                              cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   const int pairs = (n + 1) / 2;
-  split_pair_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(x, n, hi, lo);
+  split_pair_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(x, n, hi, lo, pair_f16);
   return cudaGetLastError();
 }
 

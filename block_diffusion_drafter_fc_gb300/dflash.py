@@ -20,7 +20,7 @@ PKG = pathlib.Path(__file__).resolve().parent
 LIB_PATH = PKG / "libdflash.so"
 HEADER = PKG.parent / "include" / "dflash.h"
 
-DTYPE = {"f32": 0, "bf16": 1, "fp8": 2}
+DTYPE = {"f32": 0, "bf16": 1, "fp8": 2, "fp4": 3}
 MAX_LAYERS = 16
 PROF_N = 11
 PROF_CLASSES = ("embed", "qkv", "attention", "attn_merge", "o_proj", "gate_up", "down", "lm_head",

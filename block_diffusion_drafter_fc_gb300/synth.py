@@ -17,6 +17,23 @@ copies: one f32 scale per output row, s[n] = max_k |w[n,k]| / 448, and the
 stored byte is the E4M3 (fn variant) code of w[n,k] / s[n], rounded to
 nearest-even and clamped to +-448.  That is weight preparation, not a step
 of the drafter; the cast itself is torch's float8_e4m3fn conversion.
+
+FP4 weights (dflash_head.rs names an NVFP4 LM head; its layout is not on the
+pages, so the format here is self-defined in the same spirit): an E2M1 code
+per weight (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives), one E4M3
+block scale per 16 consecutive weights of a row and one f32 scale per row:
+w = s_row * e4m3(block) * e2m1(code).  s_row = max |w_row| / (6 * 448); the
+block scale is the E4M3 rounding of max |w_block| / (6 s_row); codes are the
+nearest E2M1 values of w / (s_row * block) (ties to the even code, +-6 at
+most).  Stored per matrix as one byte buffer: N x K/2 code bytes, then the
+block scales of each group of 16 rows.  Codes: row-major; within each 16-byte
+group of a row (32 weights) byte 4t + j holds the codes of k = 2 (t + 4j) (low
+nibble) and k + 1 (high nibble), t, j = 0..3, so the four bytes one lane of the
+16-row kernel's MMA fragment needs for two k16 steps sit in one word.  Scales:
+ceil(N/16) x K/16 blocks of 16 bytes; block b of row group G holds the scales of
+block b of rows 16G + (0, 8, 1, 9, ..., 7, 15) (rows past N are zero), so a
+lane reads the scales of rows g and g + 8 as one 16-bit pair and the 16 rows x
+256 k of one pipeline stage are 256 contiguous bytes.
 """
 from __future__ import annotations
 
@@ -32,7 +49,9 @@ import torch
 BLOCK = 16          # tokens in one noise block (anchor + 15 masks)
 FP8_MAX = 448.0     # largest finite E4M3 (fn) magnitude
 
-DTYPES = ("f32", "bf16", "fp8")
+DTYPES = ("f32", "bf16", "fp8", "fp4")
+FP4_MAX = 6.0       # largest E2M1 magnitude
+FP4_BLOCK = 16      # weights per E4M3 block scale
 _TORCH = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -49,7 +68,7 @@ class DraftConfig:
     n_ff: int
     window: int
     n_vocab: int
-    weight_dtype: str           # q/k/v/o/gate/up/down and lm_head: f32 | bf16 | fp8
+    weight_dtype: str           # q/k/v/o/gate/up/down and lm_head: f32 | bf16 | fp8 | fp4
     dense_dtype: str            # tok_embd, fc, norm weights, target features: f32 | bf16
     ring_dtype: str             # ring K/V: f32 | bf16
     n_seq: int = 1
@@ -117,7 +136,11 @@ def _cfg_list() -> List[DraftConfig]:
         n_ff=12288, window=2048, n_vocab=32768, weight_dtype="fp8", dense_dtype="bf16",
         ring_dtype="bf16", n_seq=32, fill_lo=256, fill_hi=2048, offset_hi=65535,
         mismatch="geometric", mismatch_p=0.35, seed=1004)
-    return [tiny, small, real_bf16, real_f32, batched_fp8]
+    # the real-dimension drafter with FP4 projection weights (the quantized drafter
+    # of the dflash-ops model card, Measured: a ~4.6-bit drafter; here 4.5 bits a
+    # weight + one f32 per row)
+    real_fp4 = real_bf16.with_(name="real_fp4", weight_dtype="fp4", seed=1005)
+    return [tiny, small, real_bf16, real_f32, batched_fp8, real_fp4]
 
 
 CONFIGS: List[DraftConfig] = _cfg_list()
@@ -155,8 +178,14 @@ MANY_SEQ = DraftConfig(
     name="many_seq_bf16", n_layer=1, n_embd=256, n_head=8, n_head_kv=4, head_dim=64,
     n_ff=512, window=128, n_vocab=512, weight_dtype="bf16", dense_dtype="bf16",
     ring_dtype="bf16", n_seq=80, fill_lo=16, fill_hi=128, offset_hi=4000, seed=2008)
+# FP4 weights: K (n_embd, qd, n_ff) multiples of 256, several sequences
+SMALL_FP4 = DraftConfig(
+    name="small_fp4", n_layer=2, n_embd=512, n_head=8, n_head_kv=2, head_dim=64,
+    n_ff=1536, window=128, n_vocab=3000, weight_dtype="fp4", dense_dtype="bf16",
+    ring_dtype="bf16", n_seq=3, fill_lo=32, fill_hi=128, offset_hi=65535, seed=2009)
 TEST_CONFIGS: Dict[str, DraftConfig] = {c.name: c for c in (RAGGED, SMALL_FP8, MIXED_F32, DENSE_FP8,
-                                                            DENSE_BF16, WIDE_FP8, WIDE_BF16, MANY_SEQ)}
+                                                            DENSE_BF16, WIDE_FP8, WIDE_BF16, MANY_SEQ,
+                                                            SMALL_FP4)}
 
 
 def get_config(name: str) -> DraftConfig:
@@ -192,17 +221,81 @@ def quantize_fp8_rows(w: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
     return q, s
 
 
+# E2M1 magnitudes by code (bit 3 is the sign) and the rounding boundaries
+# between neighbours: a tie rounds to the code with an even mantissa bit
+_E2M1 = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _e2m1_codes(y: torch.Tensor) -> torch.Tensor:
+    """Nearest E2M1 code (4 bits) of each value, ties to the even code, +-6 at most."""
+    a = y.abs().clamp(max=FP4_MAX)
+    # magnitude code = number of grid points below the value's rounding interval
+    mids = (_E2M1[1:] + _E2M1[:-1]) / 2            # 0.25 0.75 1.25 1.75 2.5 3.5 5
+    idx = torch.bucketize(a, mids, right=False)     # a <= mid -> lower point
+    # at an exact midpoint bucketize chose the lower point: keep it when that code is
+    # even, else take the upper one
+    tie = (idx < 7) & (a == mids[idx.clamp(max=6)]) & (idx % 2 == 1)
+    idx = idx + tie.to(idx.dtype)
+    return (idx | ((y < 0) & (idx > 0)).to(idx.dtype) << 3).to(torch.uint8)
+
+
+def fp4_nbytes(n_rows: int, k: int) -> int:
+    """Size of the FP4 byte buffer of an [N, K] matrix: codes + padded block scales."""
+    return n_rows * k // 2 + -(-n_rows // 16) * 16 * (k // FP4_BLOCK)
+
+
+def quantize_fp4_rows(w: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """FP4 copy of a f32 matrix [N, K] (K % 32 == 0): (bytes uint8 [fp4_nbytes]
+    = codes then block scales, row scales f32 [N]), in row blocks on the pool."""
+    n_rows, k = w.shape
+    nb = k // FP4_BLOCK
+    codes = torch.empty((n_rows, k // 2), dtype=torch.uint8)
+    bsc = torch.empty((n_rows, nb), dtype=torch.uint8)
+    s = torch.empty(n_rows, dtype=torch.float32)
+    step = max(1, _CHUNK // max(1, k))
+
+    def blk(r0):
+        x = w[r0:r0 + step]
+        amax = x.abs().amax(dim=1)
+        sr = torch.where(amax > 0, amax / (FP4_MAX * FP8_MAX), torch.ones_like(amax)).to(torch.float32)
+        s[r0:r0 + step] = sr
+        xb = x.view(x.shape[0], nb, FP4_BLOCK)
+        bmax = xb.abs().amax(dim=2)
+        b8 = (bmax / (FP4_MAX * sr[:, None])).clamp_(max=FP8_MAX).to(torch.float8_e4m3fn)
+        bsc[r0:r0 + step] = b8.view(torch.uint8)
+        b = b8.to(torch.float32)
+        denom = (b * sr[:, None])[:, :, None]
+        y = torch.where(denom > 0, xb / torch.where(denom > 0, denom, torch.ones_like(denom)),
+                        torch.zeros_like(xb))
+        c = _e2m1_codes(y.reshape(x.shape[0], k))
+        pairs = (c[:, 0::2] | (c[:, 1::2] << 4)).reshape(x.shape[0], k // 32, 4, 4)
+        codes[r0:r0 + step] = pairs.transpose(2, 3).reshape(x.shape[0], k // 2)
+
+    list(_POOL.map(blk, range(0, n_rows, step)))
+    # scale blocks by 16-row group: [G][K/16][16], rows within a group in the
+    # order 0, 8, 1, 9, ..., 7, 15 (rows past N zero)
+    groups = -(-n_rows // 16)
+    padded = torch.zeros((groups * 16, nb), dtype=torch.uint8)
+    padded[:n_rows] = bsc
+    order = torch.tensor([r // 2 + 8 * (r % 2) for r in range(16)])
+    grouped = padded.view(groups, 16, nb)[:, order, :].permute(0, 2, 1).contiguous()
+    return torch.cat([codes.reshape(-1), grouped.reshape(-1)]), s
+
+
 @dataclass
 class Weight:
-    """One stored matrix or vector: raw tensor in its storage format (+ FP8 scales)."""
+    """One stored matrix or vector: raw tensor in its storage format (+ FP8 / FP4
+    row scales).  FP4 data is the flat byte buffer of quantize_fp4_rows; `dims`
+    holds its [N, K]."""
 
-    data: torch.Tensor                  # f32 / bf16 tensor, or uint8 codes for fp8
+    data: torch.Tensor                  # f32 / bf16 tensor, uint8 codes (fp8), bytes (fp4)
     dtype: str
-    scale: Optional[torch.Tensor] = None  # f32 [rows] for fp8
+    scale: Optional[torch.Tensor] = None  # f32 [rows] for fp8 / fp4
+    dims: Optional[Tuple[int, int]] = None
 
     @property
     def shape(self):
-        return tuple(self.data.shape)
+        return tuple(self.dims) if self.dims is not None else tuple(self.data.shape)
 
     def nbytes(self) -> int:
         n = self.data.numel() * self.data.element_size()
@@ -305,6 +398,9 @@ def make_weights(cfg: DraftConfig, g: torch.Generator = None) -> Dict[str, Weigh
         if cfg.weight_dtype == "fp8":
             q, s = quantize_fp8_rows(draw(shape, std))
             return Weight(q, "fp8", s)
+        if cfg.weight_dtype == "fp4":
+            q, s = quantize_fp4_rows(draw(shape, std))
+            return Weight(q, "fp4", s, dims=tuple(shape))
         return Weight(draw(shape, std, dtype=cfg.weight_dtype), cfg.weight_dtype)
 
     def dense_mat(shape, std):

@@ -64,7 +64,19 @@ typedef enum {
 typedef enum {
   DFLASH_DTYPE_F32 = 0,
   DFLASH_DTYPE_BF16 = 1,
-  DFLASH_DTYPE_FP8_E4M3 = 2      /* E4M3 "fn" codes + one f32 scale per output row */
+  DFLASH_DTYPE_FP8_E4M3 = 2,     /* E4M3 "fn" codes + one f32 scale per output row */
+  /* E2M1 codes with one E4M3 scale per 16 weights of a row and one f32 scale per
+   * row: w[n][k] = s[n] * e4m3(b[n][k/16]) * e2m1(q[n][k]).  A matrix [N][K] is
+   * one buffer of N*K/2 code bytes (row-major) followed by N*K/16 block-scale
+   * bytes; the row scales use the *_scale pointer.  Within each 16-byte group of
+   * a row (32 weights) byte 4t + j holds the codes of k = 2(t + 4j) (low nibble)
+   * and k + 1 (high nibble), t, j = 0..3.  Projection weights only
+   * (q/k/v/o/gate/up/down, lm_head); every K (n_embd, n_head*head_dim, n_ff) a
+   * multiple of 256.  The products run in fp16 against an fp16 hi/lo activation
+   * pair (exact weights, activations to 2^-22 relative), so projection inputs
+   * must stay below 65504 in magnitude.  dflash_head.rs (field lm_head_nvfp4)
+   * names an NVFP4 LM head but not its layout: this one is the library's own. */
+  DFLASH_DTYPE_FP4_E2M1 = 3
 } dflash_dtype;
 
 /* Bits of the device status word (dflash_read_status). */

@@ -3,7 +3,8 @@
 TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
 CPU-baseline leg may import this module.  It shares no code with the CUDA
 path: it reads the same stored bytes (bf16 bit patterns, f32 values, E4M3
-codes with per-row f32 scales) and computes the step directly from its
+codes with per-row f32 scales, E2M1 codes with E4M3 block and f32 row scales)
+and computes the step directly from its
 definition in float64, with no tiling, no online softmax and no fusion.
 
 Sources (the pages that define the method):
@@ -93,15 +94,53 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     return np.where((e == 15) & (m == 7), np.nan, v)
 
 
+def e2m1_to_f64(codes: np.ndarray) -> np.ndarray:
+    """FP4 E2M1 codes (4 bits: sign, 2 exponent bits with bias 1, 1 mantissa bit;
+    no infinities or NaN) -> float64: 0, 0.5, 1, 1.5, 2, 3, 4, 6 and negatives."""
+    c = np.asarray(codes, dtype=np.int64) & 0xF
+    s = np.where(c & 8, -1.0, 1.0)
+    e = (c >> 1) & 3
+    m = (c & 1).astype(np.float64)
+    return s * np.where(e == 0, 0.5 * m, (1.0 + 0.5 * m) * np.exp2(e - 1.0))
+
+
 def decode(raw: np.ndarray, dtype: str, scale: Optional[np.ndarray] = None) -> np.ndarray:
     """Stored tensor -> float64 values.  FP8 rows are multiplied by their f32
-    scale: y[n] = s[n] * sum_k q[n,k] x[k] is the same as using s[n] * q[n,k]."""
+    scale: y[n] = s[n] * sum_k q[n,k] x[k] is the same as using s[n] * q[n,k].
+    FP4 (the self-defined block-scaled format of the weights) is one flat byte
+    buffer per [N, K] matrix, N = len(scale): w[n,k] = s[n] *
+    e4m3(block[n, k // 16]) * e2m1(code[n,k]).  The first N K/2 bytes are the
+    codes, row-major; within each 16-byte group of a row (32 weights) byte
+    4t + j holds the codes of k = 2 (t + 4j) (low nibble) and k + 1 (high
+    nibble), t, j = 0..3.  Then ceil(N/16) x K/16 blocks of 16 scale bytes:
+    block b of row group G holds block b's scales of rows 16G + (0, 8, 1, 9,
+    ..., 7, 15)."""
     if dtype == "bf16":
         return bf16_to_f64(raw)
     if dtype == "f32":
         return np.asarray(raw, dtype=np.float32).astype(np.float64)
     if dtype == "fp8":
         v = e4m3_to_f64(raw)
+        return v * np.asarray(scale, dtype=np.float64)[:, None]
+    if dtype == "fp4":
+        r = np.asarray(raw, dtype=np.uint8).reshape(-1)
+        n = len(scale)
+        groups = -(-n // 16)
+        k = 2 * r.size // (n + 2 * groups)          # size = n k/2 + groups 16 k/16
+        codes = r[:n * k // 2].reshape(n, k // 2)
+        # stored byte 4t + j of a group -> code pair t + 4j (the 4 x 4 transpose)
+        codes = codes.reshape(n, k // 32, 4, 4).transpose(0, 1, 3, 2).reshape(n, k // 2)
+        # scale byte p of block (G, b) -> row 16G + p // 2 + 8 (p % 2)
+        sb = r[n * k // 2:].reshape(groups, k // 16, 16)
+        p = np.arange(16)
+        blocks = np.empty((groups * 16, k // 16), dtype=np.uint8)
+        blocks[(np.arange(groups)[:, None] * 16 + p // 2 + 8 * (p % 2)).reshape(-1)] = \
+            sb.transpose(0, 2, 1).reshape(groups * 16, k // 16)
+        blocks = blocks[:n]
+        v = np.empty((n, k), dtype=np.float64)
+        v[:, 0::2] = e2m1_to_f64(codes & 0xF)
+        v[:, 1::2] = e2m1_to_f64(codes >> 4)
+        v *= np.repeat(e4m3_to_f64(blocks), 16, axis=1)
         return v * np.asarray(scale, dtype=np.float64)[:, None]
     raise ValueError(dtype)
 

@@ -158,6 +158,45 @@ def pin_e4m3_decode_all():
     assert np.array_equal(got[m], want[m]), "e4m3 decode"
 
 
+def pin_e2m1_decode_all():
+    """The 16 E2M1 codes decode to the format's values: 0, 0.5, 1, 1.5, 2, 3, 4, 6
+    (codes 0..7) and their negatives (codes 8..15, with -0)."""
+    want = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    got = O.e2m1_to_f64(np.arange(16))
+    assert np.array_equal(got[:8], want) and np.array_equal(got[8:], [-v for v in want])
+
+
+def pin_fp4_block_decode_bruteforce():
+    """A small FP4 matrix (19 rows: a ragged last row group) decoded element by
+    element from its flat buffer: code nibble, block scale and row scale each
+    located by the stated byte layout, one weight at a time, against the
+    oracle's vectorised decode."""
+    g = np.random.default_rng(5)
+    n, k = 19, 96
+    groups = (n + 15) // 16
+    buf = g.integers(0, 256, size=n * k // 2 + groups * 16 * (k // 16), dtype=np.uint8)
+    sc_off = n * k // 2
+    # keep every block scale finite and positive (E4M3 0x7f / 0xff are NaN)
+    buf[sc_off:] &= 0x7e
+    srow = g.uniform(0.5, 2.0, size=n)
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    want = np.zeros((n, k))
+    for r in range(n):
+        for c in range(k):
+            # the pair index within the 32-weight group is t + 4j, stored at byte 4t + j
+            pair = (c % 32) // 2
+            byte = r * (k // 2) + 16 * (c // 32) + 4 * (pair % 4) + pair // 4
+            nib = (int(buf[byte]) >> (4 * (c % 2))) & 0xF
+            v = table[nib & 7] * (-1.0 if nib & 8 else 1.0)
+            # rows 16G + (0, 8, 1, 9, ...): row r sits at position 2 (r % 8) + (r % 16) // 8
+            pos = 2 * (r % 8) + (r % 16) // 8
+            sbyte = sc_off + ((r // 16) * (k // 16) + c // 16) * 16 + pos
+            want[r, c] = srow[r] * float(O.e4m3_to_f64(np.array([buf[sbyte]]))[0]) * v
+    got = O.decode(buf, "fp4", srow)
+    # the three factors are multiplied in another order: a few ulp of |w| <= 5400
+    _close(got, want, 1e-11, "fp4 decode")
+
+
 def pin_fp8_row_scale():
     """y[n] = s[n] * sum_k q[n,k] x[k] (dflash_head.rs, enum DflashQuantization)."""
     g = torch.Generator().manual_seed(13)

@@ -57,6 +57,8 @@ def test_config_validation():
     assert _bad(weight_dtype=7) == -1
     assert _bad(n_layer=17) == -2
     assert _bad(weight_dtype=2, n_embd=288) == -2   # FP8 needs multiples of 64
+    assert _bad(weight_dtype=3, n_embd=384) == -2   # FP4 needs multiples of 256
+    assert _bad(weight_dtype=4) == -1
     assert _bad(n_head=18, n_head_kv=2, head_dim=128) == -2   # more than 8 q heads per kv head
 
 

@@ -37,7 +37,7 @@ def _turn_inputs(cfg, ref_drafts, turn):
     return targets, feats
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "ragged_bf16", "small_fp8", "many_seq_bf16"])
+@pytest.mark.parametrize("name", ["tiny_f32", "ragged_bf16", "small_fp8", "many_seq_bf16", "small_fp4"])
 def test_loop_turns_match_oracle(name):
     from block_diffusion_drafter_fc_gb300 import dflash as D
     cfg = get_config(name)

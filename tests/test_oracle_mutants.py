@@ -150,6 +150,52 @@ def _advance_variant(inject_rows, bonus_shift, past_shift):
     return adv
 
 
+def _fp4_variant(swap_nibbles, block_len, zero_code_half, transpose=True):
+    """The oracle's FP4 decode with one planted mistake."""
+    def dec(raw, dtype, scale=None):
+        if dtype != "fp4":
+            return _orig["decode"](raw, dtype, scale)
+        r = np.asarray(raw, dtype=np.uint8).reshape(-1)
+        n = len(scale)
+        groups = -(-n // 16)
+        k = 2 * r.size // (n + 2 * groups)
+        codes = r[:n * k // 2].reshape(n, k // 2)
+        if transpose:
+            codes = codes.reshape(n, k // 32, 4, 4).transpose(0, 1, 3, 2).reshape(n, k // 2)
+        sb = r[n * k // 2:].reshape(groups, k // 16, 16)
+        p = np.arange(16)
+        blocks = np.empty((groups * 16, k // 16), dtype=np.uint8)
+        blocks[(np.arange(groups)[:, None] * 16 + p // 2 + 8 * (p % 2)).reshape(-1)] = \
+            sb.transpose(0, 2, 1).reshape(groups * 16, k // 16)
+        blocks = blocks[:n]
+        lo, hi = (codes >> 4, codes & 0xF) if swap_nibbles else (codes & 0xF, codes >> 4)
+        v = np.empty((n, k), dtype=np.float64)
+        v[:, 0::2] = O.e2m1_to_f64(lo)
+        v[:, 1::2] = O.e2m1_to_f64(hi)
+        if zero_code_half:      # the subnormal code 1 read as 0
+            v[:, 0::2][(lo & 7) == 1] = 0.0
+            v[:, 1::2][(hi & 7) == 1] = 0.0
+        bs = np.repeat(O.e4m3_to_f64(blocks), block_len, axis=1)
+        bs = np.concatenate([bs] * (k // bs.shape[1] + 1), axis=1)[:, :k]
+        return v * bs * np.asarray(scale, dtype=np.float64)[:, None]
+    return dec
+
+
+def _fp4_scale_rows_plain(raw, dtype, scale=None):
+    """FP4 decode that reads the 16 scale bytes of a block in plain row order."""
+    if dtype != "fp4":
+        return _orig["decode"](raw, dtype, scale)
+    r = np.asarray(raw, dtype=np.uint8).reshape(-1).copy()
+    n = len(scale)
+    groups = -(-n // 16)
+    k = 2 * r.size // (n + 2 * groups)
+    sb = r[n * k // 2:].reshape(groups, k // 16, 16)
+    # un-permute to plain order, then let the original decode re-permute it
+    order = np.array([2 * (i % 8) + i // 8 for i in range(16)])
+    r[n * k // 2:] = sb[:, :, order].reshape(-1)
+    return _orig["decode"](r, dtype, scale)
+
+
 MUTANTS = {
     "rmsnorm drops eps": ("rmsnorm", _rms_no_eps),
     "rmsnorm sums instead of mean": ("rmsnorm", _rms_sum),
@@ -169,6 +215,11 @@ MUTANTS = {
     "bf16 truncation": ("f64_to_bf16", _bf16_truncate),
     "e4m3 wrong bias": ("e4m3_to_f64", _e4m3_bias8),
     "fp8 scale dropped": ("decode", _decode_no_scale),
+    "fp4 nibbles swapped": ("decode", _fp4_variant(True, 16, False)),
+    "fp4 block of 32 weights": ("decode", _fp4_variant(False, 32, False)),
+    "fp4 code 0.5 read as 0": ("decode", _fp4_variant(False, 16, True)),
+    "fp4 bytes read in plain order": ("decode", _fp4_variant(False, 16, False, transpose=False)),
+    "fp4 scale rows in plain order": ("decode", _fp4_scale_rows_plain),
     "V roped at injection": ("inject_kv", _inject_kv_v_roped),
     "K not normed at injection": ("inject_kv", _inject_kv_no_knorm),
     "encode drops hidden_norm": ("encode", _encode_no_norm_weight),
