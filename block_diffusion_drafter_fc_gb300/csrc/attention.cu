@@ -24,6 +24,7 @@
 
 #include <math_constants.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -69,6 +70,14 @@ DF_DEVICE void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* b
       : "memory");
 }
 
+DF_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+
 DF_DEVICE void ldsm_x4(uint32_t (&r)[4], const void* smem) {
   const unsigned a = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -91,19 +100,21 @@ struct AttnPlan {
 // plan of large batched grids stages two sub-chunks with four warps so that
 // two CTAs share an SM and overlap one another's copies and math.
 constexpr int kLatencyPlans = 4;
-inline int plans_for(bool f32, int G, AttnPlan (&out)[kLatencyPlans + 1]) {
-  const int nb = f32 ? 2 : 4;
+inline int plans_for(bool f32, int G, int n_sub, AttnPlan (&out)[kLatencyPlans + 1]) {
+  const int nb_max = f32 ? 2 : 4;
   int n = 0;
   const int hpcs[3] = {4, 2, 1};
   const int kqs[3] = {4, 2, 1};
   for (int hpc : hpcs) {
     if (G % hpc) continue;
     for (int kq : kqs) {
-      if (hpc * kq > 8 || kq > nb || hpc * kq < 4 || n >= kLatencyPlans) continue;
+      if (hpc * kq > 8 || kq > nb_max || hpc * kq < 4 || n >= kLatencyPlans) continue;
+      // no more buffers than the slice has sub-chunks (rounded up to the key lanes)
+      const int nb = std::min(nb_max, std::max(kq, (n_sub + kq - 1) / kq * kq));
       out[n++] = AttnPlan{hpc, kq, nb};
     }
   }
-  if (n == 0) out[n++] = AttnPlan{1, nb, nb};  // groups of odd size
+  if (n == 0) out[n++] = AttnPlan{1, nb_max, nb_max};  // groups of odd size
   int h2 = G % 2 == 0 ? 2 : 1;
   out[n++] = AttnPlan{h2, 2, 2};               // throughput plan (last)
   return n;
@@ -113,12 +124,19 @@ template <int HD>
 struct AttnSmem {
   static constexpr int KS = HD + kPad;
   static constexpr int TILE = kSub * KS;               // one [64][KS] bf16 tile (elements)
+  // a bf16 ring with hd >= 64 is staged by TMA: [64 slots][HD] tiles of 64-dim
+  // boxes, 128-byte swizzled (no padding), the buffers 1024-byte aligned
+  static constexpr bool kTma = HD >= 64;
+  static constexpr int TILE_SW = kSub * HD;
   // buffer b: K hi, V hi, K lo, V lo (lo only used by an fp32 ring)
   static constexpr int BUF = 4 * TILE;
   static constexpr int BLK = 4 * kBlock * KS;          // block keys: K hi/lo, V hi/lo [16][KS]
   // staging: nb sub-chunk buffers, the block keys, nb x 64 slot positions
+  static constexpr __host__ __device__ size_t buf_elems(bool f32) {
+    return f32 ? BUF : (kTma ? 2 * TILE_SW : 2 * TILE);
+  }
   static size_t stage_bytes(bool f32, int nb) {
-    return (size_t)nb * (f32 ? BUF : 2 * TILE) * 2 + (size_t)BLK * 2 + (size_t)nb * kSub * 4;
+    return (size_t)nb * buf_elems(f32) * 2 + (size_t)BLK * 2 + (size_t)nb * kSub * 4;
   }
   // merge: per-warp fragments [warps][HD/8][32] float4 + (m, l) float4 per lane,
   // then the CTA's partial [R][HD] + (m, l)
@@ -127,13 +145,21 @@ struct AttnSmem {
            (size_t)R * 8;
   }
   static size_t bytes(bool f32, const AttnPlan& pl) {
-    const size_t a = stage_bytes(f32, pl.nb), b = merge_bytes(pl.kq * pl.hpc, kBlock * pl.hpc);
+    const size_t a = stage_bytes(f32, pl.nb) + (kTma && !f32 ? 1024 : 0),
+                 b = merge_bytes(pl.kq * pl.hpc, kBlock * pl.hpc);
     return (a > b ? a : b) + 256;
   }
 };
 
 // Online-softmax update of one warp's 16 rows with one tile of up to 64 keys.
-template <int HD, bool SPLIT>
+// element offset of (row, dim) in a swizzled [64][HD] ring tile: 64-dim boxes of
+// 64 rows x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)
+template <int HD>
+DF_DEVICE int sw_off(int row, int dim) {
+  return (dim >> 6) * (kSub * 64) + row * 64 + ((((dim & 63) >> 3) ^ (row & 7)) << 3);
+}
+
+template <int HD, bool SPLIT, bool SW = false>
 DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql)[HD / 16][4],
                            const uint16_t* k_hi, const uint16_t* k_lo, const uint16_t* v_hi,
                            const uint16_t* v_lo, int KS, int nt, const int* kpos, bool blk, int p0,
@@ -157,7 +183,8 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
         int off[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          off[u] = (8 * (j0 + 2 * u + (lm >> 1)) + (lane & 7)) * KS + ks * 16 + (lm & 1) * 8;
+          const int row = 8 * (j0 + 2 * u + (lm >> 1)) + (lane & 7), dim = ks * 16 + (lm & 1) * 8;
+          off[u] = SW ? sw_off<HD>(row, dim) : row * KS + dim;
           if (j0 + 2 * u < nt) ldsm_x4(b[u], k_hi + off[u]);
         }
 #pragma unroll
@@ -267,7 +294,10 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
         const int key = 16 * kk + (lmat & 1) * 8 + lrow;
         uint32_t b[2][4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) ldsm_x4_t(b[u], v_hi + key * KS + 8 * (jd + 2 * u) + (lmat >> 1) * 8);
+        for (int u = 0; u < 2; ++u) {
+          const int dim = 8 * (jd + 2 * u) + (lmat >> 1) * 8;
+          ldsm_x4_t(b[u], v_hi + (SW ? sw_off<HD>(key, dim) : key * KS + dim));
+        }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           mma_bf16_16816(O[jd + 2 * u], ph[kk], b[u][0], b[u][1]);
@@ -307,9 +337,11 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int nwarps = (int)(blockDim.x >> 5);
   const int hl = warp / kq, lk = warp - hl * kq;    // head within the CTA, key lane
+  constexpr bool TMA = !RING_F32 && SM::kTma;
   extern __shared__ __align__(16) uint8_t sm_raw[];
-  uint16_t* bufs = reinterpret_cast<uint16_t*>(sm_raw);
-  const int buf_elems = RING_F32 ? SM::BUF : 2 * SM::TILE;
+  uint16_t* bufs = reinterpret_cast<uint16_t*>(
+      TMA ? (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023) : reinterpret_cast<uintptr_t>(sm_raw));
+  const int buf_elems = (int)SM::buf_elems(RING_F32);
   uint16_t* blk_k_hi = bufs + nb * buf_elems;
   uint16_t* blk_k_lo = blk_k_hi + kBlock * KS;
   uint16_t* blk_v_hi = blk_k_lo + kBlock * KS;
@@ -339,7 +371,27 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
   // threads.
   auto stage_round = [&](int j0) {
     const int jn = min(n_sub, j0 + nb);
-    if (!RING_F32) {
+    if (TMA) {
+      // per sub-chunk: K and V as HD/64 boxes of 64 slots x 64 dims each (slots
+      // past the CTA's range are the next ones in memory or the zero fill past
+      // the ring: finite, and masked by their slot position)
+      __syncthreads();  // earlier reads of the buffers are done
+      if (tid == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const int row_k = (int)(kbase / HD), row_v = (int)(vbase / HD);
+        for (int j = j0; j < jn; ++j) {
+          mbar_expect_tx(&s_bar[j % nb], (uint32_t)(2 * SM::TILE_SW * 2));
+          uint16_t* dst = bufs + (j % nb) * buf_elems;
+          const int s0 = s_begin + j * kSub;
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+            for (int hb = 0; hb < HD / 64; ++hb)
+              tma_load_2d(dst + kv * SM::TILE_SW + hb * kSub * 64, &p.tm_ring, hb * 64,
+                          (kv ? row_v : row_k) + s0, &s_bar[j % nb]);
+        }
+      }
+    } else if (!RING_F32) {
       if (tid == 0)
         for (int j = j0; j < jn; ++j) {
           const int nk = min(kSub, s_end - (s_begin + j * kSub));
@@ -507,9 +559,14 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
                                                    (kb >= 0 && kb < p0 && p0 - kb < p.window));
       if (active && any) {
         const uint16_t* kh = bufs + (j % nb) * buf_elems;
-        attend_tile<HD, RING_F32>(qh, ql, kh, kh + 2 * SM::TILE, kh + SM::TILE, kh + 3 * SM::TILE,
-                                  KS, 8, kpos + (j % nb) * kSub, false, p0, p.window, 16, m0, m1, l0,
-                                  l1, O, lane);
+        if (TMA)
+          attend_tile<HD, false, true>(qh, ql, kh, nullptr, kh + SM::TILE_SW, nullptr, KS, 8,
+                                       kpos + (j % nb) * kSub, false, p0, p.window, 16, m0, m1, l0,
+                                       l1, O, lane);
+        else
+          attend_tile<HD, RING_F32>(qh, ql, kh, kh + 2 * SM::TILE, kh + SM::TILE, kh + 3 * SM::TILE,
+                                    KS, 8, kpos + (j % nb) * kSub, false, p0, p.window, 16, m0, m1, l0,
+                                    l1, O, lane);
       }
     }
     __syncthreads();  // the buffers are restaged by the next round
@@ -589,11 +646,11 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
     if (lane < CL) ml = cluster.map_shared_rank(part_ml, lane)[r];
     float M = ml.x;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int o = kMaxCluster / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float wgt = (lane < CL && ml.x != -CUDART_INF_F) ? exp2f(ml.x - M) : 0.f;
     float L = wgt * ml.y;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    for (int o = kMaxCluster / 2; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     L = __shfl_sync(0xffffffffu, L, 0);  // lanes 0..7 hold the total
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -637,7 +694,7 @@ static size_t smem_of_hd(int hd, bool f32, const AttnPlan& pl) {
 
 size_t attn_cluster_smem(int group, int hd, int ring_f32) {
   AttnPlan pls[kLatencyPlans + 1];
-  const int n = plans_for(ring_f32 != 0, group, pls);
+  const int n = plans_for(ring_f32 != 0, group, 1 << 20, pls);   // the deepest staging of any window
   size_t best = 0;
   for (int i = 0; i < n; ++i) {
     const size_t b = smem_of_hd(hd, ring_f32 != 0, pls[i]);
@@ -694,8 +751,8 @@ static int active_clusters(const AttnPlan& pl, int CL, bool query) {
 template <int HD, bool F32>
 static AttnPlan choose_plan(int G, int CL, int n_head_kv, int n_seq, int window, bool query) {
   AttnPlan pls[kLatencyPlans + 1];
-  const int n = plans_for(F32, G, pls);
   const int per = (window + CL - 1) / CL, n_sub = (per + kSub - 1) / kSub;
+  const int n = plans_for(F32, G, n_sub, pls);
   AttnPlan best = pls[n - 1];
   double best_cost = 1e30;
   for (int i = 0; i < n - 1; ++i) {
@@ -717,7 +774,7 @@ static AttnPlan choose_plan(int G, int CL, int n_head_kv, int n_seq, int window,
 }
 
 template <int HD, bool F32>
-static cudaError_t configure_cl(size_t smem, int G, int CL, int n_head_kv) {
+static cudaError_t configure_cl(size_t smem, int G, int CL, int n_head_kv, int window) {
   static size_t configured = 0;   // only ever raised, so every live handle still fits
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(attn_cluster_kernel<HD, F32>,
@@ -726,7 +783,8 @@ static cudaError_t configure_cl(size_t smem, int G, int CL, int n_head_kv) {
     configured = smem;
   }
   AttnPlan pls[kLatencyPlans + 1];
-  const int n = plans_for(F32, G, pls);
+  const int per = (window + CL - 1) / CL, n_sub = (per + kSub - 1) / kSub;
+  const int n = plans_for(F32, G, n_sub, pls);
   for (int i = 0; i < n; ++i) (void)active_clusters<HD, F32>(pls[i], CL, true);
   (void)n_head_kv;
   return cudaSuccess;
@@ -736,12 +794,12 @@ cudaError_t configure_attention_cluster(int group, int hd, int ring_f32, int win
   const size_t smem = attn_cluster_smem(group, hd, ring_f32);
   const int CL = attn_cluster_size(window);
   switch (hd) {
-    case 32: return ring_f32 ? configure_cl<32, true>(smem, group, CL, n_head_kv)
-                             : configure_cl<32, false>(smem, group, CL, n_head_kv);
-    case 64: return ring_f32 ? configure_cl<64, true>(smem, group, CL, n_head_kv)
-                             : configure_cl<64, false>(smem, group, CL, n_head_kv);
-    case 128: return ring_f32 ? configure_cl<128, true>(smem, group, CL, n_head_kv)
-                              : configure_cl<128, false>(smem, group, CL, n_head_kv);
+    case 32: return ring_f32 ? configure_cl<32, true>(smem, group, CL, n_head_kv, window)
+                             : configure_cl<32, false>(smem, group, CL, n_head_kv, window);
+    case 64: return ring_f32 ? configure_cl<64, true>(smem, group, CL, n_head_kv, window)
+                             : configure_cl<64, false>(smem, group, CL, n_head_kv, window);
+    case 128: return ring_f32 ? configure_cl<128, true>(smem, group, CL, n_head_kv, window)
+                              : configure_cl<128, false>(smem, group, CL, n_head_kv, window);
   }
   return cudaErrorInvalidValue;
 }

@@ -224,6 +224,8 @@ struct dflash_handle {
   CUtensorMap td_xn[2], td_attn[2], td_act[2];
   // FP4: the injection input pair for the 16-row kernel
   CUtensorMap tm_inj[2];
+  // bf16 ring with hd >= 64: the attention kernel's staging map
+  CUtensorMap tm_ring;
   // prefill on the tcgen05 path (>= 128 rows): fc (bf16 features), all-layer
   // wk / wv, and the injection input pair
   bool enc_dense = false, inj_dense = false;
@@ -468,6 +470,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.scale = (float)(1.0 / std::sqrt((double)g.hd));
     a.out_hi = h->S<uint16_t>(L.attn_hi); a.out_lo = h->S<uint16_t>(L.attn_lo);
     a.pair_f16 = g.wt == W_FP4;
+    a.tm_ring = h->tm_ring;
     a.status = h->status();
     a.block_width = h->width;
     PROF(h, PC_ATTN, st, launch_attention_cluster(a, n_seq, st));
@@ -563,6 +566,12 @@ bool build_maps(dflash_handle* h) {
     }
     if (!make_map(&h->td_inj[0], h->scratch + L.inj_hi, W_BF16, g.d, g.max_inject, 64, 128, true) ||
         !make_map(&h->td_inj[1], h->scratch + L.inj_lo, W_BF16, g.d, g.max_inject, 64, 128, true))
+      return false;
+  }
+  if (g.ring_bf16 && g.hd >= 64) {
+    const uint64_t rows = (uint64_t)g.max_seq * g.L * 2 * g.Hkv * g.W;
+    if (rows >= (1ull << 31) ||
+        !make_map(&h->tm_ring, h->ring, W_BF16, g.hd, rows, 64, 64, true))
       return false;
   }
   if (g.wt == W_FP4 && g.max_inject > 0 &&

@@ -128,6 +128,10 @@ struct GemmParams {
 };
 
 struct AttnParams {
+  // bf16 ring with hd >= 64: the whole ring as a 2-D bf16 tensor [rows][hd]
+  // (row = ((((seq L + layer) 2 + k|v) Hkv + kv head) W + slot), 64 x 64 boxes,
+  // 128-byte swizzle; the kernel stages 64-slot sub-chunks with it
+  CUtensorMap tm_ring;
   const float* q;         // [M][qd], roped
   const float* kblk;      // [M][kvd], roped
   const float* vblk;      // [M][kvd]
