@@ -105,7 +105,7 @@ def gemm_source_hash():
     """Hash of the sources of the projection kernels (TMA-fed and tcgen05): a
     committed ncu traffic figure is used only while it matches."""
     h = hashlib.sha256()
-    for f in ("gemm_tma.cu", "gemm_umma.cu", "gemm_common.cuh", "common.cuh", "internal.h"):
+    for f in ("gemm_tma.cu", "gemm_umma.cu", "gemm_fp4.cu", "gemm_common.cuh", "common.cuh", "internal.h"):
         h.update((ROOT / "block_diffusion_drafter_fc_gb300" / "csrc" / f).read_bytes())
     return h.hexdigest()[:16]
 

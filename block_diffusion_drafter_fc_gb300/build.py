@@ -21,7 +21,7 @@ LIB = PKG / "libdflash.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", f"-I{ROOT / 'include'}", f"-I{CSRC}"]
-SOURCES = ["dflash_api.cu", "attention.cu", "gemm.cu", "gemm_tma.cu", "gemm_umma.cu", "kernels.cu", "noalloc.cu"]
+SOURCES = ["dflash_api.cu", "attention.cu", "gemm.cu", "gemm_tma.cu", "gemm_umma.cu", "gemm_fp4.cu", "kernels.cu", "noalloc.cu"]
 
 
 def nvcc() -> str:

@@ -216,7 +216,16 @@ struct dflash_handle {
   // the LM head) and of the three activation-pair buffers
   CUtensorMap tm_layer[DFLASH_MAX_LAYERS][7];
   CUtensorMap tm_lm;
+  // bf16 / E4M3 weights in 64-row boxes for the 16-row kernel
+  CUtensorMap tm_layer64[DFLASH_MAX_LAYERS][7];
+  CUtensorMap tm_lm64;
+  // FP4: block scales as [groups of 16 rows][K bytes], 256 x 4 boxes
+  CUtensorMap tm_scale64[DFLASH_MAX_LAYERS][7];
+  CUtensorMap tm_lm_s64;
   CUtensorMap tm_xn[2], tm_attn[2], tm_act[2];
+  // FP4: the same pairs as 4-D hi+lo maps (all three, then the injection pair)
+  CUtensorMap tm_x4[4];
+  bool x4 = false;
   // the same for the tcgen05 kernel (128-row activation boxes, 32-row weight boxes)
   bool dense = false;
   CUtensorMap td_layer[DFLASH_MAX_LAYERS][7];
@@ -406,11 +415,19 @@ cudaError_t launch_projection(const dflash_handle* h, GemmParams& p, int l,
   const CUtensorMap* xs[3] = {dense ? h->td_xn : h->tm_xn, dense ? h->td_attn : h->tm_attn,
                               dense ? h->td_act : h->tm_act};
   set_tma_inputs(p, xs[xi]);
+  if (h->x4) {
+    p.tm_x4 = h->tm_x4[xi];
+    p.x4 = 1;
+  }
   int i = 0;
   for (int w : wi) {
+    p.tm_w64[i] = l < 0 ? h->tm_lm64 : h->tm_layer64[l][w];
+    if (h->g.wt == W_FP4) p.tm_s64[i] = l < 0 ? h->tm_lm_s64 : h->tm_scale64[l][w];
     p.tm_w[i++] = l < 0 ? (dense ? h->td_lm : h->tm_lm)
                         : (dense ? h->td_layer[l][w] : h->tm_layer[l][w]);
   }
+  p.w64 = h->g.wt == W_BF16 || h->g.wt == W_FP8 || h->g.wt == W_FP4;
+  if (h->g.wt == W_FP4) return launch_gemm_fp4(p, st);
   if (!dense) return launch_gemm_tma(h->g.wt, p, st);
   p.cpt = cdiv(p.K, 64);
   return launch_gemm_umma(h->g.wt, p, st);
@@ -530,6 +547,34 @@ bool make_fp4_map(CUtensorMap* codes, const void* base, uint64_t cols, uint64_t 
   return make_map(codes, base, W_FP8, cols / 2, rows, 128, 16, true);
 }
 
+// The same codes in 64-row boxes, and the block scales behind them as a 2-D
+// byte tensor [ceil(rows/16) groups][cols bytes] in boxes of 256 bytes x 4
+// groups (the scales of 64 rows x 256 k)
+// An activation pair (hi at `hi`, lo at `lo` > hi, each [rows][cols] bf16-sized
+// elements) as one 4-D tensor: dims (64 k, rows, hi|lo, cols/64 k boxes),
+// boxes of 64 x 16 x 2 x 4 with the 128-byte swizzle: per 64 k, 16 hi rows then
+// 16 lo rows
+bool make_pair_map4(CUtensorMap* m, const void* hi, const void* lo, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || lo <= hi) return false;
+  const cuuint64_t dims[4] = {64, rows, 2, cols / 64};
+  const cuuint64_t strides[3] = {cols * 2,
+                                 (cuuint64_t)(static_cast<const char*>(lo) - static_cast<const char*>(hi)),
+                                 128};
+  const cuuint32_t box[4] = {64, 16, 2, 4};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(hi), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_fp4_maps64(CUtensorMap* codes, CUtensorMap* scales, const void* base, uint64_t cols,
+                     uint64_t rows) {
+  const char* b = static_cast<const char*>(base);
+  return make_map(codes, b, W_FP8, cols / 2, rows, 128, 64, true) &&
+         make_map(scales, b + rows * cols / 2, W_FP8, cols, (rows + 15) / 16, 256, 4, false);
+}
+
 bool build_maps(dflash_handle* h) {
   const Geometry& g = h->g;
   const Layout& L = h->L;
@@ -542,11 +587,20 @@ bool build_maps(dflash_handle* h) {
       const bool ok = g.wt == W_FP4 ? make_fp4_map(&h->tm_layer[l][i], mats[i], cols[i], rows[i])
                                     : make_map(&h->tm_layer[l][i], mats[i], g.wt, cols[i], rows[i]);
       if (!ok) return false;
+      if ((g.wt == W_BF16 || g.wt == W_FP8) &&
+          !make_map(&h->tm_layer64[l][i], mats[i], g.wt, cols[i], rows[i], g.wt == W_BF16 ? 64 : 128, 64, true))
+        return false;
+      if (g.wt == W_FP4 && !make_fp4_maps64(&h->tm_layer64[l][i], &h->tm_scale64[l][i], mats[i], cols[i], rows[i]))
+        return false;
     }
   }
   if (g.wt == W_FP4 ? !make_fp4_map(&h->tm_lm, h->w.lm_head, g.d, g.V)
                     : !make_map(&h->tm_lm, h->w.lm_head, g.wt, g.d, g.V))
     return false;
+  if ((g.wt == W_BF16 || g.wt == W_FP8) &&
+      !make_map(&h->tm_lm64, h->w.lm_head, g.wt, g.d, g.V, g.wt == W_BF16 ? 64 : 128, 64, true))
+    return false;
+  if (g.wt == W_FP4 && !make_fp4_maps64(&h->tm_lm64, &h->tm_lm_s64, h->w.lm_head, g.d, g.V)) return false;
   const size_t pairs[3][2] = {{L.xn_hi, L.xn_lo}, {L.attn_hi, L.attn_lo}, {L.act_hi, L.act_lo}};
   const int kdim[3] = {g.d, g.qd, g.F};
   CUtensorMap* dst[3] = {h->tm_xn, h->tm_attn, h->tm_act};
@@ -573,6 +627,16 @@ bool build_maps(dflash_handle* h) {
     if (rows >= (1ull << 31) ||
         !make_map(&h->tm_ring, h->ring, W_BF16, g.hd, rows, 64, 64, true))
       return false;
+  }
+  if (g.wt == W_FP4) {
+    // the 4-D pair maps; a driver that refuses them leaves the 2-D path (x4 off)
+    h->x4 = true;
+    for (int i = 0; i < 3; ++i)
+      h->x4 = h->x4 && make_pair_map4(&h->tm_x4[i], h->scratch + pairs[i][0], h->scratch + pairs[i][1],
+                                      kdim[i], g.M_max);
+    if (g.max_inject > 0)
+      h->x4 = h->x4 && make_pair_map4(&h->tm_x4[3], h->scratch + L.inj_hi, h->scratch + L.inj_lo, g.d,
+                                      g.max_inject);
   }
   if (g.wt == W_FP4 && g.max_inject > 0 &&
       (!make_map(&h->tm_inj[0], h->scratch + L.inj_hi, W_BF16, g.d, g.max_inject) ||
@@ -673,6 +737,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
     e = launch_fill_i32(h->ring_pos(0), cfg->max_seq * cfg->window, -1, nullptr);
   if (e == cudaSuccess) e = configure_gemm(kXkMax);
   if (e == cudaSuccess) e = configure_gemm_tma();
+  if (e == cudaSuccess) e = configure_gemm_fp4();
   if (e == cudaSuccess) e = configure_gemm_umma();
   if (e == cudaSuccess && !build_maps(h)) e = cudaErrorNotSupported;
   if (e == cudaSuccess)
@@ -778,6 +843,15 @@ int run_inject(dflash_handle* h, int seq, const float* H_t, const int32_t* pos, 
       q.has_lo = 1;
       q.tm_w[0] = h->tm_layer[l][1];
       q.tm_w[1] = h->tm_layer[l][2];
+      q.tm_w64[0] = h->tm_layer64[l][1];
+      q.tm_w64[1] = h->tm_layer64[l][2];
+      q.tm_s64[0] = h->tm_scale64[l][1];
+      q.tm_s64[1] = h->tm_scale64[l][2];
+      q.w64 = 1;
+      if (h->x4) {
+        q.tm_x4 = h->tm_x4[3];
+        q.x4 = 1;
+      }
       q.seg[0] = {lw.wk, lw.wk_scale, 0, g.kvd};
       q.seg[1] = {lw.wv, lw.wv_scale, g.kvd, g.kvd};
       q.k_norm_l[0] = lw.k_norm;
@@ -785,7 +859,7 @@ int run_inject(dflash_handle* h, int seq, const float* H_t, const int32_t* pos, 
       q.epi = EPI_INJECT; q.ring_seq = h->ring_seq(seq) + (size_t)l * layer_bytes; q.pos = pos;
       q.rope_cs = rope;
       q.rows_per_seq = rows_per_seq; q.row_count = count; q.ring_seq_stride = h->L.ring_seq_bytes;
-      DF_CHECK(h, launch_gemm_tma(g.wt, q, st));
+      DF_CHECK(h, launch_gemm_fp4(q, st));
     }
     prof_end(h, st);
     return DFLASH_OK;

@@ -33,21 +33,13 @@ template <>
 struct TT<W_FP8> {   // 128 k per chunk: one 128-byte E4M3 box, two activation boxes
   static constexpr int CK = 128, WBOX_K = 128, WBOXES = 1, XBOXES = 2, S = 4, STEPS = 8;
 };
-template <>
-struct TT<W_FP4> {   // 256 k per chunk: one 128-byte E2M1 box + a 16-byte block-scale box
-  static constexpr int CK = 256, WBOX_K = 128, WBOXES = 1, XBOXES = 4, S = 3, STEPS = 16;
-};
 
 constexpr int kBox = 16 * 128;  // one 16-row x 128-byte box
 constexpr long long kWaitCycles = 4000000000LL;
 
-constexpr int kScaleBox = 16 * 16;  // FP4: 16 rows x 16 block scales (one 256-k chunk)
-
 template <int WT>
 struct Layout {
-  // weight boxes of the 8 row groups, then (FP4) their block-scale boxes
-  static constexpr int SC_OFF = 8 * kBox * TT<WT>::WBOXES;
-  static constexpr int W_BYTES = SC_OFF + (WT == W_FP4 ? 8 * kScaleBox : 0);
+  static constexpr int W_BYTES = 8 * kBox * TT<WT>::WBOXES;   // the 8 row groups' weight boxes
   static constexpr int X_BYTES = kBox * TT<WT>::XBOXES;  // one of hi / lo
   static constexpr int STAGE = W_BYTES + 2 * X_BYTES;
   static constexpr int ACC = TT<WT>::S * STAGE;
@@ -62,7 +54,6 @@ size_t gemm_tma_smem_bytes(int wt) {
     case W_F32: return Layout<W_F32>::TOTAL;
     case W_BF16: return Layout<W_BF16>::TOTAL;
     case W_FP8: return Layout<W_FP8>::TOTAL;
-    case W_FP4: return Layout<W_FP4>::TOTAL;
   }
   return 0;
 }
@@ -118,15 +109,6 @@ DF_DEVICE void tma_load_hint(void* dst, const CUtensorMap* map, int x, int y, ui
       "l"(map), "r"(x), "r"(y), "r"(su32(bar)), "l"(policy)
       : "memory");
 }
-// Contiguous global -> shared copy by the bulk-copy engine (16-byte aligned
-// addresses, size a multiple of 16) with an L2 eviction-priority hint.
-DF_DEVICE void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(su32(dst)),
-      "l"(src), "r"(bytes), "r"(su32(bar)), "l"(policy)
-      : "memory");
-}
 DF_DEVICE uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -157,8 +139,8 @@ DF_DEVICE void x_frags(uint32_t (&b)[4], const uint8_t* box, int kchunk0, int la
 
 template <>
 struct Consume<W_BF16> {
-  static DF_DEVICE void run(const uint8_t* w, const uint8_t*, const uint8_t* xh, const uint8_t* xl,
-                            bool has_lo, int lane, float (&acc)[2][4]) {
+  static DF_DEVICE void run(const uint8_t* w, const uint8_t* xh, const uint8_t* xl, bool has_lo,
+                            int lane, float (&acc)[2][4]) {
     const int lmat = lane >> 3, lrow = lane & 7;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
@@ -179,8 +161,8 @@ struct Consume<W_BF16> {
 
 template <>
 struct Consume<W_FP8> {
-  static DF_DEVICE void run(const uint8_t* w, const uint8_t*, const uint8_t* xh, const uint8_t* xl,
-                            bool has_lo, int lane, float (&acc)[2][4]) {
+  static DF_DEVICE void run(const uint8_t* w, const uint8_t* xh, const uint8_t* xl, bool has_lo,
+                            int lane, float (&acc)[2][4]) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
@@ -204,101 +186,10 @@ struct Consume<W_FP8> {
   }
 };
 
-// FP4 weights: the warps split the chunk's k as well as its rows.  Warp w owns
-// rows 64 (w & 1) .. + 63 of the tile (four m16 tiles) and the k16 steps
-// 4 (w >> 1) .. + 3 of the 256-k chunk, so each activation fragment it loads
-// feeds four weight tiles (the 16-row kernels of the other formats give every
-// warp all of k: there the activation fragments are re-read by all eight warps,
-// which FP4's quarter-size weight stream cannot afford in shared-memory
-// bandwidth).  Codes are widened with the hardware E2M1 -> fp16 conversion and
-// multiplied by their E4M3 block scale in fp16 (code x scale has at most six
-// significant bits and lies in [2^-10, 2688]: exact), so the products run as
-// fp16 MMAs against the fp16 activation pair; the row scale is applied in the
-// epilogue.  Code layout in a row's 16-byte group (32 weights, two k16 steps):
-// byte 4t + j holds the codes of k = 2 (t + 4j) and + 1, so lane t of a quad
-// reads its four bytes of both steps as one word.
-// The eight E2M1 codes of a word as four fp16x2 (byte j -> element j; low
-// nibble -> low half): exact.
-DF_DEVICE void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
-      : "r"(w));
-}
-DF_DEVICE __half2 e4m3x2_to_half2(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xffffu), __NV_E4M3);
-  return *reinterpret_cast<const __half2*>(&h);
-}
-DF_DEVICE uint32_t hmul2_u32(uint32_t a, __half2 s) {
-  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), s);
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-DF_DEVICE uint32_t lds_u32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
-DF_DEVICE uint32_t lds_u16(uint32_t a) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
-DF_DEVICE void ldsm_x4_a(uint32_t (&r)[4], uint32_t a) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(a));
-}
-
-struct ConsumeFp4 {
-  // Shared-space addresses of the stage: w, its eight 16-row code boxes; ws,
-  // their block scales (per group 256 bytes: [k16 step][rows 0, 8, 1, 9, ...]);
-  // xh / xl, the four 64-k boxes of the fp16 activation pair.
-  static DF_DEVICE void run(uint32_t w, uint32_t ws, uint32_t xh, uint32_t xl, int rh, int kq, int lane,
-                            float (&acc)[4][2][4]) {
-    const int g = lane >> 2, t = lane & 3;
-    const int lmat = lane >> 3, brow = (lmat >> 1) * 8 + (lane & 7), bhalf = lmat & 1;
-    const uint32_t wrow0 = w + (4 * rh) * kBox, srow0 = ws + (4 * rh) * kScaleBox + 2 * g;
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * kq + cc;  // 16-byte code group: k16 steps 2c and 2c + 1
-      // activation fragments of both steps
-      uint32_t bh[2][4], bl[2][4];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const uint32_t boff = kq * kBox + swz(brow, 2 * (2 * cc + hf) + bhalf);
-        ldsm_x4_a(bh[hf], xh + boff);
-        ldsm_x4_a(bl[hf], xl + boff);
-      }
-      const uint32_t off0 = swz(g, c) + 4 * t, off1 = swz(g + 8, c) + 4 * t;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        // rows g and g + 8 of tile i: one code word each (bytes: k 2t and 2t + 8
-        // of step 2c, then of step 2c + 1) and the pair of block scales per step
-        uint32_t q0[4], q1[4];
-        e2m1x8_to_f16x2x4(lds_u32(wrow0 + i * kBox + off0), q0);
-        e2m1x8_to_f16x2x4(lds_u32(wrow0 + i * kBox + off1), q1);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const __half2 sc = e4m3x2_to_half2(lds_u16(srow0 + i * kScaleBox + (2 * c + hf) * 16));
-          const __half2 sa = __low2half2(sc), sb = __high2half2(sc);
-          const uint32_t a[4] = {hmul2_u32(q0[2 * hf], sa), hmul2_u32(q1[2 * hf], sb),
-                                 hmul2_u32(q0[2 * hf + 1], sa), hmul2_u32(q1[2 * hf + 1], sb)};
-          mma_f16_16816(acc[i][0], a, bh[hf][0], bh[hf][1]);
-          mma_f16_16816(acc[i][1], a, bh[hf][2], bh[hf][3]);
-          mma_f16_16816(acc[i][0], a, bl[hf][0], bl[hf][1]);
-          mma_f16_16816(acc[i][1], a, bl[hf][2], bl[hf][3]);
-        }
-      }
-    }
-  }
-};
-
 template <>
 struct Consume<W_F32> {
-  static DF_DEVICE void run(const uint8_t* w, const uint8_t*, const uint8_t* xh, const uint8_t* xl,
-                            bool has_lo, int lane, float (&acc)[2][4]) {
+  static DF_DEVICE void run(const uint8_t* w, const uint8_t* xh, const uint8_t* xl, bool has_lo,
+                            int lane, float (&acc)[2][4]) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
@@ -363,80 +254,6 @@ DF_DEVICE void prefetch_share(const GemmParams& p, int b, int G) {
   }
 }
 
-// Consumer warps of the FP4 kernel: the stream-K walk of gemm_tma_kernel with
-// the k-split warps of ConsumeFp4; at the end of a segment the four k quarters
-// of each row are summed into acc_s in quarter order (deterministic).
-template <typename Lt, typename T>
-DF_DEVICE void consume_fp4(const GemmParams& p, uint8_t* sm, float* acc_s, float* inv_rms, float* scale_s,
-                           uint64_t* full, uint64_t* empty, long long ub0, long long ub1, long long U,
-                           int G, int b, int* s_flag, volatile int* s_abort) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rh = warp & 1, kq = warp >> 1;
-  long long it = 0;
-  for (long long u = ub0; u < ub1;) {
-    const int item = (int)(u / p.cpt);
-    const int c0 = (int)(u - (long long)item * p.cpt);
-    const int c1 = (int)min((long long)p.cpt, c0 + (ub1 - u));
-    u += c1 - c0;
-    const int tile = item / p.n_mb, mb = item - tile * p.n_mb;
-    csync();  // the previous segment is done with acc_s / scale_s / inv_rms
-    if (tid < kTileRows) {
-      const float* sc = nullptr;
-      const uint8_t* r = map_row(p, tile, tid, 1, &sc);
-      scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
-    }
-    if (p.row_scale) compute_inv_rms(p, inv_rms, mb * 16);
-    float acc[4][2][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 2; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
-    for (int c = c0; c < c1; ++c, ++it) {
-      const int st = (int)(it % T::S);
-      if (!*s_abort) {
-        if (mbar_wait(&full[st], (uint32_t)((it / T::S) & 1))) {
-          const uint32_t base = su32(sm) + st * Lt::STAGE;
-          ConsumeFp4::run(base, base + Lt::SC_OFF, base + Lt::W_BYTES, base + Lt::W_BYTES + Lt::X_BYTES,
-                          rh, kq, lane, acc);
-        } else {
-          if (lane == 0) atomicOr(p.status, 0x4u);
-          *s_abort = 1;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (kq == q) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int cc = 8 * j + 2 * t, r = 64 * rh + 16 * i + g;
-            float* d0 = acc_s + cc * kTileRows + r;
-            float* d1 = acc_s + (cc + 1) * kTileRows + r;
-            if (q == 0) {
-              d0[0] = acc[i][j][0];
-              d1[0] = acc[i][j][1];
-              d0[8] = acc[i][j][2];
-              d1[8] = acc[i][j][3];
-            } else {
-              d0[0] += acc[i][j][0];
-              d1[0] += acc[i][j][1];
-              d0[8] += acc[i][j][2];
-              d1[8] += acc[i][j][3];
-            }
-          }
-      }
-      csync();
-    }
-    if (!segment_fixup(p, acc_s, item, c0, c1, U, G, b, s_flag)) continue;
-    run_epilogue(p, acc_s, scale_s, inv_rms, mb, tile, s_flag);
-  }
-}
-
 template <int WT>
 __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __grid_constant__ GemmParams p) {
   using T = TT<WT>;
@@ -495,23 +312,30 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
         uint8_t* dst = sm + st * Lt::STAGE;
         const int k = c * T::CK;
         mbar_expect_tx(&full[st], stage_bytes);
+        if (T::WBOXES == 1 && p.w64) {
+          // four 16-row groups of one segment with consecutive rows are one
+          // 64-row box (the same swizzled layout as four stacked 16-row
+          // boxes): fewer, larger copies
 #pragma unroll
-        for (int grp = 0; grp < 8; ++grp)
+          for (int hq = 0; hq < 2; ++hq) {
+            const int g0 = 4 * hq;
+            if (gmap[g0 + 3] == gmap[g0] && grow[g0 + 3] == grow[g0] + 48) {
+              tma_load_hint(dst + g0 * kBox, &p.tm_w64[gmap[g0]], k, grow[g0],
+                            &full[st], w_policy);
+            } else {
 #pragma unroll
-          for (int wb = 0; wb < T::WBOXES; ++wb)
-            tma_load_hint(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]],
-                          (WT == W_FP4 ? k / 2 : k) + wb * T::WBOX_K, grow[grp], &full[st], w_policy);
-        if (WT == W_FP4) {
-          // block scales: 16 rows x 256 k of a row group are 256 contiguous bytes
-          // (groups past the matrix copy group 0: their codes are zero-filled)
-#pragma unroll
-          for (int grp = 0; grp < 8; ++grp) {
-            const GemmSeg& sg = p.seg[gmap[grp]];
-            const int G = grow[grp] < sg.rows ? grow[grp] / 16 : 0;
-            const char* src = static_cast<const char*>(sg.w) + (size_t)sg.rows * (p.K / 2) +
-                              ((size_t)G * (p.K / 16) + k / 16) * 16;
-            bulk_load_hint(dst + Lt::SC_OFF + grp * kScaleBox, src, kScaleBox, &full[st], w_policy);
+              for (int grp = g0; grp < g0 + 4; ++grp)
+                tma_load_hint(dst + grp * kBox, &p.tm_w[gmap[grp]], k, grow[grp],
+                              &full[st], w_policy);
+            }
           }
+        } else {
+#pragma unroll
+          for (int grp = 0; grp < 8; ++grp)
+#pragma unroll
+            for (int wb = 0; wb < T::WBOXES; ++wb)
+              tma_load_hint(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]],
+                            k + wb * T::WBOX_K, grow[grp], &full[st], w_policy);
         }
         if (!waited) {  // activations may come from the previous kernel
           pdl_wait();
@@ -539,9 +363,7 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
 
   // -------------------------------------------------------------- consumers
   pdl_wait();
-  if constexpr (WT == W_FP4) {
-    consume_fp4<Lt, T>(p, sm, acc_s, inv_rms, scale_s, full, empty, ub0, ub1, U, G, b, &s_flag, &s_abort);
-  } else {
+  {
     long long it = 0;
     for (long long u = ub0; u < ub1;) {
       const int item = (int)(u / p.cpt);
@@ -562,8 +384,8 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
         if (!s_abort) {
           if (mbar_wait(&full[st], (uint32_t)((it / T::S) & 1))) {
             const uint8_t* base = sm + st * Lt::STAGE;
-            Consume<WT>::run(base + warp * T::WBOXES * kBox, base + Lt::SC_OFF + warp * kScaleBox,
-                             base + Lt::W_BYTES, base + Lt::W_BYTES + Lt::X_BYTES, has_lo, lane, acc);
+            Consume<WT>::run(base + warp * T::WBOXES * kBox, base + Lt::W_BYTES,
+                             base + Lt::W_BYTES + Lt::X_BYTES, has_lo, lane, acc);
           } else {
             if (lane == 0) atomicOr(p.status, 0x4u);
             s_abort = 1;
@@ -597,9 +419,6 @@ cudaError_t configure_gemm_tma() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(gemm_tma_kernel<W_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)gemm_tma_smem_bytes(W_FP8));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tma_kernel<W_FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)gemm_tma_smem_bytes(W_FP4));
   return e;
 }
 
@@ -623,12 +442,11 @@ cudaError_t launch_gemm_tma(int wt, const GemmParams& p, cudaStream_t st) {
     case W_F32: return launch_tma_t<W_F32>(p, st);
     case W_BF16: return launch_tma_t<W_BF16>(p, st);
     case W_FP8: return launch_tma_t<W_FP8>(p, st);
-    case W_FP4:  // its consumers always read the lo half of the activation pair
-      return p.has_lo ? launch_tma_t<W_FP4>(p, st) : cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;
 }
 
+// (FP4 weights: the 256-k units of the FP4 kernel)
 int tma_chunk_k(int wt) { return wt == W_FP4 ? 256 : wt == W_FP8 ? 128 : 64; }
 
 }  // namespace dflash

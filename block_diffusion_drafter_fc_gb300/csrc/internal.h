@@ -47,8 +47,17 @@ struct GemmSeg {
 struct GemmParams {
   // TMA path: tensor maps of the weight segments and of the activation pair
   CUtensorMap tm_w[4];
+  // the same weights in 64-row boxes (one copy for four 16-row groups; bf16 and
+  // E4M3 16-row kernel), used when w64 is set
+  CUtensorMap tm_w64[4];
+  CUtensorMap tm_s64[4];    // FP4: the block scales of 64 rows x 256 k per box
+  int w64;
   CUtensorMap tm_xh;
   CUtensorMap tm_xl;
+  // FP4 kernel: the activation pair as one 4-D tensor [K/64][hi, lo][rows][64]
+  // (boxes of 64 k x 16 rows x hi+lo x 4: a stage's 256 k in one copy); x4 set
+  CUtensorMap tm_x4;
+  int x4;
   int has_lo;
   // activations: x[m][k], m < M, row stride ldx (elements)
   const void* x;
@@ -160,6 +169,12 @@ size_t gemm_tma_smem_bytes(int wt);
 cudaError_t configure_gemm_tma();
 cudaError_t launch_gemm_tma(int wt, const GemmParams& p, cudaStream_t st);
 int tma_chunk_k(int wt);   // k per pipeline stage of the TMA projection kernel
+
+// FP4 projection on tcgen05 with the decoded weights in tensor memory (16-row
+// activation blocks; the schedule fields as for the 16-row kernels, K % 256 == 0)
+size_t gemm_fp4_smem_bytes();
+cudaError_t configure_gemm_fp4();
+cudaError_t launch_gemm_fp4(const GemmParams& p, cudaStream_t st);
 
 // tcgen05 projection for >= 128 activation rows (bf16 or E4M3 weights)
 size_t gemm_umma_smem_bytes();
