@@ -53,7 +53,7 @@ extern "C" {
 typedef enum {
   DFLASH_OK = 0,
   DFLASH_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad enum value */
-  DFLASH_ERR_UNSUPPORTED = -2,   /* geometry or dtype mix this build does not run */
+  DFLASH_ERR_UNSUPPORTED = -2,   /* geometry or dtype mix the library does not run */
   DFLASH_ERR_TOO_MANY_ROWS = -3, /* T > window, or T > max_inject */
   DFLASH_ERR_SEQ_RANGE = -4,     /* sequence index or n_seq outside [0, max_seq) */
   DFLASH_ERR_CUDA = -5,          /* a CUDA runtime call failed; see dflash_last_error */

@@ -7,7 +7,7 @@ codes with per-row f32 scales, E2M1 codes with E4M3 block and f32 row scales)
 and computes the step directly from its
 definition in float64, with no tiling, no online softmax and no fusion.
 
-Sources (the pages that define the method):
+Sources (the documents that define the method):
   * dflash-ops model card, sections "Method", "Usage" and "Requirements and
     limits": KV injection through wk/wv with no attn_norm in front, per-head
     RMSNorm + NEOX rope on K, V stored raw, ring slot = pos mod window, the
@@ -25,7 +25,7 @@ Sources (the pages that define the method):
     DFlashDraftBlock (pre-norm attention and SwiGLU MLP with residuals) and
     DFlashSpeculativeVerifier.verify_block (accepted = matching prefix length).
 
-Readings taken where the pages are silent (each is listed in the design notes):
+Readings taken where the sources are silent (each is listed in the design notes):
   * row 0 of the block sits at position n_past, row i at n_past + i;
   * a ring slot is a key for row i iff it holds a position p with 0 <= p < n_past
     and (n_past + i) - p < window; every block key is visible to every row;
@@ -33,7 +33,7 @@ Readings taken where the pages are silent (each is listed in the design notes):
   * per-head RMSNorm comes before rope, on the block's q and k and on injected k;
   * block K/V are not written to the ring;
   * argmax ties resolve to the lowest index; the greedy decision is taken on the
-    logits rounded to fp32, the precision the pages fix for the arithmetic;
+    logits rounded to fp32, the precision the model card fixes for the arithmetic;
   * ring values are the fp64 results rounded once (nearest-even) to the ring dtype.
 
 Every function here is pinned by the CPU tests against closed forms,

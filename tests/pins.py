@@ -1,4 +1,4 @@
-"""Pins of the fp64 oracle: checks against what the pages and the mathematics fix.
+"""Pins of the fp64 oracle: checks against what the sources and the mathematics fix.
 
 Each pin is a plain function that raises AssertionError when the oracle
 disagrees.  `test_oracle_pins.py` runs them; `test_oracle_mutants.py` plants

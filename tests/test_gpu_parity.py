@@ -153,11 +153,13 @@ def test_empty_ring_step():
     d.close()
 
 
-def test_graph_replay_bitwise_with_eager_traffic():
+@pytest.mark.parametrize("name", ["small_fp8", "small_fp4", "dense_bf16"])
+def test_graph_replay_bitwise_with_eager_traffic(name):
     """The captured step (+accept) replays bitwise equal to the eager step, before
     and after eager GEMMs run on the same stream between replays (dflash-ops
-    model card, Method: interleaved eager traffic between replays)."""
-    wl = make_workload(get_config("small_fp8"))
+    model card, Method: interleaved eager traffic between replays): the 16-row,
+    FP4 and tcgen05 projection paths."""
+    wl = make_workload(get_config(name))
     ref = OB.oracle_full(wl)
     g = GH.gpu_run(wl, targets=ref["targets"], keep=True)
     dr = g["drafter"]

@@ -17,7 +17,7 @@ from oracle import dflash_oracle as O
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "ragged_bf16", "small_fp8"])
+@pytest.mark.parametrize("name", ["tiny_f32", "ragged_bf16", "small_fp8", "small_fp4"])
 def test_block_width_matches_oracle(name):
     from block_diffusion_drafter_fc_gb300 import dflash as D
     cfg = get_config(name)
