@@ -50,12 +50,13 @@ constexpr int kCodes = 8 * kBox;            // the tile's code boxes
 constexpr int kScales = 8 * kScaleBox;
 constexpr int kX = 4 * kBox;                // 256 k of one half of the activation pair
 constexpr int kAB = 2;                      // A buffers (128 TMEM columns each)
+constexpr int kDB = 2;                      // accumulator buffers per MMA warp (32 columns each)
 constexpr int kStage = kCodes + kScales + 2 * kX;
 constexpr int kOffAcc = kS * kStage;        // 16 x 128 fp32 fix-up tile
 constexpr int kOffInv = kOffAcc + 16 * kTileRows * 4;
 constexpr int kOffScale = kOffInv + 16 * 4;
-constexpr int kOffBars = kOffScale + kTileRows * 4;   // full, empty [S]; afull, aempty [AB]; accf, acce [2]
-constexpr int kOffTmem = kOffBars + (2 * kS + 2 * kAB + 4) * 8;
+constexpr int kOffBars = kOffScale + kTileRows * 4;   // full, empty [S]; afull, aempty [AB]; accf, acce [DB]
+constexpr int kOffTmem = kOffBars + (2 * kS + 2 * kAB + 2 * kDB) * 8;
 constexpr int kSmem = kOffTmem + 16 + 1024;            // + alignment slack
 constexpr int kDecoders = 16;               // decoder warps (the first 8 also run the epilogue)
 constexpr int kIssuers = 4;                 // MMA warps: issuer i takes k16 steps 4i .. 4i + 3
@@ -63,7 +64,7 @@ constexpr int kThreads = 32 * (kDecoders + 1 + kIssuers);
 constexpr int kProducer = kDecoders, kIssuer = kDecoders + 1;
 constexpr int kTmemCols = 512;              // A: 2 x 128 columns; D: issuers x 2 x 32 columns
 constexpr int kDCol = 128 * kAB;
-static_assert(kDCol + kIssuers * 64 <= kTmemCols, "tensor memory columns");
+static_assert(kDCol + kIssuers * kDB * 32 <= kTmemCols, "tensor memory columns");
 constexpr long long kWait = 4000000000LL;
 static_assert(kStage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled boxes");
 static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "one CTA per SM (it owns the SM's TMEM)");
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
   uint64_t* afull = empty + kS;   // A buffer a decoded
   uint64_t* aempty = afull + kAB; // A buffer a read by its MMAs
   uint64_t* accf = aempty + kAB;  // accumulator d holds a finished segment
-  uint64_t* acce = accf + 2;      // accumulator d has been read out
+  uint64_t* acce = accf + kDB;    // accumulator d has been read out
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
   __shared__ int s_flag;
   __shared__ volatile int s_abort;
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
       bar_init(&afull[a], kDecoders);
       bar_init(&aempty[a], kIssuers);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kDB; ++b) {
       bar_init(&accf[b], kIssuers);
       bar_init(&acce[b], 8);
     }
@@ -352,14 +353,14 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
         const int c0 = (int)(u - (long long)item * p.cpt);
         const int c1 = (int)min((long long)p.cpt, c0 + (ub1 - u));
         u += c1 - c0;
-        const int db = seg & 1;
-        if (!bar_wait(&acce[db], (uint32_t)((seg >> 1) & 1) ^ 1)) {
+        const int db = seg % kDB;
+        if (!bar_wait(&acce[db], (uint32_t)((seg / kDB) & 1) ^ 1)) {
           atomicOr(p.status, 0x4u);
           s_abort = 1;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t d = tmem + kDCol + iss * 64 + db * 32;
+        const uint32_t d = tmem + kDCol + (iss * kDB + db) * 32;
         bool ok = true;
         for (int c = c0; c < c1; ++c, ++it) {
           const int st = (int)(it % kS), ab = (int)(it % kAB);
@@ -447,8 +448,8 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
       // the segment's accumulators -> acc_s[m][row] = sum over the issuers of
       // D[row][m] + D[row][16 + m] (the hi and lo products): warp (q, h) takes
       // m = 8h .. 8h + 7
-      const int db = seg & 1;
-      if (!s_abort && !bar_wait(&accf[db], (uint32_t)((seg >> 1) & 1))) {
+      const int db = seg % kDB;
+      if (!s_abort && !bar_wait(&accf[db], (uint32_t)((seg / kDB) & 1))) {
         if (lane == 0) atomicOr(p.status, 0x4u);
         s_abort = 1;
       }
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
             asm volatile(
                 "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
-                : "r"(tmem + lane_base + kDCol + i * 64 + db * 32 + 16 * hl + 8 * h));
+                : "r"(tmem + lane_base + kDCol + (i * kDB + db) * 32 + 16 * hl + 8 * h));
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
             for (int e = 0; e < 8; ++e) sum[e] += __uint_as_float(v[e]);
