@@ -14,12 +14,14 @@
 // Stream-K over 128-row x 256-k units as in the 16-row kernels (one CTA per
 // SM, each a contiguous run of units; shared tiles summed by the last
 // contributor in CTA order), warp-specialised:
-//   warp 16 (one lane) TMA producer: per unit the tile's eight 16-row code boxes
-//                      (16 rows x 128 bytes), their block scales (256
-//                      contiguous bytes per 16 rows) and the activation pair
-//                      (per 64 k a 16-row hi box followed by its lo box: one
-//                      32-row operand) into a 5-stage ring, across tile
-//                      boundaries;
+//   warp 16 (one lane) TMA producer: per unit the tile's codes (a 64-row box of
+//                      128 bytes per row for every four 16-row groups of one
+//                      segment, else 16-row boxes), their block scales (a
+//                      2-D box of 4 groups x 256 bytes, else 256 contiguous
+//                      bytes per group) and the activation pair (per 64 k a
+//                      16-row hi box followed by its lo box: one 32-row
+//                      operand; one 4-D copy, else 8 boxes) into a 5-stage
+//                      ring, across tile boundaries;
 //   warps 0..15        decoders: warp w owns TMEM lanes 32 (w % 4) .. + 31 (the
 //                      tile's rows) and a quarter of the unit's k; a lane widens
 //                      its row's 64 codes with cvt.rn.f16x2.e2m1x2, multiplies
