@@ -153,6 +153,20 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def replica_timing(ms_local, steps, world, device=None):
+    """Max over the ranks of the timed region (ms) and the whole-job throughput of
+    `world` independent replicas (steps/s: every rank's steps over the slowest
+    rank's time).  Needs an initialised process group when world > 1."""
+    ms = float(ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * steps / (ms / 1e3)
+
+
 def run_ours(args, rank, world, local):
     import numpy as np
     import torch
@@ -210,13 +224,8 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, value = replica_timing(e0.elapsed_time(e1), args.steps, world, dev)
     ms_step = ms / args.steps
-    value = world * args.steps / (ms / 1e3)
 
     # live per-class device times of eager steps (events on the launching stream)
     dr.dflash_profile_enable(True)

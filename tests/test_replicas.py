@@ -1,0 +1,53 @@
+"""The multi-process path of bench.py (replicas only: no collective in the data
+path), on CPU with gloo: the timing reduction over ranks and the reference arm's
+rank filter."""
+import os
+import pathlib
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = pathlib.Path(__file__).resolve().parents[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    sys.path.insert(0, str(ROOT))
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        dist.barrier()
+        # rank r timed 10 (r + 1) ms for 100 steps: the job's time is the slowest rank's
+        ms, value = bench.replica_timing(10.0 * (rank + 1), 100, world, "cpu")
+        out[rank] = (ms, value)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_replica_timing_takes_the_slowest_rank(world):
+    port = 29500 + 17 * world + os.getpid() % 1000
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
+        res = dict(out)
+    assert sorted(res) == list(range(world))
+    for ms, value in res.values():
+        assert ms == 10.0 * world
+        assert abs(value - world * 100 / (10.0 * world / 1e3)) < 1e-9
+
+
+def test_single_replica_needs_no_process_group():
+    sys.path.insert(0, str(ROOT))
+    import bench
+    assert bench.replica_timing(5.0, 50, 1) == (5.0, 50 / 0.005)
+
+
+def test_reference_arm_other_ranks_exit_silently():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference", "--gpus", "2"],
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
