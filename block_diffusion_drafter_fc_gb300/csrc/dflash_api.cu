@@ -433,6 +433,13 @@ cudaError_t launch_projection(const dflash_handle* h, GemmParams& p, int l,
   return launch_gemm_umma(h->g.wt, p, st);
 }
 
+// the embedding kernel's blocks per row (each writes one partial sum of squares)
+int embed_parts(const Geometry& g, const Layout& L) {
+  int parts = std::min(4, L.ss_parts);
+  while (parts > 1 && g.d % (8 * parts) != 0) --parts;
+  return parts;
+}
+
 int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t* n_past,
              float* logits, int32_t* drafts, cudaStream_t st) {
   clear_stale_error();
@@ -450,8 +457,8 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   PROF(h, PC_EMBED, st, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id,
                                      id_last, n_past, n_seq, h->S<double>(L.inv_freq), g.hd, hbuf, ss,
                                      rope, h->w.layers[0].attn_norm, xn_hi, xn_lo, g.wt == W_FP4,
-                                     h->status(), st));
-  int n_ss = 1;
+                                     embed_parts(g, L), L.ss_ld, h->status(), st));
+  int n_ss = embed_parts(g, L);
   for (int l = 0; l < g.L; ++l) {
     const dflash_layer_weights& lw = h->w.layers[l];
     // q/k/v of RMSNorm(h) (the 1/rms row scale after the product), per-head

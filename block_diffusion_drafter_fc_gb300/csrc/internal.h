@@ -194,7 +194,7 @@ cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
                          const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
                          const void* norm0, uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
-                         unsigned* status, cudaStream_t st);
+                         int parts, int ss_ld, unsigned* status, cudaStream_t st);
 cudaError_t launch_rope_table(const int32_t* pos, int T, const double* inv_freq, int hd,
                               float2* rope_cs, int32_t* ring_pos, int window, int rows_per_seq,
                               const int32_t* count, unsigned* status, cudaStream_t st);

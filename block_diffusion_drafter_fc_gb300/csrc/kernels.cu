@@ -12,36 +12,39 @@ namespace dflash {
 
 // Block rows: token id_last for row 0, mask_token for rows 1..15 (dflash-ops model
 // card, Method; dflash_head.rs field mask_token_id).  Writes h (fp32) and the
-// row's sum of squares for the first layer's RMSNorm.  Extra blocks fill the
-// rope table of the block positions n_past + i from the host fp64
-// inverse-frequency table (angle and sin/cos in fp64, then rounded to fp32).
+// row's sums of squares for the first layer's RMSNorm: block b covers part
+// b % parts of row b / parts and writes ss[part][row].  Extra blocks (64 entries
+// each: fp64 is slow, so it is spread over many SMs) fill the rope table of the
+// block positions n_past + i from the host fp64 inverse-frequency table (angle
+// and sin/cos in fp64, then rounded to fp32).
 __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int dense_bf16, int d,
                                                     int V, int mask_token, const int32_t* id_last,
                                                     const int32_t* n_past, int n_seq,
                                                     const double* inv_freq, int half, float* h,
                                                     float* ss, float2* rope_cs, const void* norm0,
                                                     uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
-                                                    unsigned* status) {
+                                                    int parts, int ss_ld, unsigned* status) {
   const int M = n_seq * kBlock;
-  if ((int)blockIdx.x < M) {
-    const int m = blockIdx.x, seq = m / kBlock, i = m % kBlock;
+  if ((int)blockIdx.x < M * parts) {
+    const int m = blockIdx.x / parts, part = blockIdx.x - m * parts, seq = m / kBlock, i = m % kBlock;
+    const int span = d / parts, kbeg = part * span, kend = kbeg + span;
     int tok = i == 0 ? id_last[seq] : mask_token;
     if (tok < 0 || tok >= V) {
-      if (threadIdx.x == 0) atomicOr(status, 0x1u);
+      if (threadIdx.x == 0 && part == 0) atomicOr(status, 0x1u);
       tok = tok < 0 ? 0 : V - 1;
     }
     // 8 elements per thread and round (one 16-byte bf16 load or two float4
     // loads), all loads of a round issued before any store
     float s = 0.f;
     constexpr int kRound = 4;
-    for (int k0 = threadIdx.x * 8; k0 < d; k0 += kRound * (int)blockDim.x * 8) {
+    for (int k0 = kbeg + threadIdx.x * 8; k0 < kend; k0 += kRound * (int)blockDim.x * 8) {
       float v[kRound][8];
 #pragma unroll
       for (int r = 0; r < kRound; ++r) {
         const int k = k0 + r * blockDim.x * 8;
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[r][e] = 0.f;
-        if (k >= d) continue;
+        if (k >= kend) continue;
         if (dense_bf16) {
           const uint4 b = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(tok_embd) +
                                                          (size_t)tok * d + k);
@@ -62,7 +65,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
 #pragma unroll
       for (int r = 0; r < kRound; ++r) {
         const int k = k0 + r * blockDim.x * 8;
-        if (k >= d) continue;
+        if (k >= kend) continue;
         float4* dst = reinterpret_cast<float4*>(h + (size_t)m * d + k);
         dst[0] = make_float4(v[r][0], v[r][1], v[r][2], v[r][3]);
         dst[1] = make_float4(v[r][4], v[r][5], v[r][6], v[r][7]);
@@ -87,11 +90,12 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
     if (threadIdx.x == 0) {
       float t = 0.f;
       for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-      ss[m] = t;
+      ss[(size_t)part * ss_ld + m] = t;
     }
     return;
   }
-  const int e = (blockIdx.x - M) * blockDim.x + threadIdx.x;
+  if (threadIdx.x >= 64) return;
+  const int e = (blockIdx.x - M * parts) * 64 + threadIdx.x;
   if (e >= M * half) return;
   const int m = e / half, j = e - m * half, seq = m / kBlock;
   int p0 = n_past[seq];
@@ -108,12 +112,13 @@ cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
                          const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
                          const void* norm0, uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
-                         unsigned* status, cudaStream_t st) {
+                         int parts, int ss_ld, unsigned* status, cudaStream_t st) {
   const int M = n_seq * kBlock, half = hd / 2;
-  const int tb = (M * half + 255) / 256;
-  embed_kernel<<<M + tb, 256, 0, st>>>(tok_embd, dense_bf16, n_embd, n_vocab, mask_token, id_last,
-                                       n_past, n_seq, inv_freq, half, h, ss, rope_cs, norm0, x_hi,
-                                       x_lo, pair_f16, status);
+  const int tb = (M * half + 63) / 64;
+  if (parts < 1 || n_embd % (8 * parts) != 0) return cudaErrorInvalidValue;
+  embed_kernel<<<M * parts + tb, 256, 0, st>>>(tok_embd, dense_bf16, n_embd, n_vocab, mask_token,
+                                               id_last, n_past, n_seq, inv_freq, half, h, ss, rope_cs,
+                                               norm0, x_hi, x_lo, pair_f16, parts, ss_ld, status);
   return cudaGetLastError();
 }
 
