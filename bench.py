@@ -185,8 +185,10 @@ def run_ours(args, rank, world, local):
     max_inject = max(c[2] for c in wl.inject_calls)
     dr = D.Drafter(cfg, dw, max_seq=cfg.n_seq, max_inject=max_inject, device=dev)
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    p0.record()
-    dr.prefill(wl, feats)                     # encode + inject of the whole context (untimed)
+    dr.prefill(wl, feats)                     # encode + inject of the whole context (untimed);
+    torch.cuda.synchronize()                  # the second pass (same positions, same ring) is
+    p0.record()                               # timed without first-launch costs
+    dr.prefill(wl, feats)
     p1.record()
     torch.cuda.synchronize()
     prefill_ms = p0.elapsed_time(p1)
