@@ -22,15 +22,16 @@
 //                      16-row hi box followed by its lo box: one 32-row
 //                      operand; one 4-D copy, else 8 boxes) into a 5-stage
 //                      ring, across tile boundaries;
-//   warps 0..15        decoders: warp w owns TMEM lanes 32 (w % 4) .. + 31 (the
-//                      tile's rows) and a quarter of the unit's k; a lane widens
-//                      its row's 64 codes with cvt.rn.f16x2.e2m1x2, multiplies
+//   warps 8..15        decoders: warp w owns TMEM lanes 32 (w % 4) .. + 31 (the
+//                      tile's rows) and half of the unit's k; a lane widens its
+//                      row's 128 codes with cvt.rn.f16x2.e2m1x2, multiplies
 //                      them by their block scale in fp16 (exact: at most six
-//                      significant bits, within [2^-10, 2688]) and stores the 32
+//                      significant bits, within [2^-10, 2688]) and stores the 64
 //                      fp16 pairs with tcgen05.st into one of two A buffers;
-//                      at the end of a segment warps 0..7 read the accumulator
+//   warps 0..7         at the end of each segment read the accumulator
 //                      (tcgen05.ld) into the 16 x 128 tile of the shared fix-up
-//                      and run the fused epilogue;
+//                      and run the fused epilogue, while the decoders and MMA
+//                      warps go on with the next segment;
 //   warps 17..20       (one lane each) per unit 4 k-step MMAs each into its own
 //                      accumulator of the segment (one of two per warp; the
 //                      epilogue adds the eight halves: a single issuing thread
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
       bar_init(&empty[s], kIssuers);
     }
     for (int a = 0; a < kAB; ++a) {
-      bar_init(&afull[a], kDecoders);
+      bar_init(&afull[a], kDecoders / 2);   // the decoding warps 8..15
       bar_init(&aempty[a], kIssuers);
     }
     for (int b = 0; b < kDB; ++b) {
@@ -394,9 +395,12 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
   } else {
     // ---------------------------------------------------------------- decoders + epilogue
     pdl_wait();   // the epilogues read the previous kernels' outputs
-    const int q = warp & 3, kq = warp >> 2;
+    // warps 8..15 decode (lane quarter q, k half kh of each unit); warps 0..7 run
+    // the segment epilogues meanwhile (the next segment's units keep decoding)
+    const int q = warp & 3;
     const bool epi = warp < 8;
     const int h = warp >> 2;    // epilogue warps: column half of the accumulator
+    const int kh = (warp >> 2) & 1;
     const int r = 32 * q + lane, grp = r >> 4, rr = r & 15;
     const int pos = 2 * (rr & 7) + (rr >> 3);   // the row's byte in a block of 16 scales
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
       const int c1 = (int)min((long long)p.cpt, c0 + (ub1 - u));
       u += c1 - c0;
       const int tile = item / p.n_mb, mb = item - tile * p.n_mb;
-      for (int c = c0; c < c1; ++c, ++it) {
+      for (int c = c0; c < c1 && !epi; ++c, ++it) {
         const int st = (int)(it % kS), ab = (int)(it % kAB);
         if (!s_abort && (!bar_wait(&full[st], (uint32_t)((it / kS) & 1)) ||
                          !bar_wait(&aempty[ab], (uint32_t)((it / kAB) & 1) ^ 1))) {
@@ -418,29 +422,33 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint8_t* cbox = sm + st * kStage + grp * kBox;
         const uint8_t* sbox = sm + st * kStage + kCodes + grp * kScaleBox + pos;
-        // this lane's row, k16 steps 4kq .. 4kq + 3: code groups 2kq, 2kq + 1
-        // (all loads first)
-        uint4 w4[2];
-        uint32_t sc[4];
 #pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2) w4[g2] = *reinterpret_cast<const uint4*>(cbox + swz(rr, 2 * kq + g2));
+        for (int hf = 0; hf < 2; ++hf) {
+          // this lane's row, k16 steps 4kq .. 4kq + 3: code groups 2kq, 2kq + 1
+          // (all loads first)
+          const int kq = 2 * kh + hf;
+          uint4 w4[2];
+          uint32_t sc[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[e] = sbox[(4 * kq + e) * 16];
-        uint32_t v[32];
+          for (int g2 = 0; g2 < 2; ++g2) w4[g2] = *reinterpret_cast<const uint4*>(cbox + swz(rr, 2 * kq + g2));
 #pragma unroll
-        for (int g2 = 0; g2 < 2; ++g2) {
-          const uint32_t s0 = e4m3_pair(sc[2 * g2]), s1 = e4m3_pair(sc[2 * g2 + 1]);
-          const uint32_t ws[4] = {w4[g2].x, w4[g2].y, w4[g2].z, w4[g2].w};
+          for (int e = 0; e < 4; ++e) sc[e] = sbox[(4 * kq + e) * 16];
+          uint32_t v[32];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            uint32_t o[4];
-            e2m1x8(ws[t], o);
-            // byte 4t + j holds the pair t + 4j of the group (k16 step 2cg + j / 2)
+          for (int g2 = 0; g2 < 2; ++g2) {
+            const uint32_t s0 = e4m3_pair(sc[2 * g2]), s1 = e4m3_pair(sc[2 * g2 + 1]);
+            const uint32_t ws[4] = {w4[g2].x, w4[g2].y, w4[g2].z, w4[g2].w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[16 * g2 + t + 4 * j] = hmul2u(o[j], j < 2 ? s0 : s1);
+            for (int t = 0; t < 4; ++t) {
+              uint32_t o[4];
+              e2m1x8(ws[t], o);
+              // byte 4t + j holds the pair t + 4j of the group (k16 step 2cg + j / 2)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[16 * g2 + t + 4 * j] = hmul2u(o[j], j < 2 ? s0 : s1);
+            }
           }
+          tmem_st32(tmem + lane_base + ab * 128 + 32 * kq, v);
         }
-        tmem_st32(tmem + lane_base + ab * 128 + 32 * kq, v);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
