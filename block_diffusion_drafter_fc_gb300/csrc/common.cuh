@@ -4,7 +4,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
-#include <cuda_fp4.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 

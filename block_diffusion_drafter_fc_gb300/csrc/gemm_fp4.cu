@@ -61,10 +61,11 @@ constexpr int kOffScale = kOffInv + 16 * 4;
 constexpr int kOffBars = kOffScale + kTileRows * 4;   // full, empty [S]; afull, aempty [AB]; accf, acce [DB]
 constexpr int kOffTmem = kOffBars + (2 * kS + 2 * kAB + 2 * kDB) * 8;
 constexpr int kSmem = kOffTmem + 16 + 1024;            // + alignment slack
-constexpr int kDecoders = 16;               // decoder warps (the first 8 also run the epilogue)
+constexpr int kEpilogue = 8;                // warps 0..7: segment read-out, fix-up and epilogue
+constexpr int kDecoders = 8;                // warps 8..15: decoding
 constexpr int kIssuers = 4;                 // MMA warps: issuer i takes k16 steps 4i .. 4i + 3
-constexpr int kThreads = 32 * (kDecoders + 1 + kIssuers);
-constexpr int kProducer = kDecoders, kIssuer = kDecoders + 1;
+constexpr int kThreads = 32 * (kEpilogue + kDecoders + 1 + kIssuers);
+constexpr int kProducer = kEpilogue + kDecoders, kIssuer = kProducer + 1;
 constexpr int kTmemCols = 512;              // A: 2 x 128 columns; D: issuers x 2 x 32 columns
 constexpr int kDCol = 128 * kAB;
 static_assert(kDCol + kIssuers * kDB * 32 <= kTmemCols, "tensor memory columns");
@@ -246,12 +247,12 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
       bar_init(&empty[s], kIssuers);
     }
     for (int a = 0; a < kAB; ++a) {
-      bar_init(&afull[a], kDecoders / 2);   // the decoding warps 8..15
+      bar_init(&afull[a], kDecoders);
       bar_init(&aempty[a], kIssuers);
     }
     for (int b = 0; b < kDB; ++b) {
       bar_init(&accf[b], kIssuers);
-      bar_init(&acce[b], 8);
+      bar_init(&acce[b], kEpilogue);
     }
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
     // warps 8..15 decode (lane quarter q, k half kh of each unit); warps 0..7 run
     // the segment epilogues meanwhile (the next segment's units keep decoding)
     const int q = warp & 3;
-    const bool epi = warp < 8;
+    const bool epi = warp < kEpilogue;
     const int h = warp >> 2;    // epilogue warps: column half of the accumulator
     const int kh = (warp >> 2) & 1;
     const int r = 32 * q + lane, grp = r >> 4, rr = r & 15;
