@@ -17,7 +17,7 @@ import oracle_bridge as OB
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
-FULL = ["small_bf16", "real_bf16", "real_f32", "batched_fp8"]
+FULL = ["small_bf16", "real_bf16", "real_f32", "batched_fp8", "real_fp4"]
 
 
 def _replay(g, wl, targets):
