@@ -183,9 +183,15 @@ SMALL_FP4 = DraftConfig(
     name="small_fp4", n_layer=2, n_embd=512, n_head=8, n_head_kv=2, head_dim=64,
     n_ff=1536, window=128, n_vocab=3000, weight_dtype="fp4", dense_dtype="bf16",
     ring_dtype="bf16", n_seq=3, fill_lo=32, fill_hi=128, offset_hi=65535, seed=2009)
+# FP4 with head_dim 32 and one kv head: the k and v segments (32 rows each) do
+# not fill 64-row boxes, the vocabulary leaves a ragged last tile
+RAGGED_FP4 = DraftConfig(
+    name="ragged_fp4", n_layer=1, n_embd=256, n_head=8, n_head_kv=1, head_dim=32,
+    n_ff=512, window=64, n_vocab=333, weight_dtype="fp4", dense_dtype="bf16",
+    ring_dtype="bf16", n_seq=2, fill_lo=20, fill_hi=64, offset_hi=500, seed=2010)
 TEST_CONFIGS: Dict[str, DraftConfig] = {c.name: c for c in (RAGGED, SMALL_FP8, MIXED_F32, DENSE_FP8,
                                                             DENSE_BF16, WIDE_FP8, WIDE_BF16, MANY_SEQ,
-                                                            SMALL_FP4)}
+                                                            SMALL_FP4, RAGGED_FP4)}
 
 
 def get_config(name: str) -> DraftConfig:
