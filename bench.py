@@ -153,6 +153,18 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+def workload_config(cfg, wl, world):
+    """The `config` object of both arms' JSON line."""
+    return {"workload": f"{cfg.name}: {cfg.n_layer} layers, n_embd {cfg.n_embd}, heads "
+                        f"{cfg.n_head}/{cfg.n_head_kv} x {cfg.head_dim}, n_ff {cfg.n_ff}, window "
+                        f"{cfg.window} (ring full), block 16, vocab {cfg.n_vocab}, "
+                        f"{cfg.weight_dtype} weights, {cfg.ring_dtype} ring, fp32 arithmetic",
+            "sequences": cfg.n_seq, "rows_per_step": 16 * cfg.n_seq,
+            "l2": f"inputs larger than L2: {wl.weight_bytes() / 1e9:.2f} GB of weights per step",
+            "timing": "CUDA-graph replays (step + accept), CUDA events on the replay stream",
+            "parallelism": f"replicas x{world}"}
+
+
 def replica_timing(ms_local, steps, world, device=None):
     """Max over the ranks of the timed region (ms) and the whole-job throughput of
     `world` independent replicas (steps/s: every rank's steps over the slowest
@@ -283,14 +295,7 @@ def run_ours(args, rank, world, local):
         "us_per_step": round(ms_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded random weights ~N(0,1/fan_in), features ~N(0,1))",
-        "config": {"workload": f"{cfg.name}: {cfg.n_layer} layers, n_embd {cfg.n_embd}, heads "
-                               f"{cfg.n_head}/{cfg.n_head_kv} x {cfg.head_dim}, n_ff {cfg.n_ff}, window "
-                               f"{cfg.window} (ring full), block 16, vocab {cfg.n_vocab}, "
-                               f"{cfg.weight_dtype} weights, {cfg.ring_dtype} ring, fp32 arithmetic",
-                   "sequences": cfg.n_seq, "rows_per_step": 16 * cfg.n_seq,
-                   "l2": f"inputs larger than L2: {wl.weight_bytes() / 1e9:.2f} GB of weights per step",
-                   "timing": "CUDA-graph replays (step + accept), CUDA events on the replay stream",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(cfg, wl, world),
         "prefill_ms": round(prefill_ms, 3),
         "step_bytes": sbytes,
         "hbm_gbs": round(sbytes / (ms_step / 1e3) / 1e9, 1),
@@ -344,26 +349,40 @@ def run_reference(args):
     w = OB.oracle_weights(wl)
     names = [f"l{i}.{n}" for i in range(cfg.n_layer) for n in ("wq", "wk", "wv", "wo", "gate", "up", "down")]
     names.append("lm_head")
-    total = sum(int(np.prod(w.raw[n].shape)) for n in names)
+    dims = {n: tuple(wl.weights[n].shape) for n in names}    # [N, K] of every matrix
+    total = sum(dims[n][0] * dims[n][1] for n in names)
     rng = np.random.default_rng(0)
-    x = {k: rng.standard_normal((16 * cfg.n_seq, k)) for k in {w.raw[n].shape[1] for n in names}}
+    x = {k: rng.standard_normal((16 * cfg.n_seq, k)) for k in {dims[n][1] for n in names}}
+
+    def rows_of(n, r0, rows):
+        """The stored bytes of rows r0 .. r0 + rows of matrix n (FP4: its codes and
+        the block scales of those 16-row groups, as one buffer; r0, rows % 16 == 0)."""
+        raw = w.raw[n]
+        if w.dtype_of(n) != "fp4":
+            return raw[r0:r0 + rows]
+        N, K = dims[n]
+        flat = raw.reshape(-1)
+        codes = flat[r0 * K // 2:(r0 + rows) * K // 2]
+        scales = flat[N * K // 2 + (r0 // 16) * K:N * K // 2 + ((r0 + rows) // 16) * K]
+        return np.concatenate([codes, scales])
 
     def sample(i, rows):
         n = names[i % len(names)]
-        raw = w.raw[n]
-        r0 = (i * rows) % max(1, raw.shape[0] - rows)
+        N, K = dims[n]
+        r0 = ((i * rows) % max(1, N - rows)) // 16 * 16
+        rr = min(rows, N - r0) // 16 * 16 or min(rows, N - r0)
         sc = w.scales.get(n)
-        W = O.decode(raw[r0:r0 + rows], w.dtype_of(n), None if sc is None else sc[r0:r0 + rows])
-        O.linear(x[raw.shape[1]], W)
-        return rows * raw.shape[1]
+        W = O.decode(rows_of(n, r0, rr), w.dtype_of(n), None if sc is None else sc[r0:r0 + rr])
+        O.linear(x[K], W)
+        return rr * K
 
     # size a sample so warmup + steps end within ~3 minutes
     t0 = time.perf_counter()
     el = sample(0, 256)
     rate = el / max(time.perf_counter() - t0, 1e-6)
     per_step_s = 180.0 / max(1, args.steps + args.warmup)
-    avg_k = total / sum(w.raw[n].shape[0] for n in names)
-    rows = int(max(16, min(4096, rate * per_step_s / avg_k)))
+    avg_k = total / sum(dims[n][0] for n in names)
+    rows = int(max(16, min(4096, rate * per_step_s / avg_k))) // 16 * 16
     for i in range(args.warmup):
         sample(i, rows)
     done = 0
@@ -376,7 +395,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 / value, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "sequences": cfg.n_seq},
+            "config": workload_config(cfg, wl, args.gpus),
             "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": os.cpu_count(),
                              "kind": "oracle",
                              "sample": f"{rows} weight rows of one projection per step (decode + "
