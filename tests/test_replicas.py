@@ -51,3 +51,13 @@ def test_reference_arm_other_ranks_exit_silently():
     r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference", "--gpus", "2"],
                        env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_both_arms_share_the_config_object():
+    sys.path.insert(0, str(ROOT))
+    import bench
+    from block_diffusion_drafter_fc_gb300.synth import get_config, make_workload
+    cfg = get_config("tiny_f32")
+    c = bench.workload_config(cfg, make_workload(cfg), 1)
+    assert c["workload"].startswith("tiny_f32: 1 layers") and c["parallelism"] == "replicas x1"
+    assert set(c) == {"workload", "sequences", "rows_per_step", "l2", "timing", "parallelism"}
