@@ -140,7 +140,9 @@ def _cfg_list() -> List[DraftConfig]:
     # of the dflash-ops model card, Measured: a ~4.6-bit drafter; here 4.5 bits a
     # weight + one f32 per row)
     real_fp4 = real_bf16.with_(name="real_fp4", weight_dtype="fp4", seed=1005)
-    return [tiny, small, real_bf16, real_f32, batched_fp8, real_fp4]
+    # ... and with E4M3 projection weights (one sequence: the 16-row E4M3 path)
+    real_fp8 = real_bf16.with_(name="real_fp8", weight_dtype="fp8", seed=1006)
+    return [tiny, small, real_bf16, real_f32, batched_fp8, real_fp4, real_fp8]
 
 
 CONFIGS: List[DraftConfig] = _cfg_list()
