@@ -30,7 +30,7 @@ def _worker(rank, world, port, out):
 @pytest.mark.parametrize("world", [2, 3])
 def test_replica_timing_takes_the_slowest_rank(world):
     port = 29500 + 17 * world + os.getpid() % 1000
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
         res = dict(out)
