@@ -61,3 +61,25 @@ def test_both_arms_share_the_config_object():
     c = bench.workload_config(cfg, make_workload(cfg), 1)
     assert c["workload"].startswith("tiny_f32: 1 layers") and c["parallelism"] == "replicas x1"
     assert set(c) == {"workload", "sequences", "rows_per_step", "l2", "timing", "parallelism"}
+
+
+@pytest.mark.parametrize("config", ["tiny_f32", "small_fp4"])
+def test_reference_arm_prints_the_contract_line(config):
+    import json
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference", "--config", config,
+                        "--steps", "2", "--warmup", "1"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in out, key
+    assert out["impl"] == "reference" and out["steps"] == 2 and out["warmup"] == 1
+    assert out["value"] > 0 and abs(out["ms_per_step"] - 1e3 / out["value"]) < 1e-3 * out["ms_per_step"] + 1e-3
+    assert out["config"]["workload"].startswith(config + ":")
+    cb = out["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == out["value"] and cb["cores"] >= 1
+    assert out["e2e"] == {"value": out["value"], "unit": out["unit"], "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
