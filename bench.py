@@ -101,24 +101,29 @@ def class_bytes(cfg, wl):
     }
 
 
-def gemm_source_hash():
-    """Hash of the sources of the projection kernels (TMA-fed and tcgen05): a
-    committed ncu traffic figure is used only while it matches."""
+ALL_GEMM_SOURCES = ("gemm_tma.cu", "gemm_umma.cu", "gemm_fp4.cu", "gemm_common.cuh", "common.cuh",
+                    "internal.h")
+
+
+def gemm_source_hash(files=ALL_GEMM_SOURCES):
+    """Hash of the sources a projection kernel is compiled from: a committed ncu
+    traffic figure is used only while it matches."""
     h = hashlib.sha256()
-    for f in ("gemm_tma.cu", "gemm_umma.cu", "gemm_fp4.cu", "gemm_common.cuh", "common.cuh", "internal.h"):
+    for f in files:
         h.update((ROOT / "block_diffusion_drafter_fc_gb300" / "csrc" / f).read_bytes())
     return h.hexdigest()[:16]
 
 
 def committed_traffic(cfg_name, cls):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; else None."""
+    the current source of that kernel (the entry's "sources", else every
+    projection source); else None."""
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
         return None
     d = json.loads(p.read_text())
     e = d.get(f"{cfg_name}/{cls}")
-    if not e or e.get("source_sha") != gemm_source_hash():
+    if not e or e.get("source_sha") != gemm_source_hash(tuple(e.get("sources", ALL_GEMM_SOURCES))):
         return None
     return e.get("dram_bytes_per_launch")
 

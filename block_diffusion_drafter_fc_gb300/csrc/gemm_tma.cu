@@ -23,15 +23,15 @@ template <int WT>
 struct TT;
 template <>
 struct TT<W_BF16> {  // 64 k per chunk: one 128-byte weight box, one activation box
-  static constexpr int CK = 64, WBOX_K = 64, WBOXES = 1, XBOXES = 1, S = 4, STEPS = 4;
+  static constexpr int CK = 64, WBOX_K = 64, WBOXES = 1, XBOXES = 1, S = 4, STEPS = 4, PEN = 4;
 };
 template <>
 struct TT<W_F32> {   // 64 k per chunk: two 128-byte weight boxes of 32 fp32
-  static constexpr int CK = 64, WBOX_K = 32, WBOXES = 2, XBOXES = 1, S = 2, STEPS = 4;
+  static constexpr int CK = 64, WBOX_K = 32, WBOXES = 2, XBOXES = 1, S = 2, STEPS = 4, PEN = 2;
 };
 template <>
 struct TT<W_FP8> {   // 128 k per chunk: one 128-byte E4M3 box, two activation boxes
-  static constexpr int CK = 128, WBOX_K = 128, WBOXES = 1, XBOXES = 2, S = 4, STEPS = 8;
+  static constexpr int CK = 128, WBOX_K = 128, WBOXES = 1, XBOXES = 2, S = 4, STEPS = 8, PEN = 4;
 };
 
 constexpr int kBox = 16 * 128;  // one 16-row x 128-byte box
@@ -237,6 +237,86 @@ DF_DEVICE void group_coord(const GemmParams& p, int tile, int grp, int& map, int
   row = vr - p.seg[s].row0;
 }
 
+// Stream-K split over a weighted axis.  A CTA whose range crosses into a new
+// item stops its chunk stream for that item's partial publication (stores made
+// visible at GPU scope, then the ticket), which costs it about as long as
+// streaming PEN chunks.  So every item is PEN + cpt units long on the split
+// axis - PEN for the crossing, then its cpt chunks - and the G CTAs share that
+// axis equally: the CTAs that cross an item boundary get fewer chunks.
+// Chunk unit of split position v (a position inside an item's crossing part
+// maps to the item's first chunk).
+DF_DEVICE long long vsplit_unit(long long v, int cpt, int pen) {
+  const long long i = v / (cpt + pen), r = v - i * (cpt + pen);
+  return i * cpt + (r > pen ? r - pen : 0);
+}
+// The CTA whose range holds chunk unit u.
+DF_DEVICE int vsplit_owner(long long u, int cpt, int pen, long long V, int G) {
+  const long long i = u / cpt, v = i * (cpt + pen) + pen + (u - i * cpt);
+  return (int)(((v + 1) * G - 1) / V);
+}
+
+// segment_fixup for the weighted split: after a segment [c0, c1) of `item` has
+// been accumulated into acc_s, publish it if the tile is shared and, for the
+// last contributor (acquire-release ticket), sum all partials in CTA order.
+// Returns true when this CTA must run the tile's epilogue.
+template <int PEN>
+DF_DEVICE bool vsplit_fixup(const GemmParams& p, float* acc_s, int item, int c0, int c1,
+                            long long V, int G, int b, int* s_flag) {
+  constexpr int kVec = 16 * kTileRows / 4;  // float4 per partial tile
+  constexpr int kPer = kVec / kGemmThreads;  // float4 per thread
+  constexpr int kBatch = 4;
+  const int tid = threadIdx.x;
+  if (c0 == 0 && c1 == p.cpt) return true;
+  const long long iu0 = (long long)item * p.cpt;
+  const int first = vsplit_owner(iu0, p.cpt, PEN, V, G);
+  const int last = vsplit_owner(iu0 + p.cpt - 1, p.cpt, PEN, V, G);
+  float4* acc4 = reinterpret_cast<float4*>(acc_s);
+  auto part_of = [&](int c) {
+    const size_t sl = 2 * (size_t)c + (c == first ? 1 : 0);
+    return reinterpret_cast<float4*>(p.partial + sl * (16 * kTileRows));
+  };
+  float4* mine = part_of(b);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) __stcg(mine + tid + k * kGemmThreads, acc4[tid + k * kGemmThreads]);
+  csync();
+  if (tid == 0) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "l"(p.counters + item)
+                 : "memory");
+    *s_flag = old == last - first;
+  }
+  csync();
+  if (!*s_flag) return false;
+  float4 sum[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) sum[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int cb = first; cb <= last; cb += kBatch) {
+    float4 v[kBatch][kPer];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+      for (int k = 0; k < kPer; ++k)
+        if (cb + j <= last) v[j][k] = __ldcg(part_of(cb + j) + tid + k * kGemmThreads);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+      for (int k = 0; k < kPer; ++k)
+        if (cb + j <= last) {
+          sum[k].x += v[j][k].x;
+          sum[k].y += v[j][k].y;
+          sum[k].z += v[j][k].z;
+          sum[k].w += v[j][k].w;
+        }
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc4[tid + k * kGemmThreads] = sum[k];
+  if (tid == 0) p.counters[item] = 0;
+  csync();
+  return true;
+}
+
 // This CTA's 1/G share of the prefetch ranges (16-byte aligned pieces of at
 // most 32 KB): the next kernel's input moves into L2 while this kernel's last
 // weight stages are still streaming.
@@ -281,8 +361,9 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
   pdl_trigger();
 
   const int G = gridDim.x, b = blockIdx.x;
-  const long long U = (long long)p.n_tiles * p.n_mb * p.cpt;
-  const long long ub0 = U * b / G, ub1 = U * (b + 1) / G;
+  const long long V = (long long)p.n_tiles * p.n_mb * (p.cpt + T::PEN);
+  const long long ub0 = vsplit_unit(V * b / G, p.cpt, T::PEN),
+                  ub1 = vsplit_unit(V * (b + 1) / G, p.cpt, T::PEN);
   const bool has_lo = p.has_lo != 0;
   const uint32_t stage_bytes = Lt::W_BYTES + Lt::X_BYTES * (has_lo ? 2 : 1);
 
@@ -404,7 +485,7 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
         acc_s[(cc + 1) * kTileRows + r + 8] = acc[j][3];
       }
       csync();
-      if (!segment_fixup(p, acc_s, item, c0, c1, U, G, b, &s_flag)) continue;
+      if (!vsplit_fixup<T::PEN>(p, acc_s, item, c0, c1, V, G, b, &s_flag)) continue;
       run_epilogue(p, acc_s, scale_s, inv_rms, mb, tile, &s_flag);
     }
   }
