@@ -196,6 +196,76 @@ def _fp4_scale_rows_plain(raw, dtype, scale=None):
     return _orig["decode"](r, dtype, scale)
 
 
+def _linear_square_transposed(x, w):
+    """y = x W for square weights (the operand orientation lost), x W^T otherwise."""
+    return x @ (w if w.shape[0] == w.shape[1] else w.T)
+
+
+class _SwappedWeights:
+    """The model's weights with one norm weight read in place of another."""
+
+    def __init__(self, w, read_as):
+        self._w, self._read_as = w, read_as
+
+    def __getattr__(self, name):
+        return getattr(self._w, name)
+
+    def get(self, name):
+        for suffix, other in self._read_as.items():
+            if name.endswith(suffix):
+                return self._w.get(name[: -len(suffix)] + other)
+        return self._w.get(name)
+
+
+def _step_hidden_reading(read_as):
+    def sh(w, rings, tokens, n_past, causal=False):
+        return _orig["step_hidden"](_SwappedWeights(w, read_as), rings, tokens, n_past, causal)
+    return sh
+
+
+def _inject_slot_plus_one(w, ring, H_t, positions):
+    cfg = w.cfg
+    positions = np.asarray(positions, dtype=np.int64)
+    inv_freq = O.inv_freq_table(cfg.rope_theta, cfg.head_dim)
+    for layer in range(cfg.n_layer):
+        k, v = O.inject_kv(w, layer, H_t, positions, inv_freq)
+        ks, vs = O.store(k, cfg.ring_dtype), O.store(v, cfg.ring_dtype)
+        for t, p in enumerate(positions):
+            slot = (int(p) + 1) % cfg.window
+            ring.k[layer, :, slot, :] = ks[t]
+            ring.v[layer, :, slot, :] = vs[t]
+    for p in positions:
+        ring.pos[(int(p) + 1) % cfg.window] = int(p)
+
+
+def _step_hidden_no_attn_residual(w, rings, tokens, n_past, causal=False):
+    """The oracle's layer loop with h = attn wo^T instead of h + attn wo^T."""
+    cfg = w.cfg
+    n_seq, B = tokens.shape
+    inv_freq = O.inv_freq_table(cfg.rope_theta, cfg.head_dim)
+    hd, hq, hkv = cfg.head_dim, cfg.n_head, cfg.n_head_kv
+    h = w.rows("tok_embd", tokens.reshape(-1)).reshape(n_seq, B, cfg.n_embd)
+    pos = np.asarray(n_past, dtype=np.int64)[:, None] + np.arange(B)[None, :]
+    for layer in range(cfg.n_layer):
+        L = f"l{layer}."
+        x = O.rmsnorm(h, w.get(L + "attn_norm"), cfg.eps)
+        q = O.linear(x, w.get(L + "wq")).reshape(n_seq, B, hq, hd)
+        k = O.linear(x, w.get(L + "wk")).reshape(n_seq, B, hkv, hd)
+        v = O.linear(x, w.get(L + "wv")).reshape(n_seq, B, hkv, hd)
+        q = O.rope_neox(O.rmsnorm(q, w.get(L + "q_norm"), cfg.eps), pos, inv_freq)
+        k = O.rope_neox(O.rmsnorm(k, w.get(L + "k_norm"), cfg.eps), pos, inv_freq)
+        att = np.zeros((n_seq, B, hq, hd))
+        for s in range(n_seq):
+            kr, vr = rings[s].values(layer)
+            valid = O.ring_mask(rings[s].pos, int(n_past[s]), cfg.window, B)
+            att[s] = O.attention(q[s], k[s], v[s], kr, vr, valid)
+        h = O.linear(att.reshape(n_seq, B, hq * hd), w.get(L + "wo"))
+        x2 = O.rmsnorm(h, w.get(L + "ffn_norm"), cfg.eps)
+        mlp = O.silu(O.linear(x2, w.get(L + "gate"))) * O.linear(x2, w.get(L + "up"))
+        h = h + O.linear(mlp, w.get(L + "down"))
+    return h
+
+
 MUTANTS = {
     "rmsnorm drops eps": ("rmsnorm", _rms_no_eps),
     "rmsnorm sums instead of mean": ("rmsnorm", _rms_sum),
@@ -230,6 +300,12 @@ MUTANTS = {
     "advance bonus from the next row": ("advance", _advance_variant(lambda m: m + 1, 1, 0)),
     "advance n_past grows by n_ok": ("advance", _advance_variant(lambda m: m + 1, 0, -1)),
     "advance drops the anchor row": ("advance", _advance_variant(lambda m: m, 0, 0)),
+    "square weights transposed": ("linear", _linear_square_transposed),
+    "q normed with the k norm weight": ("step_hidden", _step_hidden_reading({"q_norm": "k_norm"})),
+    "ffn norm reads the attention norm": ("step_hidden", _step_hidden_reading({"ffn_norm": "attn_norm"})),
+    "gate and up swapped": ("step_hidden", _step_hidden_reading({"gate": "up", "up": "gate"})),
+    "ring slot off by one": ("inject", _inject_slot_plus_one),
+    "attention residual dropped": ("step_hidden", _step_hidden_no_attn_residual),
 }
 
 
