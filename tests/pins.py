@@ -299,6 +299,29 @@ def pin_accept_example():
     assert t[0, n_ok] == ex["expect_bonus"]
 
 
+def pin_greedy_drafts_ties_and_rows():
+    """Drafts come from block rows 1..15 only, ties go to the lowest index, and
+    the decision is taken on fp32 logits: values that differ in float64 but
+    round to the same float32 are a tie (dflash-ops model card, Method: greedy
+    drafts at rows 1..15, fp32 arithmetic)."""
+    V = 12
+    logits = np.zeros((2, 16, V))
+    logits[:, 0, 9] = 100.0                       # row 0 is never drafted
+    for j in range(1, 16):
+        a, b = (j * 5) % V, (j * 5 + 3) % V
+        lo, hi = min(a, b), max(a, b)
+        logits[0, j, hi] = 2.0 + j                # exact tie: the lower index wins
+        logits[0, j, lo] = 2.0 + j
+        logits[1, j, hi] = 1.0 + 2.0 ** -40       # larger in float64, equal in float32
+        logits[1, j, lo] = 1.0
+    d = O.greedy_drafts(logits)
+    assert d.shape == (2, 15) and d.dtype == np.int32
+    for j in range(1, 16):
+        a, b = (j * 5) % V, (j * 5 + 3) % V
+        assert d[0, j - 1] == min(a, b), (j, d[0, j - 1])
+        assert d[1, j - 1] == min(a, b), (j, d[1, j - 1])
+
+
 def pin_accept_bruteforce():
     g = np.random.default_rng(23)
     for _ in range(200):

@@ -266,6 +266,16 @@ def _step_hidden_no_attn_residual(w, rings, tokens, n_past, causal=False):
     return h
 
 
+def _drafts_ties_highest(logits):
+    l32 = np.asarray(logits).astype(np.float32)[..., 1:, :]
+    V = l32.shape[-1]
+    return (V - 1 - np.argmax(l32[..., ::-1], axis=-1)).astype(np.int32)
+
+
+def _drafts_in_f64(logits):
+    return np.argmax(np.asarray(logits, dtype=np.float64)[..., 1:, :], axis=-1).astype(np.int32)
+
+
 MUTANTS = {
     "rmsnorm drops eps": ("rmsnorm", _rms_no_eps),
     "rmsnorm sums instead of mean": ("rmsnorm", _rms_sum),
@@ -306,6 +316,8 @@ MUTANTS = {
     "gate and up swapped": ("step_hidden", _step_hidden_reading({"gate": "up", "up": "gate"})),
     "ring slot off by one": ("inject", _inject_slot_plus_one),
     "attention residual dropped": ("step_hidden", _step_hidden_no_attn_residual),
+    "argmax ties to the highest index": ("greedy_drafts", _drafts_ties_highest),
+    "drafts decided on float64 logits": ("greedy_drafts", _drafts_in_f64),
 }
 
 
