@@ -101,6 +101,21 @@ def class_bytes(cfg, wl):
     }
 
 
+def class_rates(cfg, wl, prof):
+    """Algorithmic GB/s of every kernel class from the live per-class event times:
+    bytes per launch (projection weights + scales, the LM head's logits; for
+    attention one layer's ring K/V of every sequence) / mean launch time."""
+    per_launch = dict(class_bytes(cfg, wl))
+    per_launch["attention"] = (step_bytes(cfg, wl) - wl.weight_bytes()
+                               - cfg.n_seq * 16 * cfg.n_vocab * 4) / cfg.n_layer
+    out = {}
+    for k, nbytes in per_launch.items():
+        ms, n = prof.get(k, (0.0, 0))
+        if n and ms > 0:
+            out[k] = round(nbytes / (ms / n / 1e3) / 1e9, 1)
+    return out
+
+
 ALL_GEMM_SOURCES = ("gemm_tma.cu", "gemm_umma.cu", "gemm_fp4.cu", "gemm_common.cuh", "common.cuh",
                     "internal.h")
 
@@ -323,6 +338,7 @@ def run_ours(args, rank, world, local):
         "roofline": roof,
         "kernel_classes_us_per_step": {k: round(v[0] / max(1, args.profile_steps) * 1e3, 2)
                                        for k, v in prof.items() if v[1]},
+        "kernel_classes_gbs": class_rates(cfg, wl, prof),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": {"value": round(1.0 / e2e_s * world, 3) if n_e2e else None, "unit": UNIT,

@@ -83,3 +83,23 @@ def test_reference_arm_prints_the_contract_line(config):
     assert cb["kind"] == "oracle" and cb["value"] == out["value"] and cb["cores"] >= 1
     assert out["e2e"] == {"value": out["value"], "unit": out["unit"], "h2d_bytes_per_step": 0,
                           "d2h_bytes_per_step": 0}
+
+
+@pytest.mark.parametrize("config", ["tiny_f32", "small_fp8"])
+def test_class_rates_cover_every_class(config):
+    sys.path.insert(0, str(ROOT))
+    import bench
+    from block_diffusion_drafter_fc_gb300.synth import get_config, make_workload
+    cfg = get_config(config)
+    wl = make_workload(cfg)
+    cb = bench.class_bytes(cfg, wl)
+    # every class took 10 us per launch over 3 launches; the embedding is not rated
+    prof = {k: (0.03, 3) for k in list(cb) + ["attention", "embed"]}
+    r = bench.class_rates(cfg, wl, prof)
+    assert set(r) == set(cb) | {"attention"}
+    for k, nbytes in cb.items():
+        assert abs(r[k] - round(nbytes / 1e-5 / 1e9, 1)) < 0.051
+    ring = bench.step_bytes(cfg, wl) - wl.weight_bytes() - cfg.n_seq * 16 * cfg.n_vocab * 4
+    assert ring > 0 and abs(r["attention"] - round(ring / cfg.n_layer / 1e-5 / 1e9, 1)) < 0.051
+    # classes that did not run are left out
+    assert bench.class_rates(cfg, wl, {k: (0.0, 0) for k in prof}) == {}
