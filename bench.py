@@ -116,6 +116,8 @@ def class_rates(cfg, wl, prof):
     return out
 
 
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal
+
 ALL_GEMM_SOURCES = ("gemm_tma.cu", "gemm_umma.cu", "gemm_fp4.cu", "gemm_common.cuh", "common.cuh",
                     "internal.h")
 
@@ -335,6 +337,7 @@ def run_ours(args, rank, world, local):
         "step_bytes": sbytes,
         "hbm_gbs": round(sbytes / (ms_step / 1e3) / 1e9, 1),
         "hbm_frac_of_measured": round(sbytes / (ms_step / 1e3) / 1e9 / peak, 4),
+        "hbm_frac_of_nominal": round(sbytes / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
         "roofline": roof,
         "kernel_classes_us_per_step": {k: round(v[0] / max(1, args.profile_steps) * 1e3, 2)
                                        for k, v in prof.items() if v[1]},
