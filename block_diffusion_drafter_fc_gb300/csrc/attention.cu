@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
     for (int b = 0; b < nb; ++b) mbar_init(&s_bar[b], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (tid == 0) stamp_begin(p.stamp);
   __syncthreads();
   pdl_trigger();
   pdl_wait();
@@ -673,6 +674,7 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
     }
   }
   cluster.sync();  // peers may still be reading this CTA's partials
+  if (tid == 0) stamp_finish(p.stamp);
 }
 
 int attn_cluster_size(int window) {

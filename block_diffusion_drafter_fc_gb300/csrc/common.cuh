@@ -138,6 +138,24 @@ DF_DEVICE void prefetch_l2(const void* p, uint32_t bytes) {
 DF_DEVICE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 DF_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------- launch timestamps
+
+// Per-launch timing inside a replayed graph (profiling captures only; a null
+// slot records nothing).  Slot s: s[0] = ~(earliest CTA start), s[1] = latest
+// CTA end, both %globaltimer nanoseconds, so one zero fill resets a slot and
+// both updates are atomicMax.  One thread per CTA calls each.
+DF_DEVICE unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+DF_DEVICE void stamp_begin(unsigned long long* s) {
+  if (s) atomicMax(s, ~global_ns());
+}
+DF_DEVICE void stamp_finish(unsigned long long* s) {
+  if (s) atomicMax(s + 1, global_ns());
+}
+
 // ---------------------------------------------------------------- tensor cores
 
 // D += A * B for one m16n8k16 bf16 tile with fp32 accumulation.

@@ -21,7 +21,9 @@ constexpr int kCtasPerSm = 2;        // projection CTAs resident per SM (registe
 // largest ring slice (all sequences of one layer) prefetched into L2 ahead of attention
 constexpr size_t kRingPrefetchMax = 32u << 20;
 constexpr int kGemmGrid = kPlanSMs * kCtasPerSm;
-constexpr int kXkMax = 960;          // activation stage width (3 CTAs of ~72 KB per SM)
+constexpr int kXkMax = kGemmXkMax;   // activation stage width of the register-fed kernel
+// launch timestamp slots of one profiled step (5 launches per layer + 3)
+constexpr int kStampSlots = 5 * DFLASH_MAX_LAYERS + 8;
 constexpr size_t kAlign = 256;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -102,7 +104,7 @@ struct Layout {
   size_t status, inv_freq, counters, h, ss, qbuf, kblk, vblk, rope_step, am_part;
   size_t xn_hi, xn_lo, attn_hi, attn_lo, act_hi, act_lo;
   size_t logits_int, drafts_int, idl_int, npast_int, partial;
-  size_t inj_raw, inj_ss, inj_rope, inj_hi, inj_lo, loop_pos, loop_cnt, loop_H, total;
+  size_t inj_raw, inj_ss, inj_rope, inj_hi, inj_lo, loop_pos, loop_cnt, loop_H, stamps, total;
   size_t partial_floats;
   int n_counters, ss_parts, ss_ld, lm_tiles;
   size_t ring_seq_bytes, ring_kv_bytes, ring_total;
@@ -164,6 +166,7 @@ Layout layout(const dflash_config& c) {
   L.loop_pos = take(sizeof(int32_t) * (size_t)g.max_seq * DFLASH_BLOCK);
   L.loop_cnt = take(sizeof(int32_t) * (size_t)g.max_seq);
   L.loop_H = take(sizeof(float) * (size_t)g.max_seq * DFLASH_BLOCK * g.d);
+  L.stamps = take(sizeof(unsigned long long) * 2 * kStampSlots);
   L.total = off;
 
   L.ring_kv_bytes = (size_t)g.L * 2 * g.Hkv * g.W * g.hd * (g.ring_bf16 ? 2 : 4);
@@ -242,13 +245,19 @@ struct dflash_handle {
   CUtensorMap td_kv[DFLASH_MAX_LAYERS][2];
   CUtensorMap td_inj[2];
   cudaStream_t cap_stream = nullptr;
-  // captured graphs, one per block width (a capture bakes its row count)
+  // captured graphs, one per block width (a capture bakes its row count): the
+  // step (+ accept) of dflash_capture and the loop turn of dflash_capture_loop
   cudaGraph_t graphs[DFLASH_BLOCK + 1] = {};
   cudaGraphExec_t execs[DFLASH_BLOCK + 1] = {};
+  cudaGraph_t loop_graphs[DFLASH_BLOCK + 1] = {};
+  cudaGraphExec_t loop_execs[DFLASH_BLOCK + 1] = {};
   int width = DFLASH_BLOCK;   // block rows of step / accept / advance / capture
   char err[512];
-  // launch-class profiling (eager calls only)
+  // launch-class profiling: events around eager calls (prof), or device
+  // timestamps of every step launch, eager or captured (stamps)
   bool prof = false;
+  bool stamps = false;
+  std::vector<int> stamp_cls;   // class of each timestamp slot of the last recorded step
   bool capturing = false;
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
@@ -359,6 +368,21 @@ void prof_end(dflash_handle* h, cudaStream_t st) {
   h->open_ev = nullptr;
 }
 
+// The next launch timestamp slot (class `cls`), or null when stamps are off.
+unsigned long long* stamp_slot(dflash_handle* h, int cls) {
+  if (!h->stamps || (int)h->stamp_cls.size() >= kStampSlots) return nullptr;
+  unsigned long long* s = h->S<unsigned long long>(h->L.stamps) + 2 * h->stamp_cls.size();
+  h->stamp_cls.push_back(cls);
+  return s;
+}
+
+// Start a new stamp record: every slot zeroed on the stream ahead of the step.
+cudaError_t stamp_reset(dflash_handle* h, cudaStream_t st) {
+  h->stamp_cls.clear();
+  if (!h->stamps) return cudaSuccess;
+  return cudaMemsetAsync(h->scratch + h->L.stamps, 0, sizeof(unsigned long long) * 2 * kStampSlots, st);
+}
+
 #define PROF(h, cls, st, call)     \
   do {                             \
     prof_begin(h, cls, st);        \
@@ -453,11 +477,13 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   float2* rope = h->S<float2>(L.rope_step);
   uint16_t* xn_hi = h->S<uint16_t>(L.xn_hi);
   uint16_t* xn_lo = h->S<uint16_t>(L.xn_lo);
+  DF_CHECK(h, stamp_reset(h, st));
   // h = embeddings; xn = split(h * attn_norm_0); ss = row sums of squares
   PROF(h, PC_EMBED, st, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id,
                                      id_last, n_past, n_seq, h->S<double>(L.inv_freq), g.hd, hbuf, ss,
                                      rope, h->w.layers[0].attn_norm, xn_hi, xn_lo, g.wt == W_FP4,
-                                     embed_parts(g, L), L.ss_ld, h->status(), st));
+                                     embed_parts(g, L), L.ss_ld, h->status(),
+                                     stamp_slot(h, PC_EMBED), st));
   int n_ss = embed_parts(g, L);
   for (int l = 0; l < g.L; ++l) {
     const dflash_layer_weights& lw = h->w.layers[l];
@@ -483,6 +509,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
         p.pf_count = n_seq;
       }
     }
+    p.stamp = stamp_slot(h, PC_QKV);
     PROF(h, PC_QKV, st, launch_projection(h, p, l, {0, 1, 2}, XP_XN, st));
     // attention over the ring window + the block (-> attn pair)
     AttnParams a;
@@ -497,6 +524,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.tm_ring = h->tm_ring;
     a.status = h->status();
     a.block_width = h->width;
+    a.stamp = stamp_slot(h, PC_ATTN);
     PROF(h, PC_ATTN, st, launch_attention_cluster(a, n_seq, st));
     // o projection + residual; next input xn = split(h * ffn_norm)
     p = base_params(h);
@@ -506,6 +534,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
     p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
     p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d; p.pair_norm = lw.ffn_norm;
+    p.stamp = stamp_slot(h, PC_O);
     PROF(h, PC_O, st, launch_projection(h, p, l, {3}, XP_ATTN, st));
     n_ss = sh[1].n_tiles;
     // gate/up of RMSNorm(h) + SwiGLU -> act pair
@@ -518,6 +547,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.nseg = 2; p.N = 2 * g.F; p.map = MAP_SWIGLU;
     p.epi = EPI_SWIGLU; p.out = nullptr;
     p.pair_hi = h->S<uint16_t>(L.act_hi); p.pair_lo = h->S<uint16_t>(L.act_lo); p.pair_ld = g.F;
+    p.stamp = stamp_slot(h, PC_GATEUP);
     PROF(h, PC_GATEUP, st, launch_projection(h, p, l, {4, 5}, XP_XN, st));
     // down projection + residual; next input xn = split(h * next norm)
     p = base_params(h);
@@ -528,6 +558,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
     p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d;
     p.pair_norm = l + 1 < g.L ? h->w.layers[l + 1].attn_norm : h->w.out_norm;
+    p.stamp = stamp_slot(h, PC_DOWN);
     PROF(h, PC_DOWN, st, launch_projection(h, p, l, {6}, XP_ACT, st));
     n_ss = sh[3].n_tiles;
   }
@@ -543,6 +574,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
   p.drafts = drafts;
   p.block_width = h->width;
+  p.stamp = stamp_slot(h, PC_LM);
   PROF(h, PC_LM, st, launch_projection(h, p, -1, {0}, XP_XN, st));
   return DFLASH_OK;
 }
@@ -770,6 +802,8 @@ void dflash_destroy(dflash_handle* h) {
   for (int w = 0; w <= DFLASH_BLOCK; ++w) {
     if (h->execs[w]) cudaGraphExecDestroy(h->execs[w]);
     if (h->graphs[w]) cudaGraphDestroy(h->graphs[w]);
+    if (h->loop_execs[w]) cudaGraphExecDestroy(h->loop_execs[w]);
+    if (h->loop_graphs[w]) cudaGraphDestroy(h->loop_graphs[w]);
   }
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   delete h;
@@ -993,7 +1027,7 @@ int dflash_accept(dflash_handle* h, int32_t n_seq, const int32_t* drafts, const 
   if (!drafts || !targets || !n_ok) return DFLASH_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   clear_stale_error();
-  PROF(h, PC_ACCEPT, st, launch_accept(drafts, targets, n_ok, n_seq, h->width, st));
+  PROF(h, PC_ACCEPT, st, launch_accept(drafts, targets, n_ok, n_seq, h->width, nullptr, st));
   return DFLASH_OK;
 }
 
@@ -1015,7 +1049,8 @@ int dflash_capture(dflash_handle* h, int32_t n_seq, const int32_t* id_last, cons
   h->capturing = true;
   int rc = run_step(h, n_seq, id_last, n_past, logits, drafts, h->cap_stream);
   if (rc == DFLASH_OK && targets) {
-    cudaError_t e = launch_accept(drafts, targets, n_ok, n_seq, h->width, h->cap_stream);
+    cudaError_t e = launch_accept(drafts, targets, n_ok, n_seq, h->width,
+                                  stamp_slot(h, PC_ACCEPT), h->cap_stream);
     if (e != cudaSuccess) rc = cuda_fail(h, e, "accept (capture)");
   }
   cudaGraph_t graph = nullptr;
@@ -1050,8 +1085,8 @@ int dflash_capture_loop(dflash_handle* h, int32_t n_seq, const int32_t* targets,
   DF_CHECK(h, cudaStreamSynchronize(st));
   {
     const int w = h->width;
-    if (h->execs[w]) { cudaGraphExecDestroy(h->execs[w]); h->execs[w] = nullptr; }
-    if (h->graphs[w]) { cudaGraphDestroy(h->graphs[w]); h->graphs[w] = nullptr; }
+    if (h->loop_execs[w]) { cudaGraphExecDestroy(h->loop_execs[w]); h->loop_execs[w] = nullptr; }
+    if (h->loop_graphs[w]) { cudaGraphDestroy(h->loop_graphs[w]); h->loop_graphs[w] = nullptr; }
   }
   DF_CHECK(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
   h->capturing = true;
@@ -1065,8 +1100,38 @@ int dflash_capture_loop(dflash_handle* h, int32_t n_seq, const int32_t* targets,
     return rc;
   }
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
-  h->graphs[h->width] = graph;
-  DF_CHECK(h, cudaGraphInstantiate(&h->execs[h->width], graph, 0));
+  h->loop_graphs[h->width] = graph;
+  DF_CHECK(h, cudaGraphInstantiate(&h->loop_execs[h->width], graph, 0));
+  return DFLASH_OK;
+}
+
+int dflash_replay_loop(dflash_handle* h, void* stream) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (!h->loop_execs[h->width]) return DFLASH_ERR_NOT_CAPTURED;
+  DF_CHECK(h, cudaGraphLaunch(h->loop_execs[h->width], static_cast<cudaStream_t>(stream)));
+  return DFLASH_OK;
+}
+
+int dflash_graph_nodes(dflash_handle* h, int32_t loop, int32_t* kernels, int32_t* mem_alloc,
+                       int32_t* other) {
+  if (!h || !kernels || !mem_alloc || !other) return DFLASH_ERR_INVALID_ARG;
+  cudaGraph_t g = loop ? h->loop_graphs[h->width] : h->graphs[h->width];
+  if (!g) return DFLASH_ERR_NOT_CAPTURED;
+  size_t n = 0;
+  DF_CHECK(h, cudaGraphGetNodes(g, nullptr, &n));
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (n) DF_CHECK(h, cudaGraphGetNodes(g, nodes.data(), &n));
+  int k = 0, m = 0, o = 0;
+  for (size_t i = 0; i < n; ++i) {
+    cudaGraphNodeType t;
+    DF_CHECK(h, cudaGraphNodeGetType(nodes[i], &t));
+    if (t == cudaGraphNodeTypeKernel) ++k;
+    else if (t == cudaGraphNodeTypeMemAlloc || t == cudaGraphNodeTypeMemFree) ++m;
+    else ++o;
+  }
+  *kernels = k;
+  *mem_alloc = m;
+  *other = o;
   return DFLASH_OK;
 }
 
@@ -1115,8 +1180,30 @@ int dflash_read_status(dflash_handle* h, uint32_t* status, void* stream) {
 
 int dflash_profile_enable(dflash_handle* h, int enable) {
   if (!h) return DFLASH_ERR_INVALID_ARG;
-  if (h->capturing) return DFLASH_ERR_INVALID_ARG;
-  h->prof = enable != 0;
+  if (h->capturing || enable < 0 || enable > 2) return DFLASH_ERR_INVALID_ARG;
+  h->prof = enable == 1;
+  h->stamps = enable == 2;
+  return DFLASH_OK;
+}
+
+int dflash_profile_stamps(dflash_handle* h, int32_t max, int32_t* cls, double* start_us,
+                          double* end_us, int32_t* n, void* stream) {
+  if (!h || !cls || !start_us || !end_us || !n || max < 0) return DFLASH_ERR_INVALID_ARG;
+  const int k = std::min<int>(max, (int)h->stamp_cls.size());
+  std::vector<unsigned long long> raw(2 * (size_t)std::max(k, 1));
+  DF_CHECK(h, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  if (k) DF_CHECK(h, cudaMemcpy(raw.data(), h->scratch + h->L.stamps, sizeof(unsigned long long) * 2 * k,
+                                cudaMemcpyDeviceToHost));
+  unsigned long long t0 = ~0ull;
+  for (int i = 0; i < k; ++i)
+    if (raw[2 * i + 1]) t0 = std::min(t0, ~raw[2 * i]);
+  for (int i = 0; i < k; ++i) {
+    cls[i] = h->stamp_cls[i];
+    const bool ran = raw[2 * i + 1] != 0;
+    start_us[i] = ran ? (double)(~raw[2 * i] - t0) * 1e-3 : -1.0;
+    end_us[i] = ran ? (double)(raw[2 * i + 1] - t0) * 1e-3 : -1.0;
+  }
+  *n = k;
   return DFLASH_OK;
 }
 

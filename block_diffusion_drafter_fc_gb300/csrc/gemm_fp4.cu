@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
     }
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    stamp_begin(p.stamp);
   }
   if (warp == kIssuer) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -502,6 +503,7 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  if (threadIdx.x == 0) stamp_finish(p.stamp);
   if (warp == kIssuer) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols)

@@ -4,10 +4,12 @@
 // activation blocks, stream-K split, fused epilogues) for activations that
 // their producer already stored as bf16 hi + lo pairs.  Warp 8 is a producer:
 // one lane walks this CTA's stream-K units and, per k chunk (128 bytes of every
-// weight row), issues cp.async.bulk.tensor loads of the 128 weight rows (eight
-// 16-row boxes, each from the segment's own tensor map) and of the 16 activation
-// rows (hi and lo) into a ring of shared-memory stages, completing on the
-// stage's "full" mbarrier.  Warps 0..7 are consumers: each owns 16 weight rows,
+// weight row), issues cp.async.bulk.tensor loads of the 128 weight rows and of
+// the 16 activation rows (hi and lo) into a ring of shared-memory stages,
+// completing on the stage's "full" mbarrier.  The weight rows go as two 64-row
+// boxes where four 16-row groups of the tile are consecutive rows of one
+// segment (bf16 and E4M3), else as eight 16-row boxes (fp32 weights, segment
+// boundaries inside the tile), each from its segment's own tensor map.  Warps 0..7 are consumers: each owns 16 weight rows,
 // reads its A fragments and the shared B fragments with ldmatrix from the
 // 128-byte-swizzled tiles, runs mma.sync m16n8k16 (fp32 accumulation), and
 // releases the stage on its "empty" mbarrier.  The first stages' weight loads
@@ -356,6 +358,7 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
     }
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    stamp_begin(p.stamp);
   }
   __syncthreads();
   pdl_trigger();
@@ -488,6 +491,10 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
       if (!vsplit_fixup<T::PEN>(p, acc_s, item, c0, c1, V, G, b, &s_flag)) continue;
       run_epilogue(p, acc_s, scale_s, inv_rms, mb, tile, &s_flag);
     }
+  }
+  if (p.stamp) {
+    csync();
+    if (tid == 0) stamp_finish(p.stamp);
   }
 }
 

@@ -36,6 +36,10 @@ constexpr int kTileRows = 128;     // output rows (weight rows) of one CTA tile
 constexpr int kGemmThreads = 256;  // 8 warps x 16 weight rows
 constexpr int kMaxSeg = 2 * 16;
 constexpr int kMaxLayers = 16;
+// widest activation stage (k extent) of the register-fed projection kernel:
+// configure_gemm raises its shared-memory limit to this width, and every caller
+// (the handle-based calls and the allocation-free encode) plans within it
+constexpr int kGemmXkMax = 960;
 
 struct GemmSeg {
   const void* w;        // [rows][K] row-major, weight dtype
@@ -134,6 +138,7 @@ struct GemmParams {
   const char* pf_base;
   unsigned long long pf_bytes, pf_stride;
   int pf_count;
+  unsigned long long* stamp;  // launch timestamp slot (profiling captures), else null
 };
 
 struct AttnParams {
@@ -159,6 +164,7 @@ struct AttnParams {
   int pair_f16;           // fp16 pair (FP4 weights), else bf16
   unsigned* status;       // device status bits (DFLASH_DEV_TIMEOUT on a copy that never lands)
   int block_width;        // block rows that exist (2..16): block keys at or past it are masked
+  unsigned long long* stamp;  // launch timestamp slot (profiling captures), else null
 };
 
 size_t gemm_smem_bytes(int wt, int xk);
@@ -194,7 +200,8 @@ cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
                          const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
                          const void* norm0, uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
-                         int parts, int ss_ld, unsigned* status, cudaStream_t st);
+                         int parts, int ss_ld, unsigned* status, unsigned long long* stamp,
+                         cudaStream_t st);
 cudaError_t launch_rope_table(const int32_t* pos, int T, const double* inv_freq, int hd,
                               float2* rope_cs, int32_t* ring_pos, int window, int rows_per_seq,
                               const int32_t* count, unsigned* status, cudaStream_t st);
@@ -205,7 +212,7 @@ cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss
                              int n, const void* normw, int norm_bf16, float eps, float* out,
                              cudaStream_t st);
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t* n_ok, int n_seq,
-                          int width, cudaStream_t st);
+                          int width, unsigned long long* stamp, cudaStream_t st);
 cudaError_t launch_fill_i32(int32_t* p, int n, int32_t v, cudaStream_t st);
 // x (fp32, n values) -> bf16 hi + lo with x = hi + lo + O(2^-17 |x|) (pair_f16:
 // fp16 hi + lo)

@@ -23,8 +23,10 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
                                                     const double* inv_freq, int half, float* h,
                                                     float* ss, float2* rope_cs, const void* norm0,
                                                     uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
-                                                    int parts, int ss_ld, unsigned* status) {
+                                                    int parts, int ss_ld, unsigned* status,
+                                                    unsigned long long* stamp) {
   const int M = n_seq * kBlock;
+  if (threadIdx.x == 0) stamp_begin(stamp);
   if ((int)blockIdx.x < M * parts) {
     const int m = blockIdx.x / parts, part = blockIdx.x - m * parts, seq = m / kBlock, i = m % kBlock;
     const int span = d / parts, kbeg = part * span, kend = kbeg + span;
@@ -91,6 +93,7 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
       float t = 0.f;
       for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
       ss[(size_t)part * ss_ld + m] = t;
+      stamp_finish(stamp);
     }
     return;
   }
@@ -106,19 +109,22 @@ __global__ void __launch_bounds__(256) embed_kernel(const void* tok_embd, int de
   double sn, cs;
   sincos((double)(p0 + (m % kBlock)) * inv_freq[j], &sn, &cs);
   rope_cs[e] = make_float2((float)cs, (float)sn);
+  if (threadIdx.x == 0) stamp_finish(stamp);
 }
 
 cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,
                          const double* inv_freq, int hd, float* h, float* ss, float2* rope_cs,
                          const void* norm0, uint16_t* x_hi, uint16_t* x_lo, int pair_f16,
-                         int parts, int ss_ld, unsigned* status, cudaStream_t st) {
+                         int parts, int ss_ld, unsigned* status, unsigned long long* stamp,
+                         cudaStream_t st) {
   const int M = n_seq * kBlock, half = hd / 2;
   const int tb = (M * half + 63) / 64;
   if (parts < 1 || n_embd % (8 * parts) != 0) return cudaErrorInvalidValue;
   embed_kernel<<<M * parts + tb, 256, 0, st>>>(tok_embd, dense_bf16, n_embd, n_vocab, mask_token,
                                                id_last, n_past, n_seq, inv_freq, half, h, ss, rope_cs,
-                                               norm0, x_hi, x_lo, pair_f16, parts, ss_ld, status);
+                                               norm0, x_hi, x_lo, pair_f16, parts, ss_ld, status,
+                                               stamp);
   return cudaGetLastError();
 }
 
@@ -193,20 +199,22 @@ cudaError_t launch_rms_apply(const float* raw, const float* ss, int n_ss, int ss
 // matches (15 when none): dflash-ops model card, Usage (device-side accept) and
 // dflash_engine.py, DFlashSpeculativeVerifier.verify_block.
 __global__ void accept_kernel(const int32_t* drafts, const int32_t* targets, int32_t* n_ok,
-                              int n_seq, int width) {
+                              int n_seq, int width, unsigned long long* stamp) {
   const int seq = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) stamp_begin(stamp);
   if (seq >= n_seq) return;
   bool miss = false;
   if (lane < kBlock - 1)
     miss = lane >= width - 1 || drafts[seq * (kBlock - 1) + lane] != targets[seq * (kBlock - 1) + lane];
   const unsigned mask = __ballot_sync(0xffffffffu, miss);
   if (lane == 0) n_ok[seq] = mask ? __ffs(mask) - 1 : kBlock - 1;
+  if (threadIdx.x == 0) stamp_finish(stamp);
 }
 
 cudaError_t launch_accept(const int32_t* drafts, const int32_t* targets, int32_t* n_ok, int n_seq,
-                          int width, cudaStream_t st) {
-  accept_kernel<<<(n_seq + 7) / 8, 256, 0, st>>>(drafts, targets, n_ok, n_seq, width);
+                          int width, unsigned long long* stamp, cudaStream_t st) {
+  accept_kernel<<<(n_seq + 7) / 8, 256, 0, st>>>(drafts, targets, n_ok, n_seq, width, stamp);
   return cudaGetLastError();
 }
 

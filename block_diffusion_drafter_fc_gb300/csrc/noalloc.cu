@@ -25,7 +25,7 @@ namespace {
 
 constexpr size_t kScratchBytes = 8u << 20;          // 8 MiB per device
 constexpr int kNaGrid = 152 * 2;                    // projection CTAs (one resident wave)
-constexpr int kNaXk = 960;                          // activation stage width
+constexpr int kNaXk = kGemmXkMax;                   // activation stage width (shared limit)
 constexpr size_t kCounterBytes = 64u << 10;         // tickets: 16384 ints
 constexpr size_t kPartialBytes = (size_t)2 * kNaGrid * 16 * kTileRows * sizeof(float);
 constexpr size_t kSsBytes = kScratchBytes - kCounterBytes - kPartialBytes;
@@ -80,6 +80,9 @@ extern "C" DFLASH_API int dflash_encode_noalloc(const dflash_config* cfg, const 
       (size_t)n_tiles * T * sizeof(float) > kSsBytes)
     return DFLASH_ERR_TOO_MANY_ROWS;
 
+  // the runtime's last-error slot is shared with all CUDA work of the process:
+  // an error left there by earlier work is not this call's
+  (void)cudaGetLastError();
   unsigned char* base = nullptr;
   if (setup(&base) != cudaSuccess) return DFLASH_ERR_CUDA;
   int* counters = reinterpret_cast<int*>(base);

@@ -14,7 +14,7 @@ from typing import Dict, List, Optional
 
 import torch
 
-from .synth import BLOCK, DraftConfig, Workload
+BLOCK = 16          # rows of one noise block (anchor + 15 masks)
 
 PKG = pathlib.Path(__file__).resolve().parent
 LIB_PATH = PKG / "libdflash.so"
@@ -73,6 +73,11 @@ def _load() -> C.CDLL:
         "dflash_accept": (C.c_int, [vp, i32, vp, vp, vp, vp]),
         "dflash_capture": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_replay": (C.c_int, [vp, vp]),
+        "dflash_replay_loop": (C.c_int, [vp, vp]),
+        "dflash_graph_nodes": (C.c_int, [vp, i32, C.POINTER(i32), C.POINTER(i32), C.POINTER(i32)]),
+        "dflash_profile_stamps": (C.c_int, [vp, i32, C.POINTER(i32), C.POINTER(C.c_double),
+                                            C.POINTER(C.c_double), C.POINTER(i32), vp]),
+        "dflash_encode_noalloc": (C.c_int, [C.POINTER(dflash_config), vp, vp, vp, i32, vp, vp]),
         "dflash_advance": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_set_block_width": (C.c_int, [vp, i32]),
         "dflash_capture_loop": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
@@ -119,8 +124,12 @@ def _stream(stream=None) -> int:
     return s.cuda_stream
 
 
-def make_config(cfg: DraftConfig, max_seq: Optional[int] = None,
+def make_config(cfg, max_seq: Optional[int] = None,
                 max_inject: Optional[int] = None) -> dflash_config:
+    """dflash_config from any object with the drafter's geometry attributes
+    (n_layer, n_embd, n_head, n_head_kv, head_dim, n_ff, window, n_vocab,
+    n_target_layers, d_t, n_seq, mask_token_id, weight_dtype, dense_dtype,
+    ring_dtype as "f32" | "bf16" | "fp8" | "fp4", eps, rope_theta)."""
     c = dflash_config()
     c.n_layer, c.n_embd, c.n_head, c.n_head_kv = cfg.n_layer, cfg.n_embd, cfg.n_head, cfg.n_head_kv
     c.head_dim, c.n_ff, c.window, c.n_vocab = cfg.head_dim, cfg.n_ff, cfg.window, cfg.n_vocab
@@ -141,12 +150,17 @@ def workspace_size(c: dflash_config):
 
 
 class Drafter:
-    """A libdflash handle over device copies of a workload's weights.
+    """A libdflash handle over the caller's device weights.
 
-    The ring and scratch areas are torch uint8 tensors owned by this object; the
-    weights are the caller's device tensors (kept referenced here)."""
+    `cfg` is any object with the geometry attributes make_config reads;
+    `dev_weights` maps "tok_embd", "lm_head", "fc", "hidden_norm", "out_norm"
+    and "l{i}.{attn_norm, wq, wk, wv, wo, q_norm, k_norm, ffn_norm, gate, up,
+    down}" to DeviceWeight(data, scale) pairs of device tensors in the stored
+    layout the header describes.  The ring and scratch areas are torch uint8
+    tensors owned by this object; the weights stay the caller's (kept
+    referenced here)."""
 
-    def __init__(self, cfg: DraftConfig, dev_weights: Dict[str, "DeviceWeight"],
+    def __init__(self, cfg, dev_weights: Dict[str, "DeviceWeight"],
                  max_seq: Optional[int] = None, max_inject: Optional[int] = None,
                  device: str = "cuda"):
         self.cfg = cfg
@@ -229,6 +243,16 @@ class Drafter:
     def dflash_replay(self, stream=None):
         _check(LIB.dflash_replay(self.h, _stream(stream)), self.h, "replay")
 
+    def dflash_replay_loop(self, stream=None):
+        _check(LIB.dflash_replay_loop(self.h, _stream(stream)), self.h, "replay_loop")
+
+    def dflash_graph_nodes(self, loop: bool = False):
+        """(kernel nodes, memory alloc/free nodes, other nodes) of the captured graph."""
+        k, m, o = C.c_int32(), C.c_int32(), C.c_int32()
+        _check(LIB.dflash_graph_nodes(self.h, int(loop), C.byref(k), C.byref(m), C.byref(o)),
+               self.h, "graph_nodes")
+        return k.value, m.value, o.value
+
     def dflash_set_block_width(self, width: int):
         _check(LIB.dflash_set_block_width(self.h, int(width)), self.h, "set_block_width")
 
@@ -266,26 +290,20 @@ class Drafter:
         _check(LIB.dflash_profile_read(self.h, ms, n), self.h, "profile_read")
         return {PROF_CLASSES[i]: (ms[i], n[i]) for i in range(PROF_N)}
 
-    # ---- convenience: run a workload's prefill (encode + inject per call)
-    def prefill(self, wl: Workload, dev_feats: List[torch.Tensor], stream=None):
-        dev = self.ring_mem.device
-        for call in wl.inject_calls:
-            seq, p0, cnt, r0 = call
-            f = dev_feats[seq][r0:r0 + cnt]
-            H = torch.empty((cnt, self.cfg.n_embd), dtype=torch.float32, device=dev)
-            self.dflash_encode(f, H, stream)
-            pos = torch.arange(p0, p0 + cnt, dtype=torch.int32, device=dev)
-            self.dflash_inject(seq, H, pos, stream)
+    def dflash_profile_stamps(self, stream=None, max_launches: int = 128):
+        """[(class name, start_us, end_us)] of the last recorded step's launches."""
+        cls = (C.c_int32 * max_launches)()
+        t0 = (C.c_double * max_launches)()
+        t1 = (C.c_double * max_launches)()
+        n = C.c_int32()
+        _check(LIB.dflash_profile_stamps(self.h, max_launches, cls, t0, t1, C.byref(n),
+                                         _stream(stream)), self.h, "profile_stamps")
+        return [(PROF_CLASSES[cls[i]], t0[i], t1[i]) for i in range(n.value)]
 
 
 class DeviceWeight:
+    """One weight tensor on the device in its stored layout, and its per-row f32
+    scales (FP8 / FP4 projections; None otherwise)."""
+
     def __init__(self, data: torch.Tensor, scale: Optional[torch.Tensor]):
         self.data, self.scale = data, scale
-
-
-def to_device(wl: Workload, device: str = "cuda"):
-    """Device copies of a workload's weights and features (same bytes)."""
-    dw = {n: DeviceWeight(w.data.to(device), None if w.scale is None else w.scale.to(device))
-          for n, w in wl.weights.items()}
-    feats = [f.to(device) for f in wl.feats]
-    return dw, feats

@@ -228,6 +228,10 @@ DFLASH_API int dflash_encode(dflash_handle* h, const void* feats, int32_t T, flo
  * calls.  All calls share the array: calls that overlap on the GPU (on
  * different streams, or from different threads) race; it is cleared where it
  * must start at zero at the start of every call.  Asynchronous on `stream`.
+ * There is no handle to hold an error text: DFLASH_ERR_CUDA from this call
+ * carries no further detail (the runtime's own cudaGetLastError does).  The
+ * runtime's last-error slot is cleared on entry, so an error left by earlier
+ * unrelated work is not reported as this call's.
  */
 DFLASH_API int dflash_encode_noalloc(const dflash_config* cfg, const void* fc, const void* hidden_norm,
                                      const void* feats, int32_t T, float* H_t, void* stream);
@@ -295,14 +299,25 @@ DFLASH_API int dflash_accept(dflash_handle* h, int32_t n_seq, const int32_t* dra
  * model card, Method: the captured step allocates nothing, so eager work may
  * run between replays).  Capture runs on an internal stream; nothing is
  * launched.  `stream` orders the capture after earlier work on it.
- * Replaces a previous capture.
+ * Replaces a previous dflash_capture of the current block width (a loop-turn
+ * graph of dflash_capture_loop is kept separately and is not affected).
  */
 DFLASH_API int dflash_capture(dflash_handle* h, int32_t n_seq, const int32_t* id_last, const int32_t* n_past,
                    float* logits, int32_t* drafts, const int32_t* targets, int32_t* n_ok,
                    void* stream);
 
-/* Launch the captured graph on `stream` (NOT_CAPTURED if there is none). */
+/* Launch the current width's dflash_capture graph on `stream` (NOT_CAPTURED if there is none). */
 DFLASH_API int dflash_replay(dflash_handle* h, void* stream);
+
+/*
+ * Node counts of the current width's captured graph (loop = 0: dflash_capture,
+ * loop != 0: dflash_capture_loop), host int32 outputs: kernel launches, memory
+ * allocation or free nodes (always 0: nothing in a step allocates), and every
+ * other node (memset nodes of profiling captures).  NOT_CAPTURED if there is no
+ * such graph.
+ */
+DFLASH_API int dflash_graph_nodes(dflash_handle* h, int32_t loop, int32_t* kernels,
+                                  int32_t* mem_alloc, int32_t* other);
 
 /*
  * One turn of the speculative loop on the device, after the target model has
@@ -334,8 +349,9 @@ DFLASH_API int dflash_advance(dflash_handle* h, int32_t n_seq, const int32_t* dr
 
 /*
  * Capture one whole loop turn - dflash_advance followed by dflash_step with
- * the updated id_last / n_past - into the handle's graph (replacing any
- * previous capture; dflash_replay launches it).  With these exact pointers,
+ * the updated id_last / n_past - into the handle's loop graph of the current
+ * block width (replacing a previous loop capture of that width; a dflash_capture
+ * graph is kept separately; dflash_replay_loop launches it).  With these exact pointers,
  * each replay consumes the target's tokens and features for the block drafted
  * by the previous replay (or step) and leaves the next block's logits and
  * drafts in `logits` / `drafts`.  Capture runs on an internal stream; nothing
@@ -344,6 +360,9 @@ DFLASH_API int dflash_advance(dflash_handle* h, int32_t n_seq, const int32_t* dr
 DFLASH_API int dflash_capture_loop(dflash_handle* h, int32_t n_seq, const int32_t* targets,
                                    const void* feats, int32_t* id_last, int32_t* n_past,
                                    int32_t* n_ok, float* logits, int32_t* drafts, void* stream);
+
+/* Launch the current width's dflash_capture_loop graph on `stream` (NOT_CAPTURED if there is none). */
+DFLASH_API int dflash_replay_loop(dflash_handle* h, void* stream);
 
 /*
  * The same step as dflash_step, driven from host memory: copies id_last and
@@ -365,9 +384,12 @@ DFLASH_API int dflash_ring_reset(dflash_handle* h, int32_t seq, void* stream);
 DFLASH_API int dflash_read_status(dflash_handle* h, uint32_t* status, void* stream);
 
 /*
- * Launch-class profiling of eager calls (not of captured graphs).  While
- * enabled, every kernel launch of dflash_step / dflash_encode / dflash_inject /
- * dflash_accept is bracketed by CUDA events recorded on the launching stream.
+ * Profiling.  dflash_profile_enable(h, mode): 0 off; 1 launch-class events on
+ * eager calls; 2 device timestamps of every step launch.
+ *
+ * Mode 1 (eager calls, not captured graphs): every kernel launch of
+ * dflash_step / dflash_encode / dflash_inject / dflash_accept is bracketed by
+ * CUDA events recorded on the launching stream.
  * dflash_profile_read waits for those events, writes the summed device time in
  * milliseconds and the launch count of each class (arrays of DFLASH_PROF_N
  * entries, host memory) and clears the record.  Classes: 0 embedding + rope
@@ -379,6 +401,21 @@ DFLASH_API int dflash_read_status(dflash_handle* h, uint32_t* status, void* stre
 #define DFLASH_PROF_N 11
 DFLASH_API int dflash_profile_enable(dflash_handle* h, int enable);
 DFLASH_API int dflash_profile_read(dflash_handle* h, double* ms, int32_t* launches);
+
+/*
+ * Mode 2: every kernel of a step (and of the acceptance scan of dflash_capture)
+ * records the %globaltimer of its first CTA's start and of its last CTA's end
+ * in a scratch slot, from eager calls and from graphs captured while mode 2 is
+ * on (such a graph also zeroes the slots with one memset node ahead of the
+ * step); the kernels, their order and their launch attributes are those of the
+ * unprofiled step.  dflash_profile_stamps waits for `stream`, then writes, for
+ * the launches of the last recorded step in launch order (at most `max`), the
+ * class (as in mode 1) and the start and end in microseconds relative to the
+ * earliest start (-1 for a launch that has not run), and their count to *n
+ * (host arrays).  Synchronous.
+ */
+DFLASH_API int dflash_profile_stamps(dflash_handle* h, int32_t max, int32_t* cls, double* start_us,
+                                     double* end_us, int32_t* n, void* stream);
 
 /* Text of a dflash_status code (static storage). */
 DFLASH_API const char* dflash_status_string(int status);

@@ -21,12 +21,35 @@ def logit_tol(cfg) -> float:
     return LOGIT_TOL["bf16"]
 
 
+def to_device(wl: Workload, device: str = "cuda"):
+    """Device copies of a workload's weights (as the binding's DeviceWeight
+    pairs) and features: the same bytes the oracle reads."""
+    from block_diffusion_drafter_fc_gb300.dflash import DeviceWeight
+    dw = {n: DeviceWeight(w.data.to(device), None if w.scale is None else w.scale.to(device))
+          for n, w in wl.weights.items()}
+    feats = [f.to(device) for f in wl.feats]
+    return dw, feats
+
+
+def prefill(dr, wl: Workload, dev_feats, stream=None):
+    """Run a workload's inject schedule through the C ABI: per call, encode the
+    call's feature rows, then inject them at their positions."""
+    dev = dr.ring_mem.device
+    for call in wl.inject_calls:
+        seq, p0, cnt, r0 = call
+        f = dev_feats[seq][r0:r0 + cnt]
+        H = torch.empty((cnt, dr.cfg.n_embd), dtype=torch.float32, device=dev)
+        dr.dflash_encode(f, H, stream)
+        pos = torch.arange(p0, p0 + cnt, dtype=torch.int32, device=dev)
+        dr.dflash_inject(seq, H, pos, stream)
+
+
 def gpu_run(wl: Workload, n_seq: Optional[int] = None, targets: Optional[np.ndarray] = None,
             max_seq: Optional[int] = None, keep: bool = False) -> Dict:
     from block_diffusion_drafter_fc_gb300 import dflash as D
     cfg = wl.cfg
     dev = "cuda"
-    dw, feats = D.to_device(wl, dev)
+    dw, feats = to_device(wl, dev)
     max_inject = max(c[2] for c in wl.inject_calls)
     dr = D.Drafter(cfg, dw, max_seq=max_seq or cfg.n_seq, max_inject=max_inject)
     Hts = []
@@ -62,27 +85,46 @@ def gpu_run(wl: Workload, n_seq: Optional[int] = None, targets: Optional[np.ndar
     return out
 
 
-def compare_drafts(gpu_logits, gpu_drafts, ref_logits, ref_drafts, err):
-    """Drafts must equal the oracle's wherever the oracle's top-2 gap is wider
-    than twice the measured logit error; inside that band (a near tie the two
-    precisions may order differently) the GPU's token must be one of the
-    oracle's two best.  The GPU's drafts must always be the argmax of its own
-    logits (lowest index on ties).  Returns the number of positions whose token
-    differs from the oracle's (0 unless a near tie flipped)."""
+# The workloads the drafter's statement of the target names (tiny fp32, small
+# bf16, real bf16, real fp32, batched FP8): their drafts and acceptance counts
+# must equal the oracle's exactly, with no allowance for near ties.
+EXACT_DRAFTS = frozenset({"tiny_f32", "small_bf16", "real_bf16", "real_f32", "batched_fp8"})
+
+
+def compare_drafts(gpu_logits, gpu_drafts, ref_logits, ref_drafts, err, name=None):
+    """Greedy drafts against the oracle's.
+
+    The GPU's drafts must always be the argmax of its own logits (lowest index
+    on ties).  For the named target workloads (EXACT_DRAFTS) they must equal the
+    oracle's drafts at every position.  For the other test geometries a
+    position whose oracle top-2 gap is within twice the measured logit error (a
+    near tie the two precisions may order differently) may hold either of the
+    oracle's two best tokens; every such flip is reported as a warning (shown
+    in pytest's warnings summary).  Returns the number of flipped positions."""
+    import warnings
     own = np.argmax(gpu_logits[:, 1:, :], axis=-1)
     assert np.array_equal(own, gpu_drafts), "drafts are not the argmax of the GPU logits"
     r32 = ref_logits.astype(np.float32)[:, 1:, :]
     top2 = np.sort(r32, axis=-1)[..., -2:]
     gap = top2[..., 1] - top2[..., 0]
+    diff = np.argwhere(gpu_drafts != ref_drafts)
+    detail = [(int(s), int(j), int(gpu_drafts[s, j]), int(ref_drafts[s, j]), float(gap[s, j]))
+              for s, j in diff[:8]]
+    if name is None or name in EXACT_DRAFTS:
+        assert diff.size == 0, f"drafts differ from the oracle at (seq, pos, gpu, oracle, gap) {detail}"
+        return 0
     clear = gap > 2 * err
-    assert np.array_equal(gpu_drafts[clear], ref_drafts[clear]), "draft mismatch on a clear row"
+    assert np.array_equal(gpu_drafts[clear], ref_drafts[clear]), \
+        f"draft mismatch on a clear row {detail}"
     if (~clear).any():
         best2 = np.argsort(r32, axis=-1)[..., -2:]
         amb = np.nonzero(~clear)
         for s, j in zip(*amb):
             assert gpu_drafts[s, j] in best2[s, j], (s, j)
-    # positions where the tokens actually differ (only possible inside the band)
-    return int((gpu_drafts != ref_drafts).sum())
+    n = int(diff.shape[0])
+    if n:
+        warnings.warn(f"{name}: {n} draft positions flipped inside the near-tie band {detail}")
+    return n
 
 
 def ring_ulps(gpu_vals: np.ndarray, ref_raw: np.ndarray, dtype: str) -> np.ndarray:

@@ -47,10 +47,10 @@ def test_loop_turns_match_oracle(name):
     idl, npast = wl.id_last.numpy()[:n].astype(np.int32), wl.n_past.numpy()[:n].astype(np.int32)
     ref_logits, ref_drafts = O.step(w, rings, idl, npast)
 
-    dw, feats0 = D.to_device(wl, "cuda")
+    dw, feats0 = GH.to_device(wl, "cuda")
     max_inject = max(max(c[2] for c in wl.inject_calls), BLOCK * n)
     dr = D.Drafter(cfg, dw, max_seq=n, max_inject=max_inject)
-    dr.prefill(wl, feats0)
+    GH.prefill(dr, wl, feats0)
     id_last = wl.id_last[:n].cuda()
     n_past = wl.n_past[:n].cuda()
     logits = torch.empty((n, BLOCK, cfg.n_vocab), device="cuda")
@@ -66,7 +66,7 @@ def test_loop_turns_match_oracle(name):
         lg = logits.cpu().numpy()
         err = float(np.max(np.abs(lg - ref_logits)))
         assert err <= tol, f"turn {turn}: logits max |diff| {err:.3e} > {tol}"
-        GH.compare_drafts(lg, drafts.cpu().numpy(), ref_logits, ref_drafts, err)
+        GH.compare_drafts(lg, drafts.cpu().numpy(), ref_logits, ref_drafts, err, name)
         if ref_nok is not None:
             assert np.array_equal(n_ok.cpu().numpy(), ref_nok), turn
         assert np.array_equal(id_last.cpu().numpy(), idl), turn
@@ -91,10 +91,20 @@ def test_loop_turns_match_oracle(name):
             dr.dflash_step(id_last, n_past, logits, drafts)
         else:
             if turn == 2:
+                # a plain step graph first: the loop capture keeps it (own slot)
+                dr.dflash_capture(id_last, n_past, logits, drafts)
                 dr.dflash_capture_loop(targets_d, feats_d, id_last, n_past, n_ok, logits, drafts)
-            dr.dflash_replay()
+                assert dr.dflash_graph_nodes(loop=True)[1] == 0
+            dr.dflash_replay_loop()
         check(turn, ref_nok)
         prev_drafts = ref_drafts
+    # the step graph captured before the loop graph still replays: one step at
+    # the state the last loop turn left, bitwise equal to that turn's outputs
+    lg, dd = logits.clone(), drafts.clone()
+    logits.zero_()
+    dr.dflash_replay()
+    torch.cuda.synchronize()
+    assert torch.equal(logits, lg) and torch.equal(drafts, dd)
     dr.close()
 
 
@@ -102,7 +112,7 @@ def test_advance_rejects_bad_sizes():
     from block_diffusion_drafter_fc_gb300 import dflash as D
     cfg = get_config("tiny_f32")
     wl = make_workload(cfg)
-    dw, _ = D.to_device(wl, "cuda")
+    dw, _ = GH.to_device(wl, "cuda")
     dr = D.Drafter(cfg, dw, max_seq=2, max_inject=16)       # room for one sequence's block only
     z = torch.zeros((2, BLOCK), dtype=torch.int32, device="cuda")
     f = torch.zeros((2, BLOCK, cfg.feat_dim), dtype=torch.float32, device="cuda")

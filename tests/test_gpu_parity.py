@@ -92,10 +92,13 @@ def test_step_logits_drafts_accept(name):
     wl, ref, gpu = _case(name)
     err = float(np.abs(gpu["logits"] - ref["logits"]).max())
     assert err <= GH.logit_tol(wl.cfg), err
-    amb = GH.compare_drafts(gpu["logits"], gpu["drafts"], ref["logits"], ref["drafts"], err)
+    amb = GH.compare_drafts(gpu["logits"], gpu["drafts"], ref["logits"], ref["drafts"], err, name)
     if amb == 0:
         assert np.array_equal(gpu["drafts"], ref["drafts"])
         assert np.array_equal(gpu["n_ok"], ref["n_ok"])
+    else:   # a reported near-tie flip (extra test geometries only): n_ok follows the GPU's drafts
+        from oracle import dflash_oracle as O
+        assert np.array_equal(gpu["n_ok"], O.accept(gpu["drafts"], ref["targets"]))
     assert gpu["status"] == 0
 
 
@@ -105,7 +108,7 @@ def test_accept_synthetic_against_oracle():
     from block_diffusion_drafter_fc_gb300 import dflash as D
     from oracle import dflash_oracle as O
     wl = make_workload(get_config("ragged_bf16"))
-    dw, _ = D.to_device(wl)
+    dw, _ = GH.to_device(wl)
     dr = D.Drafter(wl.cfg, dw, max_seq=37)
     g = np.random.default_rng(3)
     drafts = g.integers(0, 1000, size=(37, 15)).astype(np.int32)
@@ -142,7 +145,7 @@ def test_empty_ring_step():
     rings = [O.OracleRing(w.cfg)]
     lg, dr_ = O.step(w, rings, [int(wl.id_last[0])], [0])
     from block_diffusion_drafter_fc_gb300 import dflash as D
-    dw, _ = D.to_device(wl)
+    dw, _ = GH.to_device(wl)
     d = D.Drafter(wl.cfg, dw)
     logits = torch.empty((1, BLOCK, wl.cfg.n_vocab), device="cuda")
     drafts = torch.empty((1, 15), dtype=torch.int32, device="cuda")
@@ -207,7 +210,7 @@ def test_step_host_matches_device_step():
 def test_host_side_errors_on_gpu_handle():
     from block_diffusion_drafter_fc_gb300 import dflash as D
     wl = make_workload(get_config("tiny_f32"))
-    dw, feats = D.to_device(wl)
+    dw, feats = GH.to_device(wl)
     dr = D.Drafter(wl.cfg, dw, max_inject=80)
     H = torch.zeros((80, wl.cfg.n_embd), device="cuda")
     pos = torch.arange(80, dtype=torch.int32, device="cuda")
@@ -235,5 +238,6 @@ def test_small_bf16_full():
     _check_ring(wl, ref, gpu)
     err = float(np.abs(gpu["logits"] - ref["logits"]).max())
     assert err <= GH.logit_tol(wl.cfg), err
-    GH.compare_drafts(gpu["logits"], gpu["drafts"], ref["logits"], ref["drafts"], err)
+    GH.compare_drafts(gpu["logits"], gpu["drafts"], ref["logits"], ref["drafts"], err, "small_bf16")
+    assert np.array_equal(gpu["drafts"], ref["drafts"])
     assert np.array_equal(gpu["n_ok"], ref["n_ok"])

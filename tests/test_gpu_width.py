@@ -25,9 +25,9 @@ def test_block_width_matches_oracle(name):
     n = cfg.n_seq
     w, rings, _ = OB.oracle_prefill(wl)
     idl, npast = wl.id_last.numpy()[:n], wl.n_past.numpy()[:n]
-    dw, feats = D.to_device(wl, "cuda")
+    dw, feats = GH.to_device(wl, "cuda")
     dr = D.Drafter(cfg, dw, max_seq=n, max_inject=max(c[2] for c in wl.inject_calls))
-    dr.prefill(wl, feats)
+    GH.prefill(dr, wl, feats)
     id_last, n_past = wl.id_last[:n].cuda(), wl.n_past[:n].cuda()
     logits = torch.empty((n, BLOCK, cfg.n_vocab), device="cuda")
     drafts = torch.empty((n, BLOCK - 1), dtype=torch.int32, device="cuda")
@@ -43,7 +43,7 @@ def test_block_width_matches_oracle(name):
         lg, dd = logits.cpu().numpy(), drafts.cpu().numpy()
         err = float(np.max(np.abs(lg[:, :B] - ref_logits)))
         assert err <= tol, f"width {B}: logits max |diff| {err:.3e}"
-        GH.compare_drafts(lg[:, :B], dd[:, :B - 1], ref_logits, ref_drafts, err)
+        GH.compare_drafts(lg[:, :B], dd[:, :B - 1], ref_logits, ref_drafts, err, name)
         assert (dd[:, B - 1:] == -1).all(), f"width {B}: drafts past the block"
         # acceptance: the target agrees with the oracle's drafts up to a drawn m <= B-1
         m = torch.randint(0, B, (n,), generator=g).numpy()
@@ -54,7 +54,7 @@ def test_block_width_matches_oracle(name):
                                cfg.n_vocab)
         want = O.accept(ref_drafts, targets[:, :B - 1])
         dr.dflash_accept(drafts, torch.from_numpy(targets).cuda(), n_ok)
-        if not GH.compare_drafts(lg[:, :B], dd[:, :B - 1], ref_logits, ref_drafts, err):
+        if not GH.compare_drafts(lg[:, :B], dd[:, :B - 1], ref_logits, ref_drafts, err, name):
             assert np.array_equal(n_ok.cpu().numpy(), want), f"width {B}: n_ok"
         eager[B] = (lg.copy(), dd.copy())
     # one graph per width, replayed alternately: bitwise equal to the eager steps

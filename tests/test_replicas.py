@@ -103,3 +103,40 @@ def test_class_rates_cover_every_class(config):
     assert ring > 0 and abs(r["attention"] - round(ring / cfg.n_layer / 1e-5 / 1e9, 1)) < 0.051
     # classes that did not run are left out
     assert bench.class_rates(cfg, wl, {k: (0.0, 0) for k in prof}) == {}
+
+
+def test_reference_arm_times_whole_steps_when_they_fit():
+    import json
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference", "--config",
+                        "tiny_f32", "--steps", "3", "--warmup", "2"], env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    assert out["cpu_baseline"]["sample"].startswith("3 whole fp64 oracle block steps of tiny_f32")
+
+
+def test_graph_breakdown_charges_the_critical_path():
+    """Each launch is charged from the previous launch's end to its own end
+    (launches overlap under programmatic dependent launch), so the classes sum
+    to the last end; spans are each launch's own start-to-end."""
+    sys.path.insert(0, str(ROOT))
+    import bench
+
+    class FakeDrafter:
+        def dflash_replay(self, stream):
+            pass
+
+        def dflash_profile_stamps(self, stream):
+            return [("embed", 0.0, 5.0), ("qkv", 3.0, 30.0), ("attention", 25.0, 40.0),
+                    ("qkv", 38.0, 61.0), ("accept", 60.0, 62.0)]
+
+    class FakeTraffic:
+        def run(self):
+            pass
+
+    crit, span, launches, total = bench.graph_breakdown(FakeDrafter(), None, FakeTraffic(), 3)
+    assert crit == {"embed": 5.0, "qkv": 25.0 + 21.0, "attention": 10.0, "accept": 1.0}
+    assert abs(sum(crit.values()) - 62.0) < 1e-9 and total == 62.0
+    assert span == {"embed": 5.0, "qkv": 25.0, "attention": 15.0, "accept": 2.0}
+    assert launches == {"embed": 1, "qkv": 2, "attention": 1, "accept": 1}
