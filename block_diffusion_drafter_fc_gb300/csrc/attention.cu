@@ -677,6 +677,355 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
   if (tid == 0) stamp_finish(p.stamp);
 }
 
+// ---------------------------------------------------------------------------
+// Split-window attention (grids that the GPU holds at once).
+//
+// The cluster kernel above caps a kv head's window at kMaxCluster CTAs, and a
+// cluster of 8 must find 8 free SMs in one GPC: one sequence of the real drafter
+// (8 kv heads) ran on 64 of the 152 SMs.  Here the window of a (sequence, kv
+// head, head group) is split into n_split independent CTAs of kq x 64 slots,
+// one 64-key sub-chunk per key lane (one staging round), so the whole GPU
+// works on one sequence.  Split 0 also attends to the block's 16 keys.  A CTA
+// merges its key lanes in shared memory and publishes its partial rows - the
+// running max m, the sum l and the un-normalised O of each query row - to
+// global scratch, then arrives on its group's counter.  Once all n_split CTAs
+// of the group have arrived (a wait bounded by ~2 s: the launcher uses this
+// kernel only when the whole grid is resident at once, so every CTA of the
+// group runs), CTA s merges rows s, s + n_split, ... of the group - weights
+// exp2(m_c - max m) summed over the splits in split order, so results do not
+// depend on arrival order - and writes the o projection's input pair.  The
+// group's last CTA to finish its merge resets the two counters for the next
+// launch.
+// ---------------------------------------------------------------------------
+
+constexpr int kMaxSplit = 32;   // splits per window (one lane each in the merge)
+
+DF_DEVICE int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+DF_DEVICE int atom_add_release_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+DF_DEVICE int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+template <int HD, bool RING_F32>
+__global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constant__ AttnParams p) {
+  using SM = AttnSmem<HD>;
+  constexpr int KS = SM::KS;
+  const int G = p.n_head / p.n_head_kv, hpc = p.hpc, kq = p.kq, n_hgrp = G / hpc;
+  const int split = blockIdx.x, n_split = gridDim.x;
+  const int kvh = blockIdx.y / n_hgrp, hg = blockIdx.y - kvh * n_hgrp, seq = blockIdx.z;
+  const int group = (seq * p.n_head_kv + kvh) * n_hgrp + hg;
+  const int R = kBlock * hpc;                       // rows of this CTA (head-major)
+  const int head0 = kvh * G + hg * hpc;             // first query head of the CTA
+  const int qd = p.n_head * HD, kvd = p.n_head_kv * HD;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int nwarps = (int)(blockDim.x >> 5);
+  const int hl = warp / kq, lk = warp - hl * kq;    // head within the CTA, key lane
+  constexpr bool TMA = !RING_F32 && SM::kTma;
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  uint16_t* bufs = reinterpret_cast<uint16_t*>(
+      TMA ? (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023) : reinterpret_cast<uintptr_t>(sm_raw));
+  const int buf_elems = (int)SM::buf_elems(RING_F32);
+  uint16_t* blk_k_hi = bufs + kq * buf_elems;
+  uint16_t* blk_k_lo = blk_k_hi + kBlock * KS;
+  uint16_t* blk_v_hi = blk_k_lo + kBlock * KS;
+  uint16_t* blk_v_lo = blk_v_hi + kBlock * KS;
+  int* kpos = reinterpret_cast<int*>(blk_v_lo + kBlock * KS);  // [kq][64]
+  __shared__ __align__(8) uint64_t s_bar[4];                    // one per sub-chunk buffer
+  __shared__ int s_last;
+
+  if (!RING_F32 && tid == 0) {
+    for (int b = 0; b < kq; ++b) mbar_init(&s_bar[b], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid == 0) stamp_begin(p.stamp);
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  const int p0 = max(p.n_past[seq], 0);
+  const int SL = kq * kSub;
+  const int s_begin = min(p.window, split * SL), s_end = min(p.window, s_begin + SL);
+  const int n_sub = (s_end - s_begin + kSub - 1) / kSub;
+  const size_t plane = (size_t)p.window * HD;
+  const size_t kbase = ((((size_t)seq * p.n_layer + p.layer) * 2 + 0) * p.n_head_kv + kvh) * plane;
+  const size_t vbase = kbase + (size_t)p.n_head_kv * plane;
+
+  // stage sub-chunk j of the split into buffer j (the only round)
+  if (TMA) {
+    if (tid == 0) {
+      const int row_k = (int)(kbase / HD), row_v = (int)(vbase / HD);
+      for (int j = 0; j < n_sub; ++j) {
+        mbar_expect_tx(&s_bar[j], (uint32_t)(2 * SM::TILE_SW * 2));
+        uint16_t* dst = bufs + j * buf_elems;
+        const int s0 = s_begin + j * kSub;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+          for (int hb = 0; hb < HD / 64; ++hb)
+            tma_load_2d(dst + kv * SM::TILE_SW + hb * kSub * 64, &p.tm_ring, hb * 64,
+                        (kv ? row_v : row_k) + s0, &s_bar[j]);
+      }
+    }
+  } else if (!RING_F32) {
+    if (tid == 0)
+      for (int j = 0; j < n_sub; ++j) {
+        const int nk = min(kSub, s_end - (s_begin + j * kSub));
+        mbar_expect_tx(&s_bar[j], (uint32_t)nk * HD * 2 * 2);
+      }
+    __syncthreads();  // expectations before any copy can complete
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const uint16_t* r = reinterpret_cast<const uint16_t*>(p.ring);
+    for (int idx = tid; idx < n_sub * 2 * kSub; idx += blockDim.x) {
+      const int j = idx / (2 * kSub), rem = idx - j * 2 * kSub;
+      const int kv = rem / kSub, row = rem - kv * kSub;
+      const int s0 = s_begin + j * kSub, nk = min(kSub, s_end - s0);
+      uint16_t* dst = bufs + j * buf_elems + kv * SM::TILE + row * KS;
+      if (row < nk) {
+        bulk_copy(dst, r + (kv ? vbase : kbase) + (size_t)(s0 + row) * HD, HD * 2, &s_bar[j]);
+      } else {
+#pragma unroll
+        for (int d = 0; d < HD; d += 8) *reinterpret_cast<uint4*>(dst + d) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  } else {
+    const float* r = reinterpret_cast<const float*>(p.ring);
+    for (int j = 0; j < n_sub; ++j) {
+      uint16_t* kh = bufs + j * buf_elems;
+      uint16_t* vh = kh + SM::TILE;
+      uint16_t* kl = vh + SM::TILE;
+      uint16_t* vl = kl + SM::TILE;
+      const int s0 = s_begin + j * kSub, nk = min(kSub, s_end - s0);
+      for (int idx = tid; idx < kSub * (HD / 4); idx += blockDim.x) {
+        const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+        float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+        if (row < nk) {
+          kv = *reinterpret_cast<const float4*>(r + kbase + (size_t)(s0 + row) * HD + d);
+          vv = *reinterpret_cast<const float4*>(r + vbase + (size_t)(s0 + row) * HD + d);
+        }
+        uint2 h, l;
+        split_bf16x2(kv.x, kv.y, h.x, l.x);
+        split_bf16x2(kv.z, kv.w, h.y, l.y);
+        *reinterpret_cast<uint2*>(kh + row * KS + d) = h;
+        *reinterpret_cast<uint2*>(kl + row * KS + d) = l;
+        split_bf16x2(vv.x, vv.y, h.x, l.x);
+        split_bf16x2(vv.z, vv.w, h.y, l.y);
+        *reinterpret_cast<uint2*>(vh + row * KS + d) = h;
+        *reinterpret_cast<uint2*>(vl + row * KS + d) = l;
+      }
+    }
+  }
+
+  // independent loads: this warp's q rows, the block's keys (split 0), slot positions
+  float2 qraw[HD / 16][4];
+  {
+    const float* qr0 = p.q + (size_t)(seq * kBlock + g) * qd + (head0 + hl) * HD;
+    const float* qr1 = qr0 + (size_t)8 * qd;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      const int k0 = ks * 16 + 2 * t;
+      qraw[ks][0] = *reinterpret_cast<const float2*>(qr0 + k0);
+      qraw[ks][1] = *reinterpret_cast<const float2*>(qr1 + k0);
+      qraw[ks][2] = *reinterpret_cast<const float2*>(qr0 + k0 + 8);
+      qraw[ks][3] = *reinterpret_cast<const float2*>(qr1 + k0 + 8);
+    }
+  }
+  if (split == 0) {  // the block's own 16 keys (fp32: split hi/lo), <= 4 float4 per thread a pass
+    constexpr int kBlkPer = 4, n = kBlock * (HD / 4);
+    for (int base = 0; base < n; base += kBlkPer * (int)blockDim.x) {
+      float4 kr[kBlkPer], vr[kBlkPer];
+#pragma unroll
+      for (int u = 0; u < kBlkPer; ++u) {
+        const int idx = base + u * (int)blockDim.x + tid;
+        kr[u] = vr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (idx < n) {
+          const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+          const size_t o = (size_t)(seq * kBlock + row) * kvd + kvh * HD + d;
+          kr[u] = *reinterpret_cast<const float4*>(p.kblk + o);
+          vr[u] = *reinterpret_cast<const float4*>(p.vblk + o);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBlkPer; ++u) {
+        const int idx = base + u * (int)blockDim.x + tid;
+        if (idx >= n) continue;
+        const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+        uint2 h, l;
+        split_bf16x2(kr[u].x, kr[u].y, h.x, l.x);
+        split_bf16x2(kr[u].z, kr[u].w, h.y, l.y);
+        *reinterpret_cast<uint2*>(blk_k_hi + row * KS + d) = h;
+        *reinterpret_cast<uint2*>(blk_k_lo + row * KS + d) = l;
+        split_bf16x2(vr[u].x, vr[u].y, h.x, l.x);
+        split_bf16x2(vr[u].z, vr[u].w, h.y, l.y);
+        *reinterpret_cast<uint2*>(blk_v_hi + row * KS + d) = h;
+        *reinterpret_cast<uint2*>(blk_v_lo + row * KS + d) = l;
+      }
+    }
+  }
+  for (int idx = tid; idx < kq * kSub; idx += blockDim.x) {
+    const int j = idx / kSub, row = idx - j * kSub, s = s_begin + j * kSub + row;
+    kpos[idx] = j < n_sub && s < s_end ? p.ring_pos[(size_t)seq * p.window + s] : -1;
+  }
+  uint32_t qh[HD / 16][4], ql[HD / 16][4];
+  const float qscale = p.scale * kLog2e;
+#pragma unroll
+  for (int ks = 0; ks < HD / 16; ++ks)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      split_bf16x2(qraw[ks][e].x * qscale, qraw[ks][e].y * qscale, qh[ks][e], ql[ks][e]);
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  float O[HD / 8][4];
+#pragma unroll
+  for (int jd = 0; jd < HD / 8; ++jd) O[jd][0] = O[jd][1] = O[jd][2] = O[jd][3] = 0.f;
+  __syncthreads();  // zero-filled rows, fp32 tiles, block keys and slot positions
+  if (split == 0 && lk == n_sub % kq)
+    attend_tile<HD, true>(qh, ql, blk_k_hi, blk_k_lo, blk_v_hi, blk_v_lo, KS, 2, nullptr, true, p0,
+                          p.window, p.block_width, m0, m1, l0, l1, O, lane);
+  if (lk < n_sub) {
+    if (!RING_F32 && !mbar_wait(&s_bar[lk], 0)) {
+      if (lane == 0) atomicOr(p.status, 0x4u);
+      mbar_wait(&s_bar[lk], 0);  // a second bounded wait before moving on
+    }
+    // row 0 has the widest window: a sub-chunk with no key for it has none for any row
+    const int* kp = kpos + lk * kSub;
+    const int ka = kp[lane], kb = kp[lane + 32];
+    const bool any = __any_sync(0xffffffffu, (ka >= 0 && ka < p0 && p0 - ka < p.window) ||
+                                                 (kb >= 0 && kb < p0 && p0 - kb < p.window));
+    if (any) {
+      const uint16_t* kh = bufs + lk * buf_elems;
+      if (TMA)
+        attend_tile<HD, false, true>(qh, ql, kh, nullptr, kh + SM::TILE_SW, nullptr, KS, 8, kp, false,
+                                     p0, p.window, 16, m0, m1, l0, l1, O, lane);
+      else
+        attend_tile<HD, RING_F32>(qh, ql, kh, kh + 2 * SM::TILE, kh + SM::TILE, kh + 3 * SM::TILE, KS,
+                                  8, kp, false, p0, p.window, 16, m0, m1, l0, l1, O, lane);
+    }
+  }
+  __syncthreads();  // the staging buffers become the key-lane merge area
+
+  // key lanes 1.. hand their (max, sum, O) fragments to key lane 0 through
+  // shared memory; it merges them in lane order and publishes the CTA's rows
+  float4* frag_o = reinterpret_cast<float4*>(sm_raw);                 // [warps][HD/8][32]
+  float4* frag_ml = frag_o + (size_t)nwarps * (HD / 8) * 32;          // [warps][32]
+  if (lk > 0) {
+#pragma unroll
+    for (int jd = 0; jd < HD / 8; ++jd)
+      frag_o[((size_t)warp * (HD / 8) + jd) * 32 + lane] = make_float4(O[jd][0], O[jd][1], O[jd][2], O[jd][3]);
+    frag_ml[warp * 32 + lane] = make_float4(m0, m1, l0, l1);
+  }
+  __syncthreads();
+  const size_t part0 = ((size_t)group * n_split + split) * R;   // this CTA's first partial row
+  if (lk == 0) {
+    for (int q = 1; q < kq; ++q) {
+      const int w = warp + q;
+      const float4 ml = frag_ml[w * 32 + lane];
+      const float n0 = fmaxf(m0, ml.x), n1 = fmaxf(m1, ml.y);
+      const float a0 = m0 == -CUDART_INF_F ? 0.f : exp2f(m0 - n0);
+      const float b0 = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - n0);
+      const float a1 = m1 == -CUDART_INF_F ? 0.f : exp2f(m1 - n1);
+      const float b1 = ml.y == -CUDART_INF_F ? 0.f : exp2f(ml.y - n1);
+      m0 = n0;
+      m1 = n1;
+      l0 = a0 * l0 + b0 * ml.z;
+      l1 = a1 * l1 + b1 * ml.w;
+#pragma unroll
+      for (int jd = 0; jd < HD / 8; ++jd) {
+        const float4 v = frag_o[((size_t)w * (HD / 8) + jd) * 32 + lane];
+        O[jd][0] = a0 * O[jd][0] + b0 * v.x;
+        O[jd][1] = a0 * O[jd][1] + b0 * v.y;
+        O[jd][2] = a1 * O[jd][2] + b1 * v.z;
+        O[jd][3] = a1 * O[jd][3] + b1 * v.w;
+      }
+    }
+    float* o0 = p.part_o + (part0 + hl * kBlock + g) * HD;
+    float* o1 = o0 + (size_t)8 * HD;
+#pragma unroll
+    for (int jd = 0; jd < HD / 8; ++jd) {
+      __stcg(reinterpret_cast<float2*>(o0 + 8 * jd + 2 * t), make_float2(O[jd][0], O[jd][1]));
+      __stcg(reinterpret_cast<float2*>(o1 + 8 * jd + 2 * t), make_float2(O[jd][2], O[jd][3]));
+    }
+    if (t == 0) {
+      __stcg(p.part_ml + part0 + hl * kBlock + g, make_float2(m0, l0));
+      __stcg(p.part_ml + part0 + hl * kBlock + g + 8, make_float2(m1, l1));
+    }
+  }
+  // arrive (release: every thread's partial stores are ordered before it by the
+  // barrier), then wait until the group's n_split CTAs have arrived (acquire)
+  __syncthreads();
+  int* arrive = p.counters + 2 * group;
+  if (tid == 0) {
+    atom_add_release_gpu(arrive, 1);
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(arrive) < n_split) {
+      if (clock64() - t0 > 4000000000LL) {
+        atomicOr(p.status, 0x4u);
+        break;
+      }
+    }
+  }
+  __syncthreads();
+
+  // merge rows split, split + n_split, ... of the group: one warp per row, lane
+  // c holds split c's (m, l), every lane four output dims
+  for (int r = split + warp * n_split; r < R; r += nwarps * n_split) {
+    const size_t row0 = (size_t)group * n_split * R + r;           // split 0's copy of row r
+    float2 ml = make_float2(-CUDART_INF_F, 0.f);
+    if (lane < n_split) ml = __ldcg(p.part_ml + row0 + (size_t)lane * R);
+    const float M = warp_max(ml.x);
+    const float wgt = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
+    const float L = warp_sum(wgt * ml.y);
+    const int d = lane * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int kB = 8;
+    for (int c0 = 0; c0 < n_split; c0 += kB) {
+      float4 v[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        v[u] = c0 + u < n_split && d < HD
+                   ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (row0 + (size_t)(c0 + u) * R) * HD + d))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const float wc = __shfl_sync(0xffffffffu, wgt, (c0 + u) & 31);   // splits in order
+        if (c0 + u < n_split) {
+          acc.x += wc * v[u].x;
+          acc.y += wc * v[u].y;
+          acc.z += wc * v[u].z;
+          acc.w += wc * v[u].w;
+        }
+      }
+    }
+    if (d < HD) {
+      const int h = r / kBlock, i = r - h * kBlock;
+      const float inv = 1.f / L;
+      const size_t at = (size_t)(seq * kBlock + i) * qd + (head0 + h) * HD + d;
+      uint2 hi, lo;
+      split_pair16x2(acc.x * inv, acc.y * inv, p.pair_f16 != 0, hi.x, lo.x);
+      split_pair16x2(acc.z * inv, acc.w * inv, p.pair_f16 != 0, hi.y, lo.y);
+      *reinterpret_cast<uint2*>(p.out_hi + at) = hi;
+      *reinterpret_cast<uint2*>(p.out_lo + at) = lo;
+    }
+  }
+  // the group's last CTA past its merge resets both counters for the next launch
+  __syncthreads();
+  if (tid == 0) {
+    s_last = atom_add_acq_rel_gpu(arrive + 1, 1) == n_split - 1;
+    if (s_last) {
+      arrive[0] = 0;
+      arrive[1] = 0;
+    }
+    stamp_finish(p.stamp);
+  }
+}
+
 int attn_cluster_size(int window) {
   int cl = (window + 255) / 256;
   return cl < 1 ? 1 : (cl > kMaxCluster ? kMaxCluster : cl);
@@ -849,6 +1198,130 @@ cudaError_t launch_attention_cluster(const AttnParams& p, int n_seq, cudaStream_
     case 32: return f32 ? launch_cl<32, true>(p, n_seq, st) : launch_cl<32, false>(p, n_seq, st);
     case 64: return f32 ? launch_cl<64, true>(p, n_seq, st) : launch_cl<64, false>(p, n_seq, st);
     case 128: return f32 ? launch_cl<128, true>(p, n_seq, st) : launch_cl<128, false>(p, n_seq, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// ---- split-window launch plan: kq = 2 key lanes (128 slots per CTA), up to 4
+// query heads of the kv group per CTA
+struct SplitPlan {
+  int hpc, kq, n_split;
+};
+inline SplitPlan split_plan(int G, int window) {
+  SplitPlan s;
+  s.kq = 2;
+  s.hpc = G % 4 == 0 ? 4 : G % 2 == 0 ? 2 : 1;
+  s.n_split = (window + s.kq * kSub - 1) / (s.kq * kSub);
+  return s;
+}
+template <int HD>
+static size_t split_smem_of(bool f32, const SplitPlan& s) {
+  using SM = AttnSmem<HD>;
+  const size_t stage = (size_t)s.kq * SM::buf_elems(f32) * 2 + (size_t)SM::BLK * 2 +
+                       (size_t)s.kq * kSub * 4 + (SM::kTma && !f32 ? 1024 : 0);
+  const int warps = s.hpc * s.kq;
+  const size_t merge = (size_t)warps * (HD / 8) * 32 * 16 + (size_t)warps * 32 * 16;
+  return (stage > merge ? stage : merge) + 256;
+}
+static size_t split_smem_hd(int hd, bool f32, const SplitPlan& s) {
+  switch (hd) {
+    case 32: return split_smem_of<32>(f32, s);
+    case 64: return split_smem_of<64>(f32, s);
+    default: return split_smem_of<128>(f32, s);
+  }
+}
+size_t attn_split_smem(int group, int hd, int ring_f32) {
+  return split_smem_hd(hd, ring_f32 != 0, split_plan(group, 64));
+}
+
+// CTAs of the split kernel the GPU holds at once, measured with the occupancy
+// API when a handle is created (launches, also under capture, read the table)
+struct SplitCap {
+  const void* fn;
+  int threads;
+  size_t smem;
+  int ctas;
+};
+static std::vector<SplitCap> g_split_cap;
+
+template <int HD, bool F32>
+static int split_capacity(const SplitPlan& s, bool query) {
+  const void* fn = reinterpret_cast<const void*>(attn_split_kernel<HD, F32>);
+  const int threads = 32 * s.hpc * s.kq;
+  const size_t smem = split_smem_of<HD>(F32, s);
+  std::lock_guard<std::mutex> lk(g_occ_mu);
+  for (const SplitCap& c : g_split_cap)
+    if (c.fn == fn && c.threads == threads && c.smem == smem) return c.ctas;
+  if (!query) return 0;
+  int per_sm = 0, dev = 0, n_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_split_kernel<HD, F32>, threads, smem) !=
+          cudaSuccess ||
+      cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    per_sm = 0;
+  }
+  g_split_cap.push_back(SplitCap{fn, threads, smem, per_sm * n_sm});
+  return per_sm * n_sm;
+}
+
+template <int HD, bool F32>
+static cudaError_t configure_split(int G, int window) {
+  static size_t configured = 0;   // only ever raised, so every live handle still fits
+  const SplitPlan s = split_plan(G, window);
+  const size_t smem = split_smem_of<HD>(F32, s);
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<HD, F32>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  (void)split_capacity<HD, F32>(s, true);
+  return cudaSuccess;
+}
+
+cudaError_t configure_attention(int group, int hd, int ring_f32, int window, int n_head_kv) {
+  cudaError_t e = configure_attention_cluster(group, hd, ring_f32, window, n_head_kv);
+  if (e != cudaSuccess) return e;
+  switch (hd) {
+    case 32: return ring_f32 ? configure_split<32, true>(group, window) : configure_split<32, false>(group, window);
+    case 64: return ring_f32 ? configure_split<64, true>(group, window) : configure_split<64, false>(group, window);
+    case 128: return ring_f32 ? configure_split<128, true>(group, window) : configure_split<128, false>(group, window);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int HD, bool F32>
+static cudaError_t launch_split_or_cluster(const AttnParams& p_in, int n_seq, cudaStream_t st) {
+  const int G = p_in.n_head / p_in.n_head_kv;
+  const SplitPlan s = split_plan(G, p_in.window);
+  const long long grid = (long long)n_seq * p_in.n_head_kv * (G / s.hpc) * s.n_split;
+  const int cap = split_capacity<HD, F32>(s, false);
+  if (!p_in.part_o || s.n_split > kMaxSplit || grid > cap || grid > kAttnSplitMaxCtas)
+    return launch_cl<HD, F32>(p_in, n_seq, st);
+  AttnParams p = p_in;
+  p.hpc = s.hpc;
+  p.kq = s.kq;
+  p.nb = s.kq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.n_split, p.n_head_kv * (G / s.hpc), n_seq);
+  cfg.blockDim = dim3(32 * s.hpc * s.kq);
+  cfg.dynamicSmemBytes = split_smem_of<HD>(F32, s);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_split_kernel<HD, F32>, p);
+}
+
+cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st) {
+  const bool f32 = !p.ring_bf16;
+  switch (p.hd) {
+    case 32: return f32 ? launch_split_or_cluster<32, true>(p, n_seq, st) : launch_split_or_cluster<32, false>(p, n_seq, st);
+    case 64: return f32 ? launch_split_or_cluster<64, true>(p, n_seq, st) : launch_split_or_cluster<64, false>(p, n_seq, st);
+    case 128: return f32 ? launch_split_or_cluster<128, true>(p, n_seq, st) : launch_split_or_cluster<128, false>(p, n_seq, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -104,7 +104,9 @@ struct Layout {
   size_t status, inv_freq, counters, h, ss, qbuf, kblk, vblk, rope_step, am_part;
   size_t xn_hi, xn_lo, attn_hi, attn_lo, act_hi, act_lo;
   size_t logits_int, drafts_int, idl_int, npast_int, partial;
-  size_t inj_raw, inj_ss, inj_rope, inj_hi, inj_lo, loop_pos, loop_cnt, loop_H, stamps, total;
+  size_t inj_raw, inj_ss, inj_rope, inj_hi, inj_lo, loop_pos, loop_cnt, loop_H, stamps;
+  size_t attn_part, attn_ml, attn_cnt, total;
+  int attn_groups;
   size_t partial_floats;
   int n_counters, ss_parts, ss_ld, lm_tiles;
   size_t ring_seq_bytes, ring_kv_bytes, ring_total;
@@ -167,6 +169,12 @@ Layout layout(const dflash_config& c) {
   L.loop_cnt = take(sizeof(int32_t) * (size_t)g.max_seq);
   L.loop_H = take(sizeof(float) * (size_t)g.max_seq * DFLASH_BLOCK * g.d);
   L.stamps = take(sizeof(unsigned long long) * 2 * kStampSlots);
+  // split-window attention: partial rows of its largest grid, and two counters
+  // per (sequence, kv head, query head) - at least one per head group
+  L.attn_part = take(sizeof(float) * (size_t)kAttnSplitMaxCtas * kAttnPartFloats);
+  L.attn_ml = take(sizeof(float2) * (size_t)kAttnSplitMaxCtas * 64);
+  L.attn_groups = g.max_seq * g.Hq;
+  L.attn_cnt = take(sizeof(int) * 2 * (size_t)L.attn_groups);
   L.total = off;
 
   L.ring_kv_bytes = (size_t)g.L * 2 * g.Hkv * g.W * g.hd * (g.ring_bf16 ? 2 : 4);
@@ -201,7 +209,9 @@ int validate(const dflash_config* c) {
   // the attention CTA's staging must fit one SM's shared memory (227 KB per block,
   // 1 KB kept for its static barriers)
   if (attn_cluster_smem(c->n_head / c->n_head_kv, c->head_dim, c->ring_dtype == DFLASH_DTYPE_F32) >
-      232448 - 1024)
+          232448 - 1024 ||
+      attn_split_smem(c->n_head / c->n_head_kv, c->head_dim, c->ring_dtype == DFLASH_DTYPE_F32) >
+          232448 - 1024)
     return DFLASH_ERR_UNSUPPORTED;
   return DFLASH_OK;
 }
@@ -524,8 +534,11 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.tm_ring = h->tm_ring;
     a.status = h->status();
     a.block_width = h->width;
+    a.part_o = h->S<float>(L.attn_part);
+    a.part_ml = h->S<float2>(L.attn_ml);
+    a.counters = h->S<int>(L.attn_cnt);
     a.stamp = stamp_slot(h, PC_ATTN);
-    PROF(h, PC_ATTN, st, launch_attention_cluster(a, n_seq, st));
+    PROF(h, PC_ATTN, st, launch_attention(a, n_seq, st));
     // o projection + residual; next input xn = split(h * ffn_norm)
     p = base_params(h);
     set_plan(p, sh[1], n_seq);
@@ -768,6 +781,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
   cudaError_t e = cudaMemcpy(h->S<double>(h->L.inv_freq), inv, sizeof(double) * half,
                              cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.counters, 0, sizeof(int) * h->L.n_counters);
+  if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.attn_cnt, 0, sizeof(int) * 2 * h->L.attn_groups);
   if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.status, 0, sizeof(unsigned));
   // zero K/V (empty slots are masked, but p = 0 times a NaN left in reused memory
   // is NaN) and mark every slot empty
@@ -780,9 +794,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
   if (e == cudaSuccess) e = configure_gemm_umma();
   if (e == cudaSuccess && !build_maps(h)) e = cudaErrorNotSupported;
   if (e == cudaSuccess)
-    e = configure_attention_cluster(cfg->n_head / cfg->n_head_kv, cfg->head_dim,
-                                    cfg->ring_dtype == DFLASH_DTYPE_F32, cfg->window,
-                                    cfg->n_head_kv);
+    e = configure_attention(cfg->n_head / cfg->n_head_kv, cfg->head_dim,
+                            cfg->ring_dtype == DFLASH_DTYPE_F32, cfg->window, cfg->n_head_kv);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {

@@ -372,66 +372,105 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // One thread issues every copy, so its per-chunk work stays a handful of
+    // instructions: two cursors walk the CTA's chunks (the weights' one ahead
+    // of the activations' one during the prologue) with one division per item.
     if (lane != 0) return;
     const uint64_t w_policy = policy_evict_first();
-    long long it = 0;
-    bool waited = false;
-    for (long long u = ub0; u < ub1 && !s_abort;) {
-      const int item = (int)(u / p.cpt);
-      const int c0 = (int)(u - (long long)item * p.cpt);
-      const int c1 = (int)min((long long)p.cpt, c0 + (ub1 - u));
-      u += c1 - c0;
-      const int tile = item / p.n_mb, mb = item - tile * p.n_mb;
-      int gmap[8], grow[8];
-#pragma unroll
-      for (int grp = 0; grp < 8; ++grp) group_coord(p, tile, grp, gmap[grp], grow[grp]);
-      for (int c = c0; c < c1; ++c, ++it) {
-        const int st = (int)(it % T::S);
-        const uint32_t ph = (uint32_t)((it / T::S) & 1);
-        if (!mbar_wait(&empty[st], ph ^ 1)) {
-          atomicOr(p.status, 0x4u);
-          s_abort = 1;
-          break;
+    const long long n = ub1 - ub0;   // k chunks of this CTA
+    struct Cursor {
+      int item, c, tile, mb;
+    };
+    auto start = [&](Cursor& q) {
+      q.item = (int)(ub0 / p.cpt);
+      q.c = (int)(ub0 - (long long)q.item * p.cpt);
+      q.tile = q.item / p.n_mb;
+      q.mb = q.item - q.tile * p.n_mb;
+    };
+    auto advance = [&](Cursor& q) {
+      if (++q.c == p.cpt) {
+        q.c = 0;
+        ++q.item;
+        if (++q.mb == p.n_mb) {
+          q.mb = 0;
+          ++q.tile;
         }
-        uint8_t* dst = sm + st * Lt::STAGE;
-        const int k = c * T::CK;
-        mbar_expect_tx(&full[st], stage_bytes);
-        if (T::WBOXES == 1 && p.w64) {
-          // four 16-row groups of one segment with consecutive rows are one
-          // 64-row box (the same swizzled layout as four stacked 16-row
-          // boxes): fewer, larger copies
+      }
+    };
+    Cursor cw, cx;
+    start(cw);
+    start(cx);
+    int gmap[8], grow[8], g_tile = -1;
+    // the weight boxes of the chunk at cursor cw into stage st (arming the
+    // stage's barrier for the whole stage)
+    auto issue_w = [&](int st) {
+      if (cw.tile != g_tile) {
 #pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {
-            const int g0 = 4 * hq;
-            if (gmap[g0 + 3] == gmap[g0] && grow[g0 + 3] == grow[g0] + 48) {
-              tma_load_hint(dst + g0 * kBox, &p.tm_w64[gmap[g0]], k, grow[g0],
-                            &full[st], w_policy);
-            } else {
+        for (int grp = 0; grp < 8; ++grp) group_coord(p, cw.tile, grp, gmap[grp], grow[grp]);
+        g_tile = cw.tile;
+      }
+      uint8_t* dst = sm + st * Lt::STAGE;
+      const int k = cw.c * T::CK;
+      mbar_expect_tx(&full[st], stage_bytes);
+      if (T::WBOXES == 1 && p.w64) {
+        // four 16-row groups of one segment with consecutive rows are one
+        // 64-row box (the same swizzled layout as four stacked 16-row boxes):
+        // fewer, larger copies
 #pragma unroll
-              for (int grp = g0; grp < g0 + 4; ++grp)
-                tma_load_hint(dst + grp * kBox, &p.tm_w[gmap[grp]], k, grow[grp],
-                              &full[st], w_policy);
-            }
+        for (int hq = 0; hq < 2; ++hq) {
+          const int g0 = 4 * hq;
+          if (gmap[g0 + 3] == gmap[g0] && grow[g0 + 3] == grow[g0] + 48) {
+            tma_load_hint(dst + g0 * kBox, &p.tm_w64[gmap[g0]], k, grow[g0], &full[st], w_policy);
+          } else {
+#pragma unroll
+            for (int grp = g0; grp < g0 + 4; ++grp)
+              tma_load_hint(dst + grp * kBox, &p.tm_w[gmap[grp]], k, grow[grp], &full[st], w_policy);
           }
-        } else {
-#pragma unroll
-          for (int grp = 0; grp < 8; ++grp)
-#pragma unroll
-            for (int wb = 0; wb < T::WBOXES; ++wb)
-              tma_load_hint(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]],
-                            k + wb * T::WBOX_K, grow[grp], &full[st], w_policy);
         }
-        if (!waited) {  // activations may come from the previous kernel
-          pdl_wait();
-          waited = true;
-        }
+      } else {
 #pragma unroll
-        for (int xb = 0; xb < T::XBOXES; ++xb) {
-          tma_load(dst + Lt::W_BYTES + xb * kBox, &p.tm_xh, k + xb * 64, mb * 16, &full[st]);
-          if (has_lo)
-            tma_load(dst + Lt::W_BYTES + Lt::X_BYTES + xb * kBox, &p.tm_xl, k + xb * 64, mb * 16,
-                     &full[st]);
-        }
+        for (int grp = 0; grp < 8; ++grp)
+#pragma unroll
+          for (int wb = 0; wb < T::WBOXES; ++wb)
+            tma_load_hint(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]],
+                          k + wb * T::WBOX_K, grow[grp], &full[st], w_policy);
+      }
+      advance(cw);
+    };
+    // the activation boxes (hi, lo) of the chunk at cursor cx into stage st
+    auto issue_x = [&](int st) {
+      uint8_t* dst = sm + st * Lt::STAGE;
+      const int k = cx.c * T::CK;
+#pragma unroll
+      for (int xb = 0; xb < T::XBOXES; ++xb) {
+        tma_load(dst + Lt::W_BYTES + xb * kBox, &p.tm_xh, k + xb * 64, cx.mb * 16, &full[st]);
+        if (has_lo)
+          tma_load(dst + Lt::W_BYTES + Lt::X_BYTES + xb * kBox, &p.tm_xl, k + xb * 64, cx.mb * 16,
+                   &full[st]);
+      }
+      advance(cx);
+    };
+    // Weights do not depend on the previous kernel: every stage's weight boxes
+    // go out before the dependency wait, so the stream is already in flight
+    // when the activations become readable; then those stages' activations.
+    const int pre = n < T::S ? (int)n : T::S;
+    for (int j = 0; j < pre; ++j) issue_w(j);
+    pdl_wait();
+    for (int j = 0; j < pre; ++j) issue_x(j);
+    long long it = pre;
+    int st = pre % T::S;
+    uint32_t ph = pre / T::S;   // 0 or 1: the parity of chunk `it`'s stage round
+    for (; it < n && !s_abort; ++it) {
+      if (!mbar_wait(&empty[st], (ph & 1) ^ 1)) {
+        atomicOr(p.status, 0x4u);
+        s_abort = 1;
+        break;
+      }
+      issue_w(st);
+      issue_x(st);
+      if (++st == T::S) {
+        st = 0;
+        ++ph;
       }
     }
     if (p.pf_count > 0) prefetch_share(p, b, G);

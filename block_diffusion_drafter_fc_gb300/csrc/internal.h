@@ -165,7 +165,18 @@ struct AttnParams {
   unsigned* status;       // device status bits (DFLASH_DEV_TIMEOUT on a copy that never lands)
   int block_width;        // block rows that exist (2..16): block keys at or past it are masked
   unsigned long long* stamp;  // launch timestamp slot (profiling captures), else null
+  // split-window kernel: partial rows [CTA][16 hpc][hd] (+ (max, sum) per row) of
+  // at most kAttnSplitMaxCtas CTAs, and two counters per (sequence, kv head, head
+  // group), zero between launches (null: the cluster kernel always)
+  float* part_o;
+  float2* part_ml;
+  int* counters;
 };
+
+// split-window attention: largest grid (CTAs) it is launched with, and the
+// largest rows x head_dim of one CTA's partial (16 rows x 4 heads x 128)
+constexpr int kAttnSplitMaxCtas = 512;
+constexpr int kAttnPartFloats = 64 * 128;
 
 size_t gemm_smem_bytes(int wt, int xk);
 cudaError_t configure_gemm(int xk_max);
@@ -195,6 +206,12 @@ int attn_cluster_size(int window);
 size_t attn_cluster_smem(int group, int hd, int ring_f32);
 cudaError_t configure_attention_cluster(int group, int hd, int ring_f32, int window, int n_head_kv);
 cudaError_t launch_attention_cluster(const AttnParams& p, int n_seq, cudaStream_t st);
+// split-window kernel when the grid fits on the GPU at once (and p.part_o is
+// set), else the cluster kernel
+cudaError_t configure_attention(int group, int hd, int ring_f32, int window, int n_head_kv);
+cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st);
+// dynamic shared memory of the split-window kernel for this geometry
+size_t attn_split_smem(int group, int hd, int ring_f32);
 
 cudaError_t launch_embed(const void* tok_embd, int dense_bf16, int n_embd, int n_vocab,
                          int mask_token, const int32_t* id_last, const int32_t* n_past, int n_seq,

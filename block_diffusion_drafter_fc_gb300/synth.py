@@ -191,9 +191,21 @@ RAGGED_FP4 = DraftConfig(
     name="ragged_fp4", n_layer=1, n_embd=256, n_head=8, n_head_kv=1, head_dim=32,
     n_ff=512, window=64, n_vocab=333, weight_dtype="fp4", dense_dtype="bf16",
     ring_dtype="bf16", n_seq=2, fill_lo=20, fill_hi=64, offset_hi=500, seed=2010)
+# windows of several 128-slot attention splits: a ragged last split, partly
+# filled and wrapped rings (bf16, two query heads per kv head), and an fp32 ring
+# with head_dim 128 and four query heads per kv head, injected past the window
+SPLIT_BF16 = DraftConfig(
+    name="split_bf16", n_layer=1, n_embd=256, n_head=4, n_head_kv=2, head_dim=64,
+    n_ff=512, window=448, n_vocab=700, weight_dtype="bf16", dense_dtype="bf16",
+    ring_dtype="bf16", n_seq=2, fill_lo=100, fill_hi=448, offset_hi=3000, seed=2011)
+SPLIT_F32 = DraftConfig(
+    name="split_f32", n_layer=1, n_embd=512, n_head=8, n_head_kv=2, head_dim=128,
+    n_ff=512, window=320, n_vocab=600, weight_dtype="f32", dense_dtype="f32",
+    ring_dtype="f32", inject=((0, 320), (320, 50)), seed=2012)
 TEST_CONFIGS: Dict[str, DraftConfig] = {c.name: c for c in (RAGGED, SMALL_FP8, MIXED_F32, DENSE_FP8,
                                                             DENSE_BF16, WIDE_FP8, WIDE_BF16, MANY_SEQ,
-                                                            SMALL_FP4, RAGGED_FP4)}
+                                                            SMALL_FP4, RAGGED_FP4, SPLIT_BF16,
+                                                            SPLIT_F32)}
 
 
 def get_config(name: str) -> DraftConfig:

@@ -23,7 +23,8 @@ import oracle_bridge as OB
 pytestmark = pytest.mark.gpu
 
 SMALL = ["tiny_f32", "ragged_bf16", "mixed_f32w_bf16ring", "small_fp8", "dense_fp8", "dense_bf16",
-         "wide_fp8", "wide_bf16", "many_seq_bf16", "small_fp4", "ragged_fp4"]
+         "wide_fp8", "wide_bf16", "many_seq_bf16", "small_fp4", "ragged_fp4", "split_bf16",
+         "split_f32"]
 
 
 @functools.lru_cache(maxsize=None)
