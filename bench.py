@@ -106,13 +106,18 @@ def class_bytes(cfg, wl):
     def wb(name):
         return wl.weights[name].nbytes()
     L = cfg.n_layer
-    return {
+    out = {
         "qkv": sum(wb(f"l{i}.{n}") for i in range(L) for n in ("wq", "wk", "wv")) / L,
         "o_proj": sum(wb(f"l{i}.wo") for i in range(L)) / L,
         "gate_up": sum(wb(f"l{i}.{n}") for i in range(L) for n in ("gate", "up")) / L,
         "down": sum(wb(f"l{i}.down") for i in range(L)) / L,
         "lm_head": wb("lm_head") + cfg.n_seq * 16 * cfg.n_vocab * 4,
     }
+    # a projection chain (one launch per layer: o, gate/up, down, then the next
+    # layer's q/k/v or the LM head) streams every layer's weights but layer 0's q/k/v
+    out["chain"] = (L * (out["o_proj"] + out["gate_up"] + out["down"]) + (L - 1) * out["qkv"]
+                    + out["lm_head"]) / L
+    return out
 
 
 def class_rates(cfg, wl, prof):
@@ -253,7 +258,7 @@ def timed_replays(dr, stream, traffic, steps):
     return [a.elapsed_time(b) for a, b in ev]
 
 
-PROJ = ("qkv", "o_proj", "gate_up", "down", "lm_head")
+PROJ = ("qkv", "o_proj", "gate_up", "down", "lm_head", "chain")
 
 
 def graph_breakdown(dr, stream, traffic, replays):
@@ -378,7 +383,7 @@ def roofline_of(cfg, wl, prof, graph_span):
     """Roofline of the dominant kernel class: algorithmic bytes (or flops) per
     launch over its mean event-timed launch duration."""
     cb = class_bytes(cfg, wl)
-    dom = max(cb, key=lambda k: prof[k][0])
+    dom = max(cb, key=lambda k: prof.get(k, (0.0, 0))[0])
     dom_ms, dom_n = prof[dom]
     peak, peak_src = peaks()
     rows = 16 * cfg.n_seq

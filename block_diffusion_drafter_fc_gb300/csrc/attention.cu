@@ -750,7 +750,9 @@ __global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constan
   if (tid == 0) stamp_begin(p.stamp);
   __syncthreads();
   pdl_trigger();
-  pdl_wait();
+  // the ring, its slot positions and n_past were written before the step's
+  // first kernel (launched without overlap): they are read, and the ring staged,
+  // before the wait for the q/k/v kernel
   const int p0 = max(p.n_past[seq], 0);
   const int SL = kq * kSub;
   const int s_begin = min(p.window, split * SL), s_end = min(p.window, s_begin + SL);
@@ -824,7 +826,12 @@ __global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constan
     }
   }
 
-  // independent loads: this warp's q rows, the block's keys (split 0), slot positions
+  for (int idx = tid; idx < kq * kSub; idx += blockDim.x) {
+    const int j = idx / kSub, row = idx - j * kSub, s = s_begin + j * kSub + row;
+    kpos[idx] = j < n_sub && s < s_end ? p.ring_pos[(size_t)seq * p.window + s] : -1;
+  }
+  pdl_wait();   // q and the block's keys come from the q/k/v kernel
+  // independent loads: this warp's q rows, the block's keys (split 0)
   float2 qraw[HD / 16][4];
   {
     const float* qr0 = p.q + (size_t)(seq * kBlock + g) * qd + (head0 + hl) * HD;
@@ -869,10 +876,6 @@ __global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constan
         *reinterpret_cast<uint2*>(blk_v_lo + row * KS + d) = l;
       }
     }
-  }
-  for (int idx = tid; idx < kq * kSub; idx += blockDim.x) {
-    const int j = idx / kSub, row = idx - j * kSub, s = s_begin + j * kSub + row;
-    kpos[idx] = j < n_sub && s < s_end ? p.ring_pos[(size_t)seq * p.window + s] : -1;
   }
   uint32_t qh[HD / 16][4], ql[HD / 16][4];
   const float qscale = p.scale * kLog2e;

@@ -105,8 +105,9 @@ struct Layout {
   size_t xn_hi, xn_lo, attn_hi, attn_lo, act_hi, act_lo;
   size_t logits_int, drafts_int, idl_int, npast_int, partial;
   size_t inj_raw, inj_ss, inj_rope, inj_hi, inj_lo, loop_pos, loop_cnt, loop_H, stamps;
-  size_t attn_part, attn_ml, attn_cnt, total;
-  int attn_groups;
+  size_t attn_part, attn_ml, attn_cnt, chain_partial, chain_cnt, chain_item, chain_mb, chain_done;
+  size_t total;
+  int attn_groups, chain_item_stride;
   size_t partial_floats;
   int n_counters, ss_parts, ss_ld, lm_tiles;
   size_t ring_seq_bytes, ring_kv_bytes, ring_total;
@@ -175,6 +176,16 @@ Layout layout(const dflash_config& c) {
   L.attn_ml = take(sizeof(float2) * (size_t)kAttnSplitMaxCtas * 64);
   L.attn_groups = g.max_seq * g.Hq;
   L.attn_cnt = take(sizeof(int) * 2 * (size_t)L.attn_groups);
+  // projection chains: per phase its partial tiles and tickets, item flags and
+  // per-block counts; one chain counter
+  L.chain_partial = take(sizeof(float) * (size_t)kChainMax * 2 * kGemmGrid * 16 * kTileRows);
+  L.chain_cnt = take(sizeof(int) * (size_t)kChainMax * L.n_counters);
+  int items = 0;
+  for (auto& s : ss_) items = std::max(items, g.max_seq * s.n_tiles);
+  L.chain_item_stride = items;
+  L.chain_item = take(sizeof(int) * (size_t)kChainMax * items);
+  L.chain_mb = take(sizeof(int) * (size_t)kChainMax * g.max_seq);
+  L.chain_done = take(sizeof(int));
   L.total = off;
 
   L.ring_kv_bytes = (size_t)g.L * 2 * g.Hkv * g.W * g.hd * (g.ring_bf16 ? 2 : 4);
@@ -263,6 +274,9 @@ struct dflash_handle {
   cudaGraphExec_t loop_execs[DFLASH_BLOCK + 1] = {};
   int width = DFLASH_BLOCK;   // block rows of step / accept / advance / capture
   char err[512];
+  // 16-row steps may chain their projections (o, gate/up, down, next q/k/v) per
+  // layer (dflash_set_chain) when the device holds the chain's grid at once (chain_ok)
+  bool chain = false, chain_ok = false;
   // launch-class profiling: events around eager calls (prof), or device
   // timestamps of every step launch, eager or captured (stamps)
   bool prof = false;
@@ -349,7 +363,7 @@ bool make_map(CUtensorMap* m, const void* base, int wt, uint64_t cols, uint64_t 
 
 enum ProfClass {
   PC_EMBED = 0, PC_QKV, PC_ATTN, PC_MERGE, PC_O, PC_GATEUP, PC_DOWN, PC_LM, PC_ENCODE, PC_INJECT,
-  PC_ACCEPT
+  PC_ACCEPT, PC_CHAIN
 };
 
 cudaEvent_t prof_event(dflash_handle* h) {
@@ -438,13 +452,14 @@ void set_tma_inputs(GemmParams& p, const CUtensorMap* x) {
   p.x_mode = X_BF16;
 }
 
-// Launch one step projection: the tcgen05 kernel for >= 128 activation rows (its
-// own maps, 64-wide k chunks), else the 16-row TMA kernel.  Weight maps: layer l,
-// matrices wi[0..nw) (l < 0: the LM head); activations: pair xi (0 xn, 1 attn, 2 act).
+// Bind a step projection to its tensor maps: the tcgen05 kernel's for >= 128
+// activation rows (its own maps, 64-wide k chunks), else the 16-row kernels'.
+// Weight maps: layer l, matrices wi[0..nw) (l < 0: the LM head); activations:
+// pair xi (0 xn, 1 attn, 2 act).  launch_bound launches it on its kernel.
 enum { XP_XN = 0, XP_ATTN = 1, XP_ACT = 2 };
 
-cudaError_t launch_projection(const dflash_handle* h, GemmParams& p, int l,
-                              std::initializer_list<int> wi, int xi, cudaStream_t st) {
+void bind_projection(const dflash_handle* h, GemmParams& p, int l, std::initializer_list<int> wi,
+                     int xi) {
   const bool dense = h->dense && p.M >= 128;
   const CUtensorMap* xs[3] = {dense ? h->td_xn : h->tm_xn, dense ? h->td_attn : h->tm_attn,
                               dense ? h->td_act : h->tm_act};
@@ -461,9 +476,13 @@ cudaError_t launch_projection(const dflash_handle* h, GemmParams& p, int l,
                         : (dense ? h->td_layer[l][w] : h->tm_layer[l][w]);
   }
   p.w64 = h->g.wt == W_BF16 || h->g.wt == W_FP8 || h->g.wt == W_FP4;
+  if (dense) p.cpt = cdiv(p.K, 64);
+}
+
+cudaError_t launch_bound(const dflash_handle* h, GemmParams& p, cudaStream_t st) {
+  const bool dense = h->dense && p.M >= 128;
   if (h->g.wt == W_FP4) return launch_gemm_fp4(p, st);
   if (!dense) return launch_gemm_tma(h->g.wt, p, st);
-  p.cpt = cdiv(p.K, 64);
   return launch_gemm_umma(h->g.wt, p, st);
 }
 
@@ -494,11 +513,12 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
                                      rope, h->w.layers[0].attn_norm, xn_hi, xn_lo, g.wt == W_FP4,
                                      embed_parts(g, L), L.ss_ld, h->status(),
                                      stamp_slot(h, PC_EMBED), st));
-  int n_ss = embed_parts(g, L);
-  for (int l = 0; l < g.L; ++l) {
+  // The projections' parameters (weights, schedule, row statistics, epilogue),
+  // bound to their tensor maps by bind_projection.
+  // q/k/v of RMSNorm(h) (the 1/rms row scale after the product), per-head q/k
+  // norm + rope; n_ss partial sums of squares per row in ss
+  auto qkv_p = [&](int l, int n_ss) {
     const dflash_layer_weights& lw = h->w.layers[l];
-    // q/k/v of RMSNorm(h) (the 1/rms row scale after the product), per-head
-    // q/k norm + rope
     GemmParams p = base_params(h);
     set_plan(p, sh[0], n_seq);
     p.M = M;
@@ -510,18 +530,74 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.epi = EPI_QKV; p.out = h->S<float>(L.qbuf); p.ldo = g.qd;
     p.kblk = h->S<float>(L.kblk); p.vblk = h->S<float>(L.vblk);
     p.q_norm = lw.q_norm; p.k_norm = lw.k_norm; p.rope_cs = rope;
-    {  // this layer's ring K/V of every sequence into L2 for the attention kernel
-      const size_t layer_bytes = L.ring_kv_bytes / g.L;
-      if ((size_t)n_seq * layer_bytes <= kRingPrefetchMax) {
-        p.pf_base = h->ring + (size_t)l * layer_bytes;
-        p.pf_bytes = layer_bytes;
-        p.pf_stride = L.ring_seq_bytes;
-        p.pf_count = n_seq;
-      }
+    // this layer's ring K/V of every sequence into L2 for the attention kernel
+    const size_t layer_bytes = L.ring_kv_bytes / g.L;
+    if ((size_t)n_seq * layer_bytes <= kRingPrefetchMax) {
+      p.pf_base = h->ring + (size_t)l * layer_bytes;
+      p.pf_bytes = layer_bytes;
+      p.pf_stride = L.ring_seq_bytes;
+      p.pf_count = n_seq;
     }
-    p.stamp = stamp_slot(h, PC_QKV);
-    PROF(h, PC_QKV, st, launch_projection(h, p, l, {0, 1, 2}, XP_XN, st));
-    // attention over the ring window + the block (-> attn pair)
+    bind_projection(h, p, l, {0, 1, 2}, XP_XN);
+    return p;
+  };
+  // o projection + residual; next input xn = split(h * ffn_norm)
+  auto o_p = [&](int l) {
+    GemmParams p = base_params(h);
+    set_plan(p, sh[1], n_seq);
+    p.M = M;
+    p.seg[0] = {h->w.layers[l].wo, h->w.layers[l].wo_scale, 0, g.d};
+    p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
+    p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
+    p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d; p.pair_norm = h->w.layers[l].ffn_norm;
+    bind_projection(h, p, l, {3}, XP_ATTN);
+    return p;
+  };
+  // gate/up of RMSNorm(h) + SwiGLU -> act pair
+  auto gu_p = [&](int l) {
+    const dflash_layer_weights& lw = h->w.layers[l];
+    GemmParams p = base_params(h);
+    set_plan(p, sh[2], n_seq);
+    p.M = M;
+    p.ss = ss; p.n_ss = sh[1].n_tiles; p.ss_ld = L.ss_ld; p.row_scale = 1;
+    p.seg[0] = {lw.gate, lw.gate_scale, 0, g.F};
+    p.seg[1] = {lw.up, lw.up_scale, 0, g.F};
+    p.nseg = 2; p.N = 2 * g.F; p.map = MAP_SWIGLU;
+    p.epi = EPI_SWIGLU; p.out = nullptr;
+    p.pair_hi = h->S<uint16_t>(L.act_hi); p.pair_lo = h->S<uint16_t>(L.act_lo); p.pair_ld = g.F;
+    bind_projection(h, p, l, {4, 5}, XP_XN);
+    return p;
+  };
+  // down projection + residual; next input xn = split(h * next norm)
+  auto down_p = [&](int l) {
+    GemmParams p = base_params(h);
+    set_plan(p, sh[3], n_seq);
+    p.M = M;
+    p.seg[0] = {h->w.layers[l].down, h->w.layers[l].down_scale, 0, g.d};
+    p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
+    p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
+    p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d;
+    p.pair_norm = l + 1 < g.L ? h->w.layers[l + 1].attn_norm : h->w.out_norm;
+    bind_projection(h, p, l, {6}, XP_ACT);
+    return p;
+  };
+  // LM head of RMSNorm(h) (out_norm folded into xn by the last down projection)
+  auto lm_p = [&]() {
+    GemmParams p = base_params(h);
+    set_plan(p, sh[4], n_seq);
+    p.M = M;
+    p.ss = ss; p.n_ss = sh[3].n_tiles; p.ss_ld = L.ss_ld; p.row_scale = 1;
+    p.seg[0] = {h->w.lm_head, h->w.lm_head_scale, 0, g.V};
+    p.nseg = 1; p.N = g.V; p.map = MAP_SEGMENTS;
+    p.epi = EPI_LOGITS; p.out = logits; p.ldo = g.V;
+    p.am_part = h->S<float2>(L.am_part);
+    p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
+    p.drafts = drafts;
+    p.block_width = h->width;
+    bind_projection(h, p, -1, {0}, XP_XN);
+    return p;
+  };
+  auto attention = [&](int l) -> int {
     AttnParams a;
     std::memset(&a, 0, sizeof(a));
     a.q = h->S<float>(L.qbuf); a.kblk = h->S<float>(L.kblk); a.vblk = h->S<float>(L.vblk);
@@ -539,56 +615,62 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.counters = h->S<int>(L.attn_cnt);
     a.stamp = stamp_slot(h, PC_ATTN);
     PROF(h, PC_ATTN, st, launch_attention(a, n_seq, st));
-    // o projection + residual; next input xn = split(h * ffn_norm)
-    p = base_params(h);
-    set_plan(p, sh[1], n_seq);
-    p.M = M;
-    p.seg[0] = {lw.wo, lw.wo_scale, 0, g.d};
-    p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
-    p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
-    p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d; p.pair_norm = lw.ffn_norm;
+    return DFLASH_OK;
+  };
+
+  // 16-row blocks with bf16 / fp32 / E4M3 weights: per layer one persistent
+  // launch chains o, gate/up, down and the next layer's q/k/v (the LM head
+  // after the last layer) between two attention launches
+  if (h->chain && M < 128) {
+    GemmParams p = qkv_p(0, embed_parts(g, L));
+    p.stamp = stamp_slot(h, PC_QKV);
+    PROF(h, PC_QKV, st, launch_bound(h, p, st));
+    for (int l = 0; l < g.L; ++l) {
+      int rc = attention(l);
+      if (rc != DFLASH_OK) return rc;
+      ChainParams<kChainMax> cp;
+      std::memset(&cp, 0, sizeof(cp));
+      cp.ph[0] = o_p(l);
+      cp.ph[1] = gu_p(l);
+      cp.ph[2] = down_p(l);
+      cp.ph[3] = l + 1 < g.L ? qkv_p(l + 1, sh[3].n_tiles) : lm_p();
+      cp.n_phase = kChainMax;
+      for (int k = 0; k < kChainMax; ++k) {
+        cp.ph[k].partial = h->S<float>(L.chain_partial) + (size_t)k * 2 * kGemmGrid * 16 * kTileRows;
+        cp.ph[k].counters = h->S<int>(L.chain_cnt) + (size_t)k * L.n_counters;
+      }
+      cp.item_done = h->S<int>(L.chain_item);
+      cp.all_done = h->S<int>(L.chain_mb);
+      cp.chain_done = h->S<int>(L.chain_done);
+      cp.item_stride = L.chain_item_stride;
+      cp.mb_stride = g.max_seq;
+      cp.ph[0].stamp = stamp_slot(h, PC_CHAIN);
+      PROF(h, PC_CHAIN, st, launch_gemm_chain(g.wt, cp, st));
+    }
+    return DFLASH_OK;
+  }
+
+  int n_ss = embed_parts(g, L);
+  for (int l = 0; l < g.L; ++l) {
+    GemmParams p = qkv_p(l, n_ss);
+    p.stamp = stamp_slot(h, PC_QKV);
+    PROF(h, PC_QKV, st, launch_bound(h, p, st));
+    int rc = attention(l);
+    if (rc != DFLASH_OK) return rc;
+    p = o_p(l);
     p.stamp = stamp_slot(h, PC_O);
-    PROF(h, PC_O, st, launch_projection(h, p, l, {3}, XP_ATTN, st));
-    n_ss = sh[1].n_tiles;
-    // gate/up of RMSNorm(h) + SwiGLU -> act pair
-    p = base_params(h);
-    set_plan(p, sh[2], n_seq);
-    p.M = M;
-    p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
-    p.seg[0] = {lw.gate, lw.gate_scale, 0, g.F};
-    p.seg[1] = {lw.up, lw.up_scale, 0, g.F};
-    p.nseg = 2; p.N = 2 * g.F; p.map = MAP_SWIGLU;
-    p.epi = EPI_SWIGLU; p.out = nullptr;
-    p.pair_hi = h->S<uint16_t>(L.act_hi); p.pair_lo = h->S<uint16_t>(L.act_lo); p.pair_ld = g.F;
+    PROF(h, PC_O, st, launch_bound(h, p, st));
+    p = gu_p(l);
     p.stamp = stamp_slot(h, PC_GATEUP);
-    PROF(h, PC_GATEUP, st, launch_projection(h, p, l, {4, 5}, XP_XN, st));
-    // down projection + residual; next input xn = split(h * next norm)
-    p = base_params(h);
-    set_plan(p, sh[3], n_seq);
-    p.M = M;
-    p.seg[0] = {lw.down, lw.down_scale, 0, g.d};
-    p.nseg = 1; p.N = g.d; p.map = MAP_SEGMENTS;
-    p.epi = EPI_RESID_SS; p.out = hbuf; p.ldo = g.d; p.ss_out = ss; p.ss_out_ld = L.ss_ld;
-    p.pair_hi = xn_hi; p.pair_lo = xn_lo; p.pair_ld = g.d;
-    p.pair_norm = l + 1 < g.L ? h->w.layers[l + 1].attn_norm : h->w.out_norm;
+    PROF(h, PC_GATEUP, st, launch_bound(h, p, st));
+    p = down_p(l);
     p.stamp = stamp_slot(h, PC_DOWN);
-    PROF(h, PC_DOWN, st, launch_projection(h, p, l, {6}, XP_ACT, st));
+    PROF(h, PC_DOWN, st, launch_bound(h, p, st));
     n_ss = sh[3].n_tiles;
   }
-  // LM head of RMSNorm(h) (out_norm folded into xn by the last down projection)
-  GemmParams p = base_params(h);
-  set_plan(p, sh[4], n_seq);
-  p.M = M;
-  p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
-  p.seg[0] = {h->w.lm_head, h->w.lm_head_scale, 0, g.V};
-  p.nseg = 1; p.N = g.V; p.map = MAP_SEGMENTS;
-  p.epi = EPI_LOGITS; p.out = logits; p.ldo = g.V;
-  p.am_part = h->S<float2>(L.am_part);
-  p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
-  p.drafts = drafts;
-  p.block_width = h->width;
+  GemmParams p = lm_p();
   p.stamp = stamp_slot(h, PC_LM);
-  PROF(h, PC_LM, st, launch_projection(h, p, -1, {0}, XP_XN, st));
+  PROF(h, PC_LM, st, launch_bound(h, p, st));
   return DFLASH_OK;
 }
 
@@ -782,6 +864,9 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
                              cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.counters, 0, sizeof(int) * h->L.n_counters);
   if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.attn_cnt, 0, sizeof(int) * 2 * h->L.attn_groups);
+  // chain tickets, flags and counters (contiguous: tickets, flags, counts, done)
+  if (e == cudaSuccess)
+    e = cudaMemset(h->scratch + h->L.chain_cnt, 0, h->L.chain_done + sizeof(int) - h->L.chain_cnt);
   if (e == cudaSuccess) e = cudaMemset(h->scratch + h->L.status, 0, sizeof(unsigned));
   // zero K/V (empty slots are masked, but p = 0 times a NaN left in reused memory
   // is NaN) and mark every slot empty
@@ -797,6 +882,9 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
     e = configure_attention(cfg->n_head / cfg->n_head_kv, cfg->head_dim,
                             cfg->ring_dtype == DFLASH_DTYPE_F32, cfg->window, cfg->n_head_kv);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
+  // the chain's waits need its whole grid resident at once
+  if (e == cudaSuccess && h->g.wt != W_FP4) h->chain_ok = gemm_chain_capacity(h->g.wt) >= kGemmGrid;
+  h->chain = false;   // opt-in: measured no faster than one launch per projection
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cuda_fail(h, e, "dflash_create");
@@ -1016,6 +1104,13 @@ int dflash_advance(dflash_handle* h, int32_t n_seq, const int32_t* drafts, const
     return DFLASH_ERR_INVALID_ARG;
   return run_advance(h, n_seq, drafts, targets, feats, id_last, n_past, n_ok,
                      static_cast<cudaStream_t>(stream));
+}
+
+int dflash_set_chain(dflash_handle* h, int32_t enable) {
+  if (!h || h->capturing) return DFLASH_ERR_INVALID_ARG;
+  if (enable && !h->chain_ok) return DFLASH_ERR_UNSUPPORTED;
+  h->chain = enable != 0;
+  return DFLASH_OK;
 }
 
 int dflash_set_block_width(dflash_handle* h, int32_t width) {

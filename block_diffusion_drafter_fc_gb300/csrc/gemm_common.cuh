@@ -111,13 +111,14 @@ DF_DEVICE bool segment_fixup(const GemmParams& p, float* acc_s, int item, int c0
 }
 
 // Per-row 1 / rms of the 16 activation rows of block mb from the producer's
-// per-tile sums of squares (16 threads per row, fixed-order tree).
+// per-tile sums of squares (16 threads per row, fixed-order tree).  Read from
+// L2: in a projection chain another CTA of the same launch wrote them.
 DF_DEVICE void compute_inv_rms(const GemmParams& p, float* inv_rms, int m0) {
   const int tid = threadIdx.x;
   const int m = tid >> 4, lq = tid & 15;
   float sum = 0.f;
   if (m0 + m < p.M)
-    for (int q = lq; q < p.n_ss; q += 16) sum += p.ss[(size_t)q * p.ss_ld + m0 + m];
+    for (int q = lq; q < p.n_ss; q += 16) sum += __ldcg(p.ss + (size_t)q * p.ss_ld + m0 + m);
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lq == 0) inv_rms[m] = 1.f / sqrtf(sum / (float)p.rms_len + p.eps);

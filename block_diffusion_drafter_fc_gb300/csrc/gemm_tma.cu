@@ -336,8 +336,42 @@ DF_DEVICE void prefetch_share(const GemmParams& p, int b, int G) {
   }
 }
 
-template <int WT>
-__global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __grid_constant__ GemmParams p) {
+// ------------------------------------------------------------------ chains
+
+DF_DEVICE int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+DF_DEVICE void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+DF_DEVICE void red_release_add_gpu(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+DF_DEVICE int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// This CTA's range of a phase on the weighted stream-K axis (chunk units).  A
+// phase is split over its own p.grid CTAs (no more than it has chunk units, as
+// a launch of that projection alone would be); CTAs past them sit it out.
+template <int PEN>
+DF_DEVICE void phase_range(const GemmParams& p, int b, long long& V, long long& u0, long long& u1) {
+  V = (long long)p.n_tiles * p.n_mb * (p.cpt + PEN);
+  if (b >= p.grid) {
+    u0 = u1 = 0;
+    return;
+  }
+  u0 = vsplit_unit(V * b / p.grid, p.cpt, PEN);
+  u1 = vsplit_unit(V * (b + 1) / p.grid, p.cpt, PEN);
+}
+
+template <int WT, int NPH>
+__global__ void __launch_bounds__(kGemmThreads + 64, 2)
+    gemm_tma_kernel(const __grid_constant__ ChainParams<NPH> cp) {
   using T = TT<WT>;
   using Lt = Layout<WT>;
   extern __shared__ uint8_t smem_raw[];
@@ -351,133 +385,153 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_ph = NPH == 1 ? 1 : cp.n_phase;
   if (tid == 0) {
     for (int s = 0; s < T::S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 2);   // one arrival from each producer warp
       mbar_init(&empty[s], 8);
     }
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    stamp_begin(p.stamp);
+    stamp_begin(cp.ph[0].stamp);
   }
   __syncthreads();
   pdl_trigger();
 
   const int G = gridDim.x, b = blockIdx.x;
-  const long long V = (long long)p.n_tiles * p.n_mb * (p.cpt + T::PEN);
-  const long long ub0 = vsplit_unit(V * b / G, p.cpt, T::PEN),
-                  ub1 = vsplit_unit(V * (b + 1) / G, p.cpt, T::PEN);
-  const bool has_lo = p.has_lo != 0;
-  const uint32_t stage_bytes = Lt::W_BYTES + Lt::X_BYTES * (has_lo ? 2 : 1);
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    // One thread issues every copy, so its per-chunk work stays a handful of
-    // instructions: two cursors walk the CTA's chunks (the weights' one ahead
-    // of the activations' one during the prologue) with one division per item.
+  if (warp >= 8) {
+    // ------------------------------------------------------------ producers
+    // Two producer warps, one thread each: warp 8 issues the weight boxes,
+    // warp 9 the activation boxes (the stream is issue-bound on one thread).
+    // Both walk the CTA's chunks of phase 0, 1, ... in the same order (chunk g
+    // uses stage g % S, whose "full" barrier takes one arrival from each, with
+    // the bytes it expects) and wait for the stage to be free.  Only the
+    // activation warp waits for inputs: the previous kernel (phase 0) or the
+    // previous phase's items (chains); the weight warp runs up to S chunks ahead.
     if (lane != 0) return;
+    const bool wwarp = warp == 8;
     const uint64_t w_policy = policy_evict_first();
-    const long long n = ub1 - ub0;   // k chunks of this CTA
-    struct Cursor {
-      int item, c, tile, mb;
+    int ph = 0, item = 0, c = 0, tile = 0, mb = 0;
+    long long j = 0, n = 0;
+    auto begin_phase = [&](int k) {
+      const GemmParams& p = cp.ph[k];
+      long long V, u0, u1;
+      phase_range<T::PEN>(p, b, V, u0, u1);
+      ph = k;
+      j = 0;
+      n = u1 - u0;
+      item = (int)(u0 / p.cpt);
+      c = (int)(u0 - (long long)item * p.cpt);
+      tile = item / p.n_mb;
+      mb = item - tile * p.n_mb;
     };
-    auto start = [&](Cursor& q) {
-      q.item = (int)(ub0 / p.cpt);
-      q.c = (int)(ub0 - (long long)q.item * p.cpt);
-      q.tile = q.item / p.n_mb;
-      q.mb = q.item - q.tile * p.n_mb;
-    };
-    auto advance = [&](Cursor& q) {
-      if (++q.c == p.cpt) {
-        q.c = 0;
-        ++q.item;
-        if (++q.mb == p.n_mb) {
-          q.mb = 0;
-          ++q.tile;
-        }
-      }
-    };
-    Cursor cw, cx;
-    start(cw);
-    start(cx);
-    int gmap[8], grow[8], g_tile = -1;
-    // the weight boxes of the chunk at cursor cw into stage st (arming the
-    // stage's barrier for the whole stage)
-    auto issue_w = [&](int st) {
-      if (cw.tile != g_tile) {
-#pragma unroll
-        for (int grp = 0; grp < 8; ++grp) group_coord(p, cw.tile, grp, gmap[grp], grow[grp]);
-        g_tile = cw.tile;
+    begin_phase(0);
+    while (j >= n && ph + 1 < n_ph) begin_phase(ph + 1);
+    int gmap[8], grow[8], g_tile = -1, g_ph = -1;
+    long long g = 0;
+    bool abort = false;
+    int ready_ph = 0;   // a phase whose inputs are all complete (no more checks)
+    if (!wwarp) pdl_wait();   // phase 0's activations come from the previous kernel
+    for (; j < n; ++g) {
+      const GemmParams& p = cp.ph[ph];
+      const int st = (int)(g % T::S);
+      if (g >= T::S && !abort && !mbar_wait(&empty[st], (uint32_t)(((g / T::S) & 1) ^ 1))) {
+        atomicOr(p.status, 0x4u);
+        abort = true;   // keep arming and issuing (unchecked) so every stage completes
+        s_abort = 1;
       }
       uint8_t* dst = sm + st * Lt::STAGE;
-      const int k = cw.c * T::CK;
-      mbar_expect_tx(&full[st], stage_bytes);
-      if (T::WBOXES == 1 && p.w64) {
-        // four 16-row groups of one segment with consecutive rows are one
-        // 64-row box (the same swizzled layout as four stacked 16-row boxes):
-        // fewer, larger copies
+      if (wwarp) {
+        if (tile != g_tile || ph != g_ph) {
 #pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {
-          const int g0 = 4 * hq;
-          if (gmap[g0 + 3] == gmap[g0] && grow[g0 + 3] == grow[g0] + 48) {
-            tma_load_hint(dst + g0 * kBox, &p.tm_w64[gmap[g0]], k, grow[g0], &full[st], w_policy);
-          } else {
+          for (int grp = 0; grp < 8; ++grp) group_coord(p, tile, grp, gmap[grp], grow[grp]);
+          g_tile = tile;
+          g_ph = ph;
+        }
+        const int k = c * T::CK;
+        mbar_expect_tx(&full[st], Lt::W_BYTES);
+        if (T::WBOXES == 1 && p.w64) {
+          // four 16-row groups of one segment with consecutive rows are one
+          // 64-row box (the same swizzled layout as four stacked 16-row boxes)
 #pragma unroll
-            for (int grp = g0; grp < g0 + 4; ++grp)
-              tma_load_hint(dst + grp * kBox, &p.tm_w[gmap[grp]], k, grow[grp], &full[st], w_policy);
+          for (int hq = 0; hq < 2; ++hq) {
+            const int g0 = 4 * hq;
+            if (gmap[g0 + 3] == gmap[g0] && grow[g0 + 3] == grow[g0] + 48) {
+              tma_load_hint(dst + g0 * kBox, &p.tm_w64[gmap[g0]], k, grow[g0], &full[st], w_policy);
+            } else {
+#pragma unroll
+              for (int grp = g0; grp < g0 + 4; ++grp)
+                tma_load_hint(dst + grp * kBox, &p.tm_w[gmap[grp]], k, grow[grp], &full[st], w_policy);
+            }
           }
+        } else {
+#pragma unroll
+          for (int grp = 0; grp < 8; ++grp)
+#pragma unroll
+            for (int wb = 0; wb < T::WBOXES; ++wb)
+              tma_load_hint(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]],
+                            k + wb * T::WBOX_K, grow[grp], &full[st], w_policy);
         }
       } else {
+        if (NPH > 1 && ph > 0 && !abort && ready_ph != ph) {
+          // phase ph reads phase ph - 1's output columns [k0, k0 + CK) of this
+          // 16-row block: wait for the items that write them (acquire); once
+          // every item of the block is done, the rest of the phase needs no check
+          const GemmParams& pp = cp.ph[ph - 1];
+          const int* cnt = cp.all_done + (size_t)(ph - 1) * cp.mb_stride + mb;
+          if (ld_acquire_gpu(cnt) >= pp.n_tiles) {
+            if (pp.n_mb == 1) ready_ph = ph;
+          } else {
+            const int tc = pp.map == MAP_SWIGLU ? kTileRows / 2 : kTileRows;
+            const int k0 = c * T::CK;
+            const int* flags = cp.item_done + (size_t)(ph - 1) * cp.item_stride;
+            for (int t = k0 / tc; t <= (k0 + T::CK - 1) / tc && !abort; ++t) {
+              const int* f = flags + t * pp.n_mb + mb;
+              const long long t0 = clock64();
+              while (!ld_acquire_gpu(f)) {
+                __nanosleep(64);
+                if (clock64() - t0 > kWaitCycles) {
+                  atomicOr(p.status, 0x4u);
+                  abort = true;
+                  s_abort = 1;
+                  break;
+                }
+              }
+            }
+          }
+          // the tensor copies (async proxy) read what the epilogues' plain stores wrote
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        const int k = c * T::CK;
+        mbar_expect_tx(&full[st], Lt::X_BYTES * (p.has_lo ? 2 : 1));
 #pragma unroll
-        for (int grp = 0; grp < 8; ++grp)
-#pragma unroll
-          for (int wb = 0; wb < T::WBOXES; ++wb)
-            tma_load_hint(dst + (grp * T::WBOXES + wb) * kBox, &p.tm_w[gmap[grp]],
-                          k + wb * T::WBOX_K, grow[grp], &full[st], w_policy);
+        for (int xb = 0; xb < T::XBOXES; ++xb) {
+          tma_load(dst + Lt::W_BYTES + xb * kBox, &p.tm_xh, k + xb * 64, mb * 16, &full[st]);
+          if (p.has_lo)
+            tma_load(dst + Lt::W_BYTES + Lt::X_BYTES + xb * kBox, &p.tm_xl, k + xb * 64, mb * 16,
+                     &full[st]);
+        }
       }
-      advance(cw);
-    };
-    // the activation boxes (hi, lo) of the chunk at cursor cx into stage st
-    auto issue_x = [&](int st) {
-      uint8_t* dst = sm + st * Lt::STAGE;
-      const int k = cx.c * T::CK;
-#pragma unroll
-      for (int xb = 0; xb < T::XBOXES; ++xb) {
-        tma_load(dst + Lt::W_BYTES + xb * kBox, &p.tm_xh, k + xb * 64, cx.mb * 16, &full[st]);
-        if (has_lo)
-          tma_load(dst + Lt::W_BYTES + Lt::X_BYTES + xb * kBox, &p.tm_xl, k + xb * 64, cx.mb * 16,
-                   &full[st]);
+      // next chunk
+      ++j;
+      if (++c == p.cpt) {
+        c = 0;
+        ++item;
+        if (++mb == p.n_mb) {
+          mb = 0;
+          ++tile;
+        }
       }
-      advance(cx);
-    };
-    // Weights do not depend on the previous kernel: every stage's weight boxes
-    // go out before the dependency wait, so the stream is already in flight
-    // when the activations become readable; then those stages' activations.
-    const int pre = n < T::S ? (int)n : T::S;
-    for (int j = 0; j < pre; ++j) issue_w(j);
-    pdl_wait();
-    for (int j = 0; j < pre; ++j) issue_x(j);
-    long long it = pre;
-    int st = pre % T::S;
-    uint32_t ph = pre / T::S;   // 0 or 1: the parity of chunk `it`'s stage round
-    for (; it < n && !s_abort; ++it) {
-      if (!mbar_wait(&empty[st], (ph & 1) ^ 1)) {
-        atomicOr(p.status, 0x4u);
-        s_abort = 1;
-        break;
-      }
-      issue_w(st);
-      issue_x(st);
-      if (++st == T::S) {
-        st = 0;
-        ++ph;
-      }
+      while (j >= n && ph + 1 < n_ph) begin_phase(ph + 1);
     }
-    if (p.pf_count > 0) prefetch_share(p, b, G);
-    // no copy may still be landing when the CTA exits: wait for the last stages
-    for (long long j = it > T::S ? it - T::S : 0; j < it; ++j) {
-      if (!mbar_wait(&full[j % T::S], (uint32_t)((j / T::S) & 1))) {
-        atomicOr(p.status, 0x4u);
+    if (wwarp)
+      for (int k = 0; k < n_ph; ++k)
+        if (cp.ph[k].pf_count > 0) prefetch_share(cp.ph[k], b, G);
+    // no copy of this warp may still be landing when the CTA exits
+    for (long long q = g > T::S ? g - T::S : 0; q < g; ++q) {
+      if (!mbar_wait(&full[q % T::S], (uint32_t)((q / T::S) & 1))) {
+        atomicOr(cp.ph[0].status, 0x4u);
         break;
       }
     }
@@ -486,8 +540,12 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
 
   // -------------------------------------------------------------- consumers
   pdl_wait();
-  {
-    long long it = 0;
+  long long it = 0;
+  for (int ph = 0; ph < n_ph; ++ph) {
+    const GemmParams& p = cp.ph[ph];
+    const bool has_lo = p.has_lo != 0;
+    long long V, ub0, ub1;
+    phase_range<T::PEN>(p, b, V, ub0, ub1);
     for (long long u = ub0; u < ub1;) {
       const int item = (int)(u / p.cpt);
       const int c0 = (int)(u - (long long)item * p.cpt);
@@ -500,7 +558,8 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
         const uint8_t* r = map_row(p, tile, tid, 1, &sc);
         scale_s[tid] = r ? (sc ? *sc : 1.f) : 0.f;
       }
-      if (p.row_scale) compute_inv_rms(p, inv_rms, mb * 16);
+      // the row statistics of phase 0 come from an earlier kernel
+      if (p.row_scale && ph == 0) compute_inv_rms(p, inv_rms, mb * 16);
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       for (int c = c0; c < c1; ++c, ++it) {
         const int st = (int)(it % T::S);
@@ -527,33 +586,74 @@ __global__ void __launch_bounds__(kGemmThreads + 32, 2) gemm_tma_kernel(const __
         acc_s[(cc + 1) * kTileRows + r + 8] = acc[j][3];
       }
       csync();
-      if (!vsplit_fixup<T::PEN>(p, acc_s, item, c0, c1, V, G, b, &s_flag)) continue;
+      if (!vsplit_fixup<T::PEN>(p, acc_s, item, c0, c1, V, p.grid, b, &s_flag)) continue;
+      if (p.row_scale && ph > 0) {
+        // the 1/rms of the block's rows needs every item of the previous phase
+        // in this 16-row block (their sums of squares): wait (bounded), then read
+        if (tid == 0) {
+          const int* cnt = cp.all_done + (size_t)(ph - 1) * cp.mb_stride + mb;
+          const long long t0 = clock64();
+          while (ld_acquire_gpu(cnt) < cp.ph[ph - 1].n_tiles && !s_abort) {
+            __nanosleep(64);
+            if (clock64() - t0 > kWaitCycles) {
+              atomicOr(p.status, 0x4u);
+              s_abort = 1;
+            }
+          }
+        }
+        csync();
+        compute_inv_rms(p, inv_rms, mb * 16);
+        csync();
+      }
       run_epilogue(p, acc_s, scale_s, inv_rms, mb, tile, &s_flag);
+      if (NPH > 1 && ph + 1 < n_ph) {
+        csync();  // every thread's epilogue stores precede the release
+        if (tid == 0) {
+          st_release_gpu(cp.item_done + (size_t)ph * cp.item_stride + item, 1);
+          red_release_add_gpu(cp.all_done + (size_t)ph * cp.mb_stride + mb, 1);
+        }
+      }
     }
   }
-  if (p.stamp) {
-    csync();
-    if (tid == 0) stamp_finish(p.stamp);
+  csync();
+  if (tid == 0) {
+    stamp_finish(cp.ph[0].stamp);
+    if (NPH > 1) s_flag = atom_add_acq_rel_gpu(cp.chain_done, 1) == G - 1;
   }
+  if (NPH > 1) {
+    // the last CTA past the chain clears the flags and counters for the next
+    // launch (every CTA's producer read its last flag before its last chunk)
+    csync();
+    if (s_flag) {
+      const int n_items = (n_ph - 1) * cp.item_stride, n_mbs = (n_ph - 1) * cp.mb_stride;
+      for (int i = tid; i < n_items; i += kGemmThreads) cp.item_done[i] = 0;
+      for (int i = tid; i < n_mbs; i += kGemmThreads) cp.all_done[i] = 0;
+      if (tid == 0) *cp.chain_done = 0;
+    }
+  }
+}
+
+template <int WT, int NPH>
+static cudaError_t set_smem() {
+  return cudaFuncSetAttribute(gemm_tma_kernel<WT, NPH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)gemm_tma_smem_bytes(WT));
 }
 
 cudaError_t configure_gemm_tma() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tma_kernel<W_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)gemm_tma_smem_bytes(W_F32));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tma_kernel<W_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)gemm_tma_smem_bytes(W_BF16));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tma_kernel<W_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)gemm_tma_smem_bytes(W_FP8));
+  cudaError_t e = set_smem<W_F32, 1>();
+  if (e == cudaSuccess) e = set_smem<W_BF16, 1>();
+  if (e == cudaSuccess) e = set_smem<W_FP8, 1>();
+  if (e == cudaSuccess) e = set_smem<W_F32, kChainMax>();
+  if (e == cudaSuccess) e = set_smem<W_BF16, kChainMax>();
+  if (e == cudaSuccess) e = set_smem<W_FP8, kChainMax>();
   return e;
 }
 
-template <int WT>
-static cudaError_t launch_tma_t(const GemmParams& p, cudaStream_t st) {
+template <int WT, int NPH>
+static cudaError_t launch_tma_t(const ChainParams<NPH>& cp, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(kGemmThreads + 32);
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemmThreads + 64);
   cfg.dynamicSmemBytes = gemm_tma_smem_bytes(WT);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -561,14 +661,53 @@ static cudaError_t launch_tma_t(const GemmParams& p, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tma_kernel<WT>, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tma_kernel<WT, NPH>, cp);
 }
 
 cudaError_t launch_gemm_tma(int wt, const GemmParams& p, cudaStream_t st) {
+  ChainParams<1> cp;
+  cp.ph[0] = p;
+  cp.n_phase = 1;
+  cp.item_done = cp.all_done = cp.chain_done = nullptr;
+  cp.item_stride = cp.mb_stride = 0;
   switch (wt) {
-    case W_F32: return launch_tma_t<W_F32>(p, st);
-    case W_BF16: return launch_tma_t<W_BF16>(p, st);
-    case W_FP8: return launch_tma_t<W_FP8>(p, st);
+    case W_F32: return launch_tma_t<W_F32, 1>(cp, p.grid, st);
+    case W_BF16: return launch_tma_t<W_BF16, 1>(cp, p.grid, st);
+    case W_FP8: return launch_tma_t<W_FP8, 1>(cp, p.grid, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int WT>
+static int chain_capacity_t() {
+  int per_sm = 0, dev = 0, n_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_tma_kernel<WT, kChainMax>, kGemmThreads + 64,
+                                                    gemm_tma_smem_bytes(WT)) != cudaSuccess ||
+      cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return per_sm * n_sm;
+}
+
+int gemm_chain_capacity(int wt) {
+  switch (wt) {
+    case W_F32: return chain_capacity_t<W_F32>();
+    case W_BF16: return chain_capacity_t<W_BF16>();
+    case W_FP8: return chain_capacity_t<W_FP8>();
+  }
+  return 0;
+}
+
+// the chain's grid: the largest of its phases' grids
+cudaError_t launch_gemm_chain(int wt, const ChainParams<kChainMax>& cp, cudaStream_t st) {
+  int grid = 0;
+  for (int k = 0; k < cp.n_phase; ++k) grid = cp.ph[k].grid > grid ? cp.ph[k].grid : grid;
+  switch (wt) {
+    case W_F32: return launch_tma_t<W_F32, kChainMax>(cp, grid, st);
+    case W_BF16: return launch_tma_t<W_BF16, kChainMax>(cp, grid, st);
+    case W_FP8: return launch_tma_t<W_FP8, kChainMax>(cp, grid, st);
   }
   return cudaErrorInvalidValue;
 }

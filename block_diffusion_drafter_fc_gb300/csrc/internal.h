@@ -182,9 +182,31 @@ size_t gemm_smem_bytes(int wt, int xk);
 cudaError_t configure_gemm(int xk_max);
 cudaError_t launch_gemm(int wt, const GemmParams& p, cudaStream_t st);
 
+// A chain of 16-row projections in one persistent launch of the TMA kernel:
+// phase k + 1 reads the activation pair phase k's epilogues write.  Every CTA
+// walks its stream-K range of phase 0, then of phase 1, ...; the copies of a
+// phase's activation chunk wait (bounded) for the flags of the previous phase's
+// items that produce it, and a phase whose epilogue applies the 1/rms row scale
+// waits for all of the previous phase's items of its 16-row block (their sums
+// of squares).  Weight copies never wait on activations.  Every phase has its
+// own partial tiles and tickets; the grid is one resident wave (every wait ends).
+constexpr int kChainMax = 4;
+template <int NPH>
+struct ChainParams {
+  GemmParams ph[NPH];
+  int n_phase;
+  int* item_done;    // [NPH][item_stride]: 1 once the item's epilogue stores are visible
+  int* all_done;     // [NPH][mb_stride]: finished items of each 16-row block
+  int* chain_done;   // CTAs past the chain; the last one clears flags and counters
+  int item_stride, mb_stride;
+};
+
 size_t gemm_tma_smem_bytes(int wt);
 cudaError_t configure_gemm_tma();
 cudaError_t launch_gemm_tma(int wt, const GemmParams& p, cudaStream_t st);
+// CTAs of the chain kernel the GPU holds at once (occupancy x SMs)
+int gemm_chain_capacity(int wt);
+cudaError_t launch_gemm_chain(int wt, const ChainParams<kChainMax>& cp, cudaStream_t st);
 int tma_chunk_k(int wt);   // k per pipeline stage of the TMA projection kernel
 
 // FP4 projection on tcgen05 with the decoded weights in tensor memory (16-row

@@ -22,9 +22,9 @@ HEADER = PKG.parent / "include" / "dflash.h"
 
 DTYPE = {"f32": 0, "bf16": 1, "fp8": 2, "fp4": 3}
 MAX_LAYERS = 16
-PROF_N = 11
+PROF_N = 12
 PROF_CLASSES = ("embed", "qkv", "attention", "attn_merge", "o_proj", "gate_up", "down", "lm_head",
-                "encode", "inject", "accept")
+                "encode", "inject", "accept", "chain")
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported", -3: "too many rows",
           -4: "sequence out of range", -5: "CUDA error", -6: "not captured", -7: "device status"}
 
@@ -80,6 +80,7 @@ def _load() -> C.CDLL:
         "dflash_encode_noalloc": (C.c_int, [C.POINTER(dflash_config), vp, vp, vp, i32, vp, vp]),
         "dflash_advance": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_set_block_width": (C.c_int, [vp, i32]),
+        "dflash_set_chain": (C.c_int, [vp, i32]),
         "dflash_capture_loop": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_step_host": (C.c_int, [vp, i32, vp, vp, vp, vp, vp]),
         "dflash_ring_reset": (C.c_int, [vp, i32, vp]),
@@ -252,6 +253,9 @@ class Drafter:
         _check(LIB.dflash_graph_nodes(self.h, int(loop), C.byref(k), C.byref(m), C.byref(o)),
                self.h, "graph_nodes")
         return k.value, m.value, o.value
+
+    def dflash_set_chain(self, enable: bool):
+        _check(LIB.dflash_set_chain(self.h, int(bool(enable))), self.h, "set_chain")
 
     def dflash_set_block_width(self, width: int):
         _check(LIB.dflash_set_block_width(self.h, int(width)), self.h, "set_block_width")

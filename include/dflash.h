@@ -266,6 +266,25 @@ DFLASH_API int dflash_inject(dflash_handle* h, int32_t seq, const float* H_t, co
 DFLASH_API int dflash_set_block_width(dflash_handle* h, int32_t width);
 
 /*
+ * Projection chains (off by default).  With chains on, a step of fewer than
+ * 128 block rows with bf16, fp32 or E4M3 weights runs, per layer, one
+ * persistent launch for o, gate/up, down and the next layer's q/k/v (the LM
+ * head after the last layer) instead of four (dflash-ops model card,
+ * Requirements and limits: the whole-block megakernel is the named next step;
+ * this is its projection part).  Its CTAs wait for one another's output tiles
+ * (bounded waits that end in DFLASH_DEV_TIMEOUT), which needs the whole grid
+ * resident at once: keep chains off when other work may hold SMs for the
+ * duration of a step (a GPU shared through MPS or partitioned contexts).
+ * Results are bitwise identical either way; on a GB300 the chained step is not
+ * faster (every tile of a stream-K phase completes near the phase's end, so the
+ * next phase starts no earlier than after a kernel boundary with programmatic
+ * dependent launch).  enable = 0 or 1; UNSUPPORTED when enabling on a handle
+ * without chains (FP4 weights, or a device that cannot hold the grid);
+ * INVALID_ARG during a capture.  Takes effect for later steps and captures.
+ */
+DFLASH_API int dflash_set_chain(dflash_handle* h, int32_t enable);
+
+/*
  * One block step for sequences 0..n_seq-1 (dflash-ops model card, Usage:
  * step(id_last, n_past) -> logits [16, n_vocab]; drafts = argmax of rows 1..15).
  *   id_last: device int32 [n_seq], the anchor token of each block;
@@ -396,9 +415,12 @@ DFLASH_API int dflash_read_status(dflash_handle* h, uint32_t* status, void* stre
  * table, 1 q/k/v projection, 2 attention chunks, 3 attention merge, 4 o
  * projection, 5 gate/up projection, 6 down projection, 7 LM head + drafts,
  * 8 encode (fc + norm), 9 injection (rope table + wk/wv + ring scatter),
- * 10 acceptance scan.  Enabling while a capture is in progress is refused.
+ * 10 acceptance scan, 11 projection chain (one launch of o, gate/up, down and
+ * the next layer's q/k/v or the LM head: steps of fewer than 128 block rows
+ * with bf16, fp32 or E4M3 weights).  Enabling while a capture is in progress
+ * is refused.
  */
-#define DFLASH_PROF_N 11
+#define DFLASH_PROF_N 12
 DFLASH_API int dflash_profile_enable(dflash_handle* h, int enable);
 DFLASH_API int dflash_profile_read(dflash_handle* h, double* ms, int32_t* launches);
 

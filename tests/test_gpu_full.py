@@ -104,3 +104,10 @@ def test_full_size_against_oracle(name):
         _check_ring(wl, ref, g)
     finally:
         g["drafter"].close()
+
+
+def test_projection_chain_bitwise_at_real_dimensions():
+    """The opt-in projection chains at the real drafter's dimensions: the same
+    bits as one launch per projection."""
+    from test_gpu_parity import check_chain_bitwise
+    check_chain_bitwise("real_bf16")

@@ -242,3 +242,47 @@ def test_small_bf16_full():
     GH.compare_drafts(gpu["logits"], gpu["drafts"], ref["logits"], ref["drafts"], err, "small_bf16")
     assert np.array_equal(gpu["drafts"], ref["drafts"])
     assert np.array_equal(gpu["n_ok"], ref["n_ok"])
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "ragged_bf16", "mixed_f32w_bf16ring", "small_fp8",
+                                  "split_bf16", "split_f32"])
+def test_projection_chain_bitwise_equals_separate_launches(name):
+    check_chain_bitwise(name)
+
+
+def check_chain_bitwise(name):
+    """The per-layer projection chains (o, gate/up, down, next q/k/v or the LM
+    head in one launch) give the same bits as one launch per projection (the
+    default), eager and replayed from a graph."""
+    wl = make_workload(get_config(name))
+    g = GH.gpu_run(wl, keep=True)   # one launch per projection
+    dr = g["drafter"]
+    n = wl.cfg.n_seq
+    logits = torch.zeros((n, BLOCK, wl.cfg.n_vocab), device="cuda")
+    drafts = torch.zeros((n, 15), dtype=torch.int32, device="cuda")
+    dr.dflash_set_chain(True)
+    dr.dflash_step(g["id_last_d"], g["n_past_d"], logits, drafts)
+    torch.cuda.synchronize()
+    assert np.array_equal(logits.cpu().numpy(), g["logits"])
+    assert np.array_equal(drafts.cpu().numpy(), g["drafts"])
+    logits.zero_()
+    dr.dflash_capture(g["id_last_d"], g["n_past_d"], logits, drafts)
+    assert dr.dflash_graph_nodes()[0] == 2 + 2 * wl.cfg.n_layer   # embed, q/k/v, (attention, chain) x L
+    for _ in range(3):
+        dr.dflash_replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(logits.cpu().numpy(), g["logits"])
+    assert dr.dflash_read_status() == 0
+    dr.dflash_set_chain(False)
+    dr.close()
+
+
+def test_projection_chain_refused_where_unsupported():
+    from block_diffusion_drafter_fc_gb300 import dflash as D
+    wl = make_workload(get_config("small_fp4"))
+    dw, _ = GH.to_device(wl)
+    dr = D.Drafter(wl.cfg, dw, max_seq=wl.cfg.n_seq)
+    with pytest.raises(D.DFlashError, match=r"\[-2\]"):
+        dr.dflash_set_chain(True)
+    dr.dflash_set_chain(False)
+    dr.close()
