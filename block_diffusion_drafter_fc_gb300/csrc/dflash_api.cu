@@ -125,7 +125,7 @@ Layout layout(const dflash_config& c) {
   for (auto& s : ss_) counters = std::max(counters, g.max_seq * s.n_tiles);
   for (auto& s : is_) counters = std::max(counters, cdiv(g.max_inject, 16) * s.n_tiles);
   L.partial_floats = partial;
-  L.n_counters = counters + 1;            // + the logits-argmax ticket
+  L.n_counters = counters + g.max_seq;    // + the logits-argmax tickets (one per 16-row block)
   L.ss_parts = cdiv(g.d, kTileRows);
   L.ss_ld = std::max(g.M_max, g.max_inject);
   L.lm_tiles = ss_[4].n_tiles;
@@ -591,7 +591,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     p.nseg = 1; p.N = g.V; p.map = MAP_SEGMENTS;
     p.epi = EPI_LOGITS; p.out = logits; p.ldo = g.V;
     p.am_part = h->S<float2>(L.am_part);
-    p.am_counter = h->S<int>(L.counters) + (L.n_counters - 1);
+    p.am_counter = h->S<int>(L.counters) + (L.n_counters - g.max_seq);
     p.drafts = drafts;
     p.block_width = h->width;
     bind_projection(h, p, -1, {0}, XP_XN);

@@ -126,6 +126,8 @@ DF_DEVICE void compute_inv_rms(const GemmParams& p, float* inv_rms, int m0) {
 
 // ------------------------------------------------------------------ epilogues
 
+DF_DEVICE void argmax_ticket(const GemmParams& p, int mb0, int n_blocks, int* s_flag);
+
 DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* scale_s, int mb,
                              int tile, int* s_flag) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -190,22 +192,38 @@ DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* sca
     if (lane == 0 && m0 + m < p.M)
       p.am_part[(size_t)tile * p.M + m0 + m] = make_float2(v, __int_as_float(idx));
   }
-  // the last finished tile of the whole launch reduces the argmax partials
+  argmax_ticket(p, mb, 1, s_flag);
+}
+
+// After a CTA has written the argmax partials of 16-row blocks mb0 ..
+// mb0 + n_blocks - 1 (n_blocks <= 8) for one tile: take one ticket per block
+// (acquire-release, as in segment_fixup; am_counter[mb] counts the block's
+// finished tiles).  The CTA that takes a block's last ticket reduces the
+// block's rows over the tiles (lowest index on ties) into its drafts and resets
+// the block's counter, so the reductions spread over the CTAs.
+DF_DEVICE void argmax_ticket(const GemmParams& p, int mb0, int n_blocks, int* s_flag) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   csync();
-  if (tid == 0) {  // acquire-release ticket, as in segment_fixup
-    const int total = p.n_tiles * p.n_mb;
-    int old;
-    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
-                 : "=r"(old)
-                 : "l"(p.am_counter)
-                 : "memory");
-    *s_flag = old == total - 1;
+  if (warp == 0) {
+    bool won = false;
+    if (lane < n_blocks) {
+      int old;
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                   : "=r"(old)
+                   : "l"(p.am_counter + mb0 + lane)
+                   : "memory");
+      won = old == p.n_tiles - 1;
+      if (won) p.am_counter[mb0 + lane] = 0;   // every ticket of the block is taken
+    }
+    const unsigned mask = __ballot_sync(0xffffffffu, won);
+    if (lane == 0) *s_flag = (int)mask;
   }
   csync();
-  if (!*s_flag) return;
-  for (int row = warp; row < p.M; row += kGemmThreads / 32) {
-    const int i = row & 15;
-    if (i == 0) continue;
+  const unsigned mask = (unsigned)*s_flag;
+  if (!mask) return;
+  for (int k = warp; k < n_blocks * 16; k += kGemmThreads / 32) {
+    const int bb = k >> 4, i = k & 15, row = (mb0 + bb) * 16 + i;
+    if (!((mask >> bb) & 1u) || i == 0 || row >= p.M) continue;
     float v = -CUDART_INF_F;
     int idx = 0x7fffffff;
     for (int tt = lane; tt < p.n_tiles; tt += 32) {
@@ -215,7 +233,6 @@ DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* sca
     warp_argmax(v, idx);
     if (lane == 0) p.drafts[(row >> 4) * 15 + i - 1] = i < p.block_width ? idx : -1;
   }
-  if (tid == 0) *p.am_counter = 0;
 }
 
 DF_DEVICE void epilogue_swiglu(const GemmParams& p, const float* acc_s, const float* scale_s,

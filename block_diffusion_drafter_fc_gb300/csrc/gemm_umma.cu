@@ -39,6 +39,7 @@ constexpr long long kWait = 4000000000LL;
 constexpr int kThreads = 448;          // warps 0-7 epilogue, 8-11 E4M3 widening, 12 TMA, 13 MMA
 constexpr int kWiden = 4;              // widening warps
 constexpr int kBRow = kTileRows + 4;   // padded row (floats) of a read-out block
+constexpr int kPf = 6;                 // weight chunks prefetched into L2 ahead of the box loads
 
 // Shared-memory layout for output tiles of 128 activation rows x WR weight rows
 // (WR = 128, or 256 = two 128-row n-tiles sharing every activation chunk).
@@ -110,6 +111,11 @@ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+DF_DEVICE void tma_prefetch2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+               : "memory");
+}
+
 DF_DEVICE void mma_f16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -121,6 +127,318 @@ DF_DEVICE void mma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    su32(b))
                : "memory");
+}
+
+// 16 consecutive fp32 accumulator columns of the warp's 32 tensor-memory lanes
+// (lane i: activation row i of the warp's quadrant)
+DF_DEVICE void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  __syncwarp();   // a warp-wide load: every lane, converged
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+      " [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// The first n_ok (<= 16) of 16 values of one row: vector accesses when whole and aligned.
+DF_DEVICE void st_row16(float* dst, const float (&v)[16], int n_ok) {
+  if (n_ok >= 16 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < n_ok) dst[j] = v[j];
+  }
+}
+DF_DEVICE void ld_row16(const float* src, float (&v)[16], int n_ok) {
+  if (n_ok >= 16 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(src) + q);
+      v[4 * q] = x.x;
+      v[4 * q + 1] = x.y;
+      v[4 * q + 2] = x.z;
+      v[4 * q + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = j < n_ok ? __ldcg(src + j) : 0.f;
+  }
+}
+// The 16-bit hi/lo pair of 16 values of one row (the next projection's input).
+DF_DEVICE void st_pair16(uint16_t* hi, uint16_t* lo, const float (&v)[16], bool f16, int n_ok) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) split_pair16x2(v[2 * e], v[2 * e + 1], f16, h[e], l[e]);
+  if (n_ok >= 16 && ((reinterpret_cast<uintptr_t>(hi) | reinterpret_cast<uintptr_t>(lo)) & 15) == 0) {
+    reinterpret_cast<uint4*>(hi)[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    reinterpret_cast<uint4*>(hi)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    reinterpret_cast<uint4*>(lo)[0] = make_uint4(l[0], l[1], l[2], l[3]);
+    reinterpret_cast<uint4*>(lo)[1] = make_uint4(l[4], l[5], l[6], l[7]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < n_ok) {
+        hi[j] = (uint16_t)(h[j >> 1] >> (16 * (j & 1)));
+        lo[j] = (uint16_t)(l[j >> 1] >> (16 * (j & 1)));
+      }
+  }
+}
+
+// 1 / rms of one activation row from the previous kernel's per-tile sums of
+// squares (summed in tile order).
+DF_DEVICE float row_inv_rms(const GemmParams& p, int row) {
+  float s = 0.f;
+  int q = 0;
+  for (; q + 8 <= p.n_ss; q += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcg(p.ss + (size_t)(q + u) * p.ss_ld + row);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) s += v[u];
+  }
+  for (; q < p.n_ss; ++q) s += __ldcg(p.ss + (size_t)q * p.ss_ld + row);
+  return 1.f / sqrtf(s / (float)p.rms_len + p.eps);
+}
+
+// The epilogue of one 128-column n-tile straight from tensor memory: each
+// thread owns one activation row and 64 of the tile's columns, in one of two
+// layouts - "plain" (warp half h: columns 64h .. 64h + 63) or "paired" (32h ..
+// 32h + 31 and 64 + 32h .. 64 + 32h + 31: a SwiGLU gate column with its up
+// column, or a rope pair of a 128-dim head).  Per-column scales and norm
+// weights sit in the warp's scratch (wscr: [64] scales, [64] norm weights, in
+// the thread's column order); row sums and argmax partials that span both
+// halves are exchanged through xch ([2 parity][2 halves][128 rows]) at named
+// barrier 3 + quadrant (the quadrant's two warps).  Outputs other than the
+// residual stream go through the warp's staging tile stg (32 rows x 16
+// columns, each row's columns rotated by row / 2 so that both the row-per-lane
+// and the column-per-lane accesses are free of bank conflicts): a warp
+// instruction then writes two (fp32) or four (16-bit pairs) row segments
+// instead of 32 rows.
+DF_DEVICE void epi_direct(const GemmParams& p, uint32_t tacc, int nt, int mt, int row, float inv,
+                          int quad, int half, int lane, float* wscr, float2* xch, float* stg, int& n_xch,
+                          int* s_flag) {
+  const int epi = p.epi;
+  const bool qkv = epi == EPI_QKV, paired = epi == EPI_SWIGLU || (qkv && p.hd == 128);
+  const bool rok = row < p.M;
+  const int rowbase = row - lane;   // the quadrant's first row
+  auto col = [&](int c) { return paired ? (c < 32 ? 32 * half + c : 64 + 32 * half + c - 32) : 64 * half + c; };
+  // head of this thread's columns (q/k/v): its first output column and kind
+  const int n0h = nt * kTileRows + (paired ? 0 : 64 * half);
+  const int kind = !qkv ? 0 : (n0h < p.qd ? 0 : (n0h < p.qd + p.kvd ? 1 : 2));
+  __syncwarp();  // the previous tile's reads of the scratch are done
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int c = lane + 32 * e, cc = col(c);
+    const float* sc = nullptr;
+    const uint8_t* r = map_row(p, nt, cc, 1, &sc);
+    wscr[c] = r ? (sc ? *sc : 1.f) : 0.f;
+    float nw = 0.f;
+    const int n = nt * kTileRows + cc;
+    if (epi == EPI_RESID_SS && p.pair_hi && n < p.N) nw = load_dense(p.pair_norm, p.norm_bf16, n);
+    if (qkv && kind != 2) nw = load_dense(kind == 0 ? p.q_norm : p.k_norm, p.norm_bf16, n - n0h);
+    wscr[64 + c] = nw;
+  }
+  __syncwarp();
+  const int xrow = quad * 32 + lane;
+  float2* xb = xch + (size_t)(n_xch & 1) * 2 * 128;
+  auto exchange = [&](float2 mine) {   // -> the other half's value for this row
+    xb[half * 128 + xrow] = mine;
+    __syncwarp();
+    asm volatile("bar.sync %0, 64;" ::"r"(3 + quad) : "memory");
+    ++n_xch;
+    return xb[(half ^ 1) * 128 + xrow];
+  };
+  // staging tile: element (r, c) of the 32 x 16 chunk
+  auto at = [&](int r, int c) { return r * 16 + ((c + (r >> 1)) & 15); };
+  auto stage = [&](const float (&v)[16]) {
+    __syncwarp();   // the previous chunk's reads are done
+#pragma unroll
+    for (int j = 0; j < 16; ++j) stg[at(lane, j)] = v[j];
+    __syncwarp();
+  };
+  // columns [n0, n0 + 16) of the quadrant's rows at base + r * ld, below n_end
+  auto store_t = [&](float* base, size_t ld, int n0, int n_end) {
+#pragma unroll 4
+    for (int it = 0; it < 16; ++it) {
+      const int rr = 2 * it + (lane >> 4), c = lane & 15, r = rowbase + rr, n = n0 + c;
+      if (r < p.M && n < n_end) base[(size_t)r * ld + n] = stg[at(rr, c)];
+    }
+  };
+  // the 16-bit hi/lo pair of the staged chunk (times nw[c], if given)
+  auto store_pair_t = [&](uint16_t* hi, uint16_t* lo, size_t ld, int n0, int n_end, const float* nw) {
+    const bool f16 = p.pair_f16 != 0, even = (ld & 1) == 0;
+#pragma unroll 4
+    for (int it = 0; it < 8; ++it) {
+      const int rr = 4 * it + (lane >> 3), c = 2 * (lane & 7), r = rowbase + rr, n = n0 + c;
+      const float a = stg[at(rr, c)] * (nw ? nw[c] : 1.f), b = stg[at(rr, c + 1)] * (nw ? nw[c + 1] : 1.f);
+      uint32_t h, l;
+      split_pair16x2(a, b, f16, h, l);
+      if (r >= p.M || n >= n_end) continue;
+      const size_t o = (size_t)r * ld + n;
+      if (even && n + 1 < n_end) {
+        *reinterpret_cast<uint32_t*>(hi + o) = h;
+        *reinterpret_cast<uint32_t*>(lo + o) = l;
+      } else {
+        hi[o] = (uint16_t)(h & 0xffffu);
+        lo[o] = (uint16_t)(l & 0xffffu);
+        if (n + 1 < n_end) {
+          hi[o + 1] = (uint16_t)(h >> 16);
+          lo[o + 1] = (uint16_t)(l >> 16);
+        }
+      }
+    }
+  };
+
+  if (epi == EPI_SWIGLU) {
+    const int F = p.seg[0].rows;
+#pragma unroll 1
+    for (int s = 0; s < 2; ++s) {
+      float g[16], u[16];
+      tmem_ld16(tacc + 32 * half + 16 * s, g);
+      tmem_ld16(tacc + 64 + 32 * half + 16 * s, u);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float gv = g[j] * inv * wscr[16 * s + j];
+        const float uv = u[j] * inv * wscr[32 + 16 * s + j];
+        g[j] = gv / (1.f + expf(-gv)) * uv;
+      }
+      const int f0 = nt * (kTileRows / 2) + 32 * half + 16 * s;
+      stage(g);
+      if (p.out) store_t(p.out, p.ldo, f0, F);
+      if (p.pair_hi) store_pair_t(p.pair_hi, p.pair_lo, p.pair_ld, f0, F, nullptr);
+    }
+    return;
+  }
+
+  if (qkv) {
+    const int hd = p.hd, hh = hd / 2;
+    const int d1 = paired ? 32 * half : 0;   // dims d1 + j (x1) and d1 + hh + j (x2), j < 32
+    const int d_end = n0h < p.N ? hd : 0;   // no dims of a head past N
+    float inv_h = 1.f;
+    if (kind != 2) {
+      float ss = 0.f;
+#pragma unroll 1
+      for (int s = 0; s < 2; ++s) {
+        float a[16], b[16];
+        tmem_ld16(tacc + col(16 * s), a);
+        tmem_ld16(tacc + col(32 + 16 * s), b);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float x1 = a[j] * inv * wscr[16 * s + j], x2 = b[j] * inv * wscr[32 + 16 * s + j];
+          ss += x1 * x1 + x2 * x2;
+        }
+      }
+      if (paired) {
+        const float o = exchange(make_float2(ss, 0.f)).x;
+        ss = half == 0 ? ss + o : o + ss;   // the same order in both halves
+      }
+      inv_h = 1.f / sqrtf(ss / (float)hd + p.eps);
+    }
+    float* base = kind == 0 ? p.out + n0h : kind == 1 ? p.kblk + (n0h - p.qd) : p.vblk + (n0h - p.qd - p.kvd);
+    const size_t ld = kind == 0 ? p.qd : p.kvd;
+#pragma unroll 1
+    for (int s = 0; s < 2; ++s) {
+      float a[16], b[16];
+      tmem_ld16(tacc + col(16 * s), a);
+      tmem_ld16(tacc + col(32 + 16 * s), b);
+      const int d = d1 + 16 * s;
+      if (kind != 2) {
+        const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cs + (size_t)(rok ? row : 0) * hh + d);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 cs = __ldg(cs4 + q);   // (cos, sin) of dims d + 2q, d + 2q + 1
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int j = 2 * q + e;
+            const float c = e ? cs.z : cs.x, sn = e ? cs.w : cs.y;
+            const float x1 = a[j] * inv * wscr[16 * s + j], x2 = b[j] * inv * wscr[32 + 16 * s + j];
+            const float u = x1 * inv_h * wscr[64 + 16 * s + j];
+            const float w = x2 * inv_h * wscr[96 + 16 * s + j];
+            a[j] = u * c - w * sn;
+            b[j] = w * c + u * sn;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          a[j] = a[j] * inv * wscr[16 * s + j];
+          b[j] = b[j] * inv * wscr[32 + 16 * s + j];
+        }
+      }
+      stage(a);
+      store_t(base, ld, d, d_end);
+      stage(b);
+      store_t(base, ld, d + hh, d_end);
+    }
+    return;
+  }
+
+  // rows: store, store + sums of squares, residual + sums of squares + pair, logits
+  const bool resid = epi == EPI_RESID_SS, logits = epi == EPI_LOGITS;
+  const bool ssk = epi == EPI_STORE_SS || resid;
+  float ss = 0.f, bv = -CUDART_INF_F;
+  int bi = 0x7fffffff;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    float v[16], res[16];
+    tmem_ld16(tacc + 64 * half + 16 * s, v);
+    const int n0 = nt * kTileRows + 64 * half + 16 * s;
+    const int n_ok = rok ? max(0, min(16, p.N - n0)) : 0;
+    if (resid && n_ok > 0)
+      ld_row16(p.out + (size_t)row * p.ldo + n0, res, n_ok);
+    else
+#pragma unroll
+      for (int j = 0; j < 16; ++j) res[j] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float y = v[j] * inv * wscr[16 * s + j];
+      if (j < n_ok) {
+        y += res[j];
+        if (logits) argmax_merge(bv, bi, y, n0 + j);
+      } else {
+        y = logits ? -CUDART_INF_F : 0.f;
+      }
+      v[j] = y;
+      ss += y * y;
+    }
+    if (resid) {
+      // one tile per CTA at these shapes: the epilogue is exposed, and per-row
+      // vector accesses beat the staging round trip
+      if (n_ok > 0) {
+        st_row16(p.out + (size_t)row * p.ldo + n0, v, n_ok);
+        if (p.pair_hi) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) res[j] = v[j] * wscr[64 + 16 * s + j];
+          st_pair16(p.pair_hi + (size_t)row * p.pair_ld + n0, p.pair_lo + (size_t)row * p.pair_ld + n0, res,
+                    p.pair_f16 != 0, n_ok);
+        }
+      }
+    } else {
+      stage(v);
+      if (p.out) store_t(p.out, p.ldo, n0, p.N);
+    }
+  }
+  if (ssk) {
+    const float o = exchange(make_float2(ss, 0.f)).x;
+    if (half == 0 && rok) p.ss_out[(size_t)nt * p.ss_out_ld + row] = ss + o;
+  }
+  if (logits) {
+    const float2 o = exchange(make_float2(bv, __int_as_float(bi)));
+    if (half == 0 && rok) {
+      argmax_merge(bv, bi, o.x, __float_as_int(o.y));
+      p.am_part[(size_t)nt * p.M + row] = make_float2(bv, __int_as_float(bi));
+    }
+    argmax_ticket(p, 8 * mt, min(8, p.n_mb - 8 * mt), s_flag);
+  }
 }
 
 }  // namespace umma
@@ -186,11 +504,11 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
       pdl_wait();
       const uint32_t bytes = kTile * (p.has_lo ? 2 : 1) + (fp8 ? kWRaw : kWTile);
       long long it = 0;
-      for (int t = blockIdx.x; t < n_items && !s_abort; t += G) {
-        const int mt = t % m_tiles, wt2 = t / m_tiles;
-        int maps[WR / 32], rows[WR / 32];
+      // the WR weight rows of item t in 32-row boxes: segment map and row
+      auto tile_boxes = [&](int t, int* maps, int* rows) {
+        const int wt2 = t / m_tiles;
 #pragma unroll
-        for (int q = 0; q < WR / 32; ++q) {  // the WR weight rows in 32-row boxes, per segment map
+        for (int q = 0; q < WR / 32; ++q) {
           const int nt = kNsub * wt2 + (q >> 2), qq = q & 3;
           if (p.map == MAP_SWIGLU) {
             maps[q] = qq < 2 ? 0 : 1;
@@ -203,7 +521,23 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
             rows[q] = vr - p.seg[s].row0;
           }
         }
+      };
+      int maps[WR / 32], rows[WR / 32], nmaps[WR / 32], nrows[WR / 32];
+      for (int t = blockIdx.x; t < n_items && !s_abort; t += G) {
+        const int mt = t % m_tiles;
+        tile_boxes(t, maps, rows);
+        const bool next = t + G < n_items;
+        if (next) tile_boxes(t + G, nmaps, nrows);
         for (int k = 0; k < nk; ++k, ++it) {
+          // the weights kPf chunks ahead (this item's, or the next one's) into L2:
+          // the box load then waits on L2 rather than on DRAM
+          const bool cur = k + kPf < nk;
+          const int kk = cur ? k + kPf : k + kPf - nk;
+          if (kPf > 0 && (cur || (next && kk < nk))) {
+#pragma unroll
+            for (int q = 0; q < WR / 32; ++q)
+              tma_prefetch2d(&p.tm_w[cur ? maps[q] : nmaps[q]], kk * 64, cur ? rows[q] : nrows[q]);
+          }
           const int st = (int)(it % kS);
           if (!bar_wait(&empty[st], (uint32_t)((it / kS) & 1) ^ 1)) {
             atomicOr(p.status, 0x4u);
@@ -318,14 +652,34 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
     // ---------------------------------------------------------------- epilogue warps 0..7
     pdl_wait();
     const int quad = warp & 3, half = warp >> 2;
+    // straight from tensor memory where the epilogue's columns fit one thread
+    // per row; injection and q/k/v heads of other widths take the staged path
+    const bool direct = p.epi == EPI_SWIGLU || p.epi == EPI_RESID_SS || p.epi == EPI_STORE_SS ||
+                        p.epi == EPI_STORE || p.epi == EPI_LOGITS ||
+                        (p.epi == EPI_QKV && (p.hd == 64 || p.hd == 128));
+    float* wscr = blk + warp * 128;                              // 8 x 128 floats
+    float2* xch = reinterpret_cast<float2*>(blk + 8 * 128);     // 2 x 2 x 128 float2
+    float* stg = blk + 16 * 128 + warp * 512;                   // 8 x 512 floats (into acc_s)
+    static_assert((16 * 128 + 8 * 512) * 4 <= kOffInv - kOffBlk, "epilogue scratch");
+    int n_xch = 0;
     int i = 0;
     for (int t = blockIdx.x; t < n_items; t += G, ++i) {
       const int mt = t % m_tiles, wt2 = t / m_tiles;
       const int buf = i & 1;
+      // this lane's row and its 1 / rms, before the wait (overlaps the MMAs)
+      const int row = mt * 128 + quad * 32 + lane;
+      float inv = 1.f;
+      if (direct && p.row_scale && row < p.M) inv = row_inv_rms(p, row);
       const bool ok = s_abort || bar_wait(&accf[buf], (uint32_t)((i >> 1) & 1));
       if (!ok && lane == 0) atomicOr(p.status, 0x4u);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      for (int sub = 0; sub < kNsub; ++sub) {
+      for (int sub = 0; direct && sub < kNsub; ++sub) {
+        const int nt = kNsub * wt2 + sub;
+        if (nt >= p.n_tiles) break;
+        epi_direct(p, tmem + buf * kAccCols + ((uint32_t)(quad * 32) << 16) + sub * 128, nt, mt, row, inv,
+                   quad, half, lane, wscr, xch, stg, n_xch, &s_flag);
+      }
+      for (int sub = 0; !direct && sub < kNsub; ++sub) {
         const int nt = kNsub * wt2 + sub;
         if (nt >= p.n_tiles) break;
         csync();  // the previous n-tile's epilogues are done with scale_s

@@ -130,7 +130,7 @@ struct GemmParams {
   unsigned* status;
   // logits epilogue
   float2* am_part;        // [n_tiles][M] (value, index bits)
-  int* am_counter;
+  int* am_counter;        // [M/16] finished tiles of each 16-row block, zero between launches
   int32_t* drafts;        // [M/16][15]; rows at or past block_width draft -1
   int block_width;
   // L2 prefetch of the next kernel's input (pf_count ranges of pf_bytes at
