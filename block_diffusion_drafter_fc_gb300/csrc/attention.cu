@@ -1029,6 +1029,386 @@ __global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constan
   }
 }
 
+// ---------------------------------------------------------------------------
+// Stream-K attention (batches whose split grid does not fit one wave).
+//
+// A planning kernel, once per step, lists every sequence's 64-slot
+// sub-chunks that hold a key of block row 0's window (the widest of the
+// block's rows: a sub-chunk without one has none for any row), in ring order.
+// Work units are pairs of listed sub-chunks (one per key lane), at least one
+// per (sequence, kv head, head group) for the block's own keys; the units of
+// all groups form one axis, and a persistent grid of one CTA per SM takes
+// equal contiguous ranges of it, so every CTA attends the same number of
+// sub-chunks and no empty one is loaded.  One thread issues the next unit's
+// copies (the ring tiles by TMA, their slot positions by a bulk copy, on one
+// mbarrier per buffer set) into the other of two buffer sets while the CTA
+// attends the current one.  A group wholly inside one CTA's range is
+// normalised and written at once; a group cut by range boundaries publishes
+// one partial per contributor (slot 2c for the part that starts CTA c's range
+// or lies inside it, 2c + 1 for the part that ends it) and the last
+// contributor (acquire-release ticket) merges them in CTA order, so results do
+// not depend on timing.  The block's own keys are attended with the group's
+// first unit.
+// ---------------------------------------------------------------------------
+
+constexpr int kStreamKq = 2;       // key lanes (sub-chunks per unit)
+constexpr int kStreamMaxSub = 64;  // 64-slot sub-chunks per window (window <= 4096)
+
+__global__ void __launch_bounds__(1024) attn_plan_kernel(const int32_t* ring_pos, const int32_t* n_past, int n_seq,
+                                                         int window, int groups_per_seq, int* prefix, int* nv,
+                                                         int* sub) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_sub = (window + kSub - 1) / kSub;
+  for (int s = warp; s < n_seq; s += (int)(blockDim.x >> 5)) {
+    const int p0 = max(n_past[s], 0);
+    bool v[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int sc = lane + 32 * e;
+      bool any = false;
+      if (sc < n_sub) {
+        const int s0 = sc * kSub, nk = min(kSub, window - s0);   // a multiple of 4
+        const int4* rp = reinterpret_cast<const int4*>(ring_pos + (size_t)s * window + s0);
+        for (int i = 0; i < nk / 4; ++i) {
+          const int4 k4 = rp[i];
+          const int kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) any |= kk[q] >= 0 && kk[q] < p0 && p0 - kk[q] < window;
+        }
+      }
+      v[e] = any;
+    }
+    const unsigned b0 = __ballot_sync(0xffffffffu, v[0]), b1 = __ballot_sync(0xffffffffu, v[1]);
+    const unsigned below = (1u << lane) - 1u;
+    if (v[0]) sub[(size_t)s * kStreamMaxSub + __popc(b0 & below)] = lane;
+    if (v[1]) sub[(size_t)s * kStreamMaxSub + __popc(b0) + __popc(b1 & below)] = lane + 32;
+    if (lane == 0) nv[s] = __popc(b0) + __popc(b1);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int s = 0; s < n_seq; ++s) {
+      prefix[s] = acc;
+      acc += max(1, (nv[s] + 1) / 2) * groups_per_seq;
+    }
+    prefix[n_seq] = acc;
+  }
+}
+
+template <int HD>
+struct StreamSmem {
+  using SM = AttnSmem<HD>;
+  static constexpr size_t SET = (size_t)kStreamKq * 2 * SM::TILE_SW * 2;   // K + V tiles of each lane
+  static constexpr size_t OFF_BLK = 2 * SET;
+  static constexpr size_t OFF_FRAG = OFF_BLK + (size_t)SM::BLK * 2;
+  static constexpr size_t OFF_KPOS = OFF_FRAG + (size_t)4 * (HD / 8) * 32 * 16 + (size_t)4 * 32 * 16;
+  static constexpr size_t OFF_PLAN = OFF_KPOS + (size_t)2 * kStreamKq * kSub * 4;
+  static constexpr size_t BYTES = OFF_PLAN + (size_t)(2 * kAttnStreamMaxSeq + 1) * 4 + 1024;   // + alignment
+};
+
+template <int HD>
+__global__ void __launch_bounds__(256, 1) attn_stream_kernel(const __grid_constant__ AttnParams p) {
+  using SM = AttnSmem<HD>;
+  using SS = StreamSmem<HD>;
+  constexpr int KS = SM::KS, TS = SM::TILE_SW, KQ = kStreamKq;
+  const int G = p.n_head / p.n_head_kv, hpc = p.hpc, n_hgrp = G / hpc;
+  const int gps = p.n_head_kv * n_hgrp;   // groups per sequence
+  const int qd = p.n_head * HD, kvd = p.n_head_kv * HD;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int nthreads = (int)blockDim.x;
+  const int hl = warp / KQ, lk = warp - hl * KQ;
+  const int R = kBlock * hpc;
+  extern __shared__ __align__(16) uint8_t sm_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+  uint16_t* sets = reinterpret_cast<uint16_t*>(base);   // [2][KQ][K tile, V tile]
+  uint16_t* blk_k_hi = reinterpret_cast<uint16_t*>(base + SS::OFF_BLK);
+  uint16_t* blk_k_lo = blk_k_hi + kBlock * KS;
+  uint16_t* blk_v_hi = blk_k_lo + kBlock * KS;
+  uint16_t* blk_v_lo = blk_v_hi + kBlock * KS;
+  float4* frag_o = reinterpret_cast<float4*>(base + SS::OFF_FRAG);   // key lane 1: [hpc][HD/8][32]
+  float4* frag_ml = frag_o + (size_t)4 * (HD / 8) * 32;               // [hpc][32]
+  int* kpos = reinterpret_cast<int*>(base + SS::OFF_KPOS);            // [2][KQ][64]
+  int* s_prefix = reinterpret_cast<int*>(base + SS::OFF_PLAN);        // [n_seq + 1] units before each sequence
+  int* s_nv = s_prefix + p.n_seq + 1;                                 // [n_seq] listed sub-chunks
+  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ int s_flag;
+
+  // the plan was written by the kernel before the step's first projection
+  // (which starts only once the plan kernel has completed)
+  for (int i = tid; i <= p.n_seq; i += nthreads) s_prefix[i] = p.plan_prefix[i];
+  for (int i = tid; i < p.n_seq; i += nthreads) s_nv[i] = p.plan_nv[i];
+  if (tid == 0) {
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    stamp_begin(p.stamp);
+  }
+  __syncthreads();
+  pdl_trigger();
+  const long long T = s_prefix[p.n_seq];
+  const int b = blockIdx.x, GC = gridDim.x;
+  const long long u0 = T * b / GC, u1 = T * (b + 1) / GC;
+  auto owner = [&](long long u) { return (int)(((u + 1) * GC - 1) / T); };
+  const size_t plane = (size_t)p.window * HD;
+  struct Unit {
+    int seq, gi, k, nu, nv;
+  };
+  auto decode = [&](long long u) {
+    int lo = 0, hi = p.n_seq;   // the sequence s with prefix[s] <= u < prefix[s + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_prefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    Unit x;
+    x.seq = lo;
+    x.nv = s_nv[lo];
+    x.nu = max(1, (x.nv + 1) / 2);
+    const int local = (int)(u - s_prefix[lo]);
+    x.gi = local / x.nu;
+    x.k = local - x.gi * x.nu;
+    return x;
+  };
+
+  // copies of unit u into buffer set st (thread 0): the unit's listed
+  // sub-chunks (zero-filled past the tensor; a slot past the window gets
+  // position -1)
+  auto issue = [&](long long u, int st) {
+    const Unit x = decode(u);
+    const int kvh = x.gi / n_hgrp;
+    const size_t kbase = ((((size_t)x.seq * p.n_layer + p.layer) * 2 + 0) * p.n_head_kv + kvh) * plane;
+    const int row_k = (int)(kbase / HD), row_v = (int)((kbase + (size_t)p.n_head_kv * plane) / HD);
+    uint32_t bytes = 0;
+    int s0s[KQ], nks[KQ];
+#pragma unroll
+    for (int j = 0; j < KQ; ++j) {
+      const int li = 2 * x.k + j;
+      s0s[j] = li < x.nv ? p.plan_sub[(size_t)x.seq * kStreamMaxSub + li] * kSub : p.window;
+      nks[j] = s0s[j] < p.window ? min(kSub, p.window - s0s[j]) : 0;
+      if (nks[j] > 0) bytes += (uint32_t)(2 * TS * 2 + nks[j] * 4);
+    }
+    mbar_expect_tx(&s_bar[st], bytes);
+#pragma unroll
+    for (int j = 0; j < KQ; ++j) {
+      int* kp = kpos + (st * KQ + j) * kSub;
+      for (int i = nks[j]; i < kSub; ++i) kp[i] = -1;
+      if (nks[j] == 0) continue;
+      uint16_t* dst = sets + ((size_t)st * KQ + j) * 2 * TS;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+        for (int hb = 0; hb < HD / 64; ++hb)
+          tma_load_2d(dst + kv * TS + hb * kSub * 64, &p.tm_ring, hb * 64, (kv ? row_v : row_k) + s0s[j],
+                      &s_bar[st]);
+      bulk_copy(kp, p.ring_pos + (size_t)x.seq * p.window + s0s[j], (uint32_t)nks[j] * 4, &s_bar[st]);
+    }
+  };
+
+  // the ring and its slot positions were written before the step's first
+  // kernel (launched without overlap): the first unit is staged before the
+  // wait for the q/k/v kernel
+  if (tid == 0 && u0 < u1) issue(u0, 0);
+  pdl_wait();
+
+  const float qscale = p.scale * kLog2e;
+  uint32_t qh[HD / 16][4], ql[HD / 16][4];
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+  float O[HD / 8][4];
+  for (long long u = u0; u < u1; ++u) {
+    const int it = (int)(u - u0), st = it & 1;
+    __syncthreads();   // unit it - 1 is done with the other set, the block keys and the merge area
+    if (tid == 0 && u + 1 < u1) issue(u + 1, st ^ 1);
+    const Unit x = decode(u);
+    const int seq = x.seq, kvh = x.gi / n_hgrp, hg = x.gi - kvh * n_hgrp;
+    const int group = seq * gps + x.gi;
+    const int head0 = kvh * G + hg * hpc;
+    const int p0 = max(p.n_past[seq], 0);
+    const bool seg_first = u == u0 || x.k == 0, seg_last = u + 1 == u1 || x.k == x.nu - 1;
+    if (seg_first) {
+      const float* qr0 = p.q + (size_t)(seq * kBlock + g) * qd + (head0 + hl) * HD;
+      const float* qr1 = qr0 + (size_t)8 * qd;
+#pragma unroll
+      for (int ks = 0; ks < HD / 16; ++ks) {
+        const int k0 = ks * 16 + 2 * t;
+        const float2 a0 = *reinterpret_cast<const float2*>(qr0 + k0);
+        const float2 a1 = *reinterpret_cast<const float2*>(qr1 + k0);
+        const float2 a2 = *reinterpret_cast<const float2*>(qr0 + k0 + 8);
+        const float2 a3 = *reinterpret_cast<const float2*>(qr1 + k0 + 8);
+        split_bf16x2(a0.x * qscale, a0.y * qscale, qh[ks][0], ql[ks][0]);
+        split_bf16x2(a1.x * qscale, a1.y * qscale, qh[ks][1], ql[ks][1]);
+        split_bf16x2(a2.x * qscale, a2.y * qscale, qh[ks][2], ql[ks][2]);
+        split_bf16x2(a3.x * qscale, a3.y * qscale, qh[ks][3], ql[ks][3]);
+      }
+      m0 = m1 = -CUDART_INF_F;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int jd = 0; jd < HD / 8; ++jd) O[jd][0] = O[jd][1] = O[jd][2] = O[jd][3] = 0.f;
+    }
+    if (x.k == 0) {   // the group's first unit: the block's own 16 keys
+      for (int idx = tid; idx < kBlock * (HD / 4); idx += nthreads) {
+        const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+        const size_t o = (size_t)(seq * kBlock + row) * kvd + kvh * HD + d;
+        const float4 kr = *reinterpret_cast<const float4*>(p.kblk + o);
+        const float4 vr = *reinterpret_cast<const float4*>(p.vblk + o);
+        uint2 h, l;
+        split_bf16x2(kr.x, kr.y, h.x, l.x);
+        split_bf16x2(kr.z, kr.w, h.y, l.y);
+        *reinterpret_cast<uint2*>(blk_k_hi + row * KS + d) = h;
+        *reinterpret_cast<uint2*>(blk_k_lo + row * KS + d) = l;
+        split_bf16x2(vr.x, vr.y, h.x, l.x);
+        split_bf16x2(vr.z, vr.w, h.y, l.y);
+        *reinterpret_cast<uint2*>(blk_v_hi + row * KS + d) = h;
+        *reinterpret_cast<uint2*>(blk_v_lo + row * KS + d) = l;
+      }
+      __syncthreads();
+      // the lane without a listed sub-chunk when the group has an odd count
+      if (lk == KQ - 1)
+        attend_tile<HD, true>(qh, ql, blk_k_hi, blk_k_lo, blk_v_hi, blk_v_lo, KS, 2, nullptr, true, p0,
+                              p.window, p.block_width, m0, m1, l0, l1, O, lane);
+    }
+    if (!mbar_wait(&s_bar[st], (uint32_t)((it >> 1) & 1))) {
+      if (lane == 0) atomicOr(p.status, 0x4u);
+      mbar_wait(&s_bar[st], (uint32_t)((it >> 1) & 1));   // a second bounded wait before moving on
+    }
+    if (2 * x.k + lk < x.nv) {
+      const int* kp = kpos + (st * KQ + lk) * kSub;
+      const uint16_t* kh = sets + ((size_t)st * KQ + lk) * 2 * TS;
+      attend_tile<HD, false, true>(qh, ql, kh, nullptr, kh + TS, nullptr, KS, 8, kp, false, p0, p.window, 16,
+                                   m0, m1, l0, l1, O, lane);
+    }
+    if (!seg_last) continue;
+
+    // ---- the segment's last unit: merge the key lanes (lane order), then
+    // write the group's output or this contributor's partial
+    if (lk > 0) {
+#pragma unroll
+      for (int jd = 0; jd < HD / 8; ++jd)
+        frag_o[((size_t)hl * (HD / 8) + jd) * 32 + lane] = make_float4(O[jd][0], O[jd][1], O[jd][2], O[jd][3]);
+      frag_ml[hl * 32 + lane] = make_float4(m0, m1, l0, l1);
+    }
+    __syncthreads();
+    if (lk == 0) {
+      const float4 ml = frag_ml[hl * 32 + lane];
+      const float n0 = fmaxf(m0, ml.x), n1 = fmaxf(m1, ml.y);
+      const float a0 = m0 == -CUDART_INF_F ? 0.f : exp2f(m0 - n0);
+      const float b0 = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - n0);
+      const float a1 = m1 == -CUDART_INF_F ? 0.f : exp2f(m1 - n1);
+      const float b1 = ml.y == -CUDART_INF_F ? 0.f : exp2f(ml.y - n1);
+      m0 = n0;
+      m1 = n1;
+      l0 = a0 * l0 + b0 * ml.z;
+      l1 = a1 * l1 + b1 * ml.w;
+#pragma unroll
+      for (int jd = 0; jd < HD / 8; ++jd) {
+        const float4 v = frag_o[((size_t)hl * (HD / 8) + jd) * 32 + lane];
+        O[jd][0] = a0 * O[jd][0] + b0 * v.x;
+        O[jd][1] = a0 * O[jd][1] + b0 * v.y;
+        O[jd][2] = a1 * O[jd][2] + b1 * v.z;
+        O[jd][3] = a1 * O[jd][3] + b1 * v.w;
+      }
+    }
+    const long long gu0 = s_prefix[seq] + (long long)x.gi * x.nu;
+    const int first = owner(gu0), last = owner(gu0 + x.nu - 1);
+    if (first == last) {   // the whole window in this CTA: normalise and write
+      if (lk == 0) {
+        const float i0 = 1.f / l0, i1 = 1.f / l1;
+        uint16_t* oh = p.out_hi + (size_t)(seq * kBlock + g) * qd + (head0 + hl) * HD + 2 * t;
+        uint16_t* ol = p.out_lo + (size_t)(seq * kBlock + g) * qd + (head0 + hl) * HD + 2 * t;
+#pragma unroll
+        for (int jd = 0; jd < HD / 8; ++jd) {
+          uint32_t h, l;
+          split_pair16x2(O[jd][0] * i0, O[jd][1] * i0, p.pair_f16 != 0, h, l);
+          *reinterpret_cast<uint32_t*>(oh + 8 * jd) = h;
+          *reinterpret_cast<uint32_t*>(ol + 8 * jd) = l;
+          split_pair16x2(O[jd][2] * i1, O[jd][3] * i1, p.pair_f16 != 0, h, l);
+          *reinterpret_cast<uint32_t*>(oh + (size_t)8 * qd + 8 * jd) = h;
+          *reinterpret_cast<uint32_t*>(ol + (size_t)8 * qd + 8 * jd) = l;
+        }
+      }
+      continue;
+    }
+    auto slot_of = [&](int c) { return (size_t)(2 * c + (c == first ? 1 : 0)) * R; };
+    if (lk == 0) {
+      const size_t row0 = slot_of(b) + hl * kBlock + g;
+      float* o0 = p.part_o + row0 * HD + 2 * t;
+      float* o1 = o0 + (size_t)8 * HD;
+#pragma unroll
+      for (int jd = 0; jd < HD / 8; ++jd) {
+        __stcg(reinterpret_cast<float2*>(o0 + 8 * jd), make_float2(O[jd][0], O[jd][1]));
+        __stcg(reinterpret_cast<float2*>(o1 + 8 * jd), make_float2(O[jd][2], O[jd][3]));
+      }
+      if (t == 0) {
+        __stcg(p.part_ml + row0, make_float2(m0, l0));
+        __stcg(p.part_ml + row0 + 8, make_float2(m1, l1));
+      }
+    }
+    // ticket (acquire-release; the barrier orders every thread's partial
+    // stores before it): the last contributor merges the group
+    __syncthreads();
+    if (tid == 0) {
+      int* cnt = p.counters + 2 * group;
+      s_flag = atom_add_acq_rel_gpu(cnt, 1) == last - first;
+      if (s_flag) *cnt = 0;
+    }
+    __syncthreads();
+    if (!s_flag) continue;
+    // merge: thread -> (row, 4 dims); contributors in CTA order, online rescale
+    constexpr int kB = 4;
+    for (int i0 = tid; i0 < R * (HD / 4); i0 += kB * nthreads) {
+      float M[kB], L[kB];
+      float4 acc[kB];
+#pragma unroll
+      for (int q = 0; q < kB; ++q) {
+        M[q] = -CUDART_INF_F;
+        L[q] = 0.f;
+        acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int c = first; c <= last; ++c) {
+        const size_t s0 = slot_of(c);
+        float2 ml[kB];
+        float4 v[kB];
+#pragma unroll
+        for (int q = 0; q < kB; ++q) {
+          const int idx = i0 + q * nthreads;
+          if (idx < R * (HD / 4)) {
+            const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+            ml[q] = __ldcg(p.part_ml + s0 + row);
+            v[q] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (s0 + row) * HD + d));
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kB; ++q) {
+          if (i0 + q * nthreads >= R * (HD / 4)) continue;
+          const float n = fmaxf(M[q], ml[q].x);
+          const float a = M[q] == -CUDART_INF_F ? 0.f : exp2f(M[q] - n);
+          const float w = ml[q].x == -CUDART_INF_F ? 0.f : exp2f(ml[q].x - n);
+          M[q] = n;
+          L[q] = a * L[q] + w * ml[q].y;
+          acc[q].x = a * acc[q].x + w * v[q].x;
+          acc[q].y = a * acc[q].y + w * v[q].y;
+          acc[q].z = a * acc[q].z + w * v[q].z;
+          acc[q].w = a * acc[q].w + w * v[q].w;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kB; ++q) {
+        const int idx = i0 + q * nthreads;
+        if (idx >= R * (HD / 4)) continue;
+        const int row = idx / (HD / 4), d = (idx - row * (HD / 4)) * 4;
+        const int h = row / kBlock, i = row - h * kBlock;
+        const float inv = 1.f / L[q];
+        const size_t at = (size_t)(seq * kBlock + i) * qd + (head0 + h) * HD + d;
+        uint2 hi, lo;
+        split_pair16x2(acc[q].x * inv, acc[q].y * inv, p.pair_f16 != 0, hi.x, lo.x);
+        split_pair16x2(acc[q].z * inv, acc[q].w * inv, p.pair_f16 != 0, hi.y, lo.y);
+        *reinterpret_cast<uint2*>(p.out_hi + at) = hi;
+        *reinterpret_cast<uint2*>(p.out_lo + at) = lo;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) stamp_finish(p.stamp);
+}
+
 int attn_cluster_size(int window) {
   int cl = (window + 255) / 256;
   return cl < 1 ? 1 : (cl > kMaxCluster ? kMaxCluster : cl);
@@ -1268,6 +1648,61 @@ static int split_capacity(const SplitPlan& s, bool query) {
   return per_sm * n_sm;
 }
 
+// ---- stream-K launch: bf16 ring staged by TMA (hd >= 64), a window of at most
+// kStreamMaxSub sub-chunks whose length is a multiple of 4 slots (16-byte
+// copies of the slot positions), one CTA per SM
+static int g_n_sm = 0;
+static int sm_count() {
+  if (!g_n_sm) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      g_n_sm = n;
+    else
+      (void)cudaGetLastError();
+  }
+  return g_n_sm > 0 ? g_n_sm : 1;
+}
+template <int HD>
+static cudaError_t configure_stream() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(attn_stream_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)StreamSmem<HD>::BYTES);
+  if (e == cudaSuccess) done = true;
+  (void)sm_count();
+  return e;
+}
+template <int HD, bool F32>
+static bool stream_fits(const AttnParams& p, int n_seq) {
+  return !F32 && HD >= 64 && p.part_o && p.plan_prefix && p.window % 4 == 0 &&
+         (p.window + kSub - 1) / kSub <= kStreamMaxSub && n_seq <= kAttnStreamMaxSeq;
+}
+template <int HD>
+static cudaError_t launch_stream(const AttnParams& p_in, int n_seq, int hpc, cudaStream_t st) {
+  AttnParams p = p_in;
+  const int G = p.n_head / p.n_head_kv;
+  p.hpc = hpc;
+  p.kq = kStreamKq;
+  p.nb = 2 * kStreamKq;
+  p.n_seq = n_seq;
+  // the units are counted on the device: one CTA per SM (those past the units
+  // find an empty range); two partial slots per CTA
+  const int grid = std::min(sm_count(), kAttnSplitMaxCtas / 2);
+  (void)G;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(32 * hpc * kStreamKq);
+  cfg.dynamicSmemBytes = StreamSmem<HD>::BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_stream_kernel<HD>, p);
+}
+
 template <int HD, bool F32>
 static cudaError_t configure_split(int G, int window) {
   static size_t configured = 0;   // only ever raised, so every live handle still fits
@@ -1286,6 +1721,9 @@ static cudaError_t configure_split(int G, int window) {
 cudaError_t configure_attention(int group, int hd, int ring_f32, int window, int n_head_kv) {
   cudaError_t e = configure_attention_cluster(group, hd, ring_f32, window, n_head_kv);
   if (e != cudaSuccess) return e;
+  if (!ring_f32 && hd == 64) e = configure_stream<64>();
+  if (!ring_f32 && hd == 128) e = configure_stream<128>();
+  if (e != cudaSuccess) return e;
   switch (hd) {
     case 32: return ring_f32 ? configure_split<32, true>(group, window) : configure_split<32, false>(group, window);
     case 64: return ring_f32 ? configure_split<64, true>(group, window) : configure_split<64, false>(group, window);
@@ -1294,14 +1732,27 @@ cudaError_t configure_attention(int group, int hd, int ring_f32, int window, int
   return cudaErrorInvalidValue;
 }
 
+// Which kernel a step of n_seq sequences takes: the split kernel when its grid
+// is resident at once, else stream-K where it applies, else clusters.
+template <int HD, bool F32>
+static int attention_kind_t(const AttnParams& p, int n_seq) {
+  const int G = p.n_head / p.n_head_kv;
+  const SplitPlan s = split_plan(G, p.window);
+  const long long grid = (long long)n_seq * p.n_head_kv * (G / s.hpc) * s.n_split;
+  const int cap = split_capacity<HD, F32>(s, false);
+  if (p.part_o && s.n_split <= kMaxSplit && grid <= cap && grid <= kAttnSplitMaxCtas) return ATTN_SPLIT;
+  return stream_fits<HD, F32>(p, n_seq) ? ATTN_STREAM : ATTN_CLUSTER;
+}
+
 template <int HD, bool F32>
 static cudaError_t launch_split_or_cluster(const AttnParams& p_in, int n_seq, cudaStream_t st) {
   const int G = p_in.n_head / p_in.n_head_kv;
   const SplitPlan s = split_plan(G, p_in.window);
-  const long long grid = (long long)n_seq * p_in.n_head_kv * (G / s.hpc) * s.n_split;
-  const int cap = split_capacity<HD, F32>(s, false);
-  if (!p_in.part_o || s.n_split > kMaxSplit || grid > cap || grid > kAttnSplitMaxCtas)
-    return launch_cl<HD, F32>(p_in, n_seq, st);
+  const int kind = attention_kind_t<HD, F32>(p_in, n_seq);
+  if (kind == ATTN_STREAM) {
+    if constexpr (!F32 && HD >= 64) return launch_stream<HD>(p_in, n_seq, s.hpc, st);
+  }
+  if (kind != ATTN_SPLIT) return launch_cl<HD, F32>(p_in, n_seq, st);
   AttnParams p = p_in;
   p.hpc = s.hpc;
   p.kq = s.kq;
@@ -1317,6 +1768,26 @@ static cudaError_t launch_split_or_cluster(const AttnParams& p_in, int n_seq, cu
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, attn_split_kernel<HD, F32>, p);
+}
+
+cudaError_t launch_attention_plan(const AttnParams& p, int n_seq, cudaStream_t st) {
+  const int G = p.n_head / p.n_head_kv;
+  const int hpc = split_plan(G, p.window).hpc;
+  // no programmatic-launch attribute and no early trigger: the next kernel
+  // starts once the plan is complete and visible
+  attn_plan_kernel<<<1, 1024, 0, st>>>(p.ring_pos, p.n_past, n_seq, p.window, p.n_head_kv * (G / hpc),
+                                       p.plan_prefix, p.plan_nv, p.plan_sub);
+  return cudaGetLastError();
+}
+
+int attention_kind(const AttnParams& p, int n_seq) {
+  const bool f32 = !p.ring_bf16;
+  switch (p.hd) {
+    case 32: return f32 ? attention_kind_t<32, true>(p, n_seq) : attention_kind_t<32, false>(p, n_seq);
+    case 64: return f32 ? attention_kind_t<64, true>(p, n_seq) : attention_kind_t<64, false>(p, n_seq);
+    case 128: return f32 ? attention_kind_t<128, true>(p, n_seq) : attention_kind_t<128, false>(p, n_seq);
+  }
+  return ATTN_CLUSTER;
 }
 
 cudaError_t launch_attention(const AttnParams& p, int n_seq, cudaStream_t st) {

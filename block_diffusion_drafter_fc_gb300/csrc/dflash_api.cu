@@ -106,6 +106,7 @@ struct Layout {
   size_t logits_int, drafts_int, idl_int, npast_int, partial;
   size_t inj_raw, inj_ss, inj_rope, inj_hi, inj_lo, loop_pos, loop_cnt, loop_H, stamps;
   size_t attn_part, attn_ml, attn_cnt, chain_partial, chain_cnt, chain_item, chain_mb, chain_done;
+  size_t plan_prefix, plan_nv, plan_sub;
   size_t total;
   int attn_groups, chain_item_stride;
   size_t partial_floats;
@@ -176,6 +177,10 @@ Layout layout(const dflash_config& c) {
   L.attn_ml = take(sizeof(float2) * (size_t)kAttnSplitMaxCtas * 64);
   L.attn_groups = g.max_seq * g.Hq;
   L.attn_cnt = take(sizeof(int) * 2 * (size_t)L.attn_groups);
+  // stream-K attention plan: units before each sequence, listed sub-chunks
+  L.plan_prefix = take(sizeof(int) * (size_t)(g.max_seq + 1));
+  L.plan_nv = take(sizeof(int) * (size_t)g.max_seq);
+  L.plan_sub = take(sizeof(int) * (size_t)g.max_seq * 64);
   // projection chains: per phase its partial tiles and tickets, item flags and
   // per-block counts; one chain counter
   L.chain_partial = take(sizeof(float) * (size_t)kChainMax * 2 * kGemmGrid * 16 * kTileRows);
@@ -597,7 +602,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     bind_projection(h, p, -1, {0}, XP_XN);
     return p;
   };
-  auto attention = [&](int l) -> int {
+  auto attn_params = [&](int l) {
     AttnParams a;
     std::memset(&a, 0, sizeof(a));
     a.q = h->S<float>(L.qbuf); a.kblk = h->S<float>(L.kblk); a.vblk = h->S<float>(L.vblk);
@@ -613,10 +618,21 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.part_o = h->S<float>(L.attn_part);
     a.part_ml = h->S<float2>(L.attn_ml);
     a.counters = h->S<int>(L.attn_cnt);
+    a.plan_prefix = h->S<int>(L.plan_prefix);
+    a.plan_nv = h->S<int>(L.plan_nv);
+    a.plan_sub = h->S<int>(L.plan_sub);
+    return a;
+  };
+  auto attention = [&](int l) -> int {
+    AttnParams a = attn_params(l);
     a.stamp = stamp_slot(h, PC_ATTN);
     PROF(h, PC_ATTN, st, launch_attention(a, n_seq, st));
     return DFLASH_OK;
   };
+  // the stream-K attention's plan of this step (its ring and positions do not
+  // change within the step: one plan serves every layer)
+  if (attention_kind(attn_params(0), n_seq) == ATTN_STREAM)
+    PROF(h, PC_ATTN, st, launch_attention_plan(attn_params(0), n_seq, st));
 
   // 16-row blocks with bf16 / fp32 / E4M3 weights: per layer one persistent
   // launch chains o, gate/up, down and the next layer's q/k/v (the LM head
@@ -1111,6 +1127,19 @@ int dflash_set_chain(dflash_handle* h, int32_t enable) {
   if (enable && !h->chain_ok) return DFLASH_ERR_UNSUPPORTED;
   h->chain = enable != 0;
   return DFLASH_OK;
+}
+
+int dflash_attention_kernel(const dflash_handle* h, int32_t n_seq) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (n_seq < 1 || n_seq > h->g.max_seq) return DFLASH_ERR_SEQ_RANGE;
+  const Geometry& g = h->g;
+  AttnParams a;
+  std::memset(&a, 0, sizeof(a));
+  a.ring_bf16 = g.ring_bf16;
+  a.n_head = g.Hq; a.n_head_kv = g.Hkv; a.hd = g.hd; a.window = g.W;
+  a.part_o = h->S<float>(h->L.attn_part);
+  a.plan_prefix = h->S<int>(h->L.plan_prefix);
+  return attention_kind(a, n_seq);
 }
 
 int dflash_set_block_width(dflash_handle* h, int32_t width) {

@@ -33,7 +33,6 @@ namespace dflash {
 
 namespace umma {
 
-constexpr int kS = 3;                  // pipeline stages
 constexpr int kTile = 128 * 128;       // bytes of one [128 rows x 128 B] swizzled tile
 constexpr long long kWait = 4000000000LL;
 constexpr int kThreads = 448;          // warps 0-7 epilogue, 8-11 E4M3 widening, 12 TMA, 13 MMA
@@ -45,6 +44,8 @@ constexpr int kPf = 6;                 // weight chunks prefetched into L2 ahead
 // (WR = 128, or 256 = two 128-row n-tiles sharing every activation chunk).
 template <int WR>
 struct L {
+  // pipeline stages: as many as shared memory holds next to the epilogue scratch
+  static constexpr int kS = WR == 128 ? 4 : 3;
   static constexpr int kWTile = WR * 128;   // bf16 [WR x 64] swizzled weight tile
   static constexpr int kWRaw = WR * 64;     // raw [WR x 64] E4M3 (upper half of kWTile)
   static constexpr int kAccCols = WR;       // TMEM columns of one accumulator buffer (fp32)
@@ -451,6 +452,7 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
   constexpr int kOffBlk = Lt::kOffBlk, kOffAcc = Lt::kOffAcc, kOffInv = Lt::kOffInv;
   constexpr int kOffScale = Lt::kOffScale, kOffBars = Lt::kOffBars, kOffTmem = Lt::kOffTmem;
   constexpr int kNsub = WR / 128;   // 128-row n-tiles per output tile
+  constexpr int kS = Lt::kS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* blk = reinterpret_cast<float*>(sm + kOffBlk);
@@ -749,7 +751,9 @@ __global__ void __launch_bounds__(umma::kThreads, 1) gemm_umma_kernel(const __gr
   }
 }
 
-size_t gemm_umma_smem_bytes() { return umma::L<256>::kSmem; }
+size_t gemm_umma_smem_bytes() {
+  return umma::L<256>::kSmem > umma::L<128>::kSmem ? umma::L<256>::kSmem : umma::L<128>::kSmem;
+}
 
 cudaError_t configure_gemm_umma() {
   cudaError_t e = cudaSuccess;
@@ -780,9 +784,7 @@ static cudaError_t launch_umma_t(const GemmParams& p, int n_sm, cudaStream_t st)
 }
 
 // 256-row weight tiles (half the activation traffic per flop) when they still
-// give every SM a tile, else 128-row tiles for more parallelism.  The logits
-// epilogue (an fp32 store of every output plus the argmax partials) is the
-// heaviest; its tiles stay 128 rows so that it keeps pace with the MMAs.
+// give every SM a tile, else 128-row tiles for more parallelism.
 cudaError_t launch_gemm_umma(int wt, const GemmParams& p, cudaStream_t st) {
   static int n_sm = 0;
   if (!n_sm) {
@@ -791,7 +793,7 @@ cudaError_t launch_gemm_umma(int wt, const GemmParams& p, cudaStream_t st) {
     cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     if (n_sm <= 0) n_sm = 1;
   }
-  const bool wide = p.epi != EPI_LOGITS && (p.M + 127) / 128 * ((p.n_tiles + 1) / 2) >= n_sm;
+  const bool wide = (p.M + 127) / 128 * ((p.n_tiles + 1) / 2) >= n_sm;
   if (wt == W_BF16) return wide ? launch_umma_t<W_BF16, 256>(p, n_sm, st) : launch_umma_t<W_BF16, 128>(p, n_sm, st);
   if (wt == W_FP8) return wide ? launch_umma_t<W_FP8, 256>(p, n_sm, st) : launch_umma_t<W_FP8, 128>(p, n_sm, st);
   return cudaErrorInvalidValue;

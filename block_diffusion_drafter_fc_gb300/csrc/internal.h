@@ -171,10 +171,27 @@ struct AttnParams {
   float* part_o;
   float2* part_ml;
   int* counters;
+  int n_seq;              // sequences of the step (set by the launcher)
+  // stream-K kernel: the step's plan (attn_plan_kernel): units before each
+  // sequence [n_seq + 1], listed sub-chunks per sequence [n_seq] and their
+  // indices [n_seq][64] (null: no stream-K)
+  int* plan_prefix;
+  int* plan_nv;
+  int* plan_sub;
 };
 
+// attention kernel of a step: split window (one resident wave), stream-K over
+// all groups' windows (larger batches), or clusters with a DSMEM merge
+enum AttnKind { ATTN_SPLIT = 0, ATTN_CLUSTER = 1, ATTN_STREAM = 2 };
+int attention_kind(const AttnParams& p, int n_seq);
+// the step's stream-K plan (before the step's first projection, when
+// attention_kind is ATTN_STREAM)
+cudaError_t launch_attention_plan(const AttnParams& p, int n_seq, cudaStream_t st);
+constexpr int kAttnStreamMaxSeq = 1024;   // sequences of a stream-K step (its shared plan table)
+
 // split-window attention: largest grid (CTAs) it is launched with, and the
-// largest rows x head_dim of one CTA's partial (16 rows x 4 heads x 128)
+// largest rows x head_dim of one CTA's partial (16 rows x 4 heads x 128); the
+// stream-K kernel keeps two partials per CTA in the same scratch
 constexpr int kAttnSplitMaxCtas = 512;
 constexpr int kAttnPartFloats = 64 * 128;
 

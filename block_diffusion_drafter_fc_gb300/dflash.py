@@ -81,6 +81,7 @@ def _load() -> C.CDLL:
         "dflash_advance": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_set_block_width": (C.c_int, [vp, i32]),
         "dflash_set_chain": (C.c_int, [vp, i32]),
+        "dflash_attention_kernel": (C.c_int, [vp, i32]),
         "dflash_capture_loop": (C.c_int, [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp]),
         "dflash_step_host": (C.c_int, [vp, i32, vp, vp, vp, vp, vp]),
         "dflash_ring_reset": (C.c_int, [vp, i32, vp]),
@@ -256,6 +257,12 @@ class Drafter:
 
     def dflash_set_chain(self, enable: bool):
         _check(LIB.dflash_set_chain(self.h, int(bool(enable))), self.h, "set_chain")
+
+    def dflash_attention_kernel(self, n_seq: int) -> int:
+        """Attention kernel of a step of n_seq sequences: 0 split, 1 clusters, 2 stream-K."""
+        rc = LIB.dflash_attention_kernel(self.h, int(n_seq))
+        _check(min(rc, 0), self.h, "attention_kernel")
+        return rc
 
     def dflash_set_block_width(self, width: int):
         _check(LIB.dflash_set_block_width(self.h, int(width)), self.h, "set_block_width")

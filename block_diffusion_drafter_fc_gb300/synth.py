@@ -202,10 +202,21 @@ SPLIT_F32 = DraftConfig(
     name="split_f32", n_layer=1, n_embd=512, n_head=8, n_head_kv=2, head_dim=128,
     n_ff=512, window=320, n_vocab=600, weight_dtype="f32", dense_dtype="f32",
     ring_dtype="f32", inject=((0, 320), (320, 50)), seed=2012)
+# batches whose split grid exceeds one wave (stream-K attention): windows cut
+# across CTAs and merged, head_dim 128 with four query heads per kv head, and
+# head_dim 64 with a window that ends inside a 64-slot sub-chunk
+STREAM_H128 = DraftConfig(
+    name="stream_h128", n_layer=1, n_embd=512, n_head=8, n_head_kv=2, head_dim=128,
+    n_ff=512, window=576, n_vocab=600, weight_dtype="bf16", dense_dtype="bf16",
+    ring_dtype="bf16", n_seq=24, fill_lo=40, fill_hi=576, offset_hi=5000, seed=2013)
+STREAM_H64 = DraftConfig(
+    name="stream_h64", n_layer=2, n_embd=256, n_head=4, n_head_kv=2, head_dim=64,
+    n_ff=512, window=456, n_vocab=500, weight_dtype="bf16", dense_dtype="bf16",
+    ring_dtype="bf16", n_seq=72, fill_lo=10, fill_hi=456, offset_hi=3000, seed=2014)
 TEST_CONFIGS: Dict[str, DraftConfig] = {c.name: c for c in (RAGGED, SMALL_FP8, MIXED_F32, DENSE_FP8,
                                                             DENSE_BF16, WIDE_FP8, WIDE_BF16, MANY_SEQ,
                                                             SMALL_FP4, RAGGED_FP4, SPLIT_BF16,
-                                                            SPLIT_F32)}
+                                                            SPLIT_F32, STREAM_H128, STREAM_H64)}
 
 
 def get_config(name: str) -> DraftConfig:

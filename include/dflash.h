@@ -285,6 +285,19 @@ DFLASH_API int dflash_set_block_width(dflash_handle* h, int32_t width);
 DFLASH_API int dflash_set_chain(dflash_handle* h, int32_t enable);
 
 /*
+ * The attention kernel a step of n_seq sequences runs (the choice is
+ * automatic; this reports it for tests and benchmarks): 0 = split window (the
+ * window of every (sequence, kv head) in 128-slot CTAs that the GPU holds at
+ * once, merged through global scratch), 1 = clusters (a kv head's window over
+ * up to 8 CTAs of a cluster, merged through distributed shared memory), 2 =
+ * stream-K (one CTA per SM streaming equal ranges of all windows through a
+ * double-buffered TMA pipeline; windows cut by a range merge their partials).
+ * Returns the kind, INVALID_ARG for a null handle, SEQ_RANGE for n_seq outside
+ * 1..max_seq.
+ */
+DFLASH_API int dflash_attention_kernel(const dflash_handle* h, int32_t n_seq);
+
+/*
  * One block step for sequences 0..n_seq-1 (dflash-ops model card, Usage:
  * step(id_last, n_past) -> logits [16, n_vocab]; drafts = argmax of rows 1..15).
  *   id_last: device int32 [n_seq], the anchor token of each block;

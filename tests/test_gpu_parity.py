@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 
 SMALL = ["tiny_f32", "ragged_bf16", "mixed_f32w_bf16ring", "small_fp8", "dense_fp8", "dense_bf16",
          "wide_fp8", "wide_bf16", "many_seq_bf16", "small_fp4", "ragged_fp4", "split_bf16",
-         "split_f32"]
+         "split_f32", "stream_h128", "stream_h64"]
 
 
 @functools.lru_cache(maxsize=None)
@@ -286,3 +286,20 @@ def test_projection_chain_refused_where_unsupported():
         dr.dflash_set_chain(True)
     dr.dflash_set_chain(False)
     dr.close()
+
+
+# the attention kernel each geometry's step takes (the parity cases above run
+# all three)
+KERNEL_OF = {"split_bf16": 0, "dense_bf16": 0, "split_f32": 0, "many_seq_bf16": 0, "stream_h128": 2,
+             "stream_h64": 2}
+
+
+@pytest.mark.parametrize("name", sorted(KERNEL_OF))
+def test_attention_kernel_choice(name):
+    wl = make_workload(get_config(name))
+    g = GH.gpu_run(wl, keep=True)
+    dr = g["drafter"]
+    assert dr.dflash_attention_kernel(wl.cfg.n_seq) == KERNEL_OF[name]
+    assert dr.dflash_attention_kernel(1) == 0
+    with pytest.raises(Exception):
+        dr.dflash_attention_kernel(0)
