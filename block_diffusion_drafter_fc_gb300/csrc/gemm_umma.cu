@@ -2,29 +2,32 @@
 // steps with at least 128 activation rows (the cross-sequence batch of
 // dflash_head.rs, struct DflashBatch: 16 rows per sequence).
 //
-// Persistent: one CTA per SM walks output tiles D[128 activation rows][128
-// weight rows] (tile t = CTA, CTA + grid, ...; consecutive tiles share a weight
-// tile across the activation row blocks, so weights come from HBM once), each
-// over the whole k range, with the accumulator double-buffered in tensor memory
-// so that a tile's epilogue overlaps the next tile's MMAs:
+// Persistent: one CTA per SM walks output tiles D[128 activation rows][WR
+// weight rows] (WR = 128 or 256; tile t = CTA, CTA + grid, ...; consecutive
+// tiles share a weight tile across the activation row blocks, so weights come
+// from HBM once), each over the whole k range, with the accumulator
+// double-buffered in tensor memory so that a tile's epilogue overlaps the next
+// tile's MMAs:
 //   warp 12 (one lane)  TMA producer: per 64-wide k chunk, the activation hi and
-//                       lo boxes [128 rows x 128 B] and the weight box(es) into
-//                       a 3-stage shared-memory ring (128-byte swizzle, the UMMA
-//                       K-major canonical layout), across tile boundaries;
-//   warps 8..11         E4M3 weights only: widen the raw [128 x 64] byte tile to
+//                       lo boxes [128 rows x 128 B] and the weight boxes into a
+//                       3- or 4-stage shared-memory ring (128-byte swizzle, the
+//                       UMMA K-major canonical layout), across tile boundaries,
+//                       and an L2 prefetch of the weights kPf chunks ahead;
+//   warps 8..11         E4M3 weights only: widen the raw [WR x 64] byte tile to
 //                       the bf16 swizzled tile the MMA reads (exact), then fence
 //                       the generic-proxy writes for the async proxy;
-//   warp 13 (one lane)  allocates 2 x 128 TMEM columns and issues, per k16 step,
+//   warp 13 (one lane)  allocates 2 x WR TMEM columns and issues, per k16 step,
 //                       tcgen05.mma kind::f16 (bf16 x bf16, fp32 accumulate) for
 //                       the activation hi part and again for the lo part (the
 //                       fp32 activations are split into bf16 hi + lo) into the
 //                       tile's accumulator buffer; commits each stage back to
 //                       the producer and each finished tile to the epilogue;
-//   warps 0..7          per 32-lane quadrant of the accumulator, tcgen05.ld into
-//                       two 16-row blocks in shared memory and the fused
-//                       epilogues of the 16-row kernels on each (RMS row scale,
-//                       per-head q/k norm + rope, residual + next input, SwiGLU,
-//                       logits + argmax); then hand the buffer back to the MMA.
+//   warps 0..7          the fused epilogues of the 16-row kernels (RMS row
+//                       scale, per-head q/k norm + rope, residual + next input,
+//                       SwiGLU, logits + argmax): one thread per activation row
+//                       straight from tensor memory (tcgen05.ld), or per 16-row
+//                       block through shared memory for the ring injection;
+//                       then hand the buffer back to the MMA.
 // Every mbarrier wait gives up after ~2 s with DFLASH_DEV_TIMEOUT; tensor memory
 // is always released before exit.
 #include "gemm_common.cuh"
