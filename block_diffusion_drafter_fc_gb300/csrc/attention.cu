@@ -70,6 +70,20 @@ DF_DEVICE void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* b
       : "memory");
 }
 
+// CTA b of G's share of the attention's L2 prefetch range, in 16-byte aligned
+// pieces of at most 32 KB (thread 0: the bulk prefetches take no registers).
+DF_DEVICE void prefetch_share_attn(const AttnParams& p, long long b, long long G) {
+  if (!p.pf_bytes) return;
+  const unsigned long long x0 = (p.pf_bytes * b / G) & ~15ull;
+  const unsigned long long x1 = b == G - 1 ? p.pf_bytes : (p.pf_bytes * (b + 1) / G) & ~15ull;
+  for (unsigned long long x = x0; x < x1;) {
+    unsigned long long n = x1 - x;
+    if (n > 32768) n = 32768;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.pf_base + x), "r"((uint32_t)n) : "memory");
+    x += n;
+  }
+}
+
 DF_DEVICE void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -913,6 +927,11 @@ __global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constan
     }
   }
   __syncthreads();  // the staging buffers become the key-lane merge area
+  // this CTA reads nothing more from HBM: its share of the next projection's
+  // weights moves into L2 during the publication, group wait and merge
+  if (tid == 0)
+    prefetch_share_attn(p, ((long long)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x,
+                        (long long)gridDim.x * gridDim.y * gridDim.z);
 
   // key lanes 1.. hand their (max, sum, O) fragments to key lane 0 through
   // shared memory; it merges them in lane order and publishes the CTA's rows

@@ -178,6 +178,11 @@ struct AttnParams {
   int* plan_prefix;
   int* plan_nv;
   int* plan_sub;
+  // L2 prefetch of the next projection's weights (one contiguous range, null:
+  // none), shared out over the CTAs once the q/k/v kernel has completed: the
+  // attention reads little from HBM, the o projection then streams from L2
+  const char* pf_base;
+  unsigned long long pf_bytes;
 };
 
 // attention kernel of a step: split window (one resident wave), stream-K over
