@@ -1053,7 +1053,8 @@ __global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constan
 //
 // A planning kernel, once per step, lists every sequence's 64-slot
 // sub-chunks that hold a key of block row 0's window (the widest of the
-// block's rows: a sub-chunk without one has none for any row), in ring order.
+// block's rows: a sub-chunk without one has none for any row), in ring order;
+// the attention CTAs sum the units per sequence into a prefix in shared memory.
 // Work units are pairs of listed sub-chunks (one per key lane), at least one
 // per (sequence, kv head, head group) for the block's own keys; the units of
 // all groups form one axis, and a persistent grid of one CTA per SM takes
@@ -1073,45 +1074,38 @@ __global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constan
 constexpr int kStreamKq = 2;       // key lanes (sub-chunks per unit)
 constexpr int kStreamMaxSub = 64;  // 64-slot sub-chunks per window (window <= 4096)
 
-__global__ void __launch_bounds__(1024) attn_plan_kernel(const int32_t* ring_pos, const int32_t* n_past, int n_seq,
-                                                         int window, int groups_per_seq, int* prefix, int* nv,
-                                                         int* sub) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// One CTA per sequence, one thread per 64-slot sub-chunk (window <= 4096): all
+// of a sub-chunk's 64 slot positions are loaded at once.
+__global__ void __launch_bounds__(kStreamMaxSub) attn_plan_kernel(const int32_t* ring_pos, const int32_t* n_past,
+                                                                  int window, int* nv, int* sub) {
+  const int s = blockIdx.x, sc = threadIdx.x, lane = sc & 31, w = sc >> 5;
   const int n_sub = (window + kSub - 1) / kSub;
-  for (int s = warp; s < n_seq; s += (int)(blockDim.x >> 5)) {
-    const int p0 = max(n_past[s], 0);
-    bool v[2];
+  const int p0 = max(n_past[s], 0);
+  bool any = false;
+  if (sc < n_sub) {
+    const int s0 = sc * kSub, nk4 = min(kSub, window - s0) / 4;   // the window is a multiple of 4 slots
+    const int4* rp = reinterpret_cast<const int4*>(ring_pos + (size_t)s * window + s0);
+    int4 k4[kSub / 4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int sc = lane + 32 * e;
-      bool any = false;
-      if (sc < n_sub) {
-        const int s0 = sc * kSub, nk = min(kSub, window - s0);   // a multiple of 4
-        const int4* rp = reinterpret_cast<const int4*>(ring_pos + (size_t)s * window + s0);
-        for (int i = 0; i < nk / 4; ++i) {
-          const int4 k4 = rp[i];
-          const int kk[4] = {k4.x, k4.y, k4.z, k4.w};
+    for (int i = 0; i < kSub / 4; ++i) k4[i] = i < nk4 ? __ldg(rp + i) : make_int4(-1, -1, -1, -1);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) any |= kk[q] >= 0 && kk[q] < p0 && p0 - kk[q] < window;
-        }
-      }
-      v[e] = any;
+    for (int i = 0; i < kSub / 4; ++i) {
+      const int kk[4] = {k4[i].x, k4[i].y, k4[i].z, k4[i].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) any |= kk[q] >= 0 && kk[q] < p0 && p0 - kk[q] < window;
     }
-    const unsigned b0 = __ballot_sync(0xffffffffu, v[0]), b1 = __ballot_sync(0xffffffffu, v[1]);
-    const unsigned below = (1u << lane) - 1u;
-    if (v[0]) sub[(size_t)s * kStreamMaxSub + __popc(b0 & below)] = lane;
-    if (v[1]) sub[(size_t)s * kStreamMaxSub + __popc(b0) + __popc(b1 & below)] = lane + 32;
-    if (lane == 0) nv[s] = __popc(b0) + __popc(b1);
   }
+  __shared__ unsigned s_ball[kStreamMaxSub / 32];
+  const unsigned bal = __ballot_sync(0xffffffffu, any);
+  if (lane == 0) s_ball[w] = bal;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int s = 0; s < n_seq; ++s) {
-      prefix[s] = acc;
-      acc += max(1, (nv[s] + 1) / 2) * groups_per_seq;
-    }
-    prefix[n_seq] = acc;
+  int before = __popc(bal & ((1u << lane) - 1u)), total = 0;
+  for (int i = 0; i < kStreamMaxSub / 32; ++i) {
+    if (i < w) before += __popc(s_ball[i]);
+    total += __popc(s_ball[i]);
   }
+  if (any) sub[(size_t)s * kStreamMaxSub + before] = sc;
+  if (sc == 0) nv[s] = total;
 }
 
 template <int HD>
@@ -1153,9 +1147,34 @@ __global__ void __launch_bounds__(256, 1) attn_stream_kernel(const __grid_consta
   __shared__ int s_flag;
 
   // the plan was written by the kernel before the step's first projection
-  // (which starts only once the plan kernel has completed)
-  for (int i = tid; i <= p.n_seq; i += nthreads) s_prefix[i] = p.plan_prefix[i];
-  for (int i = tid; i < p.n_seq; i += nthreads) s_nv[i] = p.plan_nv[i];
+  // (which starts only once the plan kernel has completed): units of each
+  // sequence -> exclusive prefix over sequences (a block scan)
+  __shared__ int s_wsum[8];
+  {
+    const int per = (p.n_seq + nthreads - 1) / nthreads;
+    const int i0 = min(p.n_seq, tid * per), i1 = min(p.n_seq, i0 + per);
+    int local = 0;
+    for (int i = i0; i < i1; ++i) {
+      const int v = p.plan_nv[i];
+      s_nv[i] = v;
+      local += max(1, (v + 1) / 2) * gps;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < warp; ++w) run += s_wsum[w];
+    for (int i = i0; i < i1; ++i) {
+      s_prefix[i] = run;
+      run += max(1, (s_nv[i] + 1) / 2) * gps;
+    }
+    if (tid == nthreads - 1) s_prefix[p.n_seq] = run;
+  }
   if (tid == 0) {
     mbar_init(&s_bar[0], 1);
     mbar_init(&s_bar[1], 1);
@@ -1694,7 +1713,7 @@ static cudaError_t configure_stream() {
 }
 template <int HD, bool F32>
 static bool stream_fits(const AttnParams& p, int n_seq) {
-  return !F32 && HD >= 64 && p.part_o && p.plan_prefix && p.window % 4 == 0 &&
+  return !F32 && HD >= 64 && p.part_o && p.plan_nv && p.window % 4 == 0 &&
          (p.window + kSub - 1) / kSub <= kStreamMaxSub && n_seq <= kAttnStreamMaxSeq;
 }
 template <int HD>
@@ -1794,8 +1813,8 @@ cudaError_t launch_attention_plan(const AttnParams& p, int n_seq, cudaStream_t s
   const int hpc = split_plan(G, p.window).hpc;
   // no programmatic-launch attribute and no early trigger: the next kernel
   // starts once the plan is complete and visible
-  attn_plan_kernel<<<1, 1024, 0, st>>>(p.ring_pos, p.n_past, n_seq, p.window, p.n_head_kv * (G / hpc),
-                                       p.plan_prefix, p.plan_nv, p.plan_sub);
+  (void)hpc;
+  attn_plan_kernel<<<n_seq, kStreamMaxSub, 0, st>>>(p.ring_pos, p.n_past, p.window, p.plan_nv, p.plan_sub);
   return cudaGetLastError();
 }
 

@@ -119,7 +119,7 @@ struct Layout {
   size_t logits_int, drafts_int, idl_int, npast_int, partial;
   size_t inj_raw, inj_ss, inj_rope, inj_hi, inj_lo, loop_pos, loop_cnt, loop_H, stamps;
   size_t attn_part, attn_ml, attn_cnt, chain_partial, chain_cnt, chain_item, chain_mb, chain_done;
-  size_t plan_prefix, plan_nv, plan_sub;
+  size_t plan_nv, plan_sub;
   size_t total;
   int attn_groups, chain_item_stride;
   size_t partial_floats;
@@ -190,8 +190,7 @@ Layout layout(const dflash_config& c) {
   L.attn_ml = take(sizeof(float2) * (size_t)kAttnSplitMaxCtas * 64);
   L.attn_groups = g.max_seq * g.Hq;
   L.attn_cnt = take(sizeof(int) * 2 * (size_t)L.attn_groups);
-  // stream-K attention plan: units before each sequence, listed sub-chunks
-  L.plan_prefix = take(sizeof(int) * (size_t)(g.max_seq + 1));
+  // stream-K attention plan: listed sub-chunks of each sequence
   L.plan_nv = take(sizeof(int) * (size_t)g.max_seq);
   L.plan_sub = take(sizeof(int) * (size_t)g.max_seq * 64);
   // projection chains: per phase its partial tiles and tickets, item flags and
@@ -631,7 +630,6 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.part_o = h->S<float>(L.attn_part);
     a.part_ml = h->S<float2>(L.attn_ml);
     a.counters = h->S<int>(L.attn_cnt);
-    a.plan_prefix = h->S<int>(L.plan_prefix);
     a.plan_nv = h->S<int>(L.plan_nv);
     a.plan_sub = h->S<int>(L.plan_sub);
     // the o projection's weights into L2 while attention publishes and merges
@@ -1159,7 +1157,7 @@ int dflash_attention_kernel(const dflash_handle* h, int32_t n_seq) {
   a.ring_bf16 = g.ring_bf16;
   a.n_head = g.Hq; a.n_head_kv = g.Hkv; a.hd = g.hd; a.window = g.W;
   a.part_o = h->S<float>(h->L.attn_part);
-  a.plan_prefix = h->S<int>(h->L.plan_prefix);
+  a.plan_nv = h->S<int>(h->L.plan_nv);
   return attention_kind(a, n_seq);
 }
 

@@ -172,10 +172,8 @@ struct AttnParams {
   float2* part_ml;
   int* counters;
   int n_seq;              // sequences of the step (set by the launcher)
-  // stream-K kernel: the step's plan (attn_plan_kernel): units before each
-  // sequence [n_seq + 1], listed sub-chunks per sequence [n_seq] and their
-  // indices [n_seq][64] (null: no stream-K)
-  int* plan_prefix;
+  // stream-K kernel: the step's plan (attn_plan_kernel): listed sub-chunks per
+  // sequence [n_seq] and their indices [n_seq][64] (null: no stream-K)
   int* plan_nv;
   int* plan_sub;
   // L2 prefetch of the next projection's weights (one contiguous range, null:
