@@ -1,22 +1,26 @@
-// Sliding-window GQA attention of the noise block, one thread-block cluster per
-// (sequence, kv head, group of query heads).
+// Sliding-window GQA attention of the noise block.
 //
 // The block's 16 rows at positions n_past .. n_past + 15 attend (non-causally)
 // to every row of the block and to the ring slots holding positions p with
 // 0 <= p < n_past and (n_past + i) - p < window (dflash-ops model card, Method).
-// The ring of one kv head is split between the CL CTAs of a cluster.  Inside a
-// CTA, warp (h, q) owns query head h of the CTA's head group and key lane q:
-// the CTA's slots are cut into 64-key sub-chunks, staged into shared memory
-// with async copies kq at a time (one round), and key lane q attends to
-// sub-chunk q of each round with an online softmax, so the heads of the kv
-// group share every K/V tile and the sub-chunks of a round run in parallel.
-// Both products use the tensor cores with fp32 accumulation: q and the
-// probabilities are split into bf16 hi + lo, bf16 ring K/V are exact, fp32 K/V
-// (an fp32 ring, the block's own keys) are split too.  The key lanes' partial
-// (max, sum, O) states are merged inside the CTA, then the CTAs of the cluster
-// merge theirs through distributed shared memory in rank order and write the o
-// projection's input as a bf16 hi/lo pair.  Rank 0 also attends to the
-// block's own keys.
+// Every kernel here works on (sequence, kv head, group of query heads): the
+// ring of the kv head is cut into 64-key sub-chunks staged into shared memory
+// by async copies, warp (h, q) owns query head h of the group and key lane q,
+// and key lane q attends to its sub-chunks with an online softmax, so the
+// heads of the kv group share every K/V tile.  Both products use the tensor
+// cores (mma.sync) with fp32 accumulation: q and the probabilities are split
+// into bf16 hi + lo, bf16 ring K/V are exact, fp32 K/V (an fp32 ring, the
+// block's own keys) are split too.  Partial (max, sum, O) states are merged in
+// a fixed order, and the o projection's input is written as a 16-bit hi/lo
+// pair.  Three launch forms (launch_attention picks one per step):
+//   - split window (attn_split_kernel): every window in CTAs of 128 slots, the
+//     whole grid resident at once, merged through global scratch - one or a
+//     few sequences;
+//   - stream-K (attn_stream_kernel + attn_plan_kernel): one CTA per SM over
+//     equal ranges of all windows' non-empty sub-chunks - larger batches with
+//     a bf16 ring and head_dim >= 64;
+//   - clusters (attn_cluster_kernel): a window over the CTAs of a thread-block
+//     cluster, merged through distributed shared memory - the remaining cases.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -337,6 +341,13 @@ DF_DEVICE void attend_tile(const uint32_t (&qh)[HD / 16][4], const uint32_t (&ql
   }
 }
 
+// Cluster kernel: one thread-block cluster per (sequence, kv head, group of
+// query heads); the ring of the kv head is split between the CL CTAs of the
+// cluster, each CTA stages its slots' sub-chunks nb at a time (a round) and
+// key lane q attends to sub-chunk q of each round as soon as it lands.  The
+// key lanes merge inside the CTA, then the cluster's CTAs merge through
+// distributed shared memory in rank order; rank 0 also attends to the block's
+// own keys.
 template <int HD, bool RING_F32>
 __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant__ AttnParams p) {
   using SM = AttnSmem<HD>;
