@@ -59,6 +59,12 @@ struct Geometry {
   int wt, kc, dense_bf16, ring_bf16;
 };
 
+// The 16-bit activation pair of the projections of a step (or an injection)
+// of M rows: fp16 where the products run in fp16 - FP4 weights, and E4M3
+// weights below 128 rows (exact in fp16); bf16 otherwise (the tcgen05 kernel
+// runs E4M3 batches in bf16).
+inline int pair_f16_of(const Geometry& g, int M) { return g.wt == W_FP4 || (g.wt == W_FP8 && M < 128); }
+
 // Bytes of one [rows][K] projection weight buffer (FP4: codes, then block scales).
 inline size_t weight_bytes(int wt, int rows, int K) {
   const size_t n = (size_t)rows * K;
@@ -447,7 +453,7 @@ GemmParams base_params(const dflash_handle* h) {
   p.n_head_kv = h->g.Hkv;
   p.ring_bf16 = h->g.ring_bf16;
   // FP4 weights multiply in fp16: their projections' activation pairs are fp16
-  p.pair_f16 = h->g.wt == W_FP4;
+  p.pair_f16 = h->g.wt == W_FP4;   // the step sets its own (pair_f16_of)
   return p;
 }
 
@@ -498,7 +504,15 @@ void bind_projection(const dflash_handle* h, GemmParams& p, int l, std::initiali
 
 cudaError_t launch_bound(const dflash_handle* h, GemmParams& p, cudaStream_t st) {
   const bool dense = h->dense && p.M >= 128;
-  if (h->g.wt == W_FP4) return launch_gemm_fp4(p, st);
+  if (h->g.wt == W_FP4) return launch_gemm_fp4(W_FP4, p, st);
+  // 16-row E4M3 projections of at least 64 M weights whose k is a multiple of
+  // 256 run on the same tensor-memory pipeline (units of 128 rows x 256 k):
+  // it streams E4M3 faster than the 16-row TMA kernel's mma.sync path, whose
+  // shorter start wins below that (measured on the real drafter's projections)
+  if (h->g.wt == W_FP8 && !dense && p.K % 256 == 0 && p.has_lo && (long long)p.N * p.K >= (64ll << 20)) {
+    p.cpt = p.K / 256;
+    return launch_gemm_fp4(W_FP8, p, st);
+  }
   if (!dense) return launch_gemm_tma(h->g.wt, p, st);
   return launch_gemm_umma(h->g.wt, p, st);
 }
@@ -527,7 +541,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   // h = embeddings; xn = split(h * attn_norm_0); ss = row sums of squares
   PROF(h, PC_EMBED, st, launch_embed(h->w.tok_embd, g.dense_bf16, g.d, g.V, h->cfg.mask_token_id,
                                      id_last, n_past, n_seq, h->S<double>(L.inv_freq), g.hd, hbuf, ss,
-                                     rope, h->w.layers[0].attn_norm, xn_hi, xn_lo, g.wt == W_FP4,
+                                     rope, h->w.layers[0].attn_norm, xn_hi, xn_lo, pair_f16_of(g, M),
                                      embed_parts(g, L), L.ss_ld, h->status(),
                                      stamp_slot(h, PC_EMBED), st));
   // The projections' parameters (weights, schedule, row statistics, epilogue),
@@ -537,6 +551,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   auto qkv_p = [&](int l, int n_ss) {
     const dflash_layer_weights& lw = h->w.layers[l];
     GemmParams p = base_params(h);
+    p.pair_f16 = pair_f16_of(g, M);
     set_plan(p, sh[0], n_seq);
     p.M = M;
     p.ss = ss; p.n_ss = n_ss; p.ss_ld = L.ss_ld; p.row_scale = 1;
@@ -561,6 +576,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   // o projection + residual; next input xn = split(h * ffn_norm)
   auto o_p = [&](int l) {
     GemmParams p = base_params(h);
+    p.pair_f16 = pair_f16_of(g, M);
     set_plan(p, sh[1], n_seq);
     p.M = M;
     p.seg[0] = {h->w.layers[l].wo, h->w.layers[l].wo_scale, 0, g.d};
@@ -574,6 +590,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   auto gu_p = [&](int l) {
     const dflash_layer_weights& lw = h->w.layers[l];
     GemmParams p = base_params(h);
+    p.pair_f16 = pair_f16_of(g, M);
     set_plan(p, sh[2], n_seq);
     p.M = M;
     p.ss = ss; p.n_ss = sh[1].n_tiles; p.ss_ld = L.ss_ld; p.row_scale = 1;
@@ -588,6 +605,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   // down projection + residual; next input xn = split(h * next norm)
   auto down_p = [&](int l) {
     GemmParams p = base_params(h);
+    p.pair_f16 = pair_f16_of(g, M);
     set_plan(p, sh[3], n_seq);
     p.M = M;
     p.seg[0] = {h->w.layers[l].down, h->w.layers[l].down_scale, 0, g.d};
@@ -601,6 +619,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
   // LM head of RMSNorm(h) (out_norm folded into xn by the last down projection)
   auto lm_p = [&]() {
     GemmParams p = base_params(h);
+    p.pair_f16 = pair_f16_of(g, M);
     set_plan(p, sh[4], n_seq);
     p.M = M;
     p.ss = ss; p.n_ss = sh[3].n_tiles; p.ss_ld = L.ss_ld; p.row_scale = 1;
@@ -623,7 +642,7 @@ int run_step(dflash_handle* h, int n_seq, const int32_t* id_last, const int32_t*
     a.n_head = g.Hq; a.n_head_kv = g.Hkv; a.hd = g.hd; a.window = g.W;
     a.scale = (float)(1.0 / std::sqrt((double)g.hd));
     a.out_hi = h->S<uint16_t>(L.attn_hi); a.out_lo = h->S<uint16_t>(L.attn_lo);
-    a.pair_f16 = g.wt == W_FP4;
+    a.pair_f16 = pair_f16_of(g, M);
     a.tm_ring = h->tm_ring;
     a.status = h->status();
     a.block_width = h->width;
@@ -797,7 +816,7 @@ bool build_maps(dflash_handle* h) {
         !make_map(&h->tm_ring, h->ring, W_BF16, g.hd, rows, 64, 64, true))
       return false;
   }
-  if (g.wt == W_FP4) {
+  if (g.wt == W_FP4 || g.wt == W_FP8) {
     // the 4-D pair maps; a driver that refuses them leaves the 2-D path (x4 off)
     h->x4 = true;
     for (int i = 0; i < 3; ++i)
@@ -918,7 +937,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* ring_
                             cfg->ring_dtype == DFLASH_DTYPE_F32, cfg->window, cfg->n_head_kv);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking);
   // the chain's waits need its whole grid resident at once
-  if (e == cudaSuccess && h->g.wt != W_FP4) h->chain_ok = gemm_chain_capacity(h->g.wt) >= kGemmGrid;
+  // (chains run on the 16-row TMA kernel: not for FP4 and E4M3 weights, whose
+  // projections run on the tensor-memory pipeline)
+  if (e == cudaSuccess && h->g.wt != W_FP4 && h->g.wt != W_FP8)
+    h->chain_ok = gemm_chain_capacity(h->g.wt) >= kGemmGrid;
   h->chain = false;   // opt-in: measured no faster than one launch per projection
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -1004,11 +1026,11 @@ int run_inject(dflash_handle* h, int seq, const float* H_t, const int32_t* pos, 
   const int n_mb = cdiv(T, 16);
   GemmParams p = base_params(h);
   if (g.wt == W_FP4) {
-    // FP4 weights: H_t as a bf16 pair, then per layer its wk / wv projection on
+    // FP4 weights: H_t as an fp16 pair, then per layer its wk / wv projection on
     // the 16-row TMA kernel with the ring scatter in the epilogue (the ring
     // pointer moved to the layer's planes: the epilogue's layer 0)
     DF_CHECK(h, launch_split_pair(H_t, T * g.d, h->S<uint16_t>(h->L.inj_hi),
-                                  h->S<uint16_t>(h->L.inj_lo), g.wt == W_FP4, st));
+                                  h->S<uint16_t>(h->L.inj_lo), pair_f16_of(g, T), st));
     const size_t layer_bytes = h->L.ring_kv_bytes / g.L;
     const GemmShape kv = {cdiv(2 * g.kvd, kTileRows), g.d, tma_chunk_k(g.wt)};
     for (int l = 0; l < g.L; ++l) {
@@ -1036,17 +1058,17 @@ int run_inject(dflash_handle* h, int seq, const float* H_t, const int32_t* pos, 
       q.epi = EPI_INJECT; q.ring_seq = h->ring_seq(seq) + (size_t)l * layer_bytes; q.pos = pos;
       q.rope_cs = rope;
       q.rows_per_seq = rows_per_seq; q.row_count = count; q.ring_seq_stride = h->L.ring_seq_bytes;
-      DF_CHECK(h, launch_gemm_fp4(q, st));
+      DF_CHECK(h, launch_gemm_fp4(W_FP4, q, st));
     }
     prof_end(h, st);
     return DFLASH_OK;
   }
   if (h->inj_dense && T >= 128) {
-    // >= 128 rows: H_t as a bf16 hi/lo pair, then per layer its wk / wv
+    // >= 128 rows: H_t as a 16-bit hi/lo pair, then per layer its wk / wv
     // projection on the tcgen05 kernel with the ring scatter in the epilogue
     // (the ring pointer moved to the layer's planes: the epilogue's layer 0)
     DF_CHECK(h, launch_split_pair(H_t, T * g.d, h->S<uint16_t>(h->L.inj_hi),
-                                  h->S<uint16_t>(h->L.inj_lo), g.wt == W_FP4, st));
+                                  h->S<uint16_t>(h->L.inj_lo), pair_f16_of(g, T), st));
     const size_t layer_bytes = h->L.ring_kv_bytes / g.L;
     for (int l = 0; l < g.L; ++l) {
       const dflash_layer_weights& lw = h->w.layers[l];

@@ -46,21 +46,29 @@ namespace dflash {
 
 namespace fp4 {
 
-constexpr int kS = 5;                       // pipeline stages
 constexpr int kBox = 16 * 128;              // one 16-row x 128-byte box
 constexpr int kScaleBox = 256;              // block scales of 16 rows x 256 k
-constexpr int kCodes = 8 * kBox;            // the tile's code boxes
-constexpr int kScales = 8 * kScaleBox;
 constexpr int kX = 4 * kBox;                // 256 k of one half of the activation pair
 constexpr int kAB = 2;                      // A buffers (128 TMEM columns each)
 constexpr int kDB = 2;                      // accumulator buffers per MMA warp (32 columns each)
-constexpr int kStage = kCodes + kScales + 2 * kX;
-constexpr int kOffAcc = kS * kStage;        // 16 x 128 fp32 fix-up tile
-constexpr int kOffInv = kOffAcc + 16 * kTileRows * 4;
-constexpr int kOffScale = kOffInv + 16 * 4;
-constexpr int kOffBars = kOffScale + kTileRows * 4;   // full, empty [S]; afull, aempty [AB]; accf, acce [DB]
-constexpr int kOffTmem = kOffBars + (2 * kS + 2 * kAB + 2 * kDB) * 8;
-constexpr int kSmem = kOffTmem + 16 + 1024;            // + alignment slack
+// Shared-memory layout per weight format: a unit's codes (FP4: 128 bytes per
+// row and its block scales; E4M3: two 128-byte k halves per row), the
+// activation pair, and the fix-up / epilogue area
+template <int WF>
+struct Lay {
+  static constexpr int kS = WF == W_FP8 ? 4 : 5;                      // pipeline stages
+  static constexpr int kCodes = (WF == W_FP8 ? 2 : 1) * 8 * kBox;     // the tile's code boxes
+  static constexpr int kScales = WF == W_FP8 ? 0 : 8 * kScaleBox;
+  static constexpr int kStage = kCodes + kScales + 2 * kX;
+  static constexpr int kOffAcc = kS * kStage;        // 16 x 128 fp32 fix-up tile
+  static constexpr int kOffInv = kOffAcc + 16 * kTileRows * 4;
+  static constexpr int kOffScale = kOffInv + 16 * 4;
+  static constexpr int kOffBars = kOffScale + kTileRows * 4;   // full, empty [S]; afull, aempty [AB]; accf, acce [DB]
+  static constexpr int kOffTmem = kOffBars + (2 * kS + 2 * kAB + 2 * kDB) * 8;
+  static constexpr int kSmem = kOffTmem + 16 + 1024;            // + alignment slack
+  static_assert(kStage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled boxes");
+  static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "one CTA per SM (it owns the SM's TMEM)");
+};
 constexpr int kEpilogue = 8;                // warps 0..7: segment read-out, fix-up and epilogue
 constexpr int kDecoders = 8;                // warps 8..15: decoding
 constexpr int kIssuers = 4;                 // MMA warps: issuer i takes k16 steps 4i .. 4i + 3
@@ -70,8 +78,6 @@ constexpr int kTmemCols = 512;              // A: 2 x 128 columns; D: issuers x 
 constexpr int kDCol = 128 * kAB;
 static_assert(kDCol + kIssuers * kDB * 32 <= kTmemCols, "tensor memory columns");
 constexpr long long kWait = 4000000000LL;
-static_assert(kStage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled boxes");
-static_assert(kSmem <= 227 * 1024 && kSmem > 114 * 1024, "one CTA per SM (it owns the SM's TMEM)");
 
 DF_DEVICE uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 DF_DEVICE void bar_init(uint64_t* b, uint32_t n) {
@@ -223,8 +229,13 @@ DF_DEVICE void prefetch_share(const GemmParams& p, int b, int G) {
 
 }  // namespace fp4
 
+template <int WF>
 __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid_constant__ GemmParams p) {
   using namespace fp4;
+  using Lt = Lay<WF>;
+  constexpr int kS = Lt::kS, kStage = Lt::kStage, kCodes = Lt::kCodes, kScales = Lt::kScales;
+  constexpr int kOffAcc = Lt::kOffAcc, kOffInv = Lt::kOffInv, kOffScale = Lt::kOffScale;
+  constexpr int kOffBars = Lt::kOffBars, kOffTmem = Lt::kOffTmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* acc_s = reinterpret_cast<float*>(sm + kOffAcc);
@@ -299,7 +310,24 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
           uint8_t* dst = sm + st * kStage;
           bar_expect(&full[st], kStage);
 #pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {
+          for (int hq = 0; hq < 2 && WF == W_FP8; ++hq) {
+            // E4M3: the unit's 256 k of each row are two 128-byte halves
+            const int g0 = 4 * hq;
+            const bool w64 = p.w64 && gmap[g0 + 3] == gmap[g0] && grow[g0 + 3] == grow[g0] + 48;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+              uint8_t* cd = dst + kb * (8 * kBox);
+              if (w64) {
+                tma2d_hint(cd + g0 * kBox, &p.tm_w64[gmap[g0]], c * 256 + kb * 128, grow[g0], &full[st], pol);
+              } else {
+#pragma unroll
+                for (int grp = g0; grp < g0 + 4; ++grp)
+                  tma2d_hint(cd + grp * kBox, &p.tm_w[gmap[grp]], c * 256 + kb * 128, grow[grp], &full[st], pol);
+              }
+            }
+          }
+#pragma unroll
+          for (int hq = 0; hq < 2 && WF == W_FP4; ++hq) {
             const int g0 = 4 * hq;
             if (p.w64 && gmap[g0 + 3] == gmap[g0] && grow[g0 + 3] == grow[g0] + 48) {
               // four groups of one segment: one 64-row code box and one box of
@@ -425,7 +453,28 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
         const uint8_t* cbox = sm + st * kStage + grp * kBox;
         const uint8_t* sbox = sm + st * kStage + kCodes + grp * kScaleBox + pos;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < 2 && WF == W_FP8; ++hf) {
+          // this lane's row, 64 k of k half kq / 2: four 16-byte chunks of E4M3
+          // codes in natural order, each pair widened to fp16 (exact)
+          const int kq = 2 * kh + hf;
+          const uint8_t* cb = cbox + (kq >> 1) * (8 * kBox);
+          uint4 w4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) w4[i] = *reinterpret_cast<const uint4*>(cb + swz(rr, 4 * (kq & 1) + i));
+          uint32_t v[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t ws[4] = {w4[i].x, w4[i].y, w4[i].z, w4[i].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v[8 * i + 2 * e] = e4m3x2_to_f16x2((uint16_t)(ws[e] & 0xffffu));
+              v[8 * i + 2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(ws[e] >> 16));
+            }
+          }
+          tmem_st32(tmem + lane_base + ab * 128 + 32 * kq, v);
+        }
+#pragma unroll
+        for (int hf = 0; hf < 2 && WF == W_FP4; ++hf) {
           // this lane's row, k16 steps 4kq .. 4kq + 3: code groups 2kq, 2kq + 1
           // (all loads first)
           const int kq = 2 * kh + hf;
@@ -511,15 +560,22 @@ __global__ void __launch_bounds__(fp4::kThreads, 1) gemm_fp4_kernel(const __grid
   }
 }
 
-size_t gemm_fp4_smem_bytes() { return fp4::kSmem; }
+size_t gemm_fp4_smem_bytes() {
+  return fp4::Lay<W_FP4>::kSmem > fp4::Lay<W_FP8>::kSmem ? fp4::Lay<W_FP4>::kSmem : fp4::Lay<W_FP8>::kSmem;
+}
 
 cudaError_t configure_gemm_fp4() {
-  return cudaFuncSetAttribute(gemm_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fp4::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_fp4_kernel<W_FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       fp4::Lay<W_FP4>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_fp4_kernel<W_FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             fp4::Lay<W_FP8>::kSmem);
+  return e;
 }
 
 // p: the schedule of the 16-row kernels (n_tiles, n_mb, cpt = K / 256); the grid
 // is one CTA per SM (fewer when there are fewer units).
-cudaError_t launch_gemm_fp4(const GemmParams& p, cudaStream_t st) {
+cudaError_t launch_gemm_fp4(int wt, const GemmParams& p, cudaStream_t st) {
   static int n_sm = 0;
   if (!n_sm) {
     int dev = 0;
@@ -532,14 +588,16 @@ cudaError_t launch_gemm_fp4(const GemmParams& p, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units < n_sm ? units : n_sm));
   cfg.blockDim = dim3(fp4::kThreads);
-  cfg.dynamicSmemBytes = fp4::kSmem;
+  cfg.dynamicSmemBytes = wt == W_FP8 ? fp4::Lay<W_FP8>::kSmem : fp4::Lay<W_FP4>::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = kDependentLaunch ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel, p);
+  if (wt == W_FP8) return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<W_FP8>, p);
+  if (wt != W_FP4) return cudaErrorInvalidValue;
+  return cudaLaunchKernelEx(&cfg, gemm_fp4_kernel<W_FP4>, p);
 }
 
 }  // namespace dflash

@@ -168,21 +168,22 @@ struct Consume<W_FP8> {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
-      // E4M3 pairs (k = 16s + 2t and + 8) of rows g and g + 8, widened to bf16
+      // E4M3 pairs (k = 16s + 2t and + 8) of rows g and g + 8, widened to fp16
+      // (exact, one conversion each); the activations are an fp16 hi/lo pair
       const uint16_t q0 = *reinterpret_cast<const uint16_t*>(w + swz(g, s) + 2 * t);
       const uint16_t q1 = *reinterpret_cast<const uint16_t*>(w + swz(g + 8, s) + 2 * t);
       const uint16_t q2 = *reinterpret_cast<const uint16_t*>(w + swz(g, s) + 2 * t + 8);
       const uint16_t q3 = *reinterpret_cast<const uint16_t*>(w + swz(g + 8, s) + 2 * t + 8);
-      const uint32_t a[4] = {e4m3x2_to_bf16x2(q0), e4m3x2_to_bf16x2(q1), e4m3x2_to_bf16x2(q2),
-                             e4m3x2_to_bf16x2(q3)};
+      const uint32_t a[4] = {e4m3x2_to_f16x2(q0), e4m3x2_to_f16x2(q1), e4m3x2_to_f16x2(q2),
+                             e4m3x2_to_f16x2(q3)};
       uint32_t b[4];
       x_frags(b, xh + (s >> 2) * kBox, 2 * (s & 3), lane);
-      mma_bf16_16816(acc[0], a, b[0], b[1]);
-      mma_bf16_16816(acc[1], a, b[2], b[3]);
+      mma_f16_16816(acc[0], a, b[0], b[1]);
+      mma_f16_16816(acc[1], a, b[2], b[3]);
       if (has_lo) {
         x_frags(b, xl + (s >> 2) * kBox, 2 * (s & 3), lane);
-        mma_bf16_16816(acc[0], a, b[0], b[1]);
-        mma_bf16_16816(acc[1], a, b[2], b[3]);
+        mma_f16_16816(acc[0], a, b[0], b[1]);
+        mma_f16_16816(acc[1], a, b[2], b[3]);
       }
     }
   }

@@ -105,7 +105,7 @@ struct GemmParams {
   uint16_t* pair_hi;
   uint16_t* pair_lo;
   int pair_ld;
-  int pair_f16;           // the pair is fp16 (FP4 weights), else bf16
+  int pair_f16;           // the pair is fp16 (FP4 or E4M3 weights), else bf16
   const void* pair_norm;
   // q/k/v epilogues
   float* kblk;
@@ -161,7 +161,7 @@ struct AttnParams {
   int nb;                 // 64-key sub-chunk staging buffers (a multiple of kq)
   uint16_t* out_hi;       // [M][qd] hi/lo pair (the o projection's input)
   uint16_t* out_lo;
-  int pair_f16;           // fp16 pair (FP4 weights), else bf16
+  int pair_f16;           // fp16 pair (FP4 or E4M3 weights), else bf16
   unsigned* status;       // device status bits (DFLASH_DEV_TIMEOUT on a copy that never lands)
   int block_width;        // block rows that exist (2..16): block keys at or past it are masked
   unsigned long long* stamp;  // launch timestamp slot (profiling captures), else null
@@ -233,7 +233,7 @@ int tma_chunk_k(int wt);   // k per pipeline stage of the TMA projection kernel
 // activation blocks; the schedule fields as for the 16-row kernels, K % 256 == 0)
 size_t gemm_fp4_smem_bytes();
 cudaError_t configure_gemm_fp4();
-cudaError_t launch_gemm_fp4(const GemmParams& p, cudaStream_t st);
+cudaError_t launch_gemm_fp4(int wt, const GemmParams& p, cudaStream_t st);   // wt: W_FP4 or W_FP8
 
 // tcgen05 projection for >= 128 activation rows (bf16 or E4M3 weights)
 size_t gemm_umma_smem_bytes();

@@ -279,7 +279,7 @@ DFLASH_API int dflash_set_block_width(dflash_handle* h, int32_t width);
  * faster (every tile of a stream-K phase completes near the phase's end, so the
  * next phase starts no earlier than after a kernel boundary with programmatic
  * dependent launch).  enable = 0 or 1; UNSUPPORTED when enabling on a handle
- * without chains (FP4 weights, or a device that cannot hold the grid);
+ * without chains (FP4 or E4M3 weights, or a device that cannot hold the grid);
  * INVALID_ARG during a capture.  Takes effect for later steps and captures.
  */
 DFLASH_API int dflash_set_chain(dflash_handle* h, int32_t enable);

@@ -244,8 +244,7 @@ def test_small_bf16_full():
     assert np.array_equal(gpu["n_ok"], ref["n_ok"])
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "ragged_bf16", "mixed_f32w_bf16ring", "small_fp8",
-                                  "split_bf16", "split_f32"])
+@pytest.mark.parametrize("name", ["tiny_f32", "ragged_bf16", "mixed_f32w_bf16ring", "split_bf16", "split_f32"])
 def test_projection_chain_bitwise_equals_separate_launches(name):
     check_chain_bitwise(name)
 
@@ -277,9 +276,10 @@ def check_chain_bitwise(name):
     dr.close()
 
 
-def test_projection_chain_refused_where_unsupported():
+@pytest.mark.parametrize("name", ["small_fp4", "small_fp8"])
+def test_projection_chain_refused_where_unsupported(name):
     from block_diffusion_drafter_fc_gb300 import dflash as D
-    wl = make_workload(get_config("small_fp4"))
+    wl = make_workload(get_config(name))
     dw, _ = GH.to_device(wl)
     dr = D.Drafter(wl.cfg, dw, max_seq=wl.cfg.n_seq)
     with pytest.raises(D.DFlashError, match=r"\[-2\]"):
