@@ -128,70 +128,117 @@ DF_DEVICE void compute_inv_rms(const GemmParams& p, float* inv_rms, int m0) {
 
 DF_DEVICE void argmax_ticket(const GemmParams& p, int mb0, int n_blocks, int* s_flag);
 
-DF_DEVICE void epilogue_rows(const GemmParams& p, float* acc_s, const float* scale_s, int mb,
-                             int tile, int* s_flag) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int m0 = mb * 16;
-  const bool logits = p.epi == EPI_LOGITS;
-  constexpr int kPer = 16 * kTileRows / kGemmThreads;
-  const bool resid = p.epi == EPI_RESID_SS;
-  // the residual rows and next-norm weights this thread needs, all loads first
-  float res[kPer], nw[kPer];
+DF_DEVICE bool aligned16(const void* q) { return ((uintptr_t)q & 15) == 0; }
+
+// Row epilogues of one finished 16 x 128 tile (store; residual add + the next
+// projection's input pair + the rows' sums of squares; logits + per-row argmax).
+// Thread t owns 8 consecutive columns of row t / 16: its loads and stores are
+// 16-byte vectors (scalar at a ragged or unaligned edge), and a row's sum of
+// squares or argmax is a shuffle reduction over the row's 16 threads.  With
+// p.row_scale the accumulators are first multiplied by the row's 1 / rms.
+DF_DEVICE void epilogue_rows(const GemmParams& p, const float* acc_s, const float* scale_s,
+                             const float* inv_rms, int mb, int tile, int* s_flag) {
+  const int tid = threadIdx.x, m = tid >> 4, c0 = (tid & 15) * 8;
+  const int row = mb * 16 + m, n0 = tile * kTileRows + c0;
+  const bool logits = p.epi == EPI_LOGITS, resid = p.epi == EPI_RESID_SS;
+  const bool pair = resid && p.pair_hi != nullptr;
+  const int nv = row < p.M ? max(0, min(8, p.N - n0)) : 0;   // this thread's valid columns
+  float* o = p.out ? p.out + (size_t)row * p.ldo + n0 : nullptr;
+  uint16_t* oh = pair ? p.pair_hi + (size_t)row * p.pair_ld + n0 : nullptr;
+  uint16_t* ol = pair ? p.pair_lo + (size_t)row * p.pair_ld + n0 : nullptr;
+  const char* nwp = pair ? static_cast<const char*>(p.pair_norm) + (size_t)n0 * (p.norm_bf16 ? 2 : 4)
+                         : nullptr;
+  const bool vec = nv == 8 && (!o || aligned16(o)) &&
+                   (!pair || (aligned16(oh) && aligned16(ol) && aligned16(nwp)));
+  // the residual and the next norm's weights, all loads first
+  float res[8], nw[8];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = tid + k * kGemmThreads;
-    const int m = i / kTileRows, r = i - m * kTileRows;
-    const int n = tile * kTileRows + r, row = m0 + m;
-    const bool ok = n < p.N && row < p.M;
-    res[k] = resid && ok ? __ldcg(p.out + (size_t)row * p.ldo + n) : 0.f;
-    nw[k] = resid && ok && p.pair_hi ? load_dense(p.pair_norm, p.norm_bf16, n) : 0.f;
-  }
+  for (int j = 0; j < 8; ++j) res[j] = nw[j] = 0.f;
+  if (resid && vec) {
+    const float4 r0 = __ldcg(reinterpret_cast<const float4*>(o));
+    const float4 r1 = __ldcg(reinterpret_cast<const float4*>(o) + 1);
+    res[0] = r0.x; res[1] = r0.y; res[2] = r0.z; res[3] = r0.w;
+    res[4] = r1.x; res[5] = r1.y; res[6] = r1.z; res[7] = r1.w;
+    if (pair && p.norm_bf16) {
+      const uint4 w = *reinterpret_cast<const uint4*>(nwp);
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = tid + k * kGemmThreads;
-    const int m = i / kTileRows, r = i - m * kTileRows;
-    const int n = tile * kTileRows + r, row = m0 + m;
-    float y = acc_s[i] * scale_s[r];
-    if (n < p.N && row < p.M) {
-      if (resid) {
-        y += res[k];
-        p.out[(size_t)row * p.ldo + n] = y;
-        if (p.pair_hi) {
-          // the next projection's input: split(h * next norm weight)
-          uint16_t zh, zl;
-          split_pair16(y * nw[k], p.pair_f16 != 0, zh, zl);
-          p.pair_hi[(size_t)row * p.pair_ld + n] = zh;
-          p.pair_lo[(size_t)row * p.pair_ld + n] = zl;
-        }
-      } else if (p.out) {
-        p.out[(size_t)row * p.ldo + n] = y;
+      for (int j = 0; j < 4; ++j) {
+        nw[2 * j] = bf16_bits_to_f32((uint16_t)(wv[j] & 0xffffu));
+        nw[2 * j + 1] = bf16_bits_to_f32((uint16_t)(wv[j] >> 16));
       }
-    } else {
-      y = logits ? -CUDART_INF_F : 0.f;
+    } else if (pair) {
+      const float4 w0 = *reinterpret_cast<const float4*>(nwp);
+      const float4 w1 = *(reinterpret_cast<const float4*>(nwp) + 1);
+      nw[0] = w0.x; nw[1] = w0.y; nw[2] = w0.z; nw[3] = w0.w;
+      nw[4] = w1.x; nw[5] = w1.y; nw[6] = w1.z; nw[7] = w1.w;
     }
-    acc_s[i] = y;
+  } else if (resid) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nv) {
+        res[j] = __ldcg(o + j);
+        if (pair) nw[j] = load_dense(p.pair_norm, p.norm_bf16, n0 + j);
+      }
   }
-  csync();
-  if (p.epi == EPI_STORE_SS || p.epi == EPI_RESID_SS) {
-    for (int m = warp; m < 16; m += kGemmThreads / 32) {
-      float s = 0.f;
-      for (int r = lane; r < kTileRows; r += 32) s += acc_s[m * kTileRows + r] * acc_s[m * kTileRows + r];
-      s = warp_sum(s);
-      if (lane == 0 && m0 + m < p.M) p.ss_out[(size_t)tile * p.ss_out_ld + m0 + m] = s;
+  const float inv = p.row_scale ? inv_rms[m] : 1.f;
+  float y[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float a = acc_s[m * kTileRows + c0 + j];
+    if (p.row_scale) a *= inv;
+    y[j] = a * scale_s[c0 + j];
+    if (resid) y[j] += res[j];
+    if (j >= nv) y[j] = 0.f;
+  }
+  if (vec) {
+    if (o) {
+      reinterpret_cast<float4*>(o)[0] = make_float4(y[0], y[1], y[2], y[3]);
+      reinterpret_cast<float4*>(o)[1] = make_float4(y[4], y[5], y[6], y[7]);
     }
+    if (pair) {
+      // the next projection's input: split(h * next norm weight)
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        split_pair16x2(y[2 * j] * nw[2 * j], y[2 * j + 1] * nw[2 * j + 1], p.pair_f16 != 0, h[j], l[j]);
+      *reinterpret_cast<uint4*>(oh) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(ol) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nv) {
+        if (o) o[j] = y[j];
+        if (pair) {
+          uint16_t zh, zl;
+          split_pair16(y[j] * nw[j], p.pair_f16 != 0, zh, zl);
+          oh[j] = zh;
+          ol[j] = zl;
+        }
+      }
+  }
+  if (p.epi == EPI_STORE_SS || resid) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += y[j] * y[j];
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if ((tid & 15) == 0 && row < p.M) p.ss_out[(size_t)tile * p.ss_out_ld + row] = ss;
   }
   if (!logits) return;
-  for (int m = warp; m < 16; m += kGemmThreads / 32) {
-    float v = -CUDART_INF_F;
-    int idx = 0x7fffffff;
-    for (int r = lane; r < kTileRows; r += 32) {
-      const int n = tile * kTileRows + r;
-      if (n < p.N) argmax_merge(v, idx, acc_s[m * kTileRows + r], n);
-    }
-    warp_argmax(v, idx);
-    if (lane == 0 && m0 + m < p.M)
-      p.am_part[(size_t)tile * p.M + m0 + m] = make_float2(v, __int_as_float(idx));
+  float v = -CUDART_INF_F;
+  int idx = 0x7fffffff;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < nv) argmax_merge(v, idx, y[j], n0 + j);
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+    const int i2 = __shfl_xor_sync(0xffffffffu, idx, off);
+    argmax_merge(v, idx, v2, i2);
   }
+  if ((tid & 15) == 0 && row < p.M) p.am_part[(size_t)tile * p.M + row] = make_float2(v, __int_as_float(idx));
   argmax_ticket(p, mb, 1, s_flag);
 }
 
@@ -235,30 +282,61 @@ DF_DEVICE void argmax_ticket(const GemmParams& p, int mb0, int n_blocks, int* s_
   }
 }
 
+// SwiGLU of one finished tile (gate rows 0..63, up rows 64..127): thread t
+// owns 4 consecutive outputs of row t / 16 (8-byte pair stores, 16-byte output
+// stores; scalar at a ragged or unaligned edge).
 DF_DEVICE void epilogue_swiglu(const GemmParams& p, const float* acc_s, const float* scale_s,
-                               int mb, int tile) {
-  const int half = kTileRows / 2, F = p.seg[0].rows;
-  for (int i = threadIdx.x; i < 16 * half; i += kGemmThreads) {
-    const int m = i / half, j = i - m * half;
-    const int f = tile * half + j, row = mb * 16 + m;
-    if (f >= F || row >= p.M) continue;
-    const float gv = acc_s[m * kTileRows + j] * scale_s[j];
-    const float uv = acc_s[m * kTileRows + half + j] * scale_s[half + j];
-    const float a = gv / (1.f + expf(-gv)) * uv;
-    if (p.out) p.out[(size_t)row * p.ldo + f] = a;
-    if (p.pair_hi) {
-      uint16_t ah, al;
-      split_pair16(a, p.pair_f16 != 0, ah, al);
-      p.pair_hi[(size_t)row * p.pair_ld + f] = ah;
-      p.pair_lo[(size_t)row * p.pair_ld + f] = al;
+                               const float* inv_rms, int mb, int tile) {
+  constexpr int half = kTileRows / 2;
+  const int tid = threadIdx.x, m = tid >> 4, j0 = (tid & 15) * 4;
+  const int row = mb * 16 + m, f0 = tile * half + j0;
+  const int nv = row < p.M ? max(0, min(4, p.seg[0].rows - f0)) : 0;
+  if (nv == 0) return;
+  const float inv = p.row_scale ? inv_rms[m] : 1.f;
+  float a[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float g = acc_s[m * kTileRows + j0 + j], u = acc_s[m * kTileRows + half + j0 + j];
+    if (p.row_scale) {
+      g *= inv;
+      u *= inv;
     }
+    const float gv = g * scale_s[j0 + j], uv = u * scale_s[half + j0 + j];
+    a[j] = j < nv ? gv / (1.f + expf(-gv)) * uv : 0.f;
   }
+  float* o = p.out ? p.out + (size_t)row * p.ldo + f0 : nullptr;
+  uint16_t* oh = p.pair_hi ? p.pair_hi + (size_t)row * p.pair_ld + f0 : nullptr;
+  uint16_t* ol = p.pair_hi ? p.pair_lo + (size_t)row * p.pair_ld + f0 : nullptr;
+  const bool vec = nv == 4 && (!o || aligned16(o)) &&
+                   (!oh || ((((uintptr_t)oh | (uintptr_t)ol) & 7) == 0));
+  if (vec) {
+    if (o) *reinterpret_cast<float4*>(o) = make_float4(a[0], a[1], a[2], a[3]);
+    if (oh) {
+      uint32_t h0, l0, h1, l1;
+      split_pair16x2(a[0], a[1], p.pair_f16 != 0, h0, l0);
+      split_pair16x2(a[2], a[3], p.pair_f16 != 0, h1, l1);
+      *reinterpret_cast<uint2*>(oh) = make_uint2(h0, h1);
+      *reinterpret_cast<uint2*>(ol) = make_uint2(l0, l1);
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j < nv) {
+      if (o) o[j] = a[j];
+      if (oh) {
+        uint16_t ah, al;
+        split_pair16(a[j], p.pair_f16 != 0, ah, al);
+        oh[j] = ah;
+        ol[j] = al;
+      }
+    }
 }
 
 // Per-head RMSNorm + NEOX rope of q/k (raw v) for the block (EPI_QKV) or for
 // injected context rows scattered into the ring (EPI_INJECT).
 DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const float* scale_s,
-                              int mb, int tile) {
+                              const float* inv_rms, int mb, int tile) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hd = p.hd, half = hd >> 1, hpt = kTileRows / hd;
   for (int item = warp; item < 16 * hpt; item += kGemmThreads / 32) {
@@ -277,15 +355,36 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
       head = (w - (kind == 2 ? p.kvd : 0)) / hd;
       normw = p.k_norm_l[layer];
     }
+    // the norm weights and the row's rope entries first: their loads overlap the
+    // tile reads and the reduction
+    float wa[4], wb[4];
+    float2 cs[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = lane + 32 * u;
+      wa[u] = wb[u] = 0.f;
+      cs[u] = make_float2(0.f, 0.f);
+      if (kind != 2 && j < half) {
+        wa[u] = load_dense(normw, p.norm_bf16, j);
+        wb[u] = load_dense(normw, p.norm_bf16, j + half);
+        cs[u] = p.rope_cs[(size_t)row * half + j];
+      }
+    }
     const float* src = acc_s + m * kTileRows + hh * hd;
     const float* sc = scale_s + hh * hd;
+    const float rs = p.row_scale ? inv_rms[m] : 1.f;
     float x1[4], x2[4];
     float ss = 0.f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int j = lane + 32 * u;
-      x1[u] = j < half ? src[j] * sc[j] : 0.f;
-      x2[u] = j < half ? src[j + half] * sc[j + half] : 0.f;
+      float s1 = j < half ? src[j] : 0.f, s2 = j < half ? src[j + half] : 0.f;
+      if (p.row_scale) {
+        s1 *= rs;
+        s2 *= rs;
+      }
+      x1[u] = j < half ? s1 * sc[j] : 0.f;
+      x2[u] = j < half ? s2 * sc[j + half] : 0.f;
       ss += x1[u] * x1[u] + x2[u] * x2[u];
     }
     if (kind != 2) {
@@ -295,11 +394,10 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
       for (int u = 0; u < 4; ++u) {
         const int j = lane + 32 * u;
         if (j >= half) continue;
-        const float a = x1[u] * inv * load_dense(normw, p.norm_bf16, j);
-        const float b = x2[u] * inv * load_dense(normw, p.norm_bf16, j + half);
-        const float2 cs = p.rope_cs[(size_t)row * half + j];
-        x1[u] = a * cs.x - b * cs.y;
-        x2[u] = b * cs.x + a * cs.y;
+        const float a = x1[u] * inv * wa[u];
+        const float b = x2[u] * inv * wb[u];
+        x1[u] = a * cs[u].x - b * cs[u].y;
+        x2[u] = b * cs[u].x + a * cs[u].y;
       }
     }
     if (p.epi == EPI_QKV) {
@@ -348,25 +446,21 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
 }
 
 
-// Run the fused epilogue of one finished 16 x 128 tile.  With p.row_scale the
-// tile rows are first multiplied by 1 / rms (RMSNorm applied after the
-// projection: a per-row scalar commutes with the product).
+// Run the fused epilogue of one finished 16 x 128 tile.  With p.row_scale each
+// epilogue first multiplies the accumulators by their row's 1 / rms (RMSNorm
+// applied after the projection: a per-row scalar commutes with the product).
 DF_DEVICE void run_epilogue(const GemmParams& p, float* acc_s, const float* scale_s,
                             const float* inv_rms, int mb, int tile, int* s_flag) {
-  if (p.row_scale) {
-    for (int i = threadIdx.x; i < 16 * kTileRows; i += kGemmThreads) acc_s[i] *= inv_rms[i / kTileRows];
-    csync();
-  }
   switch (p.epi) {
     case EPI_SWIGLU:
-      epilogue_swiglu(p, acc_s, scale_s, mb, tile);
+      epilogue_swiglu(p, acc_s, scale_s, inv_rms, mb, tile);
       break;
     case EPI_QKV:
     case EPI_INJECT:
-      epilogue_heads(p, acc_s, scale_s, mb, tile);
+      epilogue_heads(p, acc_s, scale_s, inv_rms, mb, tile);
       break;
     default:
-      epilogue_rows(p, acc_s, scale_s, mb, tile, s_flag);
+      epilogue_rows(p, acc_s, scale_s, inv_rms, mb, tile, s_flag);
       break;
   }
 }
