@@ -334,17 +334,24 @@ DF_DEVICE void epilogue_swiglu(const GemmParams& p, const float* acc_s, const fl
 }
 
 // Per-head RMSNorm + NEOX rope of q/k (raw v) for the block (EPI_QKV) or for
-// injected context rows scattered into the ring (EPI_INJECT).
+// injected context rows scattered into the ring (EPI_INJECT).  One half-warp per
+// (row, head) item: lane l holds the per = hd / 32 consecutive elements
+// [l per, (l + 1) per) of the head's first half and their rope partners in the
+// second half, so the head's sum of squares is a 16-lane shuffle reduction and
+// the q/k/v stores are vectors.  Every lane takes part in the shuffles; items
+// past the tile's rows or columns are skipped only after them.
 DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const float* scale_s,
                               const float* inv_rms, int mb, int tile) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hd = p.hd, half = hd >> 1, hpt = kTileRows / hd;
-  for (int item = warp; item < 16 * hpt; item += kGemmThreads / 32) {
+  const int lane = threadIdx.x & 31, l16 = lane & 15;
+  const int hwi = (threadIdx.x >> 5) * 2 + (lane >> 4);   // half-warp 0..15
+  const int hd = p.hd, half = hd >> 1, hpt = kTileRows / hd, per = half / 16;
+  const int j0 = l16 * per;
+  for (int item = hwi; item < 16 * hpt; item += 16) {
     const int m = item / hpt, hh = item - m * hpt;
     const int n0 = tile * kTileRows + hh * hd, row = mb * 16 + m;
-    if (n0 >= p.N || row >= p.M) continue;
-    int kind, layer = 0, head = 0;
-    const void* normw;
+    const bool live = n0 < p.N && row < p.M;
+    int kind = 2, layer = 0, head = 0;
+    const void* normw = nullptr;
     if (p.epi == EPI_QKV) {
       kind = n0 < p.qd ? 0 : (n0 < p.qd + p.kvd ? 1 : 2);
       normw = kind == 0 ? p.q_norm : p.k_norm;
@@ -353,21 +360,21 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
       const int w = n0 - layer * 2 * p.kvd;
       kind = w < p.kvd ? 1 : 2;
       head = (w - (kind == 2 ? p.kvd : 0)) / hd;
-      normw = p.k_norm_l[layer];
+      if (live) normw = p.k_norm_l[layer];
     }
+    const bool rope = live && kind != 2;
     // the norm weights and the row's rope entries first: their loads overlap the
     // tile reads and the reduction
     float wa[4], wb[4];
     float2 cs[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = lane + 32 * u;
-      wa[u] = wb[u] = 0.f;
-      cs[u] = make_float2(0.f, 0.f);
-      if (kind != 2 && j < half) {
-        wa[u] = load_dense(normw, p.norm_bf16, j);
-        wb[u] = load_dense(normw, p.norm_bf16, j + half);
-        cs[u] = p.rope_cs[(size_t)row * half + j];
+    for (int q = 0; q < 4; ++q) {
+      wa[q] = wb[q] = 0.f;
+      cs[q] = make_float2(0.f, 0.f);
+      if (rope && q < per) {
+        wa[q] = load_dense(normw, p.norm_bf16, j0 + q);
+        wb[q] = load_dense(normw, p.norm_bf16, j0 + q + half);
+        cs[q] = p.rope_cs[(size_t)row * half + j0 + q];
       }
     }
     const float* src = acc_s + m * kTileRows + hh * hd;
@@ -376,41 +383,47 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
     float x1[4], x2[4];
     float ss = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int j = lane + 32 * u;
-      float s1 = j < half ? src[j] : 0.f, s2 = j < half ? src[j + half] : 0.f;
-      if (p.row_scale) {
-        s1 *= rs;
-        s2 *= rs;
+    for (int q = 0; q < 4; ++q) {
+      x1[q] = x2[q] = 0.f;
+      if (q < per) {
+        const int j = j0 + q;
+        float s1 = src[j], s2 = src[j + half];
+        if (p.row_scale) {
+          s1 *= rs;
+          s2 *= rs;
+        }
+        x1[q] = s1 * sc[j];
+        x2[q] = s2 * sc[j + half];
       }
-      x1[u] = j < half ? s1 * sc[j] : 0.f;
-      x2[u] = j < half ? s2 * sc[j + half] : 0.f;
-      ss += x1[u] * x1[u] + x2[u] * x2[u];
+      ss += x1[q] * x1[q] + x2[q] * x2[q];
     }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (!live) continue;
     if (kind != 2) {
-      ss = warp_sum(ss);
       const float inv = 1.f / sqrtf(ss / (float)hd + p.eps);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = lane + 32 * u;
-        if (j >= half) continue;
-        const float a = x1[u] * inv * wa[u];
-        const float b = x2[u] * inv * wb[u];
-        x1[u] = a * cs[u].x - b * cs[u].y;
-        x2[u] = b * cs[u].x + a * cs[u].y;
+      for (int q = 0; q < 4; ++q) {
+        const float a = x1[q] * inv * wa[q];
+        const float b = x2[q] * inv * wb[q];
+        x1[q] = a * cs[q].x - b * cs[q].y;
+        x2[q] = b * cs[q].x + a * cs[q].y;
       }
     }
     if (p.epi == EPI_QKV) {
       float* dst = kind == 0 ? p.out + (size_t)row * p.qd + n0
                  : kind == 1 ? p.kblk + (size_t)row * p.kvd + (n0 - p.qd)
                              : p.vblk + (size_t)row * p.kvd + (n0 - p.qd - p.kvd);
+      if (per == 4 && aligned16(dst)) {
+        reinterpret_cast<float4*>(dst + j0)[0] = make_float4(x1[0], x1[1], x1[2], x1[3]);
+        reinterpret_cast<float4*>(dst + half + j0)[0] = make_float4(x2[0], x2[1], x2[2], x2[3]);
+      } else {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = lane + 32 * u;
-        if (j < half) {
-          dst[j] = x1[u];
-          dst[j + half] = x2[u];
-        }
+        for (int q = 0; q < 4; ++q)
+          if (q < per) {
+            dst[j0 + q] = x1[q];
+            dst[j0 + q + half] = x2[q];
+          }
       }
     } else {
       int sq = 0;
@@ -420,7 +433,7 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
       }
       const int pos = p.pos[row];
       if (pos < 0) {
-        if (lane == 0) atomicOr(p.status, 0x2u);
+        if (l16 == 0) atomicOr(p.status, 0x2u);
         continue;
       }
       const int slot = pos % p.window;
@@ -428,17 +441,17 @@ DF_DEVICE void epilogue_heads(const GemmParams& p, const float* acc_s, const flo
           ((((size_t)layer * 2 + (kind == 2)) * p.n_head_kv + head) * p.window + slot) * hd;
       void* ring_base = static_cast<char*>(p.ring_seq) + (size_t)sq * p.ring_seq_stride;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = lane + 32 * u;
-        if (j >= half) continue;
+      for (int q = 0; q < 4; ++q) {
+        if (q >= per) continue;
+        const int j = j0 + q;
         if (p.ring_bf16) {
           uint16_t* d = reinterpret_cast<uint16_t*>(ring_base) + off;
-          d[j] = f32_to_bf16_bits(x1[u]);
-          d[j + half] = f32_to_bf16_bits(x2[u]);
+          d[j] = f32_to_bf16_bits(x1[q]);
+          d[j + half] = f32_to_bf16_bits(x2[q]);
         } else {
           float* d = reinterpret_cast<float*>(ring_base) + off;
-          d[j] = x1[u];
-          d[j + half] = x2[u];
+          d[j] = x1[q];
+          d[j + half] = x2[q];
         }
       }
     }
