@@ -1012,19 +1012,25 @@ __global__ void __launch_bounds__(256, 1) attn_split_kernel(const __grid_constan
     const size_t row0 = (size_t)group * n_split * R + r;           // split 0's copy of row r
     float2 ml = make_float2(-CUDART_INF_F, 0.f);
     if (lane < n_split) ml = __ldcg(p.part_ml + row0 + (size_t)lane * R);
-    const float M = warp_max(ml.x);
-    const float wgt = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
-    const float L = warp_sum(wgt * ml.y);
     const int d = lane * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    constexpr int kB = 8;
-    for (int c0 = 0; c0 < n_split; c0 += kB) {
-      float4 v[kB];
+    // the first kB splits' partial rows load together with (m, l): they do not
+    // depend on the weights, so the merge waits one L2 round trip, not three
+    constexpr int kB = 16;
+    float4 v[kB];
+    auto load_rows = [&](int c0) {
 #pragma unroll
       for (int u = 0; u < kB; ++u)
         v[u] = c0 + u < n_split && d < HD
                    ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (row0 + (size_t)(c0 + u) * R) * HD + d))
                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    load_rows(0);
+    const float M = warp_max(ml.x);
+    const float wgt = ml.x == -CUDART_INF_F ? 0.f : exp2f(ml.x - M);
+    const float L = warp_sum(wgt * ml.y);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < n_split; c0 += kB) {
+      if (c0 > 0) load_rows(c0);
 #pragma unroll
       for (int u = 0; u < kB; ++u) {
         const float wc = __shfl_sync(0xffffffffu, wgt, (c0 + u) & 31);   // splits in order
