@@ -25,7 +25,7 @@ template <int WT>
 struct TT;
 template <>
 struct TT<W_BF16> {  // 64 k per chunk: one 128-byte weight box, one activation box
-  static constexpr int CK = 64, WBOX_K = 64, WBOXES = 1, XBOXES = 1, S = 4, STEPS = 4, PEN = 4;
+  static constexpr int CK = 64, WBOX_K = 64, WBOXES = 1, XBOXES = 1, S = 4, STEPS = 4, PEN = 6;
 };
 template <>
 struct TT<W_F32> {   // 64 k per chunk: two 128-byte weight boxes of 32 fp32
