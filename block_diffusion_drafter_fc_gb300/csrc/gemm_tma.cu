@@ -2,18 +2,20 @@
 //
 // Same contract as gemm_rows_kernel (y[m][n] = sum_k x[m][k] W[n][k] for 16-row
 // activation blocks, stream-K split, fused epilogues) for activations that
-// their producer already stored as bf16 hi + lo pairs.  Warp 8 is a producer:
-// one lane walks this CTA's stream-K units and, per k chunk (128 bytes of every
-// weight row), issues cp.async.bulk.tensor loads of the 128 weight rows and of
-// the 16 activation rows (hi and lo) into a ring of shared-memory stages,
-// completing on the stage's "full" mbarrier.  The weight rows go as two 64-row
+// their producer already stored as bf16 hi + lo pairs.  Warps 8 and 9 are
+// producers: one lane of each walks this CTA's stream-K units and, per k chunk
+// (128 bytes of every weight row), issues cp.async.bulk.tensor loads - warp 8
+// of the 128 weight rows, warp 9 of the 16 activation rows (hi and lo) - into a
+// ring of shared-memory stages, both completing on the stage's "full" mbarrier.
+// The weight rows go as two 64-row
 // boxes where four 16-row groups of the tile are consecutive rows of one
 // segment (bf16 and E4M3), else as eight 16-row boxes (fp32 weights, segment
 // boundaries inside the tile), each from its segment's own tensor map.  Warps 0..7 are consumers: each owns 16 weight rows,
 // reads its A fragments and the shared B fragments with ldmatrix from the
 // 128-byte-swizzled tiles, runs mma.sync m16n8k16 (fp32 accumulation), and
 // releases the stage on its "empty" mbarrier.  The first stages' weight loads
-// are issued before griddepcontrol.wait, so they overlap the previous kernel.
+// are issued before griddepcontrol.wait (only the activation warp waits), so
+// they overlap the previous kernel.
 // Every mbarrier wait gives up after ~2 s, sets the device status bit
 // DFLASH_DEV_TIMEOUT and lets the CTA run to completion without further waits;
 // before exiting, the producer waits (with the same bound) for its last copies.
